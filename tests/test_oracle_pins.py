@@ -1,0 +1,287 @@
+"""Pins for the float64 oracle: each test ties an oracle function to something other
+than itself (closed forms, finite differences, torch autograd, brute force, the
+block-matrix invariants and the ReLU counterexample of the pages)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+from scipy.integrate import quad
+
+from oracle import collectives, mlp, sp
+from tensor_transformer_mlp_gb300 import workloads as wl
+
+KINDS = ("erf", "tanh")
+
+
+def _rand(shape, seed, std=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * std
+
+
+# ---------------------------------------------------------------- GeLU
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_gelu_closed_forms(kind):
+    assert mlp.gelu(0.0, kind) == 0.0
+    assert mlp.gelu_grad(0.0, kind) == 0.5
+    assert abs(mlp.gelu(12.0, kind) - 12.0) < 1e-12        # phi(x) -> x as x -> +inf
+    assert abs(mlp.gelu(-12.0, kind)) < 1e-12              # phi(x) -> 0 as x -> -inf
+    assert abs(mlp.gelu_grad(12.0, kind) - 1.0) < 1e-12
+    assert abs(mlp.gelu_grad(-12.0, kind)) < 1e-12
+
+
+def test_gelu_erf_is_x_times_normal_cdf_by_quadrature():
+    # Phi by numerical integration of the standard normal density: independent of erf.
+    pdf = lambda u: math.exp(-0.5 * u * u) / math.sqrt(2 * math.pi)
+    for x in (-3.1, -1.0, -0.25, 0.4, 1.7, 2.9):
+        cdf = quad(pdf, -np.inf, x, epsabs=1e-13, epsrel=1e-13, limit=200)[0]
+        assert abs(mlp.gelu(x, "erf") - x * cdf) < 1e-11
+
+
+def test_gelu_tanh_tracks_erf():
+    x = np.linspace(-8, 8, 20001)
+    diff = np.abs(mlp.gelu(x, "tanh") - mlp.gelu(x, "erf")).max()
+    assert 1e-5 < diff < 1e-3     # an approximation, and a close one
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_gelu_grad_matches_finite_differences(kind):
+    x = np.linspace(-6, 6, 1201)
+    h = 1e-5
+    fd = (mlp.gelu(x + h, kind) - mlp.gelu(x - h, kind)) / (2 * h)
+    assert np.abs(fd - mlp.gelu_grad(x, kind)).max() < 1e-8
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_gelu_matches_torch(kind):
+    x = torch.linspace(-7, 7, 4001, dtype=torch.float64)
+    ref = torch.nn.functional.gelu(x, approximate="none" if kind == "erf" else "tanh").numpy()
+    assert np.abs(mlp.gelu(x.numpy(), kind) - ref).max() < 1e-14
+
+
+# ---------------------------------------------------------------- MLP forward / backward
+
+def _worked_example():
+    return wl.mlp_inputs(wl.WORKED_EXAMPLE)
+
+
+def test_worked_example_shapes():
+    # "给两次投影标上跨卡尺寸": X 3x4, A 4x8, B 8x4; two 4x4 column blocks of A, two 4x4
+    # row blocks of B, two 3x4 contributions that sum to a 3x4 output.
+    inp = _worked_example()
+    assert inp["X"].shape == (3, 4) and inp["A"].shape == (4, 8) and inp["B"].shape == (8, 4)
+    views = mlp.shard_views(inp["A"], inp["B"], 2)
+    assert [v[0].shape for v in views] == [(4, 4), (4, 4)]
+    assert [v[1].shape for v in views] == [(4, 4), (4, 4)]
+    contributions = [mlp.gelu(inp["X"] @ Ai, "erf") @ Bi for Ai, Bi in views]
+    assert [c.shape for c in contributions] == [(3, 4), (3, 4)]
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_backward_matches_finite_differences(kind):
+    inp = _worked_example()
+    X, A, B, G = (inp[k].astype(np.float64) for k in "XABG")
+    grads = mlp.backward(X, A, B, G, kind)
+    loss = lambda X_, A_, B_: float((mlp.forward(X_, A_, B_, kind)["O"] * G).sum())
+    h = 1e-6
+    for name, arr, key in (("X", X, "dX"), ("A", A, "dA"), ("B", B, "dB")):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            plus, minus = arr.copy(), arr.copy()
+            plus[idx] += h
+            minus[idx] -= h
+            args_p = {"X": X, "A": A, "B": B}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = plus, minus
+            fd[idx] = (loss(args_p["X"], args_p["A"], args_p["B"]) - loss(args_m["X"], args_m["A"], args_m["B"])) / (2 * h)
+        err = np.abs(fd - grads[key]).max() / np.abs(grads[key]).max()
+        assert err < 1e-7, (name, err)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(3, 4, 8), (17, 24, 40)])
+def test_forward_backward_match_torch_autograd(kind, shape):
+    n, d, m = shape
+    X, A, B, G = _rand((n, d), 1), _rand((d, m), 2, 0.3), _rand((m, d), 3, 0.3), _rand((n, d), 4)
+    tX, tA, tB = (torch.tensor(a, requires_grad=True) for a in (X, A, B))
+    Z = tX @ tA
+    O = torch.nn.functional.gelu(Z, approximate="none" if kind == "erf" else "tanh") @ tB
+    O.backward(torch.tensor(G))
+    fwd = mlp.forward(X, A, B, kind)
+    bwd = mlp.backward(X, A, B, G, kind)
+    assert np.abs(fwd["O"] - O.detach().numpy()).max() < 1e-12
+    assert np.abs(fwd["Z"] - Z.detach().numpy()).max() < 1e-12
+    assert np.abs(bwd["dX"] - tX.grad.numpy()).max() < 1e-12
+    assert np.abs(bwd["dA"] - tA.grad.numpy()).max() < 1e-12
+    assert np.abs(bwd["dB"] - tB.grad.numpy()).max() < 1e-12
+
+
+def test_forward_brute_force_loops():
+    inp = _worked_example()
+    X, A, B = (inp[k].astype(np.float64).tolist() for k in "XAB")
+    n, d, m = 3, 4, 8
+    O = [[0.0] * d for _ in range(n)]
+    for r in range(n):
+        for j in range(m):
+            z = sum(X[r][k] * A[k][j] for k in range(d))
+            y = 0.5 * z * (1.0 + math.erf(z / math.sqrt(2.0)))
+            for c in range(d):
+                O[r][c] += y * B[j][c]
+    assert np.abs(np.array(O) - mlp.forward(inp["X"], inp["A"], inp["B"], "erf")["O"]).max() < 1e-13
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+def test_shard_sum_equals_unsharded(kind, t):
+    for X, A, B, G in ((lambda i: (i["X"], i["A"], i["B"], i["G"]))(_worked_example()),
+                       (_rand((16, 32), 5), _rand((32, 64), 6, 0.2), _rand((64, 32), 7, 0.2), _rand((16, 32), 8))):
+        ref_f, ref_b = mlp.forward(X, A, B, kind), mlp.backward(X, A, B, G, kind)
+        sh_f, sh_b = mlp.forward_sharded(X, A, B, t, kind), mlp.backward_sharded(X, A, B, G, t, kind)
+        for key in ("Z", "Y", "O"):
+            assert np.abs(sh_f[key] - ref_f[key]).max() < 1e-13 * max(1.0, np.abs(ref_f[key]).max())
+        for key in ("D", "dA", "dB", "dX"):
+            assert np.abs(sh_b[key] - ref_b[key]).max() < 1e-13 * max(1.0, np.abs(ref_b[key]).max())
+
+
+def test_uneven_split_rejected():
+    with pytest.raises(ValueError):
+        mlp.shard_views(np.zeros((4, 8)), np.zeros((8, 4)), 3)
+
+
+def test_relu_counterexample_exact():
+    # "教学算例": u = 1, v = -2 gives phi(u + v) = 0 but phi(u) + phi(v) = 1.
+    X = np.array([[1.0, -2.0]])
+    A = np.array([[1.0], [1.0]])
+    B = np.array([[1.0]])
+    assert mlp.forward(X, A, B, "relu")["O"][0, 0] == 0.0
+    assert mlp.forward_input_split(X, A, B, 2, "relu")[0, 0] == 1.0
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_input_channel_split_is_wrong(kind):
+    X, A, B = _rand((8, 16), 9), _rand((16, 32), 10, 0.5), _rand((32, 16), 11, 0.5)
+    good = mlp.forward(X, A, B, kind)["O"]
+    bad = mlp.forward_input_split(X, A, B, 2, kind)
+    assert np.abs(good - bad).max() > 0.05 * np.abs(good).max()
+
+
+# ---------------------------------------------------------------- collectives
+
+@pytest.mark.parametrize("t", [2, 4, 8])
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_allreduce_is_allgather_of_reducescatter(t, dtype):
+    parts = [np.random.default_rng(20 + i).standard_normal((8 * t, 24)).astype(dtype) for i in range(t)]
+    ar = collectives.all_reduce(parts)
+    ag_rs = collectives.all_gather(collectives.reduce_scatter(parts, axis=0), axis=0)
+    for a, b in zip(ar, ag_rs):
+        assert a.dtype == dtype and np.array_equal(a, b)
+    # and the sum really is the sum (in rank order)
+    assert np.allclose(ar[0], np.sum(np.stack(parts).astype(np.float64), axis=0), rtol=1e-5, atol=1e-5)
+
+
+# ---------------------------------------------------------------- LayerNorm
+
+def test_layernorm_statistics():
+    x = _rand((64, 256), 12, 3.0) + 5.0
+    eps = 1e-5
+    y = sp.layernorm(x, np.ones(256), np.zeros(256), eps)
+    var = x.var(axis=1)
+    assert np.abs(y.mean(axis=1)).max() < 1e-12
+    assert np.abs(y.var(axis=1) - var / (var + eps)).max() < 1e-12
+
+
+def test_layernorm_matches_torch():
+    x = _rand((32, 128), 13)
+    g, b = _rand(128, 14), _rand(128, 15)
+    ref = torch.nn.functional.layer_norm(torch.tensor(x), (128,), torch.tensor(g), torch.tensor(b), 1e-5).numpy()
+    assert np.abs(sp.layernorm(x, g, b, 1e-5) - ref).max() < 1e-12
+
+
+# ---------------------------------------------------------------- dropout hash
+
+def test_splitmix64_two_restatements_agree():
+    keys = [0, 1, 2, 0xFFFFFFFFFFFFFFFF, 0x9E3779B97F4A7C15, 1 << 63, 12345678901234567] + \
+           np.random.default_rng(16).integers(0, 2**63, size=4000, dtype=np.uint64).tolist()
+    vec = sp.splitmix64(np.array(keys, dtype=np.uint64))
+    assert [int(v) for v in vec] == [sp.splitmix64_scalar(int(k)) for k in keys]
+
+
+def test_splitmix64_zero_state_closed_form():
+    # The mixer maps 0 to 0, so the state that the golden-gamma step carries to 0
+    # must hash to 0: this fails if the increment is dropped or has the wrong value.
+    assert sp.splitmix64_scalar((1 << 64) - 0x9E3779B97F4A7C15) == 0
+    assert int(sp.splitmix64(np.array([(1 << 64) - 0x9E3779B97F4A7C15], dtype=np.uint64))[0]) == 0
+    assert sp.splitmix64_scalar(0) != 0
+
+
+def test_drop_threshold():
+    assert sp.drop_threshold(0.1) == 0x1999999999999A00
+    assert sp.drop_threshold(0.0) == 0
+    assert sp.drop_threshold(0.5) == 1 << 63
+    with pytest.raises(ValueError):
+        sp.drop_threshold(1.0)
+
+
+def test_dropout_kept_fraction():
+    N = 2 * 4096 * 4096
+    dropped = sp.drop_mask(np.arange(N, dtype=np.uint64), 0, 0.1)
+    sigma = math.sqrt(0.1 * 0.9 / N)
+    assert abs(dropped.mean() - 0.1) < 5 * sigma
+
+
+def test_dropout_p0_is_plain_residual():
+    x, y = _rand((4, 64), 17), _rand((4, 64), 18)
+    out = sp.dropout_residual(x, y, 0, 0.0, np.arange(256, dtype=np.uint64).reshape(4, 64))
+    assert np.array_equal(out, x + y)
+
+
+def test_pack_mask_bits():
+    m = np.random.default_rng(19).random(200) < 0.3
+    words = sp.pack_mask_bits(m)
+    unpacked = np.unpackbits(words.view(np.uint8), bitorder="little")[:200].astype(bool)
+    assert words.dtype == np.uint32 and words.size == 7 and np.array_equal(unpacked, m)
+
+
+# ---------------------------------------------------------------- SP block
+
+@pytest.mark.parametrize("t", [2, 4, 8])
+def test_sp_block_ranks_equal_unsharded(t):
+    b, s, h, m = 2, 16, 32, 64
+    x = _rand((b, s, h), 21)
+    A, B = _rand((h, m), 22, 0.2), _rand((m, h), 23, 0.2)
+    g, be = 1.0 + 0.1 * _rand(h, 24), 0.1 * _rand(h, 25)
+    ref = sp.sp_block(x, g, be, 1e-5, A, B, 0.1, 7, "tanh")
+    got = sp.sp_block_ranks(wl.to_shards(x, t), g, be, 1e-5, A, B, 0.1, 7, "tanh")
+    assert np.abs(wl.from_shards(got) - ref["out"]).max() < 1e-12
+    # the mask differs between shards (per-rank RNG domains) and is not all-or-nothing
+    d = ref["dropped"]
+    assert 0 < d.mean() < 0.3 and not np.array_equal(d[:, : s // t], d[:, s // t: 2 * s // t])
+
+
+# ---------------------------------------------------------------- input generator
+
+def test_bf16_rounding_matches_torch_and_ties_to_even():
+    v = np.array([1 + 2**-8, 1 + 3 * 2**-8, -1 - 2**-8, 3.14159, 1e-30, 65504.0], dtype=np.float32)
+    ours = wl.round_to_bf16(v)
+    ref = torch.tensor(v).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(ours, ref)
+    assert ours[0] == 1.0 and ours[1] == 1 + 2**-6
+    r = np.random.default_rng(26).standard_normal(100000).astype(np.float32)
+    assert np.array_equal(wl.round_to_bf16(r), torch.tensor(r).to(torch.bfloat16).to(torch.float32).numpy())
+
+
+def test_inputs_deterministic_and_chunk_invariant(monkeypatch):
+    a = wl.mlp_inputs(wl.SINGLE_BLOCK)
+    monkeypatch.setattr(wl, "_CHUNK_ELEMS", 1000)
+    b = wl.mlp_inputs(wl.SINGLE_BLOCK)
+    for k in "XABG":
+        assert np.array_equal(a[k], b[k])
+    assert abs(a["A"].std() - 0.02) < 1e-3 and abs(a["X"].std() - 1.0) < 1e-2
+
+
+def test_shard_layout_roundtrip():
+    x = _rand((2, 12, 5), 27)
+    xs = wl.to_shards(x, 4)
+    assert xs.shape == (4, 2, 3, 5)
+    assert np.array_equal(xs[2, 1, 0], x[1, 6])
+    assert np.array_equal(wl.from_shards(xs), x)
