@@ -1,0 +1,372 @@
+"""Benchmark of the tensor-parallel MLP forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one forward (FC1 + GeLU, FC2 with the shard sum in its K-loop) and one full
+backward (D, dB, dA, dX) of the tensor-parallel MLP block through the C ABI, on seeded
+synthetic bf16 inputs of the workload's shape. Throughput is algorithmic FLOPs
+(12 * n * d * m per step: six GEMMs of 2 * n * d * m) over device time.
+
+One process per GPU; with N > 1 (torchrun) every rank runs an independent replica
+(nothing in the path exchanges data), the timed region is bracketed by a barrier and a
+device synchronise, and the slowest rank's time is used. Rank 0 prints one JSON line.
+
+--impl reference times the float64 CPU oracle on the host cores instead (rank 0 only),
+each step a bounded sample of token rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tensor_transformer_mlp_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "TP-MLP fwd+bwd TFLOP/s (bf16) and fraction of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_LAUNCHES_PER_STEP = 6
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the
+# committed ncu summary named below; None until a capture of the current kernel exists.
+DOMINANT_KERNEL_TRAFFIC = None
+DOMINANT_KERNEL_PROFILE = None
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def aggregate(elapsed_s: float, units: float, world: int, device=None):
+    """Whole-job figures: (max elapsed over ranks, sum of units over ranks)."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.lines: list[str] = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.05)
+        self.skip = len(self.lines)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [ln.split(", ") for ln in self.lines[self.skip:] if ln.count(",") >= 6]
+        if not rows:
+            rows = [ln.split(", ") for ln in self.lines if ln.count(",") >= 6]
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[3:7]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+
+    props = torch.cuda.get_device_properties(device_index)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        s = str(uuid)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    return str(device_index)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+
+def oracle_rows_flops(cfg, rows: int) -> int:
+    return 12 * rows * cfg.d * cfg.m
+
+
+def time_oracle(cfg, inp, rows: int, row0: int = 0) -> float:
+    """Float64 oracle forward + backward on `rows` token rows (full weights); seconds."""
+    from oracle import mlp as omlp
+
+    sl = slice(row0, row0 + rows)
+    t0 = time.perf_counter()
+    omlp.forward(inp["X"][sl], inp["A"], inp["B"], cfg.gelu)
+    omlp.backward(inp["X"][sl], inp["A"], inp["B"], inp["G"][sl], cfg.gelu)
+    return time.perf_counter() - t0
+
+
+def calibrate_rows(cfg, inp, target_s: float, max_rows: int) -> int:
+    probe = 16
+    t = time_oracle(cfg, inp, probe)
+    rows = int(probe * target_s / max(t, 1e-3))
+    return max(probe, min(rows, max_rows, cfg.n))
+
+
+def cpu_baseline(cfg, inp, target_s=15.0):
+    rows = calibrate_rows(cfg, inp, target_s, 4096)
+    secs = time_oracle(cfg, inp, rows)
+    return {"value": oracle_rows_flops(cfg, rows) / secs / 1e12, "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"float64 numpy oracle, forward+backward of {rows} of {cfg.n} token rows with full "
+                      f"A [{cfg.d}x{cfg.m}] and B [{cfg.m}x{cfg.d}] (12*rows*d*m FLOP), {secs:.1f} s, "
+                      f"BLAS on all host threads"}
+
+
+def run_reference(args, cfg):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = wl.mlp_inputs(cfg)
+    # each step a bounded sample of token rows, so the whole run stays within a few minutes
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    rows = calibrate_rows(cfg, inp, per_step, 2048)
+    for i in range(args.warmup):
+        time_oracle(cfg, inp, rows, row0=(i * rows) % max(1, cfg.n - rows))
+    total = 0.0
+    for i in range(args.steps):
+        total += time_oracle(cfg, inp, rows, row0=(i * rows) % max(1, cfg.n - rows))
+    value = oracle_rows_flops(cfg, rows) * args.steps / total / 1e12
+    sample = (f"float64 numpy oracle, each step forward+backward of {rows} of {cfg.n} token rows with full "
+              f"weights (12*rows*d*m FLOP per step)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(cfg),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(cfg):
+    return {"workload": cfg.name, "n": cfg.n, "d": cfg.d, "m": cfg.m, "t": cfg.t, "gelu": cfg.gelu,
+            "inputs": f"seed {cfg.seed}, X~N(0,{cfg.x_std}), A,B~N(0,{cfg.w_std}), G~N(0,{cfg.g_std}) (std), "
+                      f"rounded to {cfg.dtype}",
+            "l2": "inputs larger than L2 (X, G 256+ MiB; A, B 512+ MiB per step), no flush",
+            "parallelism": "replicas (t shards on one GPU per replica)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, cfg):
+    import torch
+
+    import tensor_transformer_mlp_gb300 as tp
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    tp.load_library()
+
+    inp = wl.mlp_inputs(cfg)
+    bf = torch.bfloat16
+    X, A, B, G = (torch.from_numpy(inp[k]).to(dev).to(bf) for k in "XABG")
+    n, d, m, t = cfg.n, cfg.d, cfg.m, cfg.t
+    O = torch.empty((n, d), dtype=bf, device=dev)
+    Z = torch.empty((n, m), dtype=bf, device=dev)
+    Y = torch.empty((n, m), dtype=bf, device=dev)
+    dX = torch.empty((n, d), dtype=bf, device=dev)
+    dA = torch.empty((d, m), dtype=torch.float32, device=dev)
+    dB = torch.empty((m, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(tp.tpmlp_backward_workspace_size(n, m, bf), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        tp.tpmlp_forward(X, A, B, O, Z, Y, t, cfg.gelu, stream)
+        tp.tpmlp_backward(X, A, B, G, Z, Y, dX, dA, dB, t, cfg.gelu, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status(stream)
+
+    sampler = ClockSampler(gpu_id_for(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        tp.tpmlp_forward(X, A, B, O, Z, Y, t, cfg.gelu, stream)
+        ev[i][1].record(stream)
+        tp.tpmlp_backward(X, A, B, G, Z, Y, dX, dA, dB, t, cfg.gelu, ws, stream)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    tp.tpmlp_device_status(stream)
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    flops_step = cfg.flops_fwd_bwd
+    max_elapsed, total_flops = aggregate(elapsed, flops_step * args.steps, world, dev)
+
+    # End to end through the public API with host buffers: every step copies X, A, B, G
+    # from pinned host memory and reads O, dX, dA, dB back.
+    hX, hA, hB, hG = (x.cpu().pin_memory() for x in (X, A, B, G))
+    hO, hdX = torch.empty_like(O, device="cpu").pin_memory(), torch.empty_like(dX, device="cpu").pin_memory()
+    hdA, hdB = torch.empty_like(dA, device="cpu").pin_memory(), torch.empty_like(dB, device="cpu").pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hX, hA, hB, hG))
+    d2h = sum(x.numel() * x.element_size() for x in (hO, hdX, hdA, hdB))
+
+    def e2e_step():
+        X.copy_(hX, non_blocking=True)
+        A.copy_(hA, non_blocking=True)
+        B.copy_(hB, non_blocking=True)
+        G.copy_(hG, non_blocking=True)
+        step()
+        hO.copy_(O, non_blocking=True)
+        hdX.copy_(dX, non_blocking=True)
+        hdA.copy_(dA, non_blocking=True)
+        hdB.copy_(dB, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 2)
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_elapsed, e2e_flops = aggregate(e0.elapsed_time(e1) / 1e3, flops_step * e2e_steps, world, dev)
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    value = total_flops / max_elapsed / 1e12
+    # The dominant kernel is the tcgen05 GEMM: all six launches of a step are instances of it
+    # and nothing else runs, so its average launch is (fwd + bwd time) / 6 with 2*n*d*m FLOP.
+    gemm_ms_per_launch = (fwd_ms + bwd_ms) / (args.steps * GEMM_LAUNCHES_PER_STEP)
+    achieved = 2 * n * d * m / (gemm_ms_per_launch / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_elapsed / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(cfg),
+        "frac_of_peak": value / world / peak,
+        "fwd_tflops": 4 * n * d * m * args.steps / (fwd_ms / 1e3) / 1e12,
+        "bwd_tflops": 8 * n * d * m * args.steps / (bwd_ms / 1e3) / 1e12,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": DOMINANT_KERNEL_TRAFFIC,
+                     "kernel": "gemm_bf16_kernel (tcgen05; 6 launches per step, 2*n*d*m FLOP each)",
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                     "traffic_profile": DOMINANT_KERNEL_PROFILE},
+        "e2e": {"value": e2e_flops / e2e_elapsed / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": GEMM_LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.LARGE_MLP.name,
+                    choices=sorted(k for k, c in wl.MLP_CONFIGS.items() if c.dtype == "bf16"))
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    cfg = wl.MLP_CONFIGS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,169 @@
+/*
+ * tpmlp.h -- C ABI of libtpmlp.so: the Megatron tensor-parallel MLP block and its
+ * sequence-parallel form, with all t shards held on one GB300 (sm_103a).
+ *
+ * The operation ("024 | Megatron-LM: 按矩阵结构切分 Transformer", section 二, block
+ * "前向少通信，反向为何仍要一次归约？"): X is n x d, A is d x m split by columns into t
+ * equal shards A_i, B is m x d split by the matching rows into B_i, and
+ *     Z_i = X A_i,  Y_i = gelu(Z_i),  O = sum_i Y_i B_i;
+ * with G = dl/dO,
+ *     D_i = (G B_i^T) * gelu'(Z_i),  dA_i = X^T D_i,  dB_i = Y_i^T G,  dX = sum_i D_i A_i^T.
+ * Shard i is the column range [i*m/t, (i+1)*m/t) of A and the row range of B, so
+ * the forward all-reduce (f-bar) and the backward all-reduce (f) of the
+ * multi-GPU layout become the K-loop of one GEMM that runs over every shard in
+ * order 0..t-1 and accumulates in tensor memory.
+ *
+ * Conventions for every entry point:
+ *  - All matrices are dense and row-major, in the pages' math layout (A is d x m,
+ *    B is m x d), not torch.nn.Linear's [out, in].
+ *  - Device pointers unless stated otherwise. The caller owns every buffer,
+ *    workspace included; the library never allocates, frees or synchronises
+ *    (except tpmlp_device_status). Every call is asynchronous on `stream`
+ *    (a cudaStream_t; NULL means the legacy default stream).
+ *  - dtype TPMLP_BF16: X, A, B, G, O, Z, Y, dX are bfloat16; arithmetic is fp32
+ *    accumulation on the tcgen05 tensor cores. Row lengths d and m must be
+ *    multiples of 8 and pointers 16-byte aligned (tensor-memory-access rules).
+ *    dtype TPMLP_F32: the same tensors in fp32, computed with fp32 FMA (no TF32);
+ *    any shape, 4-byte alignment.
+ *  - dA and dB are always fp32 and are overwritten (Megatron keeps fp32 main_grad
+ *    buffers for weight gradients: "Megatron 训练" notes, mixed-precision section).
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns an error status and launches nothing. A launch failure
+ *    returns TPMLP_ERR_CUDA. tpmlp_last_error() gives a message for the calling
+ *    thread's last non-OK status. No entry point aborts or throws.
+ *  - Kernels that wait on in-kernel barriers give every wait a time limit; on
+ *    expiry they record TPMLP_ERR_TIMEOUT in a device status word, release what
+ *    they hold and return. tpmlp_device_status() reads that word.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TPMLP_OK = 0,
+  TPMLP_ERR_INVALID = 1,    /* null pointer, bad enum, negative size, p outside [0,1) */
+  TPMLP_ERR_SHAPE = 2,      /* m % t != 0, s % t != 0, t < 1 (t < 2 for the SP block), d or m not a multiple of 8 */
+  TPMLP_ERR_DTYPE = 3,      /* unsupported dtype */
+  TPMLP_ERR_ALIGN = 4,      /* pointer not 16-byte aligned (bf16) or 4-byte aligned (fp32) */
+  TPMLP_ERR_CUDA = 5,       /* a CUDA runtime/driver call or launch failed */
+  TPMLP_ERR_TIMEOUT = 6,    /* a kernel's bounded in-kernel wait expired (tpmlp_device_status) */
+  TPMLP_ERR_WORKSPACE = 7   /* workspace null or smaller than the *_workspace_size query */
+} tpmlp_status;
+
+typedef enum { TPMLP_GELU_ERF = 0, TPMLP_GELU_TANH = 1 } tpmlp_gelu;
+typedef enum { TPMLP_F32 = 0, TPMLP_BF16 = 1 } tpmlp_dtype;
+
+/* How the sequence-parallel block realises g-bar (reduce-scatter of the t row-GEMM
+ * partials back to the [b, s/t, h] shards). */
+typedef enum {
+  TPMLP_RS_FUSED = 0,   /* one row GEMM whose K-loop sums all shards; its epilogue stores rows in shard layout */
+  TPMLP_RS_SPLITK = 1   /* t row GEMMs write fp32 partials P_i; a reduce-scatter kernel sums them in shard order */
+} tpmlp_rs_mode;
+
+/*
+ * Forward: Z = X A, Y = gelu(Z), O = Y B = sum_i Y_i B_i
+ * ("024 | Megatron-LM", section 二; SenseParrots model-parallel note, section 2.1, eqs. (1)(2)).
+ *   X [n][d], A [d][m], B [m][d] (inputs, dtype dt)
+ *   O [n][d] (output, dt)
+ *   Z_save [n][m] (output, dt; may be NULL, then Z is not stored and backward cannot run)
+ *   Y_save [n][m] (output, dt; required: the row GEMM reads it)
+ *   n >= 0 tokens, d >= 1, m >= 1, 1 <= t with m % t == 0; gelu selects exact-erf or tanh GeLU.
+ *   With n == 0 nothing is launched and X, O, Z_save, Y_save may be NULL.
+ * gelu is evaluated in fp32 on the fp32 accumulator before Z and Y are rounded to dt.
+ */
+tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B,
+                           void* O, void* Z_save, void* Y_save,
+                           int64_t n, int64_t d, int64_t m, int t,
+                           tpmlp_gelu gelu, tpmlp_dtype dt, void* stream);
+
+/* Bytes of device workspace tpmlp_backward needs: D = (G B^T) * gelu'(Z), n x m in dt. */
+size_t tpmlp_backward_workspace_size(int64_t n, int64_t m, tpmlp_dtype dt);
+
+/*
+ * Backward ("024 | Megatron-LM", section 二, D_i / dA_i / dB_i equations and the dX reduction):
+ *   D = (G B^T) * gelu'(Z)  (in workspace, dt; gelu' evaluated in fp32 from the stored Z)
+ *   dB = Y^T G   [m][d] fp32     dA = X^T D   [d][m] fp32     dX = D A^T   [n][d] dt
+ *   X [n][d], A [d][m], B [m][d], G [n][d], Z_save and Y_save [n][m] as written by tpmlp_forward.
+ *   workspace: at least tpmlp_backward_workspace_size(n, m, dt) bytes, 256-byte aligned.
+ * n == 0 gives dA = dB = 0 (X, G, Z_save, Y_save, dX, workspace may then be NULL).
+ */
+tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* G,
+                            const void* Z_save, const void* Y_save,
+                            void* dX, float* dA, float* dB,
+                            int64_t n, int64_t d, int64_t m, int t,
+                            tpmlp_gelu gelu, tpmlp_dtype dt,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace tpmlp_sp_block needs (LN output, gathered tokens, Y, row-GEMM output or partials). */
+size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m, int t,
+                                     tpmlp_dtype dt, tpmlp_rs_mode rs);
+
+/*
+ * Sequence-parallel MLP block ("Megatron-SP 机制", section "通信插在层内什么位置？"):
+ *   out = x + dropout(RS(MLP(AG(LayerNorm(x)))))
+ *   x_shards, out_shards: [t][b][s/t][h] in dt (shard j holds sequence positions j*s/t .. (j+1)*s/t-1)
+ *   gamma, beta: [h] fp32; eps > 0. LayerNorm uses the biased variance and fp32 statistics.
+ *   A [h][m], B [m][h] (dt), gelu as for tpmlp_forward.
+ *   Dropout: p_drop in [0, 1) is the drop probability. Element k of the logical [b][s][h]
+ *   tensor (row-major flat index) is dropped iff splitmix64(seed ^ k) < floor(p_drop * 2^64)
+ *   (product in double); kept elements are scaled by 1/(1-p_drop); the residual is x.
+ *   mask_bits: NULL, or [ceil(b*s*h/32)] uint32 words; bit i of word w is 1 iff element
+ *   32*w+i (global flat index) was dropped. Needs h % 32 == 0.
+ *   Requires t >= 2 (sequence parallelism needs a tensor-parallel group:
+ *   "Megatron-SP 机制", section "工程约束与实测收益是什么？"), s % t == 0, m % t == 0.
+ */
+tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const float* beta, float eps,
+                            const void* A, const void* B, float p_drop, uint64_t seed,
+                            void* out_shards, uint32_t* mask_bits,
+                            int64_t b, int64_t s, int64_t h, int64_t m, int t,
+                            tpmlp_gelu gelu, tpmlp_dtype dt, tpmlp_rs_mode rs,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The sequence-parallel block's memory-bound steps as separate calls, same layouts as above.
+ *
+ * LayerNorm of `rows` rows of width h ("Megatron 训练" notes, section "LayerNorm";
+ * torch.nn.LayerNorm semantics): y = (x - mean) / sqrt(var + eps) * gamma + beta.
+ */
+tpmlp_status tpmlp_sp_layernorm(const void* x, const float* gamma, const float* beta, float eps,
+                                void* y, int64_t rows, int64_t h, tpmlp_dtype dt, void* stream);
+
+/* g forward, all-gather ("Megatron-SP 机制", f/g operator table): [t][b][s/t][h] -> [b][s][h]. */
+tpmlp_status tpmlp_sp_gather(const void* x_shards, void* x_full,
+                             int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype dt, void* stream);
+
+/* g-bar forward, reduce-scatter ("Megatron-SP 机制", f/g operator table):
+ * partials [t][b*s][h] fp32 in token order -> out_shards [t][b][s/t][h] in dt,
+ * out = sum_i partials[i], added in order i = 0..t-1 in fp32. */
+tpmlp_status tpmlp_sp_reduce_scatter(const float* partials, void* out_shards,
+                                     int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype dt, void* stream);
+
+/* Dropout + residual on shards ("Megatron-SP 机制", placement diagram, last step):
+ * out = x + keep * y / (1 - p_drop), mask definition and mask_bits as for tpmlp_sp_block.
+ * x_shards, y_shards, out_shards: [t][b][s/t][h] in dt. */
+tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shards, void* out_shards,
+                                       uint32_t* mask_bits, float p_drop, uint64_t seed,
+                                       int64_t b, int64_t s, int64_t h, int t,
+                                       tpmlp_dtype dt, void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). Never NULL. */
+const char* tpmlp_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads the current device's status word, which kernels set when a
+ * bounded in-kernel wait expires. Returns TPMLP_OK or TPMLP_ERR_TIMEOUT (or TPMLP_ERR_CUDA if
+ * the synchronisation itself fails). clear != 0 resets the word.
+ */
+tpmlp_status tpmlp_device_status(void* stream, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

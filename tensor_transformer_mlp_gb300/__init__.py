@@ -1,0 +1,25 @@
+"""GB300-native tensor-parallel MLP block (Megatron TP/SP) behind the C ABI of libtpmlp.so.
+
+The functions named tpmlp_* mirror the C entry points of include/tpmlp.h one to one;
+``forward``, ``backward`` and ``sp_block`` allocate outputs with torch and call them.
+The CUDA library is loaded on first use; there is no CPU fallback.
+"""
+from . import workloads  # noqa: F401
+from ._binding import (  # noqa: F401
+    SIGNATURES,
+    TpmlpError,
+    backward,
+    forward,
+    load_library,
+    sp_block,
+    tpmlp_backward,
+    tpmlp_backward_workspace_size,
+    tpmlp_device_status,
+    tpmlp_forward,
+    tpmlp_sp_block,
+    tpmlp_sp_block_workspace_size,
+    tpmlp_sp_dropout_residual,
+    tpmlp_sp_gather,
+    tpmlp_sp_layernorm,
+    tpmlp_sp_reduce_scatter,
+)

@@ -1,0 +1,216 @@
+"""Thin ctypes binding over libtpmlp.so (argument marshalling only).
+
+Each function takes torch CUDA tensors, checks that their shapes and dtypes agree
+with one another, and passes raw device pointers, sizes and the current CUDA
+stream to the C entry point of the same name. Every step of the computation runs
+in the library's kernels; if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+GELU = {"erf": 0, "tanh": 1}
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+RS_MODE = {"fused": 0, "splitk": 1}
+STATUS = {0: "TPMLP_OK", 1: "TPMLP_ERR_INVALID", 2: "TPMLP_ERR_SHAPE", 3: "TPMLP_ERR_DTYPE", 4: "TPMLP_ERR_ALIGN",
+          5: "TPMLP_ERR_CUDA", 6: "TPMLP_ERR_TIMEOUT", 7: "TPMLP_ERR_WORKSPACE"}
+
+# Every entry point declared in include/tpmlp.h, with its ctypes signature.
+_P, _I64, _I, _F, _U64, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
+SIGNATURES = {
+    "tpmlp_forward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
+    "tpmlp_backward_workspace_size": (_SZ, [_I64, _I64, _I]),
+    "tpmlp_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
+    "tpmlp_sp_block_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I, _I, _I]),
+    "tpmlp_sp_block": (_I, [_P, _P, _P, _F, _P, _P, _F, _U64, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _P, _SZ,
+                            _P]),
+    "tpmlp_sp_layernorm": (_I, [_P, _P, _P, _F, _P, _I64, _I64, _I, _P]),
+    "tpmlp_sp_gather": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
+    "tpmlp_sp_reduce_scatter": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
+    "tpmlp_sp_dropout_residual": (_I, [_P, _P, _P, _P, _F, _U64, _I64, _I64, _I64, _I, _I, _P]),
+    "tpmlp_last_error": (ctypes.c_char_p, []),
+    "tpmlp_device_status": (_I, [_P, _I]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class TpmlpError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if it is missing or stale) libtpmlp.so and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing and _build.is_stale():
+                _build.build()
+            if not os.path.exists(_build.LIB_PATH):
+                raise RuntimeError(f"libtpmlp.so is missing at {_build.LIB_PATH}; run the build first")
+            lib = ctypes.CDLL(_build.LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = load_library().tpmlp_last_error().decode(errors="replace")
+        raise TpmlpError(status, msg)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _cuda(*ts: torch.Tensor | None) -> None:
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype not in DTYPE:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return DTYPE[t.dtype]
+
+
+# ----------------------------------------------------------------------- C-ABI mirrors
+
+def tpmlp_forward(X, A, B, O, Z_save, Y_save, t: int, gelu: str = "tanh", stream=None) -> None:
+    n, d = X.shape
+    m = A.shape[1]
+    assert A.shape == (d, m) and B.shape == (m, d) and O.shape == (n, d) and Y_save.shape == (n, m)
+    assert Z_save is None or Z_save.shape == (n, m)
+    _cuda(X, A, B, O, Z_save, Y_save)
+    _check(load_library().tpmlp_forward(_ptr(X), _ptr(A), _ptr(B), _ptr(O), _ptr(Z_save), _ptr(Y_save), n, d, m, t,
+                                        GELU[gelu], _dt(X), _stream(stream)))
+
+
+def tpmlp_backward_workspace_size(n: int, m: int, dtype: torch.dtype) -> int:
+    return load_library().tpmlp_backward_workspace_size(n, m, DTYPE[dtype])
+
+
+def tpmlp_backward(X, A, B, G, Z_save, Y_save, dX, dA, dB, t: int, gelu: str = "tanh", workspace=None,
+                   stream=None) -> None:
+    n, d = X.shape
+    m = A.shape[1]
+    assert G.shape == (n, d) and Z_save.shape == (n, m) and Y_save.shape == (n, m) and dX.shape == (n, d)
+    assert dA.shape == (d, m) and dB.shape == (m, d) and dA.dtype == torch.float32 and dB.dtype == torch.float32
+    _cuda(X, A, B, G, Z_save, Y_save, dX, dA, dB, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().tpmlp_backward(_ptr(X), _ptr(A), _ptr(B), _ptr(G), _ptr(Z_save), _ptr(Y_save), _ptr(dX),
+                                         _ptr(dA), _ptr(dB), n, d, m, t, GELU[gelu], _dt(X), _ptr(workspace),
+                                         ws_bytes, _stream(stream)))
+
+
+def tpmlp_sp_block_workspace_size(b, s, h, m, t, dtype: torch.dtype, rs: str = "fused") -> int:
+    return load_library().tpmlp_sp_block_workspace_size(b, s, h, m, t, DTYPE[dtype], RS_MODE[rs])
+
+
+def tpmlp_sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, out_shards, mask_bits, t: int, gelu="tanh",
+                   rs="fused", workspace=None, stream=None) -> None:
+    tt, b, sl, h = x_shards.shape
+    assert tt == t and out_shards.shape == x_shards.shape
+    m = A.shape[1]
+    assert A.shape == (h, m) and B.shape == (m, h) and gamma.shape == (h,) and beta.shape == (h,)
+    assert gamma.dtype == torch.float32 and beta.dtype == torch.float32
+    if mask_bits is not None:
+        assert mask_bits.dtype in (torch.int32, torch.uint32) and mask_bits.numel() >= (b * sl * t * h + 31) // 32
+    _cuda(x_shards, gamma, beta, A, B, out_shards, mask_bits, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().tpmlp_sp_block(_ptr(x_shards), _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), p_drop,
+                                         seed, _ptr(out_shards), _ptr(mask_bits), b, sl * t, h, m, t, GELU[gelu],
+                                         _dt(x_shards), RS_MODE[rs], _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def tpmlp_sp_layernorm(x, gamma, beta, eps, y, stream=None) -> None:
+    h = x.shape[-1]
+    rows = x.numel() // h
+    assert y.shape == x.shape and gamma.shape == (h,) and beta.shape == (h,)
+    _cuda(x, gamma, beta, y)
+    _check(load_library().tpmlp_sp_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), eps, _ptr(y), rows, h, _dt(x),
+                                             _stream(stream)))
+
+
+def tpmlp_sp_gather(x_shards, x_full, stream=None) -> None:
+    t, b, sl, h = x_shards.shape
+    assert x_full.shape == (b, sl * t, h) and x_full.dtype == x_shards.dtype
+    _cuda(x_shards, x_full)
+    _check(load_library().tpmlp_sp_gather(_ptr(x_shards), _ptr(x_full), b, sl * t, h, t, _dt(x_shards),
+                                          _stream(stream)))
+
+
+def tpmlp_sp_reduce_scatter(partials, out_shards, stream=None) -> None:
+    t, b, sl, h = out_shards.shape
+    assert partials.shape == (t, b * sl * t, h) and partials.dtype == torch.float32
+    _cuda(partials, out_shards)
+    _check(load_library().tpmlp_sp_reduce_scatter(_ptr(partials), _ptr(out_shards), b, sl * t, h, t,
+                                                  _dt(out_shards), _stream(stream)))
+
+
+def tpmlp_sp_dropout_residual(x_shards, y_shards, out_shards, mask_bits, p_drop, seed, stream=None) -> None:
+    t, b, sl, h = x_shards.shape
+    assert y_shards.shape == x_shards.shape and out_shards.shape == x_shards.shape
+    _cuda(x_shards, y_shards, out_shards, mask_bits)
+    _check(load_library().tpmlp_sp_dropout_residual(_ptr(x_shards), _ptr(y_shards), _ptr(out_shards),
+                                                    _ptr(mask_bits), p_drop, seed, b, sl * t, h, t, _dt(x_shards),
+                                                    _stream(stream)))
+
+
+def tpmlp_device_status(stream=None, clear: bool = True) -> None:
+    _check(load_library().tpmlp_device_status(_stream(stream), 1 if clear else 0))
+
+
+# ----------------------------------------------------------------------- conveniences
+
+def forward(X, A, B, t: int, gelu: str = "tanh", save_z: bool = True, stream=None):
+    """Allocate O, Z, Y with torch and run tpmlp_forward. Returns (O, Z, Y)."""
+    n, m = X.shape[0], A.shape[1]
+    O = torch.empty_like(X)
+    Z = torch.empty((n, m), dtype=X.dtype, device=X.device) if save_z else None
+    Y = torch.empty((n, m), dtype=X.dtype, device=X.device)
+    tpmlp_forward(X, A, B, O, Z, Y, t, gelu, stream)
+    return O, Z, Y
+
+
+def backward(X, A, B, G, Z, Y, t: int, gelu: str = "tanh", stream=None):
+    """Allocate dX, dA, dB and the workspace with torch and run tpmlp_backward. Returns (dX, dA, dB)."""
+    n, d = X.shape
+    m = A.shape[1]
+    dX = torch.empty_like(X)
+    dA = torch.empty((d, m), dtype=torch.float32, device=X.device)
+    dB = torch.empty((m, d), dtype=torch.float32, device=X.device)
+    ws = torch.empty(max(1, tpmlp_backward_workspace_size(n, m, X.dtype)), dtype=torch.uint8, device=X.device)
+    tpmlp_backward(X, A, B, G, Z, Y, dX, dA, dB, t, gelu, ws, stream)
+    return dX, dA, dB
+
+
+def sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, t: int, gelu="tanh", rs="fused", with_mask=True,
+             stream=None):
+    """Allocate outputs and workspace and run tpmlp_sp_block. Returns (out_shards, mask_bits or None)."""
+    tt, b, sl, h = x_shards.shape
+    out = torch.empty_like(x_shards)
+    mask = torch.empty(((b * sl * t * h + 31) // 32,), dtype=torch.int32, device=x_shards.device) if with_mask else None
+    ws = torch.empty(max(1, tpmlp_sp_block_workspace_size(b, sl * t, h, A.shape[1], t, x_shards.dtype, rs)),
+                     dtype=torch.uint8, device=x_shards.device)
+    tpmlp_sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, out, mask, t, gelu, rs, ws, stream)
+    return out, mask

@@ -1,0 +1,363 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05) for every contraction of the
+// tensor-parallel MLP block ("024 | Megatron-LM: 按矩阵结构切分 Transformer", section 二):
+//   FC1      Z = X A            epilogue: Z and Y = gelu(Z)            (column-parallel GEMM)
+//   FC2      O = Y B            K-loop over all t shards = the f-bar sum  (row-parallel GEMM)
+//   dgrad-1  D = (G B^T) * gelu'(Z)
+//   wgrad    dB = Y^T G, dA = X^T D                 (fp32 out, K = tokens)
+//   dgrad-2  dX = D A^T         K-loop over all t shards = the f sum
+//
+// Design (one CTA per SM, persistent):
+//   warp 0      one thread issues TMA tile loads into a 4-stage shared-memory ring
+//   warp 1      one thread issues tcgen05.mma (M=128, N=256, K=16) into a tensor-memory
+//               accumulator; two accumulators (2 x 256 columns) let the epilogue of one
+//               tile overlap the main loop of the next
+//   warps 2..5  epilogue: tcgen05.ld the fp32 tile, apply the fused op, store
+// Operands are staged with 128-byte swizzle; K-major and MN-major layouts are both
+// read in place through the descriptors' major-ness bits, so no operand is transposed
+// in memory. Every mbarrier wait is bounded (kWaitLimitNs); on expiry the kernel
+// records a timeout, drains its own copies and MMAs, frees tensor memory and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+
+namespace tpmlp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // one 128-byte swizzle span of bf16
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box of an MN-major operand
+constexpr int NUM_ACC = 2;
+constexpr int TMEM_COLS = NUM_ACC * BN;  // 512: all of tensor memory
+constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_THREADS = 128;
+constexpr int GROUP_M = 8;
+constexpr int BARRIER_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BARRIER_BYTES + 1024;  // + alignment slack
+
+static_assert(A_STAGE_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+struct TileSched {
+  int num_mb, num_nb, num_tiles;
+  __device__ __forceinline__ void coords(int tile, int& mb, int& nb) const {
+    const int group_size = GROUP_M * num_nb;
+    const int group = tile / group_size;
+    const int first_mb = group * GROUP_M;
+    const int gsz = min(num_mb - first_mb, GROUP_M);
+    const int in_group = tile - group * group_size;
+    mb = first_mb + in_group % gsz;
+    nb = in_group / gsz;
+  }
+};
+
+__device__ __forceinline__ int64_t remap_row(const RowRemap& rm, int64_t r) {
+  if (!rm.enabled) return r;
+  const int64_t bi = r / rm.s;
+  const int64_t si = r - bi * rm.s;
+  const int64_t j = si / rm.s_per_shard;
+  const int64_t l = si - j * rm.s_per_shard;
+  return (j * rm.b + bi) * rm.s_per_shard + l;
+}
+
+// Applies the epilogue to 32 consecutive accumulator columns of one row.
+template <int EPI>
+__device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row, int col0, int N,
+                                               const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int col = col0 + g * 8;
+    if (col >= N) break;
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
+    if constexpr (EPI == kEpiStoreF32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + row * ep.ldo + col);
+      dst[0] = make_float4(a[0], a[1], a[2], a[3]);
+      dst[1] = make_float4(a[4], a[5], a[6], a[7]);
+    } else if constexpr (EPI == kEpiStore) {
+      const int64_t prow = remap_row(ep.remap, row);
+      uint4 pk = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                            pack_bf16x2(a[6], a[7]));
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + prow * ep.ldo + col) = pk;
+    } else if constexpr (EPI == kEpiGelu) {
+      const int64_t off = row * ep.ldo + col;
+      if (ep.out) {
+        uint4 z = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                             pack_bf16x2(a[6], a[7]));
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + off) = z;
+      }
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = gelu_f<false>(a[i], ep.gelu);
+      uint4 yy = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                            pack_bf16x2(y[6], y[7]));
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out2) + off) = yy;
+    } else if constexpr (EPI == kEpiDGelu) {
+      const int64_t off = row * ep.ldo + col;
+      const uint4 z = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.aux) + off);
+      const uint32_t zw[4] = {z.x, z.y, z.z, z.w};
+      float d[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 zf = unpack_bf16x2(zw[i]);
+        d[2 * i] = a[2 * i] * gelu_grad_f<false>(zf.x, ep.gelu);
+        d[2 * i + 1] = a[2 * i + 1] * gelu_grad_f<false>(zf.y, ep.gelu);
+      }
+      uint4 pk = make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]), pack_bf16x2(d[4], d[5]),
+                            pack_bf16x2(d[6], d[7]));
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + off) = pk;
+    }
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
+                     int N, int K, EpiParams ep, unsigned int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* tfull_bar = empty_bar + STAGES;
+  uint64_t* tempty_bar = tfull_bar + NUM_ACC;
+  uint64_t* drain_bar = tempty_bar + NUM_ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  TileSched sched;
+  sched.num_mb = (M + BM - 1) / BM;
+  sched.num_nb = (N + BN - 1) / BN;
+  sched.num_tiles = sched.num_mb * sched.num_nb;
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (warp == 0 && lane == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+#pragma unroll
+    for (int a = 0; a < NUM_ACC; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], NUM_EPI_THREADS);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int kiter = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < sched.num_tiles && ok; tile += gridDim.x) {
+        int mb, nb;
+        sched.coords(tile, mb, nb);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          const int s = kiter % STAGES;
+          const uint32_t parity = ((kiter / STAGES) & 1) ^ 1;
+          if (!mbar_wait(&empty_bar[s], parity, status, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
+          uint8_t* sa = smem + s * STAGE_BYTES;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          if constexpr (!A_MN) {
+            tma_load_2d(sa, &tmap_a, &full_bar[s], kb * BK, mb * BM);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d(sa + j * MN_BOX_BYTES, &tmap_a, &full_bar[s], mb * BM + j * 64, kb * BK);
+          }
+          if constexpr (!B_MN) {
+            tma_load_2d(sb, &tmap_b, &full_bar[s], kb * BK, nb * BN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sb + j * MN_BOX_BYTES, &tmap_b, &full_bar[s], nb * BN + j * 64, kb * BK);
+          }
+          ++kiter;
+        }
+      }
+      if (!ok) {
+        // Wait (bounded) for the copies still in flight before shared memory goes away.
+        for (int k = max(0, kiter - STAGES); k < kiter; ++k)
+          mbar_wait(&full_bar[k % STAGES], (k / STAGES) & 1, status, 2);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      int kiter = 0, it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < sched.num_tiles; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        if (!mbar_wait(&tempty_bar[acc], (use & 1) ^ 1, status, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          const int s = kiter % STAGES;
+          if (!mbar_wait(&full_bar[s], (kiter / STAGES) & 1, status, 4)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t b_base = a_base + A_STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // K-major: a K16 step is 32 bytes along the 128-byte row; 8-row groups 1024 B apart.
+            // MN-major: a K16 step is 16 rows of 128 bytes; 64-wide MN blocks one box apart.
+            const uint64_t adesc = A_MN ? smem_desc_sw128(a_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                        : smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? smem_desc_sw128(b_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                        : smem_desc_sw128(b_base + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
+          ++kiter;
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);  // accumulator ready for the epilogue
+      }
+      // Every MMA this thread issued must finish before tensor memory is freed.
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, status, 5);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
+    int it = 0;
+    for (int tile = blockIdx.x; tile < sched.num_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      const bool ok = mbar_wait(&tfull_bar[acc], use & 1, status, 6);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      int mb, nb;
+      sched.coords(tile, mb, nb);
+      const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = nb * BN + c * 32;
+        if (col0 >= N) break;  // uniform across the warp
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
+        tmem_ld_wait();
+        if (row < M) epilogue_row32<EPI>(ep, row, col0, N, v);
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  *fn = g_encode;
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix with row stride ld elements.
+cudaError_t make_tmap(CUtensorMap* map, const Operand& op, uint32_t box_inner, uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+  cudaError_t e = get_encode(&encode);
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(op.cols), static_cast<cuuint64_t>(op.rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(op.ld) * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.ptr), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
+                   cudaStream_t stream, const DeviceCtx& ctx) {
+  auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, M, N, K, ep, ctx.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
+                         const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaErrorInvalidValue;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return cudaErrorInvalidValue;
+  // The stored shapes must match the contraction.
+  if (a.mn_major ? (a.rows != K || a.cols != M) : (a.rows != M || a.cols != K)) return cudaErrorInvalidValue;
+  if (b.mn_major ? (b.rows != K || b.cols != N) : (b.rows != N || b.cols != K)) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  cudaError_t e = make_tmap(&ta, a, 64, a.mn_major ? BK : BM);
+  if (e != cudaSuccess) return e;
+  e = make_tmap(&tb, b, 64, b.mn_major ? BK : BN);
+  if (e != cudaSuccess) return e;
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (!a.mn_major && b.mn_major) {
+    if (epi == kEpiGelu) return launch<false, true, kEpiGelu>(ta, tb, m, n, k, ep, stream, ctx);
+    if (epi == kEpiStore) return launch<false, true, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
+    if (epi == kEpiStoreF32) return launch<false, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
+  } else if (!a.mn_major && !b.mn_major) {
+    if (epi == kEpiDGelu) return launch<false, false, kEpiDGelu>(ta, tb, m, n, k, ep, stream, ctx);
+    if (epi == kEpiStore) return launch<false, false, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
+  } else if (a.mn_major && b.mn_major) {
+    if (epi == kEpiStoreF32) return launch<true, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace tpmlp

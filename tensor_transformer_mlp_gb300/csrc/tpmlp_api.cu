@@ -1,0 +1,413 @@
+// C ABI of libtpmlp.so (declared in include/tpmlp.h): argument validation on the host,
+// then dispatch to the tensor-core (bf16) or CUDA-core (fp32) kernels. Nothing here
+// allocates, frees or synchronises, except tpmlp_device_status.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tpmlp.h"
+#include "tpmlp_internal.h"
+
+namespace tpmlp {
+
+// Device status word, one per device that loads the library (bounded-wait timeouts).
+__device__ unsigned int g_device_status;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+tpmlp_status fail(tpmlp_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+tpmlp_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(TPMLP_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_ctx_mutex;
+DeviceCtx g_ctx[kMaxDevices];
+bool g_ctx_ready[kMaxDevices] = {};
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t elt_size(tpmlp_dtype dt) { return dt == TPMLP_BF16 ? 2 : 4; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+cudaError_t get_device_ctx(DeviceCtx* ctx) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_ctx_mutex);
+  if (!g_ctx_ready[dev]) {
+    DeviceCtx c;
+    c.device = dev;
+    e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return e;
+    c.status = static_cast<unsigned int*>(p);
+    g_ctx[dev] = c;
+    g_ctx_ready[dev] = true;
+  }
+  *ctx = g_ctx[dev];
+  return cudaSuccess;
+}
+
+}  // namespace tpmlp
+
+using namespace tpmlp;
+
+namespace {
+
+tpmlp_status check_common(tpmlp_gelu gelu, tpmlp_dtype dt) {
+  if (gelu != TPMLP_GELU_ERF && gelu != TPMLP_GELU_TANH) return fail(TPMLP_ERR_INVALID, "unknown gelu variant %d", (int)gelu);
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  return TPMLP_OK;
+}
+
+tpmlp_status check_ptrs(tpmlp_dtype dt, std::initializer_list<std::pair<const void*, const char*>> ptrs) {
+  const size_t a = dt == TPMLP_BF16 ? 16 : 4;
+  for (auto& p : ptrs) {
+    if (!p.first) return fail(TPMLP_ERR_INVALID, "%s is NULL", p.second);
+    if (!aligned(p.first, a)) return fail(TPMLP_ERR_ALIGN, "%s is not %zu-byte aligned", p.second, a);
+  }
+  return TPMLP_OK;
+}
+
+tpmlp_status check_mlp_shape(int64_t n, int64_t d, int64_t m, int t, tpmlp_dtype dt) {
+  if (n < 0 || d < 1 || m < 1) return fail(TPMLP_ERR_SHAPE, "need n >= 0, d >= 1, m >= 1 (n=%lld d=%lld m=%lld)",
+                                           (long long)n, (long long)d, (long long)m);
+  if (t < 1) return fail(TPMLP_ERR_SHAPE, "t must be >= 1 (t=%d)", t);
+  if (m % t != 0) return fail(TPMLP_ERR_SHAPE, "m=%lld is not divisible by t=%d (shards are an equal split)", (long long)m, t);
+  if (dt == TPMLP_BF16 && (d % 8 != 0 || m % 8 != 0))
+    return fail(TPMLP_ERR_SHAPE, "bf16 path needs d and m to be multiples of 8 (d=%lld m=%lld)", (long long)d, (long long)m);
+  if (n > INT32_MAX || d > INT32_MAX || m > INT32_MAX) return fail(TPMLP_ERR_SHAPE, "dimension exceeds 2^31-1");
+  return TPMLP_OK;
+}
+
+#define TPMLP_TRY(expr)                 \
+  do {                                  \
+    tpmlp_status _st = (expr);          \
+    if (_st != TPMLP_OK) return _st;    \
+  } while (0)
+
+#define TPMLP_CUDA(expr, what)                      \
+  do {                                              \
+    cudaError_t _e = (expr);                        \
+    if (_e != cudaSuccess) return cuda_fail(_e, what); \
+  } while (0)
+
+// C = Aop * Bop with the path chosen by dtype.
+cudaError_t gemm(tpmlp_dtype dt, int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
+                 const EpiParams& ep, cudaStream_t s, const DeviceCtx& ctx) {
+  if (dt == TPMLP_BF16) return gemm_bf16_tc(M, N, K, a, b, epi, ep, s, ctx);
+  return gemm_f32_simt(M, N, K, a, b, epi, ep, s);
+}
+
+EpiParams epi(void* out, void* out2, const void* aux, int64_t ldo, tpmlp_gelu g) {
+  EpiParams e;
+  e.out = out;
+  e.out2 = out2;
+  e.aux = aux;
+  e.ldo = ldo;
+  e.gelu = g == TPMLP_GELU_ERF ? kGeluErf : kGeluTanh;
+  e.remap.enabled = 0;
+  e.remap.b = e.remap.s = e.remap.s_per_shard = 1;
+  return e;
+}
+
+// Forward GEMMs shared by tpmlp_forward and the sequence-parallel block.
+tpmlp_status run_forward(const void* X, const void* A, const void* B, void* O, void* Z, void* Y, int64_t n, int64_t d,
+                         int64_t m, tpmlp_gelu g, tpmlp_dtype dt, const RowRemap* remap, cudaStream_t s,
+                         const DeviceCtx& ctx) {
+  // FC1 (column-parallel, all shards at once): Z = X A, Y = gelu(Z).
+  TPMLP_CUDA(gemm(dt, n, m, d, Operand{X, n, d, d, false}, Operand{A, d, m, m, true}, kEpiGelu,
+                  epi(Z, Y, nullptr, m, g), s, ctx),
+             "FC1 GEMM");
+  // FC2 (row-parallel): O = Y B; the K-loop runs over every shard, which is the f-bar sum.
+  EpiParams e2 = epi(O, nullptr, nullptr, d, g);
+  if (remap) e2.remap = *remap;
+  TPMLP_CUDA(gemm(dt, n, d, m, Operand{Y, n, m, m, false}, Operand{B, m, d, d, true}, kEpiStore, e2, s, ctx),
+             "FC2 GEMM");
+  return TPMLP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tpmlp_last_error(void) { return g_last_error; }
+
+tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, void* O, void* Z_save, void* Y_save, int64_t n,
+                           int64_t d, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* stream) {
+  TPMLP_TRY(check_common(gelu, dt));
+  TPMLP_TRY(check_mlp_shape(n, d, m, t, dt));
+  TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
+  if (n == 0) return TPMLP_OK;  // token-sized buffers may be NULL when there are no tokens
+  TPMLP_TRY(check_ptrs(dt, {{X, "X"}, {O, "O"}, {Y_save, "Y_save"}}));
+  if (Z_save && !aligned(Z_save, dt == TPMLP_BF16 ? 16 : 4)) return fail(TPMLP_ERR_ALIGN, "Z_save is misaligned");
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  return run_forward(X, A, B, O, Z_save, Y_save, n, d, m, gelu, dt, nullptr, static_cast<cudaStream_t>(stream), ctx);
+}
+
+size_t tpmlp_backward_workspace_size(int64_t n, int64_t m, tpmlp_dtype dt) {
+  if (n <= 0 || m <= 0) return 0;
+  return round_up(static_cast<size_t>(n) * static_cast<size_t>(m) * elt_size(dt), 256);
+}
+
+tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
+                            const void* Y_save, void* dX, float* dA, float* dB, int64_t n, int64_t d, int64_t m, int t,
+                            tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
+  TPMLP_TRY(check_common(gelu, dt));
+  TPMLP_TRY(check_mlp_shape(n, d, m, t, dt));
+  TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
+  TPMLP_TRY(check_ptrs(dt, {{dA, "dA"}, {dB, "dB"}}));
+  if (n > 0)  // token-sized buffers may be NULL when there are no tokens
+    TPMLP_TRY(check_ptrs(dt, {{X, "X"}, {G, "G"}, {Z_save, "Z_save"}, {Y_save, "Y_save"}, {dX, "dX"}}));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n > 0) {
+    const size_t need = tpmlp_backward_workspace_size(n, m, dt);
+    if (!workspace || ws_bytes < need)
+      return fail(TPMLP_ERR_WORKSPACE, "backward needs %zu workspace bytes, got %zu", need, workspace ? ws_bytes : 0);
+    if (!aligned(workspace, 256)) return fail(TPMLP_ERR_ALIGN, "workspace is not 256-byte aligned");
+  }
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  if (n == 0) {
+    TPMLP_CUDA(cudaMemsetAsync(dA, 0, sizeof(float) * d * m, s), "zero dA");
+    TPMLP_CUDA(cudaMemsetAsync(dB, 0, sizeof(float) * m * d, s), "zero dB");
+    return TPMLP_OK;
+  }
+  void* D = workspace;
+  // dgrad-1 with the GeLU' mask: D = (G B^T) * gelu'(Z)   [B read as an [N][K] K-major operand]
+  TPMLP_CUDA(gemm(dt, n, m, d, Operand{G, n, d, d, false}, Operand{B, m, d, d, false}, kEpiDGelu,
+                  epi(D, nullptr, Z_save, m, gelu), s, ctx),
+             "dgrad-1 GEMM");
+  // wgrad-2: dB = Y^T G  (both operands MN-major, K = tokens)
+  TPMLP_CUDA(gemm(dt, m, d, n, Operand{Y_save, n, m, m, true}, Operand{G, n, d, d, true}, kEpiStoreF32,
+                  epi(dB, nullptr, nullptr, d, gelu), s, ctx),
+             "wgrad-2 GEMM");
+  // wgrad-1: dA = X^T D
+  TPMLP_CUDA(gemm(dt, d, m, n, Operand{X, n, d, d, true}, Operand{D, n, m, m, true}, kEpiStoreF32,
+                  epi(dA, nullptr, nullptr, m, gelu), s, ctx),
+             "wgrad-1 GEMM");
+  // dgrad-2: dX = D A^T; the K-loop over every shard is the f (backward all-reduce) sum.
+  TPMLP_CUDA(gemm(dt, n, d, m, Operand{D, n, m, m, false}, Operand{A, d, m, m, false}, kEpiStore,
+                  epi(dX, nullptr, nullptr, d, gelu), s, ctx),
+             "dgrad-2 GEMM");
+  return TPMLP_OK;
+}
+
+namespace {
+
+struct SPLayout {
+  size_t xn, xg, y, o, partials, total;
+};
+
+SPLayout sp_layout(int64_t b, int64_t s, int64_t h, int64_t m, int t, tpmlp_dtype dt, tpmlp_rs_mode rs) {
+  const size_t e = elt_size(dt);
+  const size_t tok = static_cast<size_t>(b) * static_cast<size_t>(s);
+  SPLayout L;
+  size_t off = 0;
+  L.xn = off; off += round_up(tok * h * e, 256);
+  L.xg = off; off += round_up(tok * h * e, 256);
+  L.y = off;  off += round_up(tok * m * e, 256);
+  L.o = off;  off += round_up(tok * h * e, 256);
+  L.partials = off;
+  if (rs == TPMLP_RS_SPLITK) off += round_up(static_cast<size_t>(t) * tok * h * sizeof(float), 256);
+  L.total = off;
+  return L;
+}
+
+tpmlp_status check_sp_shape(int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype dt) {
+  if (b < 0 || s < 0 || h < 1) return fail(TPMLP_ERR_SHAPE, "need b >= 0, s >= 0, h >= 1");
+  if (t < 2) return fail(TPMLP_ERR_SHAPE, "sequence parallelism needs t >= 2 (a tensor-parallel group), got t=%d", t);
+  if (s % t != 0) return fail(TPMLP_ERR_SHAPE, "s=%lld is not divisible by t=%d", (long long)s, t);
+  if (h % 8 != 0) return fail(TPMLP_ERR_SHAPE, "h=%lld must be a multiple of 8", (long long)h);
+  (void)dt;
+  return TPMLP_OK;
+}
+
+tpmlp_status check_dropout(float p) {
+  if (!(p >= 0.0f && p < 1.0f)) return fail(TPMLP_ERR_INVALID, "p_drop must lie in [0, 1), got %g", (double)p);
+  return TPMLP_OK;
+}
+
+// T = floor(p * 2^64) with the product in double; p in [0, 1).
+uint64_t drop_threshold(float p) {
+  const double v = static_cast<double>(p) * 18446744073709551616.0;
+  return static_cast<uint64_t>(v);
+}
+
+}  // namespace
+
+size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m, int t, tpmlp_dtype dt,
+                                     tpmlp_rs_mode rs) {
+  if (b <= 0 || s <= 0 || h <= 0 || m <= 0 || t <= 0) return 0;
+  return sp_layout(b, s, h, m, t, dt, rs).total;
+}
+
+tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const float* beta, float eps, const void* A,
+                            const void* B, float p_drop, uint64_t seed, void* out_shards, uint32_t* mask_bits,
+                            int64_t b, int64_t s, int64_t h, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt,
+                            tpmlp_rs_mode rs, void* workspace, size_t ws_bytes, void* stream) {
+  TPMLP_TRY(check_common(gelu, dt));
+  TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
+  TPMLP_TRY(check_mlp_shape(b * s, h, m, t, dt));
+  TPMLP_TRY(check_dropout(p_drop));
+  if (rs != TPMLP_RS_FUSED && rs != TPMLP_RS_SPLITK) return fail(TPMLP_ERR_INVALID, "unknown reduce-scatter mode %d", (int)rs);
+  if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
+  TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{gamma, "gamma"}, {beta, "beta"}}));
+  if (b * s > 0) TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x_shards, "x_shards"}, {out_shards, "out_shards"}}));
+  if (mask_bits && (h % 32 != 0 || !aligned(mask_bits, 4)))
+    return fail(TPMLP_ERR_SHAPE, "mask_bits needs h %% 32 == 0 and 4-byte alignment");
+  if (rs == TPMLP_RS_SPLITK && ((m / t) % 8 != 0 && dt == TPMLP_BF16))
+    return fail(TPMLP_ERR_SHAPE, "split-K reduce-scatter on bf16 needs m/t to be a multiple of 8");
+  const int64_t n = b * s;
+  if (n == 0) return TPMLP_OK;
+  const SPLayout L = sp_layout(b, s, h, m, t, dt, rs);
+  if (!workspace || ws_bytes < L.total)
+    return fail(TPMLP_ERR_WORKSPACE, "sp_block needs %zu workspace bytes, got %zu", L.total, workspace ? ws_bytes : 0);
+  if (!aligned(workspace, 256)) return fail(TPMLP_ERR_ALIGN, "workspace is not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  char* ws = static_cast<char*>(workspace);
+  void* xn = ws + L.xn;
+  void* xg = ws + L.xg;
+  void* Y = ws + L.y;
+  void* o = ws + L.o;
+  const bool bf16 = dt == TPMLP_BF16;
+  // LayerNorm on the shards (SP region), then g: all-gather into token order.
+  TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms), "layernorm");
+  TPMLP_CUDA(launch_gather(xn, xg, b, s, h, t, bf16, st, ctx.num_sms), "gather");
+  if (rs == TPMLP_RS_FUSED) {
+    // FC1 + GeLU, then FC2 whose K-loop sums all shards and whose epilogue writes shard-major rows.
+    RowRemap rm;
+    rm.enabled = 1;
+    rm.b = b;
+    rm.s = s;
+    rm.s_per_shard = s / t;
+    TPMLP_TRY(run_forward(xg, A, B, o, nullptr, Y, n, h, m, gelu, dt, &rm, st, ctx));
+  } else {
+    TPMLP_CUDA(gemm(dt, n, m, h, Operand{xg, n, h, h, false}, Operand{A, h, m, m, true}, kEpiGelu,
+                    epi(nullptr, Y, nullptr, m, gelu), st, ctx),
+               "FC1 GEMM");
+    // One row GEMM per shard: P_i = Y_i B_i in fp32, then the reduce-scatter kernel.
+    const int64_t mt = m / t;
+    const size_t e = elt_size(dt);
+    float* partials = reinterpret_cast<float*>(ws + L.partials);
+    for (int i = 0; i < t; ++i) {
+      const void* Yi = static_cast<const char*>(Y) + static_cast<size_t>(i) * mt * e;
+      const void* Bi = static_cast<const char*>(B) + static_cast<size_t>(i) * mt * h * e;
+      TPMLP_CUDA(gemm(dt, n, h, mt, Operand{Yi, n, mt, m, false}, Operand{Bi, mt, h, h, true}, kEpiStoreF32,
+                      epi(partials + static_cast<size_t>(i) * n * h, nullptr, nullptr, h, gelu), st, ctx),
+                 "FC2 shard GEMM");
+    }
+    TPMLP_CUDA(launch_reduce_scatter(partials, o, b, s, h, t, bf16, st, ctx.num_sms), "reduce-scatter");
+  }
+  // Dropout + residual (SP region).
+  TPMLP_CUDA(launch_dropout_residual(x_shards, o, out_shards, mask_bits, drop_threshold(p_drop),
+                                     static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))), seed, b, s, h, t,
+                                     bf16, st, ctx.num_sms),
+             "dropout+residual");
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_sp_layernorm(const void* x, const float* gamma, const float* beta, float eps, void* y, int64_t rows,
+                                int64_t h, tpmlp_dtype dt, void* stream) {
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  if (rows < 0 || h < 1) return fail(TPMLP_ERR_SHAPE, "need rows >= 0 and h >= 1");
+  if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
+  if (!x || !y || !gamma || !beta) return fail(TPMLP_ERR_INVALID, "null pointer");
+  const bool vec = h % 8 == 0;
+  if (vec) {
+    TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x, "x"}, {y, "y"}}));
+    TPMLP_TRY(check_ptrs(TPMLP_BF16, {{gamma, "gamma"}, {beta, "beta"}}));
+  }
+  if (rows == 0) return TPMLP_OK;
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  TPMLP_CUDA(launch_layernorm(x, gamma, beta, eps, y, rows, h, dt == TPMLP_BF16, static_cast<cudaStream_t>(stream),
+                              ctx.num_sms),
+             "layernorm");
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_sp_gather(const void* x_shards, void* x_full, int64_t b, int64_t s, int64_t h, int t,
+                             tpmlp_dtype dt, void* stream) {
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
+  if (b * s == 0) return TPMLP_OK;
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x_shards, "x_shards"}, {x_full, "x_full"}}));
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  TPMLP_CUDA(launch_gather(x_shards, x_full, b, s, h, t, dt == TPMLP_BF16, static_cast<cudaStream_t>(stream),
+                           ctx.num_sms),
+             "gather");
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_sp_reduce_scatter(const float* partials, void* out_shards, int64_t b, int64_t s, int64_t h, int t,
+                                     tpmlp_dtype dt, void* stream) {
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
+  if (b * s == 0) return TPMLP_OK;
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{partials, "partials"}, {out_shards, "out_shards"}}));
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  TPMLP_CUDA(launch_reduce_scatter(partials, out_shards, b, s, h, t, dt == TPMLP_BF16,
+                                   static_cast<cudaStream_t>(stream), ctx.num_sms),
+             "reduce-scatter");
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shards, void* out_shards,
+                                       uint32_t* mask_bits, float p_drop, uint64_t seed, int64_t b, int64_t s,
+                                       int64_t h, int t, tpmlp_dtype dt, void* stream) {
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
+  TPMLP_TRY(check_dropout(p_drop));
+  if (mask_bits && (h % 32 != 0 || !aligned(mask_bits, 4)))
+    return fail(TPMLP_ERR_SHAPE, "mask_bits needs h %% 32 == 0 and 4-byte alignment");
+  if (b * s == 0) return TPMLP_OK;
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x_shards, "x_shards"}, {y_shards, "y_shards"}, {out_shards, "out_shards"}}));
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  TPMLP_CUDA(launch_dropout_residual(x_shards, y_shards, out_shards, mask_bits, drop_threshold(p_drop),
+                                     static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))), seed, b, s, h, t,
+                                     dt == TPMLP_BF16, static_cast<cudaStream_t>(stream), ctx.num_sms),
+             "dropout+residual");
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_device_status(void* stream, int clear) {
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TPMLP_CUDA(cudaStreamSynchronize(s), "stream synchronize");
+  unsigned int word = 0;
+  TPMLP_CUDA(cudaMemcpy(&word, ctx.status, sizeof(word), cudaMemcpyDeviceToHost), "read status");
+  if (clear) TPMLP_CUDA(cudaMemset(ctx.status, 0, sizeof(word)), "clear status");
+  if (word & kStatusTimeoutBit)
+    return fail(TPMLP_ERR_TIMEOUT, "a kernel's bounded wait expired (status word 0x%x)", word);
+  return TPMLP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Declarations shared by the translation units of libtpmlp.so (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tpmlp {
+
+constexpr int kGeluErf = 0;
+constexpr int kGeluTanh = 1;
+
+// Device status word: bit 0 = a bounded in-kernel wait expired; bits 8.. = where.
+constexpr unsigned int kStatusTimeoutBit = 1u;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+// Epilogue applied to the fp32 accumulator tile of a GEMM C = Aop * Bop (M x N).
+enum EpiKind : int {
+  kEpiStore = 0,     // out[r][c] = acc (operand dtype); optional sequence-parallel row remap
+  kEpiStoreF32 = 1,  // out[r][c] = acc (fp32)
+  kEpiGelu = 2,      // out[r][c] = acc (Z, may be null), out2[r][c] = gelu(acc) (Y)
+  kEpiDGelu = 3,     // out[r][c] = acc * gelu'(aux[r][c])  (D = (G B^T) * gelu'(Z))
+};
+
+// Row r of a token-ordered [b][s] x h matrix is written to shard-major position
+// [j][bi][l] with r = bi*s + j*(s/t) + l (the reduce-scatter's placement).
+struct RowRemap {
+  int enabled;
+  int64_t b, s, s_per_shard;
+};
+
+struct EpiParams {
+  void* out;
+  void* out2;
+  const void* aux;
+  int64_t ldo;  // row stride of out/out2/aux, elements
+  int gelu;
+  RowRemap remap;
+};
+
+// A stored operand matrix [rows][cols] with row stride `ld` elements.
+//   A operand (M x K): K-major means stored [M][K]; MN-major means stored [K][M].
+//   B operand (K x N): K-major means stored [N][K]; MN-major means stored [K][N].
+struct Operand {
+  const void* ptr;
+  int64_t rows, cols, ld;
+  bool mn_major;
+};
+
+// Per-device context: SM count and the address of the device status word.
+struct DeviceCtx {
+  int device;
+  int num_sms;
+  unsigned int* status;
+};
+
+cudaError_t get_device_ctx(DeviceCtx* ctx);
+
+// bf16 tensor-core GEMM (tcgen05 + TMA). C = Aop(M x K) * Bop(K x N), fp32 accumulation.
+cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
+                         const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx);
+
+// fp32 FMA GEMM for the fp32 dtype, same semantics and epilogues (outputs in fp32).
+cudaError_t gemm_f32_simt(int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
+                          const EpiParams& ep, cudaStream_t stream);
+
+// Sequence-parallel memory-bound kernels. `bf16` selects the element type (else fp32).
+cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, float eps, void* y,
+                             int64_t rows, int64_t h, bool bf16, cudaStream_t stream, int num_sms);
+cudaError_t launch_gather(const void* x_shards, void* x_full, int64_t b, int64_t s, int64_t h, int t, bool bf16,
+                          cudaStream_t stream, int num_sms);
+cudaError_t launch_reduce_scatter(const float* partials, void* out_shards, int64_t b, int64_t s, int64_t h, int t,
+                                  bool bf16, cudaStream_t stream, int num_sms);
+cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, void* out_shards,
+                                    uint32_t* mask_bits, uint64_t threshold, float scale, uint64_t seed, int64_t b,
+                                    int64_t s, int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms);
+
+}  // namespace tpmlp

@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, it
+exports every entry point include/tpmlp.h declares, and bad arguments are rejected
+with the documented status before anything touches the device."""
+import os
+import re
+import subprocess
+
+import pytest
+
+from tensor_transformer_mlp_gb300 import _binding, _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tpmlp.h")
+
+OK, INVALID, SHAPE, DTYPE, ALIGN, CUDA, TIMEOUT, WORKSPACE = range(8)
+ERF, TANH = 0, 1
+F32, BF16 = 0, 1
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return set(re.findall(r"^\s*(?:const\s+char\s*\*|size_t|tpmlp_status)\s+(tpmlp_\w+)\s*\(", text, re.M))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _binding.load_library(build_if_missing=True)
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == set(_binding.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(tpmlp_\w+)$", out, re.M))
+    assert declared_functions() <= exported
+    for name in declared_functions():
+        assert getattr(lib, name) is not None
+
+
+def fwd(lib, X=FAKE, A=FAKE, B=FAKE, O=FAKE, Z=FAKE, Y=FAKE, n=256, d=512, m=1024, t=2, g=TANH, dt=BF16):
+    return lib.tpmlp_forward(X, A, B, O, Z, Y, n, d, m, t, g, dt, None)
+
+
+def test_forward_validation(lib):
+    assert fwd(lib, X=None) == INVALID
+    assert fwd(lib, Y=None) == INVALID
+    assert fwd(lib, m=1000, t=3) == SHAPE          # uneven split
+    assert fwd(lib, t=0) == SHAPE
+    assert fwd(lib, d=500) == SHAPE                # bf16 rows must be 16-byte multiples
+    assert fwd(lib, n=-1) == SHAPE
+    assert fwd(lib, A=FAKE + 8) == ALIGN
+    assert fwd(lib, g=7) == INVALID
+    assert fwd(lib, dt=5) == DTYPE
+    assert b"divisible" in (fwd(lib, m=1000, t=3) and lib.tpmlp_last_error())
+    assert fwd(lib, n=0) == OK                     # nothing to do, nothing launched
+
+
+def test_backward_validation(lib):
+    args = [FAKE] * 9 + [256, 512, 1024, 2, TANH, BF16]
+    assert lib.tpmlp_backward(*args, None, 0, None) == WORKSPACE
+    assert lib.tpmlp_backward(*args, FAKE, 100, None) == WORKSPACE
+    assert lib.tpmlp_backward(*args, FAKE + 16, 1 << 30, None) == ALIGN
+    bad = list(args)
+    bad[4] = None  # Z_save (n > 0)
+    assert lib.tpmlp_backward(*bad, FAKE, 1 << 30, None) == INVALID
+    assert lib.tpmlp_backward_workspace_size(256, 1024, BF16) == 256 * 1024 * 2
+    assert lib.tpmlp_backward_workspace_size(0, 1024, BF16) == 0
+
+
+def sp(lib, t=4, s=64, h=256, m=512, p=0.1, mask=FAKE, ws=FAKE, wsb=1 << 30, rs=0, eps=1e-5):
+    return lib.tpmlp_sp_block(FAKE, FAKE, FAKE, eps, FAKE, FAKE, p, 0, FAKE, mask, 2, s, h, m, t, TANH, BF16, rs,
+                              ws, wsb, None)
+
+
+def test_sp_block_validation(lib):
+    assert sp(lib, t=1) == SHAPE                   # sequence parallelism needs a TP group
+    assert b"t >= 2" in lib.tpmlp_last_error()
+    assert sp(lib, s=66) == SHAPE                  # s % t
+    assert sp(lib, p=1.0) == INVALID
+    assert sp(lib, p=-0.1) == INVALID
+    assert sp(lib, eps=0.0) == INVALID
+    assert sp(lib, h=264) == SHAPE                 # mask words need h % 32 == 0
+    assert sp(lib, rs=9) == INVALID
+    assert sp(lib, ws=None) == WORKSPACE
+    need = lib.tpmlp_sp_block_workspace_size(2, 64, 256, 512, 4, BF16, 0)
+    assert need > 0 and sp(lib, wsb=need - 1) == WORKSPACE
+    assert lib.tpmlp_sp_block_workspace_size(2, 64, 256, 512, 4, BF16, 1) > need
+
+
+def test_elementwise_validation(lib):
+    assert lib.tpmlp_sp_gather(FAKE, FAKE, 2, 64, 256, 1, BF16, None) == SHAPE
+    assert lib.tpmlp_sp_gather(FAKE, None, 2, 64, 256, 4, BF16, None) == INVALID
+    assert lib.tpmlp_sp_gather(None, None, 0, 64, 256, 4, BF16, None) == OK  # no rows, nothing launched
+    assert lib.tpmlp_sp_reduce_scatter(FAKE, FAKE, 2, 63, 256, 4, BF16, None) == SHAPE
+    assert lib.tpmlp_sp_dropout_residual(FAKE, FAKE, FAKE, None, 1.5, 0, 2, 64, 256, 4, BF16, None) == INVALID
+    assert lib.tpmlp_sp_layernorm(FAKE, FAKE, FAKE, 1e-5, FAKE, 4, 256, 9, None) == DTYPE
+    assert lib.tpmlp_sp_layernorm(FAKE + 2, FAKE, FAKE, 1e-5, FAKE, 4, 256, BF16, None) == ALIGN
+
+
+def test_last_error_never_null(lib):
+    assert isinstance(lib.tpmlp_last_error(), bytes)

@@ -1,0 +1,142 @@
+"""GPU parity of the tensor-parallel MLP forward and backward (through the C ABI) against
+the float64 oracle, element by element on seeded inputs; sampled rows and columns at the
+full sizes the benchmark runs."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import tensor_transformer_mlp_gb300 as tp
+from oracle import mlp as omlp
+from tensor_transformer_mlp_gb300 import workloads as wl
+
+from helpers import TOL_BF16, TOL_F32, assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_example_seed0.txt")
+
+
+def run_gpu(inp, t, gelu, dtype):
+    X, A, B, G = (dev(inp[k], dtype) for k in "XABG")
+    O, Z, Y = tp.forward(X, A, B, t, gelu)
+    dX, dA, dB = tp.backward(X, A, B, G, Z, Y, t, gelu)
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    return {"O": O, "Z": Z, "Y": Y, "dX": dX, "dA": dA, "dB": dB}
+
+
+def check_full(inp, t, gelu, dtype, tol):
+    got = run_gpu(inp, t, gelu, dtype)
+    ref = omlp.forward(inp["X"], inp["A"], inp["B"], gelu)
+    ref.update(omlp.backward(inp["X"], inp["A"], inp["B"], inp["G"], gelu))
+    report = {}
+    for k in ("Z", "Y", "O", "dX", "dA", "dB"):
+        assert_close(k, host(got[k]), ref[k], tol, report)
+    print(report)
+    return got
+
+
+def _read_golden():
+    arrays, lines = {}, [ln for ln in open(GOLDEN) if not ln.startswith("#")]
+    i = 0
+    while i < len(lines):
+        name, r, c = lines[i].split()
+        r, c = int(r), int(c)
+        arrays[name] = np.array([[float(v) for v in lines[i + 1 + j].split()] for j in range(r)])
+        i += 1 + r
+    return arrays
+
+
+def test_worked_example_f32():
+    cfg = wl.WORKED_EXAMPLE
+    inp = wl.mlp_inputs(cfg)
+    got = check_full(inp, cfg.t, cfg.gelu, "f32", TOL_F32)
+    gold = _read_golden()
+    assert np.array_equal(gold["X"], inp["X"].astype(np.float64))
+    for k in ("O", "dX", "dA", "dB"):
+        assert_close("golden " + k, host(got[k]), gold[k], TOL_F32)
+
+
+def test_single_block_bf16():
+    cfg = wl.SINGLE_BLOCK
+    check_full(wl.mlp_inputs(cfg), cfg.t, cfg.gelu, "bf16", TOL_BF16)
+
+
+@pytest.mark.parametrize("gelu", ["erf", "tanh"])
+@pytest.mark.parametrize("shape", [(300, 200, 392, 7), (129, 72, 264, 3), (1, 8, 8, 1), (517, 1032, 776, 8)])
+def test_ragged_bf16(shape, gelu):
+    n, d, m, t = shape
+    cfg = wl.MLPConfig("ragged", n, d, m, t, "bf16", gelu, 1.0, 0.05, 1.0, seed=n)
+    check_full(wl.mlp_inputs(cfg), t, gelu, "bf16", TOL_BF16)
+
+
+@pytest.mark.parametrize("gelu", ["erf", "tanh"])
+@pytest.mark.parametrize("shape", [(37, 45, 66, 3), (130, 70, 140, 2)])
+def test_ragged_f32(shape, gelu):
+    n, d, m, t = shape
+    cfg = wl.MLPConfig("ragged", n, d, m, t, "f32", gelu, 1.0, 0.1, 1.0, seed=n)
+    check_full(wl.mlp_inputs(cfg), t, gelu, "f32", TOL_F32)
+
+
+def test_shard_count_does_not_change_results():
+    # On one GPU the shard sum is the GEMM's K-loop, in shard order for every t.
+    cfg = wl.MLPConfig("t-invariance", 256, 512, 1024, 1, "bf16", "tanh", 1.0, 0.02, 1.0)
+    inp = wl.mlp_inputs(cfg)
+    base = run_gpu(inp, 1, "tanh", "bf16")
+    for t in (2, 4, 8):
+        other = run_gpu(inp, t, "tanh", "bf16")
+        for k in base:
+            assert torch.equal(base[k], other[k]), (t, k)
+
+
+def test_empty_tokens():
+    d, m = 64, 128
+    X = torch.empty((0, d), dtype=torch.bfloat16, device="cuda")
+    A = torch.ones((d, m), dtype=torch.bfloat16, device="cuda")
+    B = torch.ones((m, d), dtype=torch.bfloat16, device="cuda")
+    O, Z, Y = tp.forward(X, A, B, 2, "tanh")
+    assert O.shape == (0, d)
+    dX, dA, dB = tp.backward(X, A, B, torch.empty_like(X), Z, Y, 2, "tanh")
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dA) == 0 and torch.count_nonzero(dB) == 0
+
+
+def test_bad_arguments_raise():
+    X = torch.zeros((8, 16), dtype=torch.bfloat16, device="cuda")
+    A = torch.zeros((16, 24), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((24, 16), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tp.TpmlpError, match="SHAPE"):
+        tp.forward(X, A, B, 5, "tanh")
+
+
+def sampled_parity(cfg, n_rows=48, n_cols=48):
+    """Full-size run in the benchmark's launch configuration; the oracle computes sampled
+    token rows of O and dX and sampled intermediate columns of dA, dB, Z and Y."""
+    inp = wl.mlp_inputs(cfg)
+    got = run_gpu(inp, cfg.t, cfg.gelu, cfg.dtype)
+    R = wl.sample_indices(n_rows, cfg.n, seed=1)
+    J = wl.sample_indices(n_cols, cfg.m, seed=2)
+    rows_f = omlp.forward(inp["X"][R], inp["A"], inp["B"], cfg.gelu)
+    rows_b = omlp.backward(inp["X"][R], inp["A"], inp["B"], inp["G"][R], cfg.gelu)
+    cols_b = omlp.backward(inp["X"], inp["A"][:, J], inp["B"][J, :], inp["G"], cfg.gelu)
+    cols_f = omlp.forward(inp["X"], inp["A"][:, J], inp["B"][J, :], cfg.gelu)
+    Rt = torch.from_numpy(R).cuda()
+    Jt = torch.from_numpy(J).cuda()
+    report = {}
+    assert_close("O[R]", host(got["O"][Rt]), rows_f["O"], TOL_BF16, report)
+    assert_close("dX[R]", host(got["dX"][Rt]), rows_b["dX"], TOL_BF16, report)
+    assert_close("Z[:,J]", host(got["Z"][:, Jt]), cols_f["Z"], TOL_BF16, report)
+    assert_close("Y[:,J]", host(got["Y"][:, Jt]), cols_f["Y"], TOL_BF16, report)
+    assert_close("dA[:,J]", host(got["dA"][:, Jt]), cols_b["dA"], TOL_BF16, report)
+    assert_close("dB[J,:]", host(got["dB"][Jt, :]), cols_b["dB"], TOL_BF16, report)
+    print(cfg.name, report)
+
+
+def test_gpt_mlp_sampled():
+    sampled_parity(wl.GPT_MLP)
+
+
+def test_large_mlp_sampled():
+    sampled_parity(wl.LARGE_MLP)

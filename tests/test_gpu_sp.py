@@ -1,0 +1,158 @@
+"""GPU parity of the sequence-parallel block and its memory-bound kernels (through the C ABI)
+against the float64 oracle; dropout masks bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import tensor_transformer_mlp_gb300 as tp
+from oracle import collectives, mlp as omlp, sp as osp
+from tensor_transformer_mlp_gb300 import workloads as wl
+
+from helpers import TOL_BF16, TOL_F32, assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def mask_words(mask: torch.Tensor) -> np.ndarray:
+    return mask.cpu().numpy().view(np.uint32)
+
+
+def sp_case(cfg, rs, dtype="bf16"):
+    inp = wl.sp_inputs(cfg)
+    xs = wl.to_shards(inp["x"], cfg.t)
+    x_d = dev(xs, dtype)
+    A, B = dev(inp["A"], dtype), dev(inp["B"], dtype)
+    g = torch.from_numpy(inp["gamma"]).cuda()
+    b = torch.from_numpy(inp["beta"]).cuda()
+    out, mask = tp.sp_block(x_d, g, b, cfg.eps, A, B, cfg.p_drop, cfg.seed, cfg.t, cfg.gelu, rs)
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    return inp, out, mask
+
+
+@pytest.mark.parametrize("rs", ["fused", "splitk"])
+@pytest.mark.parametrize("shape", [(2, 256, 256, 512, 4), (3, 96, 96, 208, 2), (1, 512, 128, 1024, 8)])
+def test_sp_block_small(shape, rs):
+    b, s, h, m, t = shape
+    cfg = wl.SPConfig("sp-small", b, s, h, m, t, "tanh", 1.0, 0.05, seed=s)
+    inp, out, mask = sp_case(cfg, rs)
+    ref = osp.sp_block(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop, cfg.seed, cfg.gelu)
+    got = wl.from_shards(host(out).reshape(t, b, s // t, h))
+    assert_close("out", got, ref["out"], TOL_BF16)
+    assert np.array_equal(mask_words(mask), osp.pack_mask_bits(ref["dropped"]))
+
+
+def test_sp_block_f32():
+    cfg = wl.SPConfig("sp-f32", 2, 64, 64, 128, 4, "erf", 1.0, 0.1, dtype="f32", seed=3)
+    inp, out, mask = sp_case(cfg, "fused", "f32")
+    ref = osp.sp_block(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop, cfg.seed, cfg.gelu)
+    assert_close("out", wl.from_shards(host(out).reshape(4, 2, 16, 64)), ref["out"], 1e-4)
+    assert np.array_equal(mask_words(mask), osp.pack_mask_bits(ref["dropped"]))
+
+
+def test_sp_mask_independent_of_t():
+    b, s, h, m = 2, 128, 256, 256
+    masks = []
+    for t in (2, 4, 8):
+        cfg = wl.SPConfig("sp-t", b, s, h, m, t, "tanh", 1.0, 0.05, seed=11)
+        _, _, mask = sp_case(cfg, "fused")
+        masks.append(mask_words(mask))
+    assert all(np.array_equal(masks[0], mk) for mk in masks[1:])
+
+
+def test_sp_block_full_size_sampled():
+    """Sequence-parallel block at its benchmark size: mask bits compared in full, the block
+    output on sampled token rows."""
+    cfg = wl.SP_BLOCK
+    inp, out, mask = sp_case(cfg, "fused")
+    b, s, h, t = cfg.b, cfg.s, cfg.h, cfg.t
+    flat = np.arange(b * s * h, dtype=np.uint64)
+    assert np.array_equal(mask_words(mask), osp.pack_mask_bits(osp.drop_mask(flat, cfg.seed, cfg.p_drop)))
+    tokens = wl.sample_indices(48, b * s, seed=3)
+    x_rows = inp["x"].reshape(b * s, h)[tokens]
+    # The block acts per token: LayerNorm, MLP and dropout of a sampled row need only that row
+    # and its global flat indices.
+    xn = osp.layernorm(x_rows, inp["gamma"], inp["beta"], cfg.eps)
+    o = omlp.forward(xn, inp["A"], inp["B"], cfg.gelu)["O"]
+    flat_rows = tokens[:, None].astype(np.uint64) * np.uint64(h) + np.arange(h, dtype=np.uint64)[None, :]
+    ref_out = osp.dropout_residual(x_rows, o, cfg.seed, cfg.p_drop, flat_rows)
+    got = wl.from_shards(host(out).reshape(t, b, s // t, h)).reshape(b * s, h)[tokens]
+    assert_close("out[tokens]", got, ref_out, TOL_BF16)
+
+
+# ---------------------------------------------------------------- standalone kernels
+
+@pytest.mark.parametrize("dtype,tol", [("bf16", 8e-3), ("f32", 2e-6)])
+@pytest.mark.parametrize("h", [4096, 256, 1000, 8192, 100])
+def test_layernorm(h, dtype, tol):
+    rows = 333
+    rng = np.random.default_rng(h)
+    x = (rng.standard_normal((rows, h)) * 2 + 0.5).astype(np.float32)
+    x = wl.round_to_bf16(x) if dtype == "bf16" else x
+    g = (1 + 0.1 * rng.standard_normal(h)).astype(np.float32)
+    be = (0.1 * rng.standard_normal(h)).astype(np.float32)
+    xd = dev(x, dtype)
+    y = torch.empty_like(xd)
+    tp.tpmlp_sp_layernorm(xd, torch.from_numpy(g).cuda(), torch.from_numpy(be).cuda(), 1e-5, y)
+    torch.cuda.synchronize()
+    assert_close("ln", host(y), osp.layernorm(x, g, be, 1e-5), tol)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gather_is_exact_permutation(dtype):
+    t, b, sl, h = 4, 3, 40, 264
+    x = np.random.default_rng(5).standard_normal((t, b, sl, h)).astype(np.float32)
+    x = wl.round_to_bf16(x) if dtype == "bf16" else x
+    xd = dev(x, dtype)
+    full = torch.empty((b, sl * t, h), dtype=xd.dtype, device="cuda")
+    tp.tpmlp_sp_gather(xd, full)
+    torch.cuda.synchronize()
+    ref = collectives.all_gather([x[j] for j in range(t)], axis=1)[0]
+    assert np.array_equal(host(full), ref.astype(np.float64))
+
+
+def test_reduce_scatter_f32_bit_exact_and_allreduce_identity():
+    t, b, s, h = 4, 2, 64, 256
+    parts = np.random.default_rng(6).standard_normal((t, b * s, h)).astype(np.float32)
+    out = torch.empty((t, b, s // t, h), dtype=torch.float32, device="cuda")
+    tp.tpmlp_sp_reduce_scatter(torch.from_numpy(parts).cuda(), out)
+    torch.cuda.synchronize()
+    ref = collectives.reduce_scatter([p.reshape(b, s, h) for p in parts], axis=1)  # rank j: [b, s/t, h]
+    assert np.array_equal(out.cpu().numpy(), np.stack(ref))
+    # AllReduce == AllGather(ReduceScatter): device RS followed by device gather
+    full = torch.empty((b, s, h), dtype=torch.float32, device="cuda")
+    tp.tpmlp_sp_gather(out, full)
+    torch.cuda.synchronize()
+    ar = collectives.all_reduce([p.reshape(b, s, h) for p in parts])[0]
+    assert np.array_equal(full.cpu().numpy(), ar)
+
+
+def test_reduce_scatter_bf16():
+    t, b, s, h = 8, 2, 64, 512
+    parts = np.random.default_rng(7).standard_normal((t, b * s, h)).astype(np.float32)
+    out = torch.empty((t, b, s // t, h), dtype=torch.bfloat16, device="cuda")
+    tp.tpmlp_sp_reduce_scatter(torch.from_numpy(parts).cuda(), out)
+    torch.cuda.synchronize()
+    ref = np.stack(collectives.reduce_scatter([p.astype(np.float64).reshape(b, s, h) for p in parts], axis=1))
+    assert_close("rs", host(out), ref, 8e-3)
+
+
+@pytest.mark.parametrize("p", [0.0, 0.1, 0.5])
+def test_dropout_residual(p):
+    t, b, sl, h = 4, 2, 32, 256
+    rng = np.random.default_rng(8)
+    x = wl.round_to_bf16(rng.standard_normal((t, b, sl, h)).astype(np.float32))
+    y = wl.round_to_bf16(rng.standard_normal((t, b, sl, h)).astype(np.float32))
+    xd, yd = dev(x, "bf16"), dev(y, "bf16")
+    out = torch.empty_like(xd)
+    words = (b * sl * t * h) // 32
+    mask = torch.zeros(words, dtype=torch.int32, device="cuda")
+    tp.tpmlp_sp_dropout_residual(xd, yd, out, mask, p, 1234, )
+    torch.cuda.synchronize()
+    xl, yl = wl.from_shards(x), wl.from_shards(y)
+    flat = np.arange(b * sl * t * h, dtype=np.uint64).reshape(xl.shape)
+    assert np.array_equal(mask_words(mask), osp.pack_mask_bits(osp.drop_mask(flat, 1234, p)))
+    ref = osp.dropout_residual(xl, yl, 1234, p, flat)
+    assert_close("out", wl.from_shards(host(out).reshape(t, b, sl, h)), ref, 8e-3)
+    if p == 0.0:
+        assert not mask_words(mask).any()
