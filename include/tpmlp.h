@@ -100,6 +100,28 @@ tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const v
                             tpmlp_gelu gelu, tpmlp_dtype dt,
                             void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * tpmlp_backward without a caller workspace. The source pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory (a host that passes only the
+ * step's tensors and owns no device allocator, or code that must not allocate once its steady
+ * state has begun). It computes exactly what tpmlp_backward computes, with the same arguments
+ * minus the workspace, and keeps D in a static device array of 64 MiB (67,108,864 bytes)
+ * inside the library, which every GPU that loads the library holds until the process exits.
+ *   - n * m * element size above 64 MiB is rejected with TPMLP_ERR_WORKSPACE before anything
+ *     runs; use tpmlp_backward with a workspace for larger problems.
+ *   - It allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *   - The first call on a device looks up the array's device address on that device (once);
+ *     make that first call before any stream capture.
+ *   - Every call on a device shares the one array: calls that may overlap on the GPU (on
+ *     different streams, or from several threads) race on it and must be serialised by the
+ *     caller. D is fully rewritten by each call, so no clearing is needed between calls.
+ */
+tpmlp_status tpmlp_backward_noalloc(const void* X, const void* A, const void* B, const void* G,
+                                    const void* Z_save, const void* Y_save,
+                                    void* dX, float* dA, float* dB,
+                                    int64_t n, int64_t d, int64_t m, int t,
+                                    tpmlp_gelu gelu, tpmlp_dtype dt, void* stream);
+
 /* Bytes of device workspace tpmlp_sp_block needs (LN output, gathered tokens, Y, row-GEMM output or partials). */
 size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m, int t,
                                      tpmlp_dtype dt, tpmlp_rs_mode rs);

@@ -27,6 +27,7 @@ SIGNATURES = {
     "tpmlp_forward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_backward_workspace_size": (_SZ, [_I64, _I64, _I]),
     "tpmlp_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
+    "tpmlp_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_sp_block_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I, _I, _I]),
     "tpmlp_sp_block": (_I, [_P, _P, _P, _F, _P, _P, _F, _U64, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _P, _SZ,
                             _P]),

@@ -69,6 +69,11 @@ cudaError_t get_device_ctx(DeviceCtx* ctx) {
 
 }  // namespace tpmlp
 
+namespace tpmlp {
+// Lets other translation units of the library set the calling thread's last-error message.
+int report_error(int status, const char* msg) { return fail(static_cast<tpmlp_status>(status), "%s", msg); }
+}  // namespace tpmlp
+
 using namespace tpmlp;
 
 namespace {

@@ -56,6 +56,9 @@ struct DeviceCtx {
 
 cudaError_t get_device_ctx(DeviceCtx* ctx);
 
+// Sets the calling thread's tpmlp_last_error() message; returns `status`.
+int report_error(int status, const char* msg);
+
 // bf16 tensor-core GEMM (tcgen05 + TMA). C = Aop(M x K) * Bop(K x N), fp32 accumulation.
 cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
                          const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx);
