@@ -173,14 +173,20 @@ def time_oracle(cfg, inp, rows: int, row0: int = 0) -> float:
 
 
 def calibrate_rows(cfg, inp, target_s: float, max_rows: int) -> int:
-    probe = 16
-    t = time_oracle(cfg, inp, probe)
-    rows = int(probe * target_s / max(t, 1e-3))
-    return max(probe, min(rows, max_rows, cfg.n))
+    """Rows of oracle work that take about target_s. Doubles a probe until one run takes at
+    least a quarter of the target, then scales linearly from it (the probe's fixed part, the
+    oracle's float64 conversion of the full weights, makes this an underestimate)."""
+    rows = 16
+    while True:
+        t = time_oracle(cfg, inp, rows)
+        if t >= target_s / 4 or rows >= max_rows or rows >= cfg.n:
+            break
+        rows *= 2
+    return max(16, min(int(rows * target_s / max(t, 1e-3)), max_rows, cfg.n))
 
 
 def cpu_baseline(cfg, inp, target_s=15.0):
-    rows = calibrate_rows(cfg, inp, target_s, 4096)
+    rows = calibrate_rows(cfg, inp, target_s, 8192)
     secs = time_oracle(cfg, inp, rows)
     return {"value": oracle_rows_flops(cfg, rows) / secs / 1e12, "unit": UNIT, "cores": os.cpu_count(),
             "kind": "oracle",
@@ -196,7 +202,7 @@ def run_reference(args, cfg):
     inp = wl.mlp_inputs(cfg)
     # each step a bounded sample of token rows, so the whole run stays within a few minutes
     per_step = 90.0 / max(1, args.steps + args.warmup)
-    rows = calibrate_rows(cfg, inp, per_step, 2048)
+    rows = calibrate_rows(cfg, inp, per_step, 4096)
     for i in range(args.warmup):
         time_oracle(cfg, inp, rows, row0=(i * rows) % max(1, cfg.n - rows))
     total = 0.0
@@ -222,6 +228,82 @@ def config_dict(cfg):
                       f"rounded to {cfg.dtype}",
             "l2": "inputs larger than L2 (X, G 256+ MiB; A, B 512+ MiB per step), no flush",
             "parallelism": "replicas (t shards on one GPU per replica)"}
+
+
+# ----------------------------------------------------------------------------- SP kernels
+
+def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
+    """Times the sequence-parallel block and each of its memory-bound kernels on the SP
+    workload. Each kernel is launched `reps` times back to back, rotating over `sets` buffer
+    sets so that the bytes touched between two uses of a set exceed the L2 cache."""
+    import torch
+
+    import tensor_transformer_mlp_gb300 as tp
+
+    cfg = wl.SP_BLOCK
+    b, s, h, m, t = cfg.b, cfg.s, cfg.h, cfg.m, cfg.t
+    sl = s // t
+    inp = wl.sp_inputs(cfg)
+    bf = torch.bfloat16
+    x0 = torch.from_numpy(wl.to_shards(inp["x"], t)).to(dev).to(bf)
+    A = torch.from_numpy(inp["A"]).to(dev).to(bf)
+    B = torch.from_numpy(inp["B"]).to(dev).to(bf)
+    gamma = torch.from_numpy(inp["gamma"]).to(dev)
+    beta = torch.from_numpy(inp["beta"]).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    N = b * s * h
+    elt = 2
+
+    def timed(fn, launches):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(launches):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / launches / 1e3
+
+    xs = [x0.clone() for _ in range(sets)]
+    ys = [torch.empty_like(x0) for _ in range(sets)]
+    full = [torch.empty((b, s, h), dtype=bf, device=dev) for _ in range(sets)]
+    outs = [torch.empty_like(x0) for _ in range(sets)]
+    masks = [torch.empty((N + 31) // 32, dtype=torch.int32, device=dev) for _ in range(sets)]
+    res = {}
+    hbm = float(peaks.get("hbm_gbs"))
+
+    def entry(name, secs, nbytes, note):
+        gbs = nbytes / secs / 1e9
+        res[name] = {"us": secs * 1e6, "bytes": nbytes, "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "note": note}
+
+    sec = timed(lambda i: tp.tpmlp_sp_layernorm(xs[i % sets], gamma, beta, cfg.eps, ys[i % sets], stream), reps)
+    entry("layernorm", sec, 2 * N * elt, "read x + write LN(x), bf16")
+    sec = timed(lambda i: tp.tpmlp_sp_gather(ys[i % sets], full[i % sets], stream), reps)
+    entry("gather", sec, 2 * N * elt, "read shards + write token order, bf16")
+    sec = timed(lambda i: tp.tpmlp_sp_dropout_residual(xs[i % sets], ys[i % sets], outs[i % sets], masks[i % sets],
+                                                       cfg.p_drop, cfg.seed, stream), reps)
+    entry("dropout_residual", sec, 3 * N * elt + N // 8, "read x, y + write out (bf16) + mask bits")
+    del full
+    parts = torch.randn((t, b * s, h), dtype=torch.float32, device=dev)  # 1 GiB > L2
+    sec = timed(lambda i: tp.tpmlp_sp_reduce_scatter(parts, outs[i % sets], stream), max(10, reps // 4))
+    entry("reduce_scatter_splitk", sec, t * N * 4 + N * elt, "read t fp32 partials + write shards (bf16)")
+    del parts
+
+    out = torch.empty_like(x0)
+    mask = torch.empty((N + 31) // 32, dtype=torch.int32, device=dev)
+    for rs in ("fused", "splitk"):
+        ws = torch.empty(tp.tpmlp_sp_block_workspace_size(b, s, h, m, t, bf, rs), dtype=torch.uint8, device=dev)
+        sec = timed(lambda i: tp.tpmlp_sp_block(x0, gamma, beta, cfg.eps, A, B, cfg.p_drop, cfg.seed, out, mask, t,
+                                               cfg.gelu, rs, ws, stream), 10)
+        res[f"sp_block_{rs}"] = {"ms": sec * 1e3, "mlp_tflops": cfg.flops_mlp_fwd / sec / 1e12,
+                                 "note": "whole block; TFLOP/s counts the MLP's 4*n*h*m only"}
+        del ws
+    tp.tpmlp_device_status(stream)
+    return {"workload": cfg.name, "l2": f"{sets} rotating buffer sets per kernel (>= 3 x 128 MiB between reuses)",
+            "kernels": res}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -344,6 +426,8 @@ def run_ours(args, cfg):
         "gpu_launches": GEMM_LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks,
     }
+    if not args.no_sp:
+        line["sp"] = measure_sp(dev, peaks)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp)
     print(json.dumps(line), flush=True)
@@ -359,6 +443,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=wl.LARGE_MLP.name,
                     choices=sorted(k for k, c in wl.MLP_CONFIGS.items() if c.dtype == "bf16"))
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
+    ap.add_argument("--no-sp", action="store_true", help="skip the sequence-parallel kernel measurements")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

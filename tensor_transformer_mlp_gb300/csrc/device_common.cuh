@@ -95,6 +95,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (addresses 16-byte aligned, size a multiple of 16);
+// completes `bytes` of transaction on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05 (tensor memory + MMA)
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -210,6 +220,17 @@ __device__ __forceinline__ float gelu_grad_f(float x, int kind) {
   const float u = kSqrt2OverPi * fmaf(kTanhC * x * x, x, x);
   const float th = precise ? tanhf(u) : tanh_fast(u);
   return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * kSqrt2OverPi * fmaf(3.0f * kTanhC, x * x, 1.0f);
+}
+
+// Drop decision for one element: splitmix64(key) < threshold, with SplitMix64 as published by
+// Steele, Lea and Flood (2014) / Vigna's splitmix64.c: add the golden-gamma increment, then the
+// variant-13 mixer (xor-shift 30, multiply, xor-shift 27, multiply, xor-shift 31), mod 2^64.
+// Straight-line code: a data-dependent early exit here costs more than the full compare.
+__device__ __forceinline__ bool hash_below(uint64_t key, uint64_t threshold) {
+  uint64_t z = key + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return (z ^ (z >> 31)) < threshold;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

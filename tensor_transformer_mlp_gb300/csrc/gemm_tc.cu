@@ -71,6 +71,7 @@ __device__ __forceinline__ int64_t remap_row(const RowRemap& rm, int64_t r) {
 template <int EPI>
 __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row, int col0, int N,
                                                const uint32_t (&v)[32]) {
+  uint32_t drop_bits = 0;  // kEpiDropoutResidual: one mask word per 32 columns
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const int col = col0 + g * 8;
@@ -100,6 +101,27 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
       uint4 yy = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                             pack_bf16x2(y[6], y[7]));
       *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out2) + off) = yy;
+    } else if constexpr (EPI == kEpiDropoutResidual) {
+      const int64_t prow = remap_row(ep.remap, row);
+      const int64_t off = prow * ep.ldo + col;
+      const uint4 xr = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.aux) + off);
+      const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+      // (seed ^ k0) ^ e = seed ^ (k0 + e) because k0 = row * ldo + col is a multiple of 8
+      const uint64_t base = ep.drop.seed ^ static_cast<uint64_t>(row * ep.ldo + col);
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 xf = unpack_bf16x2(xw[i]);
+        const bool d0 = hash_below(base ^ static_cast<uint64_t>(2 * i), ep.drop.threshold);
+        const bool d1 = hash_below(base ^ static_cast<uint64_t>(2 * i + 1), ep.drop.threshold);
+        drop_bits |= (d0 ? 1u : 0u) << (g * 8 + 2 * i);
+        drop_bits |= (d1 ? 1u : 0u) << (g * 8 + 2 * i + 1);
+        o[2 * i] = d0 ? xf.x : fmaf(a[2 * i], ep.drop.scale, xf.x);
+        o[2 * i + 1] = d1 ? xf.y : fmaf(a[2 * i + 1], ep.drop.scale, xf.y);
+      }
+      uint4 pk = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                            pack_bf16x2(o[6], o[7]));
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + off) = pk;
     } else if constexpr (EPI == kEpiDGelu) {
       const int64_t off = row * ep.ldo + col;
       const uint4 z = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.aux) + off);
@@ -115,6 +137,10 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
                             pack_bf16x2(d[6], d[7]));
       *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + off) = pk;
     }
+  }
+  if constexpr (EPI == kEpiDropoutResidual) {
+    // N is a multiple of 32 here, so the 32 columns are whole and form one aligned mask word.
+    if (ep.drop.mask_bits) ep.drop.mask_bits[static_cast<uint64_t>(row * ep.ldo + col0) >> 5] = drop_bits;
   }
 }
 
@@ -351,6 +377,10 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
     if (epi == kEpiGelu) return launch<false, true, kEpiGelu>(ta, tb, m, n, k, ep, stream, ctx);
     if (epi == kEpiStore) return launch<false, true, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
     if (epi == kEpiStoreF32) return launch<false, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
+    if (epi == kEpiDropoutResidual) {
+      if (N % 32 != 0) return cudaErrorInvalidValue;
+      return launch<false, true, kEpiDropoutResidual>(ta, tb, m, n, k, ep, stream, ctx);
+    }
   } else if (!a.mn_major && !b.mn_major) {
     if (epi == kEpiDGelu) return launch<false, false, kEpiDGelu>(ta, tb, m, n, k, ep, stream, ctx);
     if (epi == kEpiStore) return launch<false, false, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);

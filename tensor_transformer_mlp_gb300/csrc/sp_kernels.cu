@@ -70,57 +70,80 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------------ LayerNorm
-// One warp per row; the row stays in registers (MAXV vectors of 8 per lane), so it is
-// read from HBM once. Statistics in fp32: mean, then the biased variance of the
-// deviations (two passes over registers).
-template <typename T, int MAXV>
-__global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x, const float* __restrict__ gamma,
-                                                        const float* __restrict__ beta, float eps, T* __restrict__ y,
-                                                        int64_t rows, int h) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+// One 128-thread CTA per row; each thread keeps CH vectors of 8 elements of the row in
+// registers, so the row is read from HBM once and 16 rows per SM are in flight. Statistics
+// in fp32: the mean, then the biased variance of the deviations (two passes over registers),
+// each reduced across the CTA through shared memory that alternates between rows.
+constexpr int kLnThreads = 128;
+
+template <typename T, int CH>
+__global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const T* __restrict__ x,
+                                                               const float* __restrict__ gamma,
+                                                               const float* __restrict__ beta, float eps,
+                                                               T* __restrict__ y, int64_t rows, int h) {
+  __shared__ float red[2][2][kLnThreads / 32];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, w = tid >> 5;
   const float inv_h = 1.0f / static_cast<float>(h);
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
+  int parity = 0;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, parity ^= 1) {
     const T* xr = x + r * h;
-    float v[MAXV][8];
+    Vec8<T> buf[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      const int c = (tid + kLnThreads * i) * 8;
+      if (c < h) buf[i].load(xr + c);
+    }
     float sum = 0.f;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int c = (lane + 32 * i) * 8;
-      if (c < h) {
-        Vec8<T> in;
-        in.load(xr + c);
-        in.to_float(v[i]);
+    for (int i = 0; i < CH; ++i) {
+      if ((tid + kLnThreads * i) * 8 < h) {
+        float f[8];
+        buf[i].to_float(f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sum += v[i][e];
+        for (int e = 0; e < 8; ++e) sum += f[e];
       }
     }
-    const float mean = warp_sum(sum) * inv_h;
+    sum = warp_sum(sum);
+    if (lane == 0) red[parity][0][w] = sum;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < kLnThreads / 32; ++k) tot += red[parity][0][k];
+    const float mean = tot * inv_h;
     float sq = 0.f;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      if ((lane + 32 * i) * 8 < h) {
+    for (int i = 0; i < CH; ++i) {
+      if ((tid + kLnThreads * i) * 8 < h) {
+        float f[8];
+        buf[i].to_float(f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float dlt = v[i][e] - mean;
+          const float dlt = f[e] - mean;
           sq = fmaf(dlt, dlt, sq);
         }
       }
     }
-    const float rstd = rsqrtf(warp_sum(sq) * inv_h + eps);
+    sq = warp_sum(sq);
+    if (lane == 0) red[parity][1][w] = sq;
+    __syncthreads();
+    float var = 0.f;
+#pragma unroll
+    for (int k = 0; k < kLnThreads / 32; ++k) var += red[parity][1][k];
+    const float rstd = rsqrtf(var * inv_h + eps);
     T* yr = y + r * h;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int c = (lane + 32 * i) * 8;
+    for (int i = 0; i < CH; ++i) {
+      const int c = (tid + kLnThreads * i) * 8;
       if (c < h) {
         const float4 g0 = reinterpret_cast<const float4*>(gamma + c)[0], g1 = reinterpret_cast<const float4*>(gamma + c)[1];
         const float4 b0 = reinterpret_cast<const float4*>(beta + c)[0], b1 = reinterpret_cast<const float4*>(beta + c)[1];
         const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-        float o[8];
+        float f[8], o[8];
+        buf[i].to_float(f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = fmaf((v[i][e] - mean) * rstd, g[e], bb[e]);
+        for (int e = 0; e < 8; ++e) o[e] = fmaf((f[e] - mean) * rstd, g[e], bb[e]);
         Vec8<T> out;
         out.from_float(o);
         out.store(yr + c);
@@ -216,20 +239,13 @@ __global__ void __launch_bounds__(256) reduce_scatter_kernel(const float* __rest
 }
 
 // ------------------------------------------------------------------ dropout + residual
-// SplitMix64 (Steele, Lea, Flood 2014; the splitmix64.c step published by Vigna):
-// golden-gamma increment, then the variant-13 mixer.
-__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
-  uint64_t z = x + 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  return z ^ (z >> 31);
-}
 
 // out = x + keep * y * scale for shard-major rows; element k of the logical token-order
-// tensor is dropped iff splitmix64(seed ^ k) < threshold. Each thread handles 8 consecutive
-// elements; 4 neighbouring lanes OR their bits into one 32-bit mask word.
-template <typename T>
-__global__ void __launch_bounds__(256) dropout_residual_kernel(const T* __restrict__ x, const T* __restrict__ y,
+// tensor is dropped iff splitmix64(seed ^ k) < threshold. Each thread handles VPT vectors of
+// 8 consecutive elements and issues all their loads before hashing; 4 neighbouring lanes OR
+// their bits into one 32-bit mask word.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(128) dropout_residual_kernel(const T* __restrict__ x, const T* __restrict__ y,
                                                                T* __restrict__ out, uint32_t* __restrict__ mask_bits,
                                                                uint64_t threshold, float scale, uint64_t seed,
                                                                int64_t rows, int64_t b, int64_t s, int64_t sl,
@@ -238,26 +254,128 @@ __global__ void __launch_bounds__(256) dropout_residual_kernel(const T* __restri
   for (int64_t R = blockIdx.x; R < rows; R += gridDim.x) {
     const int64_t r = shard_row_to_token(R, b, s, sl);
     const uint64_t flat_row = static_cast<uint64_t>(r) * static_cast<uint64_t>(h);
-    for (int v0 = 0; v0 < nvec; v0 += blockDim.x) {  // uniform trip count across the CTA
+    const T* xr = x + R * h;
+    const T* yr = y + R * h;
+    T* orow = out + R * h;
+    for (int v0 = 0; v0 < nvec; v0 += blockDim.x * VPT) {  // uniform trip count across the CTA
+      Vec8<T> xv[VPT], yv[VPT];
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = v0 + j * blockDim.x + threadIdx.x;
+        if (v < nvec) {
+          xv[j].load(xr + v * 8);
+          yv[j].load(yr + v * 8);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = v0 + j * blockDim.x + threadIdx.x;
+        uint32_t bits = 0;
+        if (v < nvec) {
+          const uint64_t base = seed ^ (flat_row + static_cast<uint64_t>(v) * 8);  // (seed^k0)^e = seed^(k0+e)
+          float xf[8], yf[8], o[8];
+          xv[j].to_float(xf);
+          yv[j].to_float(yf);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool drop = hash_below(base ^ static_cast<uint64_t>(e), threshold);
+            bits |= (drop ? 1u : 0u) << e;
+            o[e] = drop ? xf[e] : fmaf(yf[e], scale, xf[e]);
+          }
+          Vec8<T> ov;
+          ov.from_float(o);
+          ov.store(orow + v * 8);
+        }
+        if (mask_bits != nullptr) {
+          bits <<= 8 * (threadIdx.x & 3);
+          bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
+          bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
+          if (v < nvec && (threadIdx.x & 3) == 0) mask_bits[(flat_row + static_cast<uint64_t>(v) * 8) >> 5] = bits;
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ bulk-copy row pipeline
+// The staged kernels below stream whole rows through a shared-memory ring: CTA c handles rows
+// R_i = c + i * gridDim.x, and thread 0 keeps up to kRowStages of them in flight with
+// cp.async.bulk copies that complete on one mbarrier per stage, while every thread computes on
+// rows already staged. Loads therefore never stall the computing warps. Every wait is bounded;
+// the CTA agrees on a timeout through __syncthreads_or, thread 0 waits (bounded) for its copies
+// still in flight, and the kernel returns.
+__device__ __forceinline__ int64_t rows_for_cta(int64_t rows) {
+  return rows > blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+}
+
+template <int STAGES>
+__device__ __forceinline__ void drain_rows(uint64_t* full, int64_t from, int64_t to, unsigned int* status) {
+  for (int64_t k = from; k < to; ++k) mbar_wait(&full[k % STAGES], (k / STAGES) & 1, status, 21);
+}
+
+
+template <typename T, int kRowThreads, int kRowStages>
+__global__ void __launch_bounds__(kRowThreads)
+    dropout_residual_staged_kernel(const T* __restrict__ x, const T* __restrict__ y, T* __restrict__ out,
+                                   uint32_t* __restrict__ mask_bits, uint64_t threshold, float scale, uint64_t seed,
+                                   int64_t rows, int64_t b, int64_t s, int64_t sl, int h, unsigned int* status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t row_bytes = static_cast<uint32_t>(h) * sizeof(T);
+  const uint32_t stage_bytes = 2 * row_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRowStages * stage_bytes);
+  const int64_t nloc = rows_for_cta(rows);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int st = 0; st < kRowStages; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int64_t i) {
+    const int64_t R = blockIdx.x + i * gridDim.x;
+    const int st = static_cast<int>(i % kRowStages);
+    uint8_t* dst = smem + st * stage_bytes;
+    mbar_arrive_expect_tx(&full[st], stage_bytes);
+    bulk_load(dst, x + R * h, row_bytes, &full[st]);
+    bulk_load(dst + row_bytes, y + R * h, row_bytes, &full[st]);
+  };
+  if (threadIdx.x == 0)
+    for (int64_t i = 0; i < nloc && i < kRowStages; ++i) issue(i);
+  const int nvec = h >> 3;
+  int64_t i = 0;
+  bool aborted = false;
+  for (; i < nloc; ++i) {
+    const int st = static_cast<int>(i % kRowStages);
+    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / kRowStages) & 1), status, 20);
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    const int64_t R = blockIdx.x + i * gridDim.x;
+    const uint64_t flat_row = static_cast<uint64_t>(shard_row_to_token(R, b, s, sl)) * static_cast<uint64_t>(h);
+    const T* xs = reinterpret_cast<const T*>(smem + st * stage_bytes);
+    const T* ys = reinterpret_cast<const T*>(smem + st * stage_bytes + row_bytes);
+    T* orow = out + R * h;
+    for (int v0 = 0; v0 < nvec; v0 += kRowThreads) {  // uniform trip count across the CTA
       const int v = v0 + threadIdx.x;
       uint32_t bits = 0;
       if (v < nvec) {
-        const int c = v * 8;
         Vec8<T> xv, yv;
-        xv.load(x + R * h + c);
-        yv.load(y + R * h + c);
+        xv.load(xs + v * 8);
+        yv.load(ys + v * 8);
         float xf[8], yf[8], o[8];
         xv.to_float(xf);
         yv.to_float(yf);
+        // k0 is a multiple of 8, so seed ^ (k0 + e) = (seed ^ k0) ^ e.
+        const uint64_t base = seed ^ (flat_row + static_cast<uint64_t>(v) * 8);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const bool drop = splitmix64(seed ^ (flat_row + static_cast<uint64_t>(c + e))) < threshold;
+          const bool drop = hash_below(base ^ static_cast<uint64_t>(e), threshold);
           bits |= (drop ? 1u : 0u) << e;
           o[e] = drop ? xf[e] : fmaf(yf[e], scale, xf[e]);
         }
         Vec8<T> ov;
         ov.from_float(o);
-        ov.store(out + R * h + c);
+        ov.store(orow + v * 8);
       }
       if (mask_bits != nullptr) {
         bits <<= 8 * (threadIdx.x & 3);
@@ -266,8 +384,228 @@ __global__ void __launch_bounds__(256) dropout_residual_kernel(const T* __restri
         if (v < nvec && (threadIdx.x & 3) == 0) mask_bits[(flat_row + static_cast<uint64_t>(v) * 8) >> 5] = bits;
       }
     }
+    __syncthreads();  // every thread has read stage st
+    if (threadIdx.x == 0 && i + kRowStages < nloc) issue(i + kRowStages);
   }
+  if (aborted && threadIdx.x == 0) drain_rows<kRowStages>(full, i, i + kRowStages < nloc ? i + kRowStages : nloc, status);
 }
+
+// LayerNorm with rows staged through the shared-memory ring; one CTA per row at a time, each
+// thread holding CH vectors of 8 elements in registers. The statistics take one pass: every
+// thread sums d = x - x_0 and d^2 (x_0, the row's first element, is a shift that keeps the
+// one-pass variance E[d^2] - E[d]^2 free of cancellation for rows with a large mean), the
+// warps' partial sums go to per-warp shared-memory slots that every thread adds in a fixed
+// order after a single barrier (deterministic). Slots alternate between rows.
+template <typename T, int CH, int kRowThreads, int kRowStages, bool kAffineInRegs>
+__global__ void __launch_bounds__(kRowThreads)
+    layernorm_staged_kernel(const T* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ beta,
+                            float eps, T* __restrict__ y, int64_t rows, int h, unsigned int* status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float2 red[2][kRowThreads / 32];
+  const uint32_t row_bytes = static_cast<uint32_t>(h) * sizeof(T);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRowStages * row_bytes);
+  const int64_t nloc = rows_for_cta(rows);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) {
+#pragma unroll
+    for (int st = 0; st < kRowStages; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int64_t i) {
+    const int64_t R = blockIdx.x + i * gridDim.x;
+    const int st = static_cast<int>(i % kRowStages);
+    mbar_arrive_expect_tx(&full[st], row_bytes);
+    bulk_load(smem + st * row_bytes, x + R * h, row_bytes, &full[st]);
+  };
+  if (tid == 0)
+    for (int64_t i = 0; i < nloc && i < kRowStages; ++i) issue(i);
+  // A thread touches the same columns of every row, so gamma and beta can stay in registers.
+  float greg[kAffineInRegs ? CH : 1][8], breg[kAffineInRegs ? CH : 1][8];
+  if constexpr (kAffineInRegs) {
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * kRowThreads) * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        greg[c][e] = col < h ? gamma[col + e] : 0.f;
+        breg[c][e] = col < h ? beta[col + e] : 0.f;
+      }
+    }
+  }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  int64_t i = 0;
+  bool aborted = false;
+  for (; i < nloc; ++i) {
+    const int st = static_cast<int>(i % kRowStages);
+    const int p = static_cast<int>(i & 1);
+    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / kRowStages) & 1), status, 22);
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    const T* xs = reinterpret_cast<const T*>(smem + st * row_bytes);
+    const float shift = static_cast<float>(xs[0]);
+    float f[CH][8];
+    float sum = 0.f, sq = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int v = tid + c * kRowThreads;
+      if (v * 8 < h) {
+        Vec8<T> in;
+        in.load(xs + v * 8);
+        in.to_float(f[c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = f[c][e] - shift;
+          sum += d;
+          sq = fmaf(d, d, sq);
+        }
+      }
+    }
+    sum = warp_sum(sum);
+    sq = warp_sum(sq);
+    if (lane == 0) red[p][w] = make_float2(sum, sq);
+    __syncthreads();  // the row's partial sums are published, and every thread has read stage st
+    if (tid == 0 && i + kRowStages < nloc) issue(i + kRowStages);
+    float tsum = 0.f, tsq = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowThreads / 32; ++k) {
+      const float2 ps = red[p][k];
+      tsum += ps.x;
+      tsq += ps.y;
+    }
+    const float md = tsum * inv_h;  // mean of x - shift
+    const float var = fmaxf(tsq * inv_h - md * md, 0.f);
+    const float rstd = rsqrtf(var + eps);
+    const float a0 = -(md + shift) * rstd;  // (x - mean) * rstd = x * rstd + a0
+    const int64_t R = blockIdx.x + i * gridDim.x;
+    T* yr = y + R * h;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int v = tid + c * kRowThreads;
+      if (v * 8 < h) {
+        const int col = v * 8;
+        float o[8];
+        if constexpr (kAffineInRegs) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = fmaf(fmaf(f[c][e], rstd, a0), greg[c][e], breg[c][e]);
+        } else {
+          const float4 g0 = reinterpret_cast<const float4*>(gamma + col)[0], g1 = reinterpret_cast<const float4*>(gamma + col)[1];
+          const float4 b0 = reinterpret_cast<const float4*>(beta + col)[0], b1 = reinterpret_cast<const float4*>(beta + col)[1];
+          const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = fmaf(fmaf(f[c][e], rstd, a0), g[e], bb[e]);
+        }
+        Vec8<T> ov;
+        ov.from_float(o);
+        ov.store(yr + col);
+      }
+    }
+  }
+  if (aborted && tid == 0) drain_rows<kRowStages>(full, i, i + kRowStages < nloc ? i + kRowStages : nloc, status);
+}
+
+// LayerNorm, one warp per row with no CTA-wide barriers: each warp streams its own rows
+// (R = global warp index + i * total warps) through a private shared-memory ring filled by
+// bulk copies, and reads each staged row three times (sum, squared deviations, output).
+template <typename T, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+    layernorm_warp_staged_kernel(const T* __restrict__ x, const float* __restrict__ gamma,
+                                 const float* __restrict__ beta, float eps, T* __restrict__ y, int64_t rows, int h,
+                                 unsigned int* status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t row_bytes = static_cast<uint32_t>(h) * sizeof(T);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + static_cast<size_t>(warp) * STAGES * row_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(WARPS) * STAGES * row_bytes) + warp * STAGES;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * WARPS;
+  const int64_t nloc = rows > gw ? (rows - 1 - gw) / nw + 1 : 0;
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < STAGES; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  auto issue = [&](int64_t i) {
+    const int st = static_cast<int>(i % STAGES);
+    mbar_arrive_expect_tx(&full[st], row_bytes);
+    bulk_load(ring + st * row_bytes, x + (gw + i * nw) * h, row_bytes, &full[st]);
+  };
+  if (lane == 0)
+    for (int64_t i = 0; i < nloc && i < STAGES; ++i) issue(i);
+  __syncwarp();
+  const int nvec = h >> 3;
+  const float inv_h = 1.0f / static_cast<float>(h);
+  int64_t i = 0;
+  bool aborted = false;
+  for (; i < nloc; ++i) {
+    const int st = static_cast<int>(i % STAGES);
+    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / STAGES) & 1), status, 23);
+    if (__any_sync(0xffffffffu, !ok)) {
+      aborted = true;
+      break;
+    }
+    const T* xs = reinterpret_cast<const T*>(ring + st * row_bytes);
+    float sum = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      Vec8<T> in;
+      in.load(xs + v * 8);
+      float f[8];
+      in.to_float(f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += f[e];
+    }
+    const float mean = warp_sum(sum) * inv_h;
+    float sq = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      Vec8<T> in;
+      in.load(xs + v * 8);
+      float f[8];
+      in.to_float(f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float dlt = f[e] - mean;
+        sq = fmaf(dlt, dlt, sq);
+      }
+    }
+    const float rstd = rsqrtf(warp_sum(sq) * inv_h + eps);
+    T* yr = y + (gw + i * nw) * h;
+    for (int v = lane; v < nvec; v += 32) {
+      const int col = v * 8;
+      Vec8<T> in;
+      in.load(xs + col);
+      float f[8], o[8];
+      in.to_float(f);
+      const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma + col));
+      const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma + col) + 1);
+      const float4 b0 = __ldg(reinterpret_cast<const float4*>(beta + col));
+      const float4 b1 = __ldg(reinterpret_cast<const float4*>(beta + col) + 1);
+      const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = fmaf((f[e] - mean) * rstd, g[e], bb[e]);
+      Vec8<T> out;
+      out.from_float(o);
+      out.store(yr + col);
+    }
+    __syncwarp();  // every lane has read stage st
+    if (lane == 0 && i + STAGES < nloc) issue(i + STAGES);
+  }
+  if (aborted && lane == 0) drain_rows<STAGES>(full, i, i + STAGES < nloc ? i + STAGES : nloc, status);
+}
+
+// Dynamic shared memory of a staged kernel: the row ring plus one mbarrier per stage.
+size_t staged_smem(size_t stage_bytes, int stages) { return stages * stage_bytes + stages * sizeof(uint64_t); }
+
+constexpr int kLnStagedThreads = 128, kLnStages = 6;
+constexpr bool kLnAffineInRegs = true;  // gamma, beta read once per CTA
+constexpr bool kUseStagedDropout = false;  // the register kernel issues fewer instructions per element
+constexpr int kDoStagedThreads = 256, kDoStages = 4;
+
+constexpr size_t kStagedSmemMax = 100 * 1024;  // at least two CTAs per SM
 
 int rows_grid(int64_t rows, int num_sms, int per_sm) {
   const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
@@ -277,26 +615,53 @@ int rows_grid(int64_t rows, int num_sms, int per_sm) {
 }  // namespace
 
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, float eps, void* y, int64_t rows,
-                             int64_t h, bool bf16, cudaStream_t stream, int num_sms) {
+                             int64_t h, bool bf16, cudaStream_t stream, int num_sms, unsigned int* status) {
   if (rows <= 0) return cudaSuccess;
-  const bool vec_ok = (h % 8 == 0) && (h <= 32 * 8 * 16);
-  if (vec_ok) {
-    const int warps_per_cta = 8;
-    const int64_t ctas = (rows + warps_per_cta - 1) / warps_per_cta;
-    const int grid = static_cast<int>(ctas < static_cast<int64_t>(num_sms) * 8 ? ctas : static_cast<int64_t>(num_sms) * 8);
-    const int maxv = static_cast<int>((h / 8 + 31) / 32);
+  const size_t elt = bf16 ? 2 : 4;
+  const size_t ln_smem = staged_smem(static_cast<size_t>(h) * elt, kLnStages);
+  if (h % 8 == 0 && h <= kLnStagedThreads * 8 * 8 && ln_smem <= kStagedSmemMax) {
+    const int by_smem = static_cast<int>((220 * 1024) / ln_smem);
+    const int by_threads = 2048 / kLnStagedThreads;
+    const int per_sm = by_smem < by_threads ? (by_smem > 0 ? by_smem : 1) : by_threads;
+    const int grid = rows_grid(rows, num_sms, per_sm);
+    const int ch = static_cast<int>((h / 8 + kLnStagedThreads - 1) / kLnStagedThreads);
+#define TPMLP_LN_STAGED(TYPE, CHN)                                                                              \
+  do {                                                                                                          \
+    auto k = layernorm_staged_kernel<TYPE, CHN, kLnStagedThreads, kLnStages, kLnAffineInRegs>;                                   \
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ln_smem);         \
+    if (e != cudaSuccess) return e;                                                                             \
+    k<<<grid, kLnStagedThreads, ln_smem, stream>>>(static_cast<const TYPE*>(x), gamma, beta, eps,               \
+                                                   static_cast<TYPE*>(y), rows, (int)h, status);                \
+  } while (0)
+    if (bf16) {
+      if (ch <= 1) TPMLP_LN_STAGED(__nv_bfloat16, 1);
+      else if (ch <= 2) TPMLP_LN_STAGED(__nv_bfloat16, 2);
+      else if (ch <= 4) TPMLP_LN_STAGED(__nv_bfloat16, 4);
+      else TPMLP_LN_STAGED(__nv_bfloat16, 8);
+    } else {
+      if (ch <= 1) TPMLP_LN_STAGED(float, 1);
+      else if (ch <= 2) TPMLP_LN_STAGED(float, 2);
+      else if (ch <= 4) TPMLP_LN_STAGED(float, 4);
+      else TPMLP_LN_STAGED(float, 8);
+    }
+#undef TPMLP_LN_STAGED
+  } else if ((h % 8 == 0) && (h <= kLnThreads * 8 * 8)) {
+    const int grid = rows_grid(rows, num_sms, 16);
+    const int ch = static_cast<int>((h / 8 + kLnThreads - 1) / kLnThreads);
     if (bf16) {
       auto xp = static_cast<const __nv_bfloat16*>(x);
       auto yp = static_cast<__nv_bfloat16*>(y);
-      if (maxv <= 4) layernorm_kernel<__nv_bfloat16, 4><<<grid, 256, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else if (maxv <= 8) layernorm_kernel<__nv_bfloat16, 8><<<grid, 256, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else layernorm_kernel<__nv_bfloat16, 16><<<grid, 256, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      if (ch <= 1) layernorm_kernel<__nv_bfloat16, 1><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      else if (ch <= 2) layernorm_kernel<__nv_bfloat16, 2><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      else if (ch <= 4) layernorm_kernel<__nv_bfloat16, 4><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      else layernorm_kernel<__nv_bfloat16, 8><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
     } else {
       auto xp = static_cast<const float*>(x);
       auto yp = static_cast<float*>(y);
-      if (maxv <= 4) layernorm_kernel<float, 4><<<grid, 256, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else if (maxv <= 8) layernorm_kernel<float, 8><<<grid, 256, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else layernorm_kernel<float, 16><<<grid, 256, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      if (ch <= 1) layernorm_kernel<float, 1><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      else if (ch <= 2) layernorm_kernel<float, 2><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      else if (ch <= 4) layernorm_kernel<float, 4><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      else layernorm_kernel<float, 8><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
     }
   } else {
     const int grid = rows_grid(rows, num_sms, 8);
@@ -339,21 +704,46 @@ cudaError_t launch_reduce_scatter(const float* partials, void* out_shards, int64
 
 cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, void* out_shards,
                                     uint32_t* mask_bits, uint64_t threshold, float scale, uint64_t seed, int64_t b,
-                                    int64_t s, int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms) {
+                                    int64_t s, int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms,
+                                    unsigned int* status) {
   const int64_t rows = b * s;
   if (rows <= 0) return cudaSuccess;
   if (h % 8 != 0 || (mask_bits && h % 32 != 0)) return cudaErrorInvalidValue;
-  const int grid = rows_grid(rows, num_sms, 8);
+  const size_t elt = bf16 ? 2 : 4;
+  const size_t do_smem = staged_smem(2 * static_cast<size_t>(h) * elt, kDoStages);
+  if (kUseStagedDropout && do_smem <= kStagedSmemMax) {
+    const int per_sm = static_cast<int>((220 * 1024) / do_smem);
+    const int grid = rows_grid(rows, num_sms, per_sm > 0 ? per_sm : 1);
+    if (bf16) {
+      auto k = dropout_residual_staged_kernel<__nv_bfloat16, kDoStagedThreads, kDoStages>;
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)do_smem);
+      if (e != cudaSuccess) return e;
+      k<<<grid, kDoStagedThreads, do_smem, stream>>>(static_cast<const __nv_bfloat16*>(x_shards),
+                                                static_cast<const __nv_bfloat16*>(y_shards),
+                                                static_cast<__nv_bfloat16*>(out_shards), mask_bits, threshold, scale,
+                                                seed, rows, b, s, s / t, static_cast<int>(h), status);
+    } else {
+      auto k = dropout_residual_staged_kernel<float, kDoStagedThreads, kDoStages>;
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)do_smem);
+      if (e != cudaSuccess) return e;
+      k<<<grid, kDoStagedThreads, do_smem, stream>>>(static_cast<const float*>(x_shards),
+                                                static_cast<const float*>(y_shards), static_cast<float*>(out_shards),
+                                                mask_bits, threshold, scale, seed, rows, b, s, s / t,
+                                                static_cast<int>(h), status);
+    }
+    return cudaGetLastError();
+  }
+  const int grid = rows_grid(rows, num_sms, 16);
   if (bf16)
-    dropout_residual_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+    dropout_residual_kernel<__nv_bfloat16, 4><<<grid, 128, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(x_shards), static_cast<const __nv_bfloat16*>(y_shards),
         static_cast<__nv_bfloat16*>(out_shards), mask_bits, threshold, scale, seed, rows, b, s, s / t,
         static_cast<int>(h));
   else
-    dropout_residual_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(x_shards),
-                                                              static_cast<const float*>(y_shards),
-                                                              static_cast<float*>(out_shards), mask_bits, threshold,
-                                                              scale, seed, rows, b, s, s / t, static_cast<int>(h));
+    dropout_residual_kernel<float, 4><<<grid, 128, 0, stream>>>(static_cast<const float*>(x_shards),
+                                                                 static_cast<const float*>(y_shards),
+                                                                 static_cast<float*>(out_shards), mask_bits, threshold,
+                                                                 scale, seed, rows, b, s, s / t, static_cast<int>(h));
   return cudaGetLastError();
 }
 

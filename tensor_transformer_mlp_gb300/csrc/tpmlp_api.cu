@@ -132,6 +132,10 @@ EpiParams epi(void* out, void* out2, const void* aux, int64_t ldo, tpmlp_gelu g)
   e.gelu = g == TPMLP_GELU_ERF ? kGeluErf : kGeluTanh;
   e.remap.enabled = 0;
   e.remap.b = e.remap.s = e.remap.s_per_shard = 1;
+  e.drop.mask_bits = nullptr;
+  e.drop.threshold = 0;
+  e.drop.seed = 0;
+  e.drop.scale = 1.0f;
   return e;
 }
 
@@ -300,15 +304,34 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
   void* o = ws + L.o;
   const bool bf16 = dt == TPMLP_BF16;
   // LayerNorm on the shards (SP region), then g: all-gather into token order.
-  TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms), "layernorm");
+  TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms, ctx.status), "layernorm");
   TPMLP_CUDA(launch_gather(xn, xg, b, s, h, t, bf16, st, ctx.num_sms), "gather");
+  const uint64_t threshold = drop_threshold(p_drop);
+  const float scale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop)));
+  RowRemap rm;
+  rm.enabled = 1;
+  rm.b = b;
+  rm.s = s;
+  rm.s_per_shard = s / t;
+  if (rs == TPMLP_RS_FUSED && bf16 && h % 32 == 0) {
+    // FC1 + GeLU; then FC2, whose K-loop sums all shards (g-bar's reduction) and whose epilogue
+    // writes shard-major rows (g-bar's scatter) after dropout and the residual add.
+    TPMLP_CUDA(gemm(dt, n, m, h, Operand{xg, n, h, h, false}, Operand{A, h, m, m, true}, kEpiGelu,
+                    epi(nullptr, Y, nullptr, m, gelu), st, ctx),
+               "FC1 GEMM");
+    EpiParams e2 = epi(out_shards, nullptr, x_shards, h, gelu);
+    e2.remap = rm;
+    e2.drop.mask_bits = mask_bits;
+    e2.drop.threshold = threshold;
+    e2.drop.seed = seed;
+    e2.drop.scale = scale;
+    TPMLP_CUDA(gemm(dt, n, h, m, Operand{Y, n, m, m, false}, Operand{B, m, h, h, true}, kEpiDropoutResidual, e2, st,
+                    ctx),
+               "FC2 GEMM + dropout + residual");
+    return TPMLP_OK;
+  }
   if (rs == TPMLP_RS_FUSED) {
     // FC1 + GeLU, then FC2 whose K-loop sums all shards and whose epilogue writes shard-major rows.
-    RowRemap rm;
-    rm.enabled = 1;
-    rm.b = b;
-    rm.s = s;
-    rm.s_per_shard = s / t;
     TPMLP_TRY(run_forward(xg, A, B, o, nullptr, Y, n, h, m, gelu, dt, &rm, st, ctx));
   } else {
     TPMLP_CUDA(gemm(dt, n, m, h, Operand{xg, n, h, h, false}, Operand{A, h, m, m, true}, kEpiGelu,
@@ -328,9 +351,8 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
     TPMLP_CUDA(launch_reduce_scatter(partials, o, b, s, h, t, bf16, st, ctx.num_sms), "reduce-scatter");
   }
   // Dropout + residual (SP region).
-  TPMLP_CUDA(launch_dropout_residual(x_shards, o, out_shards, mask_bits, drop_threshold(p_drop),
-                                     static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))), seed, b, s, h, t,
-                                     bf16, st, ctx.num_sms),
+  TPMLP_CUDA(launch_dropout_residual(x_shards, o, out_shards, mask_bits, threshold, scale, seed, b, s, h, t, bf16, st,
+                                     ctx.num_sms, ctx.status),
              "dropout+residual");
   return TPMLP_OK;
 }
@@ -350,7 +372,7 @@ tpmlp_status tpmlp_sp_layernorm(const void* x, const float* gamma, const float* 
   DeviceCtx ctx;
   TPMLP_CUDA(get_device_ctx(&ctx), "device context");
   TPMLP_CUDA(launch_layernorm(x, gamma, beta, eps, y, rows, h, dt == TPMLP_BF16, static_cast<cudaStream_t>(stream),
-                              ctx.num_sms),
+                              ctx.num_sms, ctx.status),
              "layernorm");
   return TPMLP_OK;
 }
@@ -397,7 +419,7 @@ tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shard
   TPMLP_CUDA(get_device_ctx(&ctx), "device context");
   TPMLP_CUDA(launch_dropout_residual(x_shards, y_shards, out_shards, mask_bits, drop_threshold(p_drop),
                                      static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))), seed, b, s, h, t,
-                                     dt == TPMLP_BF16, static_cast<cudaStream_t>(stream), ctx.num_sms),
+                                     dt == TPMLP_BF16, static_cast<cudaStream_t>(stream), ctx.num_sms, ctx.status),
              "dropout+residual");
   return TPMLP_OK;
 }

@@ -20,6 +20,17 @@ enum EpiKind : int {
   kEpiStoreF32 = 1,  // out[r][c] = acc (fp32)
   kEpiGelu = 2,      // out[r][c] = acc (Z, may be null), out2[r][c] = gelu(acc) (Y)
   kEpiDGelu = 3,     // out[r][c] = acc * gelu'(aux[r][c])  (D = (G B^T) * gelu'(Z))
+  kEpiDropoutResidual = 4,  // out[R][c] = aux[R][c] + keep(r, c) * acc * scale, R = remap(r); mask bits
+};
+
+// Dropout of the sequence-parallel block applied in a GEMM epilogue: element (r, c) of the
+// token-ordered result has global flat index r * ldo + c and is dropped iff
+// splitmix64(seed ^ index) < threshold.
+struct DropoutParams {
+  uint32_t* mask_bits;  // may be null
+  uint64_t threshold;
+  uint64_t seed;
+  float scale;
 };
 
 // Row r of a token-ordered [b][s] x h matrix is written to shard-major position
@@ -36,6 +47,7 @@ struct EpiParams {
   int64_t ldo;  // row stride of out/out2/aux, elements
   int gelu;
   RowRemap remap;
+  DropoutParams drop;
 };
 
 // A stored operand matrix [rows][cols] with row stride `ld` elements.
@@ -69,13 +81,15 @@ cudaError_t gemm_f32_simt(int64_t M, int64_t N, int64_t K, const Operand& a, con
 
 // Sequence-parallel memory-bound kernels. `bf16` selects the element type (else fp32).
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, float eps, void* y,
-                             int64_t rows, int64_t h, bool bf16, cudaStream_t stream, int num_sms);
+                             int64_t rows, int64_t h, bool bf16, cudaStream_t stream, int num_sms,
+                             unsigned int* status);
 cudaError_t launch_gather(const void* x_shards, void* x_full, int64_t b, int64_t s, int64_t h, int t, bool bf16,
                           cudaStream_t stream, int num_sms);
 cudaError_t launch_reduce_scatter(const float* partials, void* out_shards, int64_t b, int64_t s, int64_t h, int t,
                                   bool bf16, cudaStream_t stream, int num_sms);
 cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, void* out_shards,
                                     uint32_t* mask_bits, uint64_t threshold, float scale, uint64_t seed, int64_t b,
-                                    int64_t s, int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms);
+                                    int64_t s, int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms,
+                                    unsigned int* status);
 
 }  // namespace tpmlp
