@@ -131,3 +131,45 @@ def sp_block_ranks(x_shards, gamma, beta, eps, A, B, p: float, seed: int, kind: 
         flat = (bi * np.uint64(s) + np.uint64(j * sl) + li) * np.uint64(h) + hi
         out.append(dropout_residual(xs[j], o_shards[j], seed, p, flat))
     return np.stack(out)
+
+
+def layernorm_backward(x, gamma, eps: float, dy):
+    """Gradients of y = LayerNorm(x) * gamma + beta (per row, biased variance) given dy.
+
+    Returns dx, dgamma (summed over rows), dbeta (summed over rows). With g = dy * gamma and
+    x_hat the normalised row, dx = (g - mean(g) - x_hat * mean(g * x_hat)) / sqrt(var + eps):
+    the gradient loses its components along 1 and along x_hat, as the "Megatron 训练" notes
+    describe in their LayerNorm section (the formulas themselves were stripped).
+    """
+    x = np.asarray(x, np.float64)
+    dy = np.asarray(dy, np.float64)
+    mean = x.mean(axis=-1, keepdims=True)
+    var = ((x - mean) ** 2).mean(axis=-1, keepdims=True)
+    rstd = 1.0 / np.sqrt(var + eps)
+    xhat = (x - mean) * rstd
+    g = dy * np.asarray(gamma, np.float64)
+    dx = rstd * (g - g.mean(axis=-1, keepdims=True) - xhat * (g * xhat).mean(axis=-1, keepdims=True))
+    lead = tuple(range(x.ndim - 1))
+    return dx, (dy * xhat).sum(axis=lead), dy.sum(axis=lead)
+
+
+def sp_block_backward(x, gamma, beta, eps, A, B, p: float, seed: int, kind: str, G_out) -> dict[str, np.ndarray]:
+    """Backward of ``sp_block`` on the logical [b, s, h] tensor, from G_out = dl/d out.
+
+    Chain (the SP backward of the "Efficient Large-Scale ... Megatron-LM" notes, section 3.5.1,
+    run per token): the residual passes G_out to x; dropout passes G_out * keep / (1 - p) to
+    the MLP output; the MLP backward gives dA, dB and the gradient at the LayerNorm output;
+    LayerNorm's backward adds its part to dx and gives dgamma, dbeta.
+    """
+    x = np.asarray(x, np.float64)
+    b, s, h = x.shape
+    rows = x.reshape(b * s, h)
+    G = np.asarray(G_out, np.float64).reshape(b * s, h)
+    xn = layernorm(rows, gamma, beta, eps)
+    flat = np.arange(b * s * h, dtype=np.uint64).reshape(b * s, h)
+    keep = ~drop_mask(flat, seed, p)
+    do = np.where(keep, G * (1.0 / (1.0 - p)), 0.0)
+    grads = mlp.backward(xn, A, B, do, kind)
+    dx_ln, dgamma, dbeta = layernorm_backward(rows, gamma, eps, grads["dX"])
+    return {"dx": (G + dx_ln).reshape(b, s, h), "dgamma": dgamma, "dbeta": dbeta, "dA": grads["dA"],
+            "dB": grads["dB"], "do": do.reshape(b, s, h), "dxn": grads["dX"].reshape(b, s, h)}

@@ -285,3 +285,67 @@ def test_shard_layout_roundtrip():
     assert xs.shape == (4, 2, 3, 5)
     assert np.array_equal(xs[2, 1, 0], x[1, 6])
     assert np.array_equal(wl.from_shards(xs), x)
+
+
+# ---------------------------------------------------------------- SP block backward
+
+def _sp_small(seed=30):
+    b, s, h, m = 1, 4, 8, 16
+    x = _rand((b, s, h), seed) * 2.0 + 0.3
+    A, B = _rand((h, m), seed + 1, 0.4), _rand((m, h), seed + 2, 0.4)
+    g, be = 1.0 + 0.2 * _rand(h, seed + 3), 0.2 * _rand(h, seed + 4)
+    G = _rand((b, s, h), seed + 5)
+    return x, g, be, A, B, G
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_sp_backward_matches_finite_differences(kind):
+    x, g, be, A, B, G = _sp_small()
+    p, seed, eps = 0.3, 5, 1e-5
+    grads = sp.sp_block_backward(x, g, be, eps, A, B, p, seed, kind, G)
+    loss = lambda x_, g_, b_, A_, B_: float((sp.sp_block(x_, g_, b_, eps, A_, B_, p, seed, kind)["out"] * G).sum())
+    args = {"x": x, "g": g, "be": be, "A": A, "B": B}
+    keys = {"x": "dx", "g": "dgamma", "be": "dbeta", "A": "dA", "B": "dB"}
+    hstep = 1e-6
+    for name, key in keys.items():
+        arr = args[name]
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            ap, am = dict(args), dict(args)
+            ap[name], am[name] = arr.copy(), arr.copy()
+            ap[name][idx] += hstep
+            am[name][idx] -= hstep
+            fd[idx] = (loss(ap["x"], ap["g"], ap["be"], ap["A"], ap["B"]) -
+                       loss(am["x"], am["g"], am["be"], am["A"], am["B"])) / (2 * hstep)
+        err = np.abs(fd - grads[key]).max() / np.abs(grads[key]).max()
+        assert err < 1e-6, (name, err)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_sp_backward_matches_torch_autograd(kind):
+    x, g, be, A, B, G = _sp_small(40)
+    p, seed, eps = 0.25, 9, 1e-5
+    b, s, h = x.shape
+    keep = ~sp.drop_mask(np.arange(b * s * h, dtype=np.uint64).reshape(b, s, h), seed, p)
+    tx, tg, tb, tA, tB = (torch.tensor(a, requires_grad=True) for a in (x, g, be, A, B))
+    xn = torch.nn.functional.layer_norm(tx, (h,), tg, tb, eps)
+    o = torch.nn.functional.gelu(xn @ tA, approximate="none" if kind == "erf" else "tanh") @ tB
+    out = tx + torch.tensor(keep) * o / (1 - p)
+    out.backward(torch.tensor(G))
+    ref = sp.sp_block_backward(x, g, be, eps, A, B, p, seed, kind, G)
+    for key, t in (("dx", tx), ("dgamma", tg), ("dbeta", tb), ("dA", tA), ("dB", tB)):
+        assert np.abs(ref[key] - t.grad.numpy()).max() < 1e-11, key
+
+
+def test_layernorm_gradient_orthogonal_to_one_and_xhat():
+    # "Megatron 训练" notes, LayerNorm section: g_LN has no component along 1 or x_hat. The
+    # x_hat part is exact for eps = 0; with eps > 0 it is off by the factor eps / (var + eps).
+    x = _rand((16, 64), 50) * 3 + 1
+    dy = _rand((16, 64), 51)
+    for eps in (0.0, 1e-5):
+        dx, _, _ = sp.layernorm_backward(x, np.ones(64), eps, dy)
+        var = x.var(1, keepdims=True)
+        xhat = (x - x.mean(1, keepdims=True)) / np.sqrt(var + eps)
+        assert np.abs(dx.sum(1)).max() < 1e-12
+        bound = 1e-12 + (eps / (var.min() + eps)) * np.abs(dx * xhat).sum(1).max() * 2
+        assert np.abs((dx * xhat).sum(1)).max() < max(bound, 1e-11)
