@@ -301,6 +301,24 @@ def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
         res[f"sp_block_{rs}"] = {"ms": sec * 1e3, "mlp_tflops": cfg.flops_mlp_fwd / sec / 1e12,
                                  "note": "whole block; TFLOP/s counts the MLP's 4*n*h*m only"}
         del ws
+    # backward of the block (activations saved by a forward with Z/Y outputs)
+    Zs = torch.empty((b * s, m), dtype=bf, device=dev)
+    Ys = torch.empty((b * s, m), dtype=bf, device=dev)
+    ws = torch.empty(tp.tpmlp_sp_block_workspace_size(b, s, h, m, t, bf, "fused"), dtype=torch.uint8, device=dev)
+    tp.tpmlp_sp_block(x0, gamma, beta, cfg.eps, A, B, cfg.p_drop, cfg.seed, out, None, t, cfg.gelu, "fused", ws,
+                      stream, Zs, Ys)
+    del ws
+    dout = torch.randn_like(x0)
+    dx = torch.empty_like(x0)
+    dgam = torch.empty(h, dtype=torch.float32, device=dev)
+    dbet = torch.empty(h, dtype=torch.float32, device=dev)
+    dA = torch.empty((h, m), dtype=torch.float32, device=dev)
+    dB = torch.empty((m, h), dtype=torch.float32, device=dev)
+    wsb = torch.empty(tp.tpmlp_sp_block_backward_workspace_size(b, s, h, m, t, bf), dtype=torch.uint8, device=dev)
+    sec = timed(lambda i: tp.tpmlp_sp_block_backward(x0, gamma, beta, cfg.eps, A, B, cfg.p_drop, cfg.seed, Zs, Ys,
+                                                     dout, dx, dgam, dbet, dA, dB, t, cfg.gelu, wsb, stream), 10)
+    res["sp_block_backward"] = {"ms": sec * 1e3, "mlp_tflops": 2 * cfg.flops_mlp_fwd / sec / 1e12,
+                                "note": "whole backward; TFLOP/s counts the four GEMMs' 8*n*h*m only"}
     tp.tpmlp_device_status(stream)
     return {"workload": cfg.name, "l2": f"{sets} rotating buffer sets per kernel (>= 3 x 128 MiB between reuses)",
             "kernels": res}
@@ -417,10 +435,11 @@ def run_ours(args, cfg):
         "fwd_tflops": 4 * n * d * m * args.steps / (fwd_ms / 1e3) / 1e12,
         "bwd_tflops": 8 * n * d * m * args.steps / (bwd_ms / 1e3) / 1e12,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": DOMINANT_KERNEL_TRAFFIC,
+                     "frac": achieved / peak,
+                     "traffic": DOMINANT_KERNEL_TRAFFIC if cfg is wl.LARGE_MLP else None,
                      "kernel": "gemm_bf16_kernel (tcgen05; 6 launches per step, 2*n*d*m FLOP each)",
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
-                     "traffic_profile": DOMINANT_KERNEL_PROFILE},
+                     "traffic_profile": DOMINANT_KERNEL_PROFILE if cfg is wl.LARGE_MLP else None},
         "e2e": {"value": e2e_flops / e2e_elapsed / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": GEMM_LAUNCHES_PER_STEP * args.steps,

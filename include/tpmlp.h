@@ -137,15 +137,40 @@ size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m,
  *   (product in double); kept elements are scaled by 1/(1-p_drop); the residual is x.
  *   mask_bits: NULL, or [ceil(b*s*h/32)] uint32 words; bit i of word w is 1 iff element
  *   32*w+i (global flat index) was dropped. Needs h % 32 == 0.
+ *   Z_save, Y_save: NULL, or [b*s][m] in dt (token order): FC1's pre- and post-GeLU activations,
+ *   kept for tpmlp_sp_block_backward (pass both or neither).
  *   Requires t >= 2 (sequence parallelism needs a tensor-parallel group:
  *   "Megatron-SP 机制", section "工程约束与实测收益是什么？"), s % t == 0, m % t == 0.
  */
 tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const float* beta, float eps,
                             const void* A, const void* B, float p_drop, uint64_t seed,
-                            void* out_shards, uint32_t* mask_bits,
+                            void* out_shards, uint32_t* mask_bits, void* Z_save, void* Y_save,
                             int64_t b, int64_t s, int64_t h, int64_t m, int t,
                             tpmlp_gelu gelu, tpmlp_dtype dt, tpmlp_rs_mode rs,
                             void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace tpmlp_sp_block_backward needs. */
+size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m, int t,
+                                              tpmlp_dtype dt);
+
+/*
+ * Backward of tpmlp_sp_block (the SP backward chain of the "Efficient Large-Scale ... Megatron-LM"
+ * notes, section 3.5.1: local dropout/LayerNorm gradients, all-gather, row-GEMM backward, GeLU
+ * backward, column-GEMM backward, reduce-scatter), from dout_shards = dl/d out_shards:
+ *   dx_shards = dout + LayerNorm'(x)^T (dl/d LN output)        [t][b][s/t][h] in dt
+ *   dgamma, dbeta: [h] fp32 (overwritten)      dA [h][m], dB [m][h]: fp32 (overwritten)
+ * Inputs as for tpmlp_sp_block, plus Z_save and Y_save ([b*s][m] in dt, token order) written by
+ * the forward call with the same arguments. The dropout mask is recomputed from (seed, p_drop).
+ * The LayerNorm output and the gathered tokens are recomputed from x (memory-bound), not saved.
+ * Requires h <= 4096 and h % 8 == 0 in addition to tpmlp_sp_block's rules.
+ */
+tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, const float* beta, float eps,
+                                     const void* A, const void* B, float p_drop, uint64_t seed,
+                                     const void* Z_save, const void* Y_save, const void* dout_shards,
+                                     void* dx_shards, float* dgamma, float* dbeta, float* dA, float* dB,
+                                     int64_t b, int64_t s, int64_t h, int64_t m, int t,
+                                     tpmlp_gelu gelu, tpmlp_dtype dt,
+                                     void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * The sequence-parallel block's memory-bound steps as separate calls, same layouts as above.

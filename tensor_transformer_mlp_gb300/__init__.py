@@ -12,11 +12,14 @@ from ._binding import (  # noqa: F401
     forward,
     load_library,
     sp_block,
+    sp_block_backward,
     tpmlp_backward,
     tpmlp_backward_workspace_size,
     tpmlp_device_status,
     tpmlp_forward,
     tpmlp_sp_block,
+    tpmlp_sp_block_backward,
+    tpmlp_sp_block_backward_workspace_size,
     tpmlp_sp_block_workspace_size,
     tpmlp_sp_dropout_residual,
     tpmlp_sp_gather,

@@ -29,8 +29,11 @@ SIGNATURES = {
     "tpmlp_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_sp_block_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I, _I, _I]),
-    "tpmlp_sp_block": (_I, [_P, _P, _P, _F, _P, _P, _F, _U64, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I, _P, _SZ,
-                            _P]),
+    "tpmlp_sp_block": (_I, [_P, _P, _P, _F, _P, _P, _F, _U64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I,
+                            _P, _SZ, _P]),
+    "tpmlp_sp_block_backward_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I, _I]),
+    "tpmlp_sp_block_backward": (_I, [_P, _P, _P, _F, _P, _P, _F, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                     _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_sp_layernorm": (_I, [_P, _P, _P, _F, _P, _I64, _I64, _I, _P]),
     "tpmlp_sp_gather": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_reduce_scatter": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
@@ -128,7 +131,7 @@ def tpmlp_sp_block_workspace_size(b, s, h, m, t, dtype: torch.dtype, rs: str = "
 
 
 def tpmlp_sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, out_shards, mask_bits, t: int, gelu="tanh",
-                   rs="fused", workspace=None, stream=None) -> None:
+                   rs="fused", workspace=None, stream=None, Z_save=None, Y_save=None) -> None:
     tt, b, sl, h = x_shards.shape
     assert tt == t and out_shards.shape == x_shards.shape
     m = A.shape[1]
@@ -136,11 +139,33 @@ def tpmlp_sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, out_shards, m
     assert gamma.dtype == torch.float32 and beta.dtype == torch.float32
     if mask_bits is not None:
         assert mask_bits.dtype in (torch.int32, torch.uint32) and mask_bits.numel() >= (b * sl * t * h + 31) // 32
-    _cuda(x_shards, gamma, beta, A, B, out_shards, mask_bits, workspace)
+    for sv in (Z_save, Y_save):
+        assert sv is None or sv.shape == (b * sl * t, m)
+    _cuda(x_shards, gamma, beta, A, B, out_shards, mask_bits, workspace, Z_save, Y_save)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().tpmlp_sp_block(_ptr(x_shards), _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), p_drop,
-                                         seed, _ptr(out_shards), _ptr(mask_bits), b, sl * t, h, m, t, GELU[gelu],
-                                         _dt(x_shards), RS_MODE[rs], _ptr(workspace), ws_bytes, _stream(stream)))
+                                         seed, _ptr(out_shards), _ptr(mask_bits), _ptr(Z_save), _ptr(Y_save), b,
+                                         sl * t, h, m, t, GELU[gelu], _dt(x_shards), RS_MODE[rs], _ptr(workspace),
+                                         ws_bytes, _stream(stream)))
+
+
+def tpmlp_sp_block_backward_workspace_size(b, s, h, m, t, dtype: torch.dtype) -> int:
+    return load_library().tpmlp_sp_block_backward_workspace_size(b, s, h, m, t, DTYPE[dtype])
+
+
+def tpmlp_sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z_save, Y_save, dout_shards, dx_shards,
+                            dgamma, dbeta, dA, dB, t: int, gelu="tanh", workspace=None, stream=None) -> None:
+    tt, b, sl, h = x_shards.shape
+    m = A.shape[1]
+    assert tt == t and dout_shards.shape == x_shards.shape and dx_shards.shape == x_shards.shape
+    assert Z_save.shape == (b * sl * t, m) and Y_save.shape == (b * sl * t, m)
+    assert dgamma.shape == (h,) and dbeta.shape == (h,) and dA.shape == (h, m) and dB.shape == (m, h)
+    _cuda(x_shards, gamma, beta, A, B, Z_save, Y_save, dout_shards, dx_shards, dgamma, dbeta, dA, dB, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().tpmlp_sp_block_backward(
+        _ptr(x_shards), _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), p_drop, seed, _ptr(Z_save), _ptr(Y_save),
+        _ptr(dout_shards), _ptr(dx_shards), _ptr(dgamma), _ptr(dbeta), _ptr(dA), _ptr(dB), b, sl * t, h, m, t,
+        GELU[gelu], _dt(x_shards), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def tpmlp_sp_layernorm(x, gamma, beta, eps, y, stream=None) -> None:
@@ -206,12 +231,37 @@ def backward(X, A, B, G, Z, Y, t: int, gelu: str = "tanh", stream=None):
 
 
 def sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, t: int, gelu="tanh", rs="fused", with_mask=True,
-             stream=None):
-    """Allocate outputs and workspace and run tpmlp_sp_block. Returns (out_shards, mask_bits or None)."""
+             save_for_backward=False, stream=None):
+    """Allocate outputs and workspace and run tpmlp_sp_block.
+    Returns (out_shards, mask_bits or None, (Z, Y) or None)."""
     tt, b, sl, h = x_shards.shape
+    n, m = b * sl * t, A.shape[1]
     out = torch.empty_like(x_shards)
-    mask = torch.empty(((b * sl * t * h + 31) // 32,), dtype=torch.int32, device=x_shards.device) if with_mask else None
-    ws = torch.empty(max(1, tpmlp_sp_block_workspace_size(b, sl * t, h, A.shape[1], t, x_shards.dtype, rs)),
+    mask = torch.empty(((n * h + 31) // 32,), dtype=torch.int32, device=x_shards.device) if with_mask else None
+    saves = None
+    if save_for_backward:
+        saves = tuple(torch.empty((n, m), dtype=x_shards.dtype, device=x_shards.device) for _ in range(2))
+    ws = torch.empty(max(1, tpmlp_sp_block_workspace_size(b, sl * t, h, m, t, x_shards.dtype, rs)),
                      dtype=torch.uint8, device=x_shards.device)
-    tpmlp_sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, out, mask, t, gelu, rs, ws, stream)
-    return out, mask
+    tpmlp_sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, out, mask, t, gelu, rs, ws, stream,
+                   *(saves if saves else (None, None)))
+    return out, mask, saves
+
+
+def sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z, Y, dout_shards, t: int, gelu="tanh",
+                      stream=None):
+    """Allocate gradients and workspace and run tpmlp_sp_block_backward.
+    Returns (dx_shards, dgamma, dbeta, dA, dB)."""
+    tt, b, sl, h = x_shards.shape
+    m = A.shape[1]
+    dev = x_shards.device
+    dx = torch.empty_like(x_shards)
+    dgamma = torch.empty(h, dtype=torch.float32, device=dev)
+    dbeta = torch.empty(h, dtype=torch.float32, device=dev)
+    dA = torch.empty((h, m), dtype=torch.float32, device=dev)
+    dB = torch.empty((m, h), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, tpmlp_sp_block_backward_workspace_size(b, sl * t, h, m, t, x_shards.dtype)),
+                     dtype=torch.uint8, device=dev)
+    tpmlp_sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z, Y, dout_shards, dx, dgamma, dbeta, dA,
+                            dB, t, gelu, ws, stream)
+    return dx, dgamma, dbeta, dA, dB

@@ -80,7 +80,8 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
     if constexpr (EPI == kEpiStoreF32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + row * ep.ldo + col);
+      const int64_t prow = remap_row(ep.remap, row);
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + prow * ep.ldo + col);
       dst[0] = make_float4(a[0], a[1], a[2], a[3]);
       dst[1] = make_float4(a[4], a[5], a[6], a[7]);
     } else if constexpr (EPI == kEpiStore) {
@@ -384,6 +385,7 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
   } else if (!a.mn_major && !b.mn_major) {
     if (epi == kEpiDGelu) return launch<false, false, kEpiDGelu>(ta, tb, m, n, k, ep, stream, ctx);
     if (epi == kEpiStore) return launch<false, false, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
+    if (epi == kEpiStoreF32) return launch<false, false, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
   } else if (a.mn_major && b.mn_major) {
     if (epi == kEpiStoreF32) return launch<true, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
   }

@@ -607,6 +607,176 @@ constexpr int kDoStagedThreads = 256, kDoStages = 4;
 
 constexpr size_t kStagedSmemMax = 100 * 1024;  // at least two CTAs per SM
 
+// ------------------------------------------------------------------ SP backward kernels
+// Inverse of shard_row_to_token: token row r = bi*s + j*sl + l -> shard-major row (j*b + bi)*sl + l.
+__device__ __forceinline__ int64_t token_to_shard_row(int64_t r, int64_t b, int64_t s, int64_t sl) {
+  const int64_t bi = r / s;
+  const int64_t si = r - bi * s;
+  const int64_t j = si / sl;
+  return (j * b + bi) * sl + (si - j * sl);
+}
+
+// Dropout backward fused with g-bar's backward (all-gather): token row r of the result is
+// dout[shard row of r] * keep / (1 - p), with the mask recomputed from the hash.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(128) dropout_grad_gather_kernel(const T* __restrict__ dout, T* __restrict__ dtok,
+                                                                  uint64_t threshold, float scale, uint64_t seed,
+                                                                  int64_t rows, int64_t b, int64_t s, int64_t sl,
+                                                                  int h) {
+  const int nvec = h >> 3;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const T* src = dout + token_to_shard_row(r, b, s, sl) * h;
+    T* dst = dtok + r * h;
+    const uint64_t flat_row = static_cast<uint64_t>(r) * static_cast<uint64_t>(h);
+    for (int v0 = 0; v0 < nvec; v0 += blockDim.x * VPT) {
+      Vec8<T> gv[VPT];
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = v0 + j * blockDim.x + threadIdx.x;
+        if (v < nvec) gv[j].load(src + v * 8);
+      }
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = v0 + j * blockDim.x + threadIdx.x;
+        if (v < nvec) {
+          const uint64_t base = seed ^ (flat_row + static_cast<uint64_t>(v) * 8);
+          float gf[8], o[8];
+          gv[j].to_float(gf);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = hash_below(base ^ static_cast<uint64_t>(e), threshold) ? 0.f : gf[e] * scale;
+          Vec8<T> ov;
+          ov.from_float(o);
+          ov.store(dst + v * 8);
+        }
+      }
+    }
+  }
+}
+
+// LayerNorm backward plus the residual, one CTA per row (persistent over rows):
+//   dx = dout + rstd * (g - mean(g) - x_hat * mean(g * x_hat)),  g = dxn * gamma,
+// with the row statistics recomputed from x in one shifted pass and all four row sums
+// (sum d, sum d^2, sum g, sum g*d with d = x - x_0) reduced together. Each thread owns CH
+// vectors of columns and accumulates dgamma (dxn * x_hat) and dbeta (dxn) for them over its
+// CTA's rows in its own columns of a [2][h] shared-memory array (no two threads share a
+// column, so no atomics); the CTA writes them to partials[blockIdx][2][h] for a fixed-order sum.
+constexpr int kLnBwdThreads = 128;
+
+template <typename T, int CH>
+__global__ void __launch_bounds__(kLnBwdThreads)
+    layernorm_backward_kernel(const T* __restrict__ x, const float* __restrict__ dxn, const T* __restrict__ dout,
+                              const float* __restrict__ gamma, float eps, T* __restrict__ dx,
+                              float* __restrict__ partials, int64_t rows, int h) {
+  __shared__ float4 red[2][kLnBwdThreads / 32];
+  extern __shared__ float acc[];  // [2][h]: dgamma then dbeta partial sums
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  float gam[CH][8];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int col = (tid + c * kLnBwdThreads) * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      gam[c][e] = col < h ? gamma[col + e] : 0.f;
+      if (col < h) acc[col + e] = acc[h + col + e] = 0.f;
+    }
+  }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  int p = 0;
+  for (int64_t R = blockIdx.x; R < rows; R += gridDim.x, p ^= 1) {
+    const T* xr = x + R * h;
+    const float* dr = dxn + R * h;
+    const float shift = static_cast<float>(xr[0]);
+    float f[CH][8], dn[CH][8];
+    float s_d = 0.f, s_dd = 0.f, s_g = 0.f, s_gd = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * kLnBwdThreads) * 8;
+      if (col < h) {
+        Vec8<T> xv;
+        xv.load(xr + col);
+        xv.to_float(f[c]);
+        Vec8<float> dv;
+        dv.load(dr + col);
+        dv.to_float(dn[c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = f[c][e] - shift;
+          const float g = dn[c][e] * gam[c][e];
+          s_d += d;
+          s_dd = fmaf(d, d, s_dd);
+          s_g += g;
+          s_gd = fmaf(g, d, s_gd);
+        }
+      }
+    }
+    s_d = warp_sum(s_d);
+    s_dd = warp_sum(s_dd);
+    s_g = warp_sum(s_g);
+    s_gd = warp_sum(s_gd);
+    if (lane == 0) red[p][w] = make_float4(s_d, s_dd, s_g, s_gd);
+    __syncthreads();
+    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kLnBwdThreads / 32; ++k) {
+      const float4 v = red[p][k];
+      t4.x += v.x;
+      t4.y += v.y;
+      t4.z += v.z;
+      t4.w += v.w;
+    }
+    const float md = t4.x * inv_h;
+    const float rstd = rsqrtf(fmaxf(t4.y * inv_h - md * md, 0.f) + eps);
+    const float mean_g = t4.z * inv_h;
+    const float mean_gxh = rstd * (t4.w * inv_h - md * mean_g);  // mean(g * x_hat)
+    const T* gr = dout + R * h;
+    T* outr = dx + R * h;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * kLnBwdThreads) * 8;
+      if (col < h) {
+        Vec8<T> gv;
+        gv.load(gr + col);
+        float go[8], o[8];
+        gv.to_float(go);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xh = (f[c][e] - shift - md) * rstd;
+          const float g = dn[c][e] * gam[c][e];
+          o[e] = go[e] + rstd * (g - mean_g - xh * mean_gxh);
+          acc[col + e] = fmaf(dn[c][e], xh, acc[col + e]);
+          acc[h + col + e] += dn[c][e];
+        }
+        Vec8<T> ov;
+        ov.from_float(o);
+        ov.store(outr + col);
+      }
+    }
+  }
+  float* pg = partials + static_cast<int64_t>(blockIdx.x) * 2 * h;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int col = (tid + c * kLnBwdThreads) * 8;
+    if (col < h) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        pg[col + e] = acc[col + e];
+        pg[h + col + e] = acc[h + col + e];
+      }
+    }
+  }
+}
+
+// dgamma[c] = sum over CTAs of partials[k][0][c], dbeta likewise, in CTA order.
+__global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restrict__ partials, int nparts, int h,
+                                                           float* __restrict__ dgamma, float* __restrict__ dbeta) {
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < 2 * h; c += gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int k = 0; k < nparts; ++k) acc += partials[static_cast<int64_t>(k) * 2 * h + c];
+    if (c < h) dgamma[c] = acc;
+    else dbeta[c - h] = acc;
+  }
+}
+
 int rows_grid(int64_t rows, int num_sms, int per_sm) {
   const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
   return static_cast<int>(rows < cap ? (rows > 0 ? rows : 1) : cap);
@@ -744,6 +914,58 @@ cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, 
                                                                  static_cast<const float*>(y_shards),
                                                                  static_cast<float*>(out_shards), mask_bits, threshold,
                                                                  scale, seed, rows, b, s, s / t, static_cast<int>(h));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint64_t threshold, float scale,
+                                       uint64_t seed, int64_t b, int64_t s, int64_t h, int t, bool bf16,
+                                       cudaStream_t stream, int num_sms) {
+  const int64_t rows = b * s;
+  if (rows <= 0) return cudaSuccess;
+  if (h % 8 != 0) return cudaErrorInvalidValue;
+  const int grid = rows_grid(rows, num_sms, 16);
+  if (bf16)
+    dropout_grad_gather_kernel<__nv_bfloat16, 4><<<grid, 128, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(dout_shards), static_cast<__nv_bfloat16*>(dtok), threshold, scale, seed,
+        rows, b, s, s / t, static_cast<int>(h));
+  else
+    dropout_grad_gather_kernel<float, 4><<<grid, 128, 0, stream>>>(static_cast<const float*>(dout_shards),
+                                                                    static_cast<float*>(dtok), threshold, scale, seed,
+                                                                    rows, b, s, s / t, static_cast<int>(h));
+  return cudaGetLastError();
+}
+
+int layernorm_backward_grid(int64_t rows, int num_sms) {
+  const int g = rows_grid(rows, num_sms, 4);
+  return g < kLnBwdMaxCtas ? g : kLnBwdMaxCtas;
+}
+
+cudaError_t launch_layernorm_backward(const void* x, const float* dxn, const void* dout, const float* gamma, float eps,
+                                      void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
+                                      bool bf16, cudaStream_t stream, int num_sms) {
+  if (rows <= 0) return cudaSuccess;
+  if (h % 8 != 0 || h > kLnBwdThreads * 8 * 4) return cudaErrorInvalidValue;
+  const int grid = layernorm_backward_grid(rows, num_sms);
+  const int ch = static_cast<int>((h / 8 + kLnBwdThreads - 1) / kLnBwdThreads);
+  const size_t acc_bytes = 2 * static_cast<size_t>(h) * sizeof(float);  // <= 32 KiB for h <= 4096
+#define TPMLP_LNB(TYPE, CHN)                                                                                     \
+  layernorm_backward_kernel<TYPE, CHN><<<grid, kLnBwdThreads, acc_bytes, stream>>>(                              \
+      static_cast<const TYPE*>(x), dxn, static_cast<const TYPE*>(dout), gamma, eps, static_cast<TYPE*>(dx), partials, \
+      rows, static_cast<int>(h))
+  if (bf16) {
+    if (ch <= 1) TPMLP_LNB(__nv_bfloat16, 1);
+    else if (ch <= 2) TPMLP_LNB(__nv_bfloat16, 2);
+    else TPMLP_LNB(__nv_bfloat16, 4);
+  } else {
+    if (ch <= 1) TPMLP_LNB(float, 1);
+    else if (ch <= 2) TPMLP_LNB(float, 2);
+    else TPMLP_LNB(float, 4);
+  }
+#undef TPMLP_LNB
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int hb = static_cast<int>((2 * h + 255) / 256);
+  sum_partials_kernel<<<hb, 256, 0, stream>>>(partials, grid, static_cast<int>(h), dgamma, dbeta);
   return cudaGetLastError();
 }
 

@@ -273,8 +273,9 @@ size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m,
 
 tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const float* beta, float eps, const void* A,
                             const void* B, float p_drop, uint64_t seed, void* out_shards, uint32_t* mask_bits,
-                            int64_t b, int64_t s, int64_t h, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt,
-                            tpmlp_rs_mode rs, void* workspace, size_t ws_bytes, void* stream) {
+                            void* Z_save, void* Y_save, int64_t b, int64_t s, int64_t h, int64_t m, int t,
+                            tpmlp_gelu gelu, tpmlp_dtype dt, tpmlp_rs_mode rs, void* workspace, size_t ws_bytes,
+                            void* stream) {
   TPMLP_TRY(check_common(gelu, dt));
   TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
   TPMLP_TRY(check_mlp_shape(b * s, h, m, t, dt));
@@ -286,6 +287,8 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
   if (b * s > 0) TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x_shards, "x_shards"}, {out_shards, "out_shards"}}));
   if (mask_bits && (h % 32 != 0 || !aligned(mask_bits, 4)))
     return fail(TPMLP_ERR_SHAPE, "mask_bits needs h %% 32 == 0 and 4-byte alignment");
+  if ((Z_save == nullptr) != (Y_save == nullptr)) return fail(TPMLP_ERR_INVALID, "pass both Z_save and Y_save, or neither");
+  if (Z_save && b * s > 0) TPMLP_TRY(check_ptrs(dt, {{Z_save, "Z_save"}, {Y_save, "Y_save"}}));
   if (rs == TPMLP_RS_SPLITK && ((m / t) % 8 != 0 && dt == TPMLP_BF16))
     return fail(TPMLP_ERR_SHAPE, "split-K reduce-scatter on bf16 needs m/t to be a multiple of 8");
   const int64_t n = b * s;
@@ -300,7 +303,7 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
   char* ws = static_cast<char*>(workspace);
   void* xn = ws + L.xn;
   void* xg = ws + L.xg;
-  void* Y = ws + L.y;
+  void* Y = Y_save ? Y_save : static_cast<void*>(ws + L.y);
   void* o = ws + L.o;
   const bool bf16 = dt == TPMLP_BF16;
   // LayerNorm on the shards (SP region), then g: all-gather into token order.
@@ -317,7 +320,7 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
     // FC1 + GeLU; then FC2, whose K-loop sums all shards (g-bar's reduction) and whose epilogue
     // writes shard-major rows (g-bar's scatter) after dropout and the residual add.
     TPMLP_CUDA(gemm(dt, n, m, h, Operand{xg, n, h, h, false}, Operand{A, h, m, m, true}, kEpiGelu,
-                    epi(nullptr, Y, nullptr, m, gelu), st, ctx),
+                    epi(Z_save, Y, nullptr, m, gelu), st, ctx),
                "FC1 GEMM");
     EpiParams e2 = epi(out_shards, nullptr, x_shards, h, gelu);
     e2.remap = rm;
@@ -332,10 +335,10 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
   }
   if (rs == TPMLP_RS_FUSED) {
     // FC1 + GeLU, then FC2 whose K-loop sums all shards and whose epilogue writes shard-major rows.
-    TPMLP_TRY(run_forward(xg, A, B, o, nullptr, Y, n, h, m, gelu, dt, &rm, st, ctx));
+    TPMLP_TRY(run_forward(xg, A, B, o, Z_save, Y, n, h, m, gelu, dt, &rm, st, ctx));
   } else {
     TPMLP_CUDA(gemm(dt, n, m, h, Operand{xg, n, h, h, false}, Operand{A, h, m, m, true}, kEpiGelu,
-                    epi(nullptr, Y, nullptr, m, gelu), st, ctx),
+                    epi(Z_save, Y, nullptr, m, gelu), st, ctx),
                "FC1 GEMM");
     // One row GEMM per shard: P_i = Y_i B_i in fp32, then the reduce-scatter kernel.
     const int64_t mt = m / t;
@@ -354,6 +357,93 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
   TPMLP_CUDA(launch_dropout_residual(x_shards, o, out_shards, mask_bits, threshold, scale, seed, b, s, h, t, bf16, st,
                                      ctx.num_sms, ctx.status),
              "dropout+residual");
+  return TPMLP_OK;
+}
+
+size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m, int t, tpmlp_dtype dt) {
+  if (b <= 0 || s <= 0 || h <= 0 || m <= 0 || t <= 0) return 0;
+  const size_t e = elt_size(dt);
+  const size_t tok = static_cast<size_t>(b) * static_cast<size_t>(s);
+  return 3 * round_up(tok * h * e, 256) + round_up(tok * m * e, 256) + round_up(tok * h * sizeof(float), 256) +
+         round_up(static_cast<size_t>(kLnBwdMaxCtas) * 2 * h * sizeof(float), 256);
+}
+
+tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, const float* beta, float eps,
+                                     const void* A, const void* B, float p_drop, uint64_t seed, const void* Z_save,
+                                     const void* Y_save, const void* dout_shards, void* dx_shards, float* dgamma,
+                                     float* dbeta, float* dA, float* dB, int64_t b, int64_t s, int64_t h, int64_t m,
+                                     int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace, size_t ws_bytes,
+                                     void* stream) {
+  TPMLP_TRY(check_common(gelu, dt));
+  TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
+  TPMLP_TRY(check_mlp_shape(b * s, h, m, t, dt));
+  TPMLP_TRY(check_dropout(p_drop));
+  if (h > 4096) return fail(TPMLP_ERR_SHAPE, "sp_block_backward supports h <= 4096 (h=%lld)", (long long)h);
+  if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
+  TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{gamma, "gamma"}, {beta, "beta"}, {dgamma, "dgamma"}, {dbeta, "dbeta"},
+                                    {dA, "dA"}, {dB, "dB"}}));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t n = b * s;
+  if (n > 0) {
+    TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x_shards, "x_shards"}, {dout_shards, "dout_shards"}, {dx_shards, "dx_shards"},
+                                      {Z_save, "Z_save"}, {Y_save, "Y_save"}}));
+    const size_t need = tpmlp_sp_block_backward_workspace_size(b, s, h, m, t, dt);
+    if (!workspace || ws_bytes < need)
+      return fail(TPMLP_ERR_WORKSPACE, "sp_block_backward needs %zu workspace bytes, got %zu", need,
+                  workspace ? ws_bytes : 0);
+    if (!aligned(workspace, 256)) return fail(TPMLP_ERR_ALIGN, "workspace is not 256-byte aligned");
+  }
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  if (n == 0) {
+    TPMLP_CUDA(cudaMemsetAsync(dA, 0, sizeof(float) * h * m, st), "zero dA");
+    TPMLP_CUDA(cudaMemsetAsync(dB, 0, sizeof(float) * m * h, st), "zero dB");
+    TPMLP_CUDA(cudaMemsetAsync(dgamma, 0, sizeof(float) * h, st), "zero dgamma");
+    TPMLP_CUDA(cudaMemsetAsync(dbeta, 0, sizeof(float) * h, st), "zero dbeta");
+    return TPMLP_OK;
+  }
+  const size_t e = elt_size(dt);
+  const size_t tok = static_cast<size_t>(n);
+  char* ws = static_cast<char*>(workspace);
+  void* xn = ws;
+  void* xg = ws + round_up(tok * h * e, 256);
+  void* dtok = ws + 2 * round_up(tok * h * e, 256);
+  void* D = ws + 3 * round_up(tok * h * e, 256);
+  float* dxn = reinterpret_cast<float*>(static_cast<char*>(D) + round_up(tok * m * e, 256));
+  float* partials = reinterpret_cast<float*>(reinterpret_cast<char*>(dxn) + round_up(tok * h * sizeof(float), 256));
+  const bool bf16 = dt == TPMLP_BF16;
+  // Recompute the LayerNorm output in token order (the forward's g), then the local dropout
+  // gradient gathered into token order (g-bar's backward).
+  TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms, ctx.status), "layernorm");
+  TPMLP_CUDA(launch_gather(xn, xg, b, s, h, t, bf16, st, ctx.num_sms), "gather");
+  TPMLP_CUDA(launch_dropout_grad_gather(dout_shards, dtok, drop_threshold(p_drop),
+                                        static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))), seed, b, s, h,
+                                        t, bf16, st, ctx.num_sms),
+             "dropout backward + gather");
+  // Row-GEMM backward with the GeLU' mask, the two weight gradients, column-GEMM backward.
+  TPMLP_CUDA(gemm(dt, n, m, h, Operand{dtok, n, h, h, false}, Operand{B, m, h, h, false}, kEpiDGelu,
+                  epi(D, nullptr, Z_save, m, gelu), st, ctx),
+             "dgrad-1 GEMM");
+  TPMLP_CUDA(gemm(dt, m, h, n, Operand{Y_save, n, m, m, true}, Operand{dtok, n, h, h, true}, kEpiStoreF32,
+                  epi(dB, nullptr, nullptr, h, gelu), st, ctx),
+             "wgrad-2 GEMM");
+  TPMLP_CUDA(gemm(dt, h, m, n, Operand{xg, n, h, h, true}, Operand{D, n, m, m, true}, kEpiStoreF32,
+                  epi(dA, nullptr, nullptr, m, gelu), st, ctx),
+             "wgrad-1 GEMM");
+  // dgrad-2: its K-loop sums every shard's D_i A_i^T and its epilogue writes fp32 rows back in
+  // shard layout (g's backward, the reduce-scatter).
+  EpiParams e5 = epi(dxn, nullptr, nullptr, h, gelu);
+  e5.remap.enabled = 1;
+  e5.remap.b = b;
+  e5.remap.s = s;
+  e5.remap.s_per_shard = s / t;
+  TPMLP_CUDA(gemm(dt, n, h, m, Operand{D, n, m, m, false}, Operand{A, h, m, m, false}, kEpiStoreF32, e5, st, ctx),
+             "dgrad-2 GEMM");
+  // LayerNorm backward on the shards plus the residual path.
+  TPMLP_CUDA(launch_layernorm_backward(x_shards, dxn, dout_shards, gamma, eps, dx_shards, partials, dgamma, dbeta, n,
+                                       h, bf16, st, ctx.num_sms),
+             "layernorm backward");
   return TPMLP_OK;
 }
 

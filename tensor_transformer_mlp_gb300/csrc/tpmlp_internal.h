@@ -92,4 +92,15 @@ cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, 
                                     int64_t s, int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms,
                                     unsigned int* status);
 
+// Sequence-parallel backward: dropout backward fused with the gather into token order; LayerNorm
+// backward plus the residual with per-CTA dgamma/dbeta partials ([grid][2][h] fp32, at most
+// kLnBwdMaxCtas CTAs) summed in CTA order.
+constexpr int kLnBwdMaxCtas = 1024;
+cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint64_t threshold, float scale,
+                                       uint64_t seed, int64_t b, int64_t s, int64_t h, int t, bool bf16,
+                                       cudaStream_t stream, int num_sms);
+cudaError_t launch_layernorm_backward(const void* x, const float* dxn, const void* dout, const float* gamma, float eps,
+                                      void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
+                                      bool bf16, cudaStream_t stream, int num_sms);
+
 }  // namespace tpmlp

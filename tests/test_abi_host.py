@@ -71,8 +71,8 @@ def test_backward_validation(lib):
 
 
 def sp(lib, t=4, s=64, h=256, m=512, p=0.1, mask=FAKE, ws=FAKE, wsb=1 << 30, rs=0, eps=1e-5):
-    return lib.tpmlp_sp_block(FAKE, FAKE, FAKE, eps, FAKE, FAKE, p, 0, FAKE, mask, 2, s, h, m, t, TANH, BF16, rs,
-                              ws, wsb, None)
+    return lib.tpmlp_sp_block(FAKE, FAKE, FAKE, eps, FAKE, FAKE, p, 0, FAKE, mask, None, None, 2, s, h, m, t, TANH,
+                              BF16, rs, ws, wsb, None)
 
 
 def test_sp_block_validation(lib):
@@ -88,6 +88,22 @@ def test_sp_block_validation(lib):
     need = lib.tpmlp_sp_block_workspace_size(2, 64, 256, 512, 4, BF16, 0)
     assert need > 0 and sp(lib, wsb=need - 1) == WORKSPACE
     assert lib.tpmlp_sp_block_workspace_size(2, 64, 256, 512, 4, BF16, 1) > need
+    # only one of the two activation saves
+    assert lib.tpmlp_sp_block(FAKE, FAKE, FAKE, 1e-5, FAKE, FAKE, 0.1, 0, FAKE, FAKE, FAKE, None, 2, 64, 256, 512, 4,
+                              TANH, BF16, 0, FAKE, 1 << 30, None) == INVALID
+
+
+def test_sp_block_backward_validation(lib):
+    def bwd(h=256, t=4, ws=FAKE, wsb=1 << 30, p=0.1, Z=FAKE):
+        return lib.tpmlp_sp_block_backward(FAKE, FAKE, FAKE, 1e-5, FAKE, FAKE, p, 0, Z, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                           FAKE, FAKE, 2, 64, h, 512, t, TANH, BF16, ws, wsb, None)
+    assert bwd(t=1) == SHAPE
+    assert bwd(h=8192) == SHAPE
+    assert bwd(p=1.0) == INVALID
+    assert bwd(Z=None) == INVALID
+    assert bwd(ws=None) == WORKSPACE
+    need = lib.tpmlp_sp_block_backward_workspace_size(2, 64, 256, 512, 4, BF16)
+    assert need > 0 and bwd(wsb=need - 1) == WORKSPACE
 
 
 def test_elementwise_validation(lib):

@@ -24,7 +24,7 @@ def sp_case(cfg, rs, dtype="bf16"):
     A, B = dev(inp["A"], dtype), dev(inp["B"], dtype)
     g = torch.from_numpy(inp["gamma"]).cuda()
     b = torch.from_numpy(inp["beta"]).cuda()
-    out, mask = tp.sp_block(x_d, g, b, cfg.eps, A, B, cfg.p_drop, cfg.seed, cfg.t, cfg.gelu, rs)
+    out, mask, _ = tp.sp_block(x_d, g, b, cfg.eps, A, B, cfg.p_drop, cfg.seed, cfg.t, cfg.gelu, rs)
     torch.cuda.synchronize()
     tp.tpmlp_device_status()
     return inp, out, mask
@@ -156,3 +156,57 @@ def test_dropout_residual(p):
     assert_close("out", wl.from_shards(host(out).reshape(t, b, sl, h)), ref, 8e-3)
     if p == 0.0:
         assert not mask_words(mask).any()
+
+
+# ---------------------------------------------------------------- SP block backward
+
+def sp_backward_case(cfg, dtype="bf16", g_std=1.0):
+    inp = wl.sp_inputs(cfg)
+    t = cfg.t
+    G = np.random.default_rng(cfg.seed + 100).standard_normal(inp["x"].shape) * g_std
+    G = wl.round_to_bf16(G.astype(np.float32)) if dtype == "bf16" else G.astype(np.float32)
+    x_d = dev(wl.to_shards(inp["x"], t), dtype)
+    A, B = dev(inp["A"], dtype), dev(inp["B"], dtype)
+    gam = torch.from_numpy(inp["gamma"]).cuda()
+    bet = torch.from_numpy(inp["beta"]).cuda()
+    out, mask, (Z, Y) = tp.sp_block(x_d, gam, bet, cfg.eps, A, B, cfg.p_drop, cfg.seed, t, cfg.gelu,
+                                    with_mask=cfg.h % 32 == 0, save_for_backward=True)
+    dout = dev(wl.to_shards(G, t), dtype)
+    grads = tp.sp_block_backward(x_d, gam, bet, cfg.eps, A, B, cfg.p_drop, cfg.seed, Z, Y, dout, t, cfg.gelu)
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    return inp, G, out, grads
+
+
+@pytest.mark.parametrize("dtype,tol", [("bf16", TOL_BF16), ("f32", 1e-4)])
+@pytest.mark.parametrize("shape", [(2, 256, 256, 512, 4), (3, 96, 96, 208, 2), (1, 64, 40, 72, 8)])
+def test_sp_block_backward_small(shape, dtype, tol):
+    b, s, h, m, t = shape
+    cfg = wl.SPConfig("sp-bwd", b, s, h, m, t, "tanh", 1.0, 0.05, p_drop=0.2, seed=s + 1, dtype=dtype)
+    inp, G, out, (dx, dgamma, dbeta, dA, dB) = sp_backward_case(cfg, dtype)
+    ref = osp.sp_block_backward(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop,
+                                cfg.seed, cfg.gelu, G)
+    rep = {}
+    assert_close("dx", wl.from_shards(host(dx).reshape(t, b, s // t, h)), ref["dx"], tol, rep)
+    assert_close("dgamma", host(dgamma), ref["dgamma"], tol, rep)
+    assert_close("dbeta", host(dbeta), ref["dbeta"], tol, rep)
+    assert_close("dA", host(dA), ref["dA"], tol, rep)
+    assert_close("dB", host(dB), ref["dB"], tol, rep)
+    print(rep)
+
+
+def test_sp_block_backward_full_size():
+    """SP block backward at the benchmark size against the full float64 oracle (about 5.5 TFLOP
+    of float64 work on the host): dx, dgamma, dbeta, dA, dB element by element."""
+    cfg = wl.SP_BLOCK
+    inp, G, out, (dx, dgamma, dbeta, dA, dB) = sp_backward_case(cfg)
+    b, s, h, t = cfg.b, cfg.s, cfg.h, cfg.t
+    ref = osp.sp_block_backward(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop,
+                                cfg.seed, cfg.gelu, G)
+    rep = {}
+    assert_close("dx", wl.from_shards(host(dx).reshape(t, b, s // t, h)), ref["dx"], TOL_BF16, rep)
+    assert_close("dgamma", host(dgamma), ref["dgamma"], TOL_BF16, rep)
+    assert_close("dbeta", host(dbeta), ref["dbeta"], TOL_BF16, rep)
+    assert_close("dA", host(dA), ref["dA"], TOL_BF16, rep)
+    assert_close("dB", host(dB), ref["dB"], TOL_BF16, rep)
+    print(rep)
