@@ -62,22 +62,35 @@ def gelu_grad(x, kind: str) -> np.ndarray:
     raise ValueError(f"unknown activation {kind!r}")
 
 
-def forward(X, A, B, kind: str) -> dict[str, np.ndarray]:
-    """Unsharded forward: Z = X A, Y = phi(Z), O = Y B (all float64)."""
+def forward(X, A, B, kind: str, b1=None, b2=None) -> dict[str, np.ndarray]:
+    """Unsharded forward: Z = X A (+ b1), Y = phi(Z), O = Y B (+ b2), all float64.
+
+    Biases follow the Megatron layers of the "Megatron 训练" notes: the column-parallel layer's
+    bias b1 [m] is split with A's columns and added before the activation; the row-parallel
+    layer's bias b2 [d] is added once, after the partial products are summed.
+    """
     X, A, B = _f64(X), _f64(A), _f64(B)
     Z = X @ A
+    if b1 is not None:
+        Z = Z + _f64(b1)
     Y = gelu(Z, kind)
     O = Y @ B
+    if b2 is not None:
+        O = O + _f64(b2)
     return {"Z": Z, "Y": Y, "O": O}
 
 
-def backward(X, A, B, G, kind: str) -> dict[str, np.ndarray]:
-    """Unsharded backward from G = dl/dO: D, dA = X^T D, dB = Y^T G, dX = D A^T."""
+def backward(X, A, B, G, kind: str, b1=None) -> dict[str, np.ndarray]:
+    """Unsharded backward from G = dl/dO: D, dA = X^T D, dB = Y^T G, dX = D A^T, and the bias
+    gradients db1 = sum over tokens of D, db2 = sum over tokens of G (the matmul-gradient rule
+    of the "Megatron 训练" notes: a broadcast bias collects the sum of its rows' gradients)."""
     X, A, B, G = _f64(X), _f64(A), _f64(B), _f64(G)
     Z = X @ A
+    if b1 is not None:
+        Z = Z + _f64(b1)
     Y = gelu(Z, kind)
     D = (G @ B.T) * gelu_grad(Z, kind)
-    return {"D": D, "dA": X.T @ D, "dB": Y.T @ G, "dX": D @ A.T}
+    return {"D": D, "dA": X.T @ D, "dB": Y.T @ G, "dX": D @ A.T, "db1": D.sum(axis=0), "db2": G.sum(axis=0)}
 
 
 def shard_views(A, B, t: int):
@@ -93,38 +106,50 @@ def shard_views(A, B, t: int):
     return [(A[:, i * mt:(i + 1) * mt], B[i * mt:(i + 1) * mt, :]) for i in range(t)]
 
 
-def forward_sharded(X, A, B, t: int, kind: str) -> dict[str, np.ndarray]:
-    """Per-shard forward: every shard reads the same X (f is the identity), and
-    O = sum_i Y_i B_i in shard order 0..t-1 (the all-reduce of f-bar).
-    Returns the concatenated Z_i, Y_i and the summed O."""
+def forward_sharded(X, A, B, t: int, kind: str, b1=None, b2=None) -> dict[str, np.ndarray]:
+    """Per-shard forward: every shard reads the same X (f is the identity), shard i adds its
+    slice of b1, and O = sum_i Y_i B_i in shard order 0..t-1 (the all-reduce of f-bar), with b2
+    added once after the sum. Returns the concatenated Z_i, Y_i and the summed O."""
     X = _f64(X)
+    m = _f64(A).shape[1]
+    mt = m // t if t else m
     Zs, Ys, O = [], [], None
-    for Ai, Bi in shard_views(_f64(A), _f64(B), t):
+    for i, (Ai, Bi) in enumerate(shard_views(_f64(A), _f64(B), t)):
         Zi = X @ Ai
+        if b1 is not None:
+            Zi = Zi + _f64(b1)[i * mt:(i + 1) * mt]
         Yi = gelu(Zi, kind)
         Pi = Yi @ Bi
         O = Pi if O is None else O + Pi
         Zs.append(Zi)
         Ys.append(Yi)
+    if b2 is not None:
+        O = O + _f64(b2)
     return {"Z": np.concatenate(Zs, axis=1), "Y": np.concatenate(Ys, axis=1), "O": O}
 
 
-def backward_sharded(X, A, B, G, t: int, kind: str) -> dict[str, np.ndarray]:
-    """Per-shard backward: D_i, dA_i, dB_i are local; dX = sum_i D_i A_i^T is the one
-    reduction the backward needs (the all-reduce in f's backward)."""
+def backward_sharded(X, A, B, G, t: int, kind: str, b1=None) -> dict[str, np.ndarray]:
+    """Per-shard backward: D_i, dA_i, dB_i and db1_i are local; dX = sum_i D_i A_i^T is the one
+    reduction the backward needs (the all-reduce in f's backward); db2 is the same on every
+    shard (G is replicated)."""
     X, G = _f64(X), _f64(G)
-    Ds, dAs, dBs, dX = [], [], [], None
-    for Ai, Bi in shard_views(_f64(A), _f64(B), t):
+    m = _f64(A).shape[1]
+    mt = m // t
+    Ds, dAs, dBs, db1s, dX = [], [], [], [], None
+    for i, (Ai, Bi) in enumerate(shard_views(_f64(A), _f64(B), t)):
         Zi = X @ Ai
+        if b1 is not None:
+            Zi = Zi + _f64(b1)[i * mt:(i + 1) * mt]
         Yi = gelu(Zi, kind)
         Di = (G @ Bi.T) * gelu_grad(Zi, kind)
         Ds.append(Di)
         dAs.append(X.T @ Di)
         dBs.append(Yi.T @ G)
+        db1s.append(Di.sum(axis=0))
         part = Di @ Ai.T
         dX = part if dX is None else dX + part
     return {"D": np.concatenate(Ds, axis=1), "dA": np.concatenate(dAs, axis=1),
-            "dB": np.concatenate(dBs, axis=0), "dX": dX}
+            "dB": np.concatenate(dBs, axis=0), "dX": dX, "db1": np.concatenate(db1s), "db2": G.sum(axis=0)}
 
 
 def forward_input_split(X, A, B, t: int, kind: str) -> np.ndarray:

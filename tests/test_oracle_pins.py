@@ -349,3 +349,36 @@ def test_layernorm_gradient_orthogonal_to_one_and_xhat():
         assert np.abs(dx.sum(1)).max() < 1e-12
         bound = 1e-12 + (eps / (var.min() + eps)) * np.abs(dx * xhat).sum(1).max() * 2
         assert np.abs((dx * xhat).sum(1)).max() < max(bound, 1e-11)
+
+
+# ---------------------------------------------------------------- biases
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_biases_match_torch_autograd(kind):
+    n, d, m = 9, 12, 24
+    X, A, B, G = _rand((n, d), 60), _rand((d, m), 61, 0.3), _rand((m, d), 62, 0.3), _rand((n, d), 63)
+    b1, b2 = _rand(m, 64, 0.5), _rand(d, 65, 0.5)
+    tX, tA, tB, tb1, tb2 = (torch.tensor(a, requires_grad=True) for a in (X, A, B, b1, b2))
+    lin1 = torch.nn.functional.linear(tX, tA.T, tb1)          # torch's [out, in] weight convention
+    O = torch.nn.functional.linear(torch.nn.functional.gelu(lin1, approximate="none" if kind == "erf" else "tanh"),
+                                   tB.T, tb2)
+    O.backward(torch.tensor(G))
+    f = mlp.forward(X, A, B, kind, b1, b2)
+    g = mlp.backward(X, A, B, G, kind, b1)
+    assert np.abs(f["O"] - O.detach().numpy()).max() < 1e-12
+    for key, t in (("dX", tX), ("dA", tA), ("dB", tB), ("db1", tb1), ("db2", tb2)):
+        assert np.abs(g[key] - t.grad.numpy()).max() < 1e-11, key
+
+
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+def test_biased_shard_sum_adds_row_bias_once(t):
+    X, A, B, G = _rand((6, 16), 66), _rand((16, 32), 67, 0.3), _rand((32, 16), 68, 0.3), _rand((6, 16), 69)
+    b1, b2 = _rand(32, 70), _rand(16, 71)
+    ref_f, ref_b = mlp.forward(X, A, B, "tanh", b1, b2), mlp.backward(X, A, B, G, "tanh", b1)
+    sh_f, sh_b = mlp.forward_sharded(X, A, B, t, "tanh", b1, b2), mlp.backward_sharded(X, A, B, G, t, "tanh", b1)
+    assert np.abs(sh_f["O"] - ref_f["O"]).max() < 1e-12
+    for key in ("dX", "dA", "dB", "db1", "db2"):
+        assert np.abs(sh_b[key] - ref_b[key]).max() < 1e-12
+    if t > 1:  # adding b2 in every shard instead of once after the sum is the mistake this rules out
+        wrong = mlp.forward_sharded(X, A, B, t, "tanh", b1, None)["O"] + t * b2
+        assert np.abs(wrong - ref_f["O"]).max() > 0.1
