@@ -122,6 +122,38 @@ tpmlp_status tpmlp_backward_noalloc(const void* X, const void* A, const void* B,
                                     int64_t n, int64_t d, int64_t m, int t,
                                     tpmlp_gelu gelu, tpmlp_dtype dt, void* stream);
 
+/*
+ * The same block with Megatron's biases ("Megatron 训练" notes: ColumnParallelLinear keeps a
+ * bias split like its output columns; RowParallelLinear keeps one full bias, added once after
+ * the all-reduce):
+ *   Z = X A + bias1, Y = gelu(Z), O = Y B + bias2
+ *   bias1 [m], bias2 [d] in dt (16-byte aligned for bf16), both required. Everything else as
+ *   for tpmlp_forward; Z_save then holds the biased pre-activation.
+ */
+tpmlp_status tpmlp_forward_biased(const void* X, const void* A, const void* B,
+                                  const void* bias1, const void* bias2,
+                                  void* O, void* Z_save, void* Y_save,
+                                  int64_t n, int64_t d, int64_t m, int t,
+                                  tpmlp_gelu gelu, tpmlp_dtype dt, void* stream);
+
+/* Bytes of device workspace tpmlp_backward_biased needs: D plus the bias-gradient partial sums. */
+size_t tpmlp_backward_biased_workspace_size(int64_t n, int64_t d, int64_t m, tpmlp_dtype dt);
+
+/*
+ * tpmlp_backward for the biased block, plus the bias gradients (the matmul-gradient rule of the
+ * "Megatron 训练" notes: a broadcast bias collects the sum of its rows' gradients):
+ *   dbias1 = sum over tokens of D   [m] fp32 (overwritten)
+ *   dbias2 = sum over tokens of G   [d] fp32 (overwritten)
+ * Z_save and Y_save come from tpmlp_forward_biased. The sums run in a fixed order
+ * (deterministic). workspace: at least tpmlp_backward_biased_workspace_size(n, d, m, dt) bytes.
+ */
+tpmlp_status tpmlp_backward_biased(const void* X, const void* A, const void* B, const void* G,
+                                   const void* Z_save, const void* Y_save,
+                                   void* dX, float* dA, float* dB, float* dbias1, float* dbias2,
+                                   int64_t n, int64_t d, int64_t m, int t,
+                                   tpmlp_gelu gelu, tpmlp_dtype dt,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
 /* Bytes of device workspace tpmlp_sp_block needs (LN output, gathered tokens, Y, row-GEMM output or partials). */
 size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m, int t,
                                      tpmlp_dtype dt, tpmlp_rs_mode rs);

@@ -14,9 +14,12 @@ from ._binding import (  # noqa: F401
     sp_block,
     sp_block_backward,
     tpmlp_backward,
+    tpmlp_backward_biased,
+    tpmlp_backward_biased_workspace_size,
     tpmlp_backward_workspace_size,
     tpmlp_device_status,
     tpmlp_forward,
+    tpmlp_forward_biased,
     tpmlp_sp_block,
     tpmlp_sp_block_backward,
     tpmlp_sp_block_backward_workspace_size,

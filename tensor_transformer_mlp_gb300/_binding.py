@@ -25,7 +25,11 @@ STATUS = {0: "TPMLP_OK", 1: "TPMLP_ERR_INVALID", 2: "TPMLP_ERR_SHAPE", 3: "TPMLP
 _P, _I64, _I, _F, _U64, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
 SIGNATURES = {
     "tpmlp_forward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
+    "tpmlp_forward_biased": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_backward_workspace_size": (_SZ, [_I64, _I64, _I]),
+    "tpmlp_backward_biased_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "tpmlp_backward_biased": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ,
+                                   _P]),
     "tpmlp_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_sp_block_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I, _I, _I]),
@@ -107,6 +111,37 @@ def tpmlp_forward(X, A, B, O, Z_save, Y_save, t: int, gelu: str = "tanh", stream
     _cuda(X, A, B, O, Z_save, Y_save)
     _check(load_library().tpmlp_forward(_ptr(X), _ptr(A), _ptr(B), _ptr(O), _ptr(Z_save), _ptr(Y_save), n, d, m, t,
                                         GELU[gelu], _dt(X), _stream(stream)))
+
+
+def tpmlp_forward_biased(X, A, B, bias1, bias2, O, Z_save, Y_save, t: int, gelu: str = "tanh", stream=None) -> None:
+    n, d = X.shape
+    m = A.shape[1]
+    assert A.shape == (d, m) and B.shape == (m, d) and O.shape == (n, d) and Y_save.shape == (n, m)
+    assert bias1.shape == (m,) and bias2.shape == (d,) and bias1.dtype == X.dtype and bias2.dtype == X.dtype
+    assert Z_save is None or Z_save.shape == (n, m)
+    _cuda(X, A, B, bias1, bias2, O, Z_save, Y_save)
+    _check(load_library().tpmlp_forward_biased(_ptr(X), _ptr(A), _ptr(B), _ptr(bias1), _ptr(bias2), _ptr(O),
+                                               _ptr(Z_save), _ptr(Y_save), n, d, m, t, GELU[gelu], _dt(X),
+                                               _stream(stream)))
+
+
+def tpmlp_backward_biased_workspace_size(n: int, d: int, m: int, dtype: torch.dtype) -> int:
+    return load_library().tpmlp_backward_biased_workspace_size(n, d, m, DTYPE[dtype])
+
+
+def tpmlp_backward_biased(X, A, B, G, Z_save, Y_save, dX, dA, dB, dbias1, dbias2, t: int, gelu: str = "tanh",
+                          workspace=None, stream=None) -> None:
+    n, d = X.shape
+    m = A.shape[1]
+    assert G.shape == (n, d) and Z_save.shape == (n, m) and Y_save.shape == (n, m) and dX.shape == (n, d)
+    assert dA.shape == (d, m) and dB.shape == (m, d) and dbias1.shape == (m,) and dbias2.shape == (d,)
+    for g_ in (dA, dB, dbias1, dbias2):
+        assert g_.dtype == torch.float32
+    _cuda(X, A, B, G, Z_save, Y_save, dX, dA, dB, dbias1, dbias2, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().tpmlp_backward_biased(_ptr(X), _ptr(A), _ptr(B), _ptr(G), _ptr(Z_save), _ptr(Y_save),
+                                                _ptr(dX), _ptr(dA), _ptr(dB), _ptr(dbias1), _ptr(dbias2), n, d, m, t,
+                                                GELU[gelu], _dt(X), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def tpmlp_backward_workspace_size(n: int, m: int, dtype: torch.dtype) -> int:
@@ -208,23 +243,35 @@ def tpmlp_device_status(stream=None, clear: bool = True) -> None:
 
 # ----------------------------------------------------------------------- conveniences
 
-def forward(X, A, B, t: int, gelu: str = "tanh", save_z: bool = True, stream=None):
-    """Allocate O, Z, Y with torch and run tpmlp_forward. Returns (O, Z, Y)."""
+def forward(X, A, B, t: int, gelu: str = "tanh", save_z: bool = True, stream=None, bias1=None, bias2=None):
+    """Allocate O, Z, Y with torch and run tpmlp_forward (tpmlp_forward_biased when biases are
+    given). Returns (O, Z, Y)."""
     n, m = X.shape[0], A.shape[1]
     O = torch.empty_like(X)
     Z = torch.empty((n, m), dtype=X.dtype, device=X.device) if save_z else None
     Y = torch.empty((n, m), dtype=X.dtype, device=X.device)
-    tpmlp_forward(X, A, B, O, Z, Y, t, gelu, stream)
+    if bias1 is not None or bias2 is not None:
+        tpmlp_forward_biased(X, A, B, bias1, bias2, O, Z, Y, t, gelu, stream)
+    else:
+        tpmlp_forward(X, A, B, O, Z, Y, t, gelu, stream)
     return O, Z, Y
 
 
-def backward(X, A, B, G, Z, Y, t: int, gelu: str = "tanh", stream=None):
-    """Allocate dX, dA, dB and the workspace with torch and run tpmlp_backward. Returns (dX, dA, dB)."""
+def backward(X, A, B, G, Z, Y, t: int, gelu: str = "tanh", stream=None, with_bias: bool = False):
+    """Allocate gradients and the workspace with torch and run tpmlp_backward (or, with_bias,
+    tpmlp_backward_biased). Returns (dX, dA, dB) or (dX, dA, dB, dbias1, dbias2)."""
     n, d = X.shape
     m = A.shape[1]
     dX = torch.empty_like(X)
     dA = torch.empty((d, m), dtype=torch.float32, device=X.device)
     dB = torch.empty((m, d), dtype=torch.float32, device=X.device)
+    if with_bias:
+        db1 = torch.empty(m, dtype=torch.float32, device=X.device)
+        db2 = torch.empty(d, dtype=torch.float32, device=X.device)
+        ws = torch.empty(max(1, tpmlp_backward_biased_workspace_size(n, d, m, X.dtype)), dtype=torch.uint8,
+                         device=X.device)
+        tpmlp_backward_biased(X, A, B, G, Z, Y, dX, dA, dB, db1, db2, t, gelu, ws, stream)
+        return dX, dA, dB, db1, db2
     ws = torch.empty(max(1, tpmlp_backward_workspace_size(n, m, X.dtype)), dtype=torch.uint8, device=X.device)
     tpmlp_backward(X, A, B, G, Z, Y, dX, dA, dB, t, gelu, ws, stream)
     return dX, dA, dB

@@ -22,6 +22,9 @@ __device__ __forceinline__ int64_t remap_row_f(const RowRemap& rm, int64_t r) {
 template <int EPI>
 __device__ __forceinline__ void epilogue_elem(const EpiParams& ep, int64_t r, int64_t c, float acc) {
   float* out = static_cast<float*>(ep.out);
+  if constexpr (EPI == kEpiStore || EPI == kEpiGelu) {
+    if (ep.bias) acc += static_cast<const float*>(ep.bias)[c];
+  }
   if constexpr (EPI == kEpiStore || EPI == kEpiStoreF32) {
     out[remap_row_f(ep.remap, r) * ep.ldo + c] = acc;
   } else if constexpr (EPI == kEpiGelu) {

@@ -79,6 +79,18 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
     float a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
+    if constexpr (EPI == kEpiGelu || EPI == kEpiStore) {
+      if (ep.bias) {  // per-column bias (bf16), uniform across the warp
+        const uint4 bv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.bias) + col);
+        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 bf = unpack_bf16x2(bw[i]);
+          a[2 * i] += bf.x;
+          a[2 * i + 1] += bf.y;
+        }
+      }
+    }
     if constexpr (EPI == kEpiStoreF32) {
       const int64_t prow = remap_row(ep.remap, row);
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + prow * ep.ldo + col);

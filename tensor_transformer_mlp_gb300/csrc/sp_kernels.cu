@@ -777,6 +777,45 @@ __global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restri
   }
 }
 
+// ------------------------------------------------------------------ column sums (bias gradients)
+// Pass 1: CTA (x, y) sums rows [y*kColSumRows, (y+1)*kColSumRows) of 8 columns per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_partial_kernel(const T* __restrict__ M, int64_t rows, int cols,
+                                                             float* __restrict__ partials) {
+  const int64_t cg = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int c0 = static_cast<int>(cg * 8);
+  if (c0 >= cols) return;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColSumRows;
+  const int64_t r1 = r0 + kColSumRows < rows ? r0 + kColSumRows : rows;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (c0 + 8 <= cols && (cols % 8) == 0) {
+#pragma unroll 4
+    for (int64_t r = r0; r < r1; ++r) {
+      Vec8<T> v;
+      v.load(M + r * cols + c0);
+      float f[8];
+      v.to_float(f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += f[e];
+    }
+  } else {
+    for (int64_t r = r0; r < r1; ++r)
+      for (int e = 0; e < 8 && c0 + e < cols; ++e) acc[e] += static_cast<float>(M[r * cols + c0 + e]);
+  }
+  float* pr = partials + static_cast<int64_t>(blockIdx.y) * cols;
+  for (int e = 0; e < 8 && c0 + e < cols; ++e) pr[c0 + e] = acc[e];
+}
+
+// Pass 2: out[c] = sum of partials[k][c] over chunks k in order.
+__global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restrict__ partials, int chunks, int cols,
+                                                           float* __restrict__ out) {
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int k = 0; k < chunks; ++k) acc += partials[static_cast<int64_t>(k) * cols + c];
+    out[c] = acc;
+  }
+}
+
 int rows_grid(int64_t rows, int num_sms, int per_sm) {
   const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
   return static_cast<int>(rows < cap ? (rows > 0 ? rows : 1) : cap);
@@ -932,6 +971,26 @@ cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint
     dropout_grad_gather_kernel<float, 4><<<grid, 128, 0, stream>>>(static_cast<const float*>(dout_shards),
                                                                     static_cast<float*>(dtok), threshold, scale, seed,
                                                                     rows, b, s, s / t, static_cast<int>(h));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_column_sums(const void* M, int64_t rows, int64_t cols, bool bf16, float* partials, float* out,
+                               cudaStream_t stream) {
+  if (cols <= 0) return cudaSuccess;
+  if (rows <= 0) return cudaMemsetAsync(out, 0, sizeof(float) * cols, stream);
+  const int64_t chunks = (rows + kColSumRows - 1) / kColSumRows;
+  if (chunks > 65535 || cols > INT32_MAX) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>((cols / 8 + 1 + 255) / 256), static_cast<unsigned>(chunks));
+  if (bf16)
+    colsum_partial_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(M), rows,
+                                                                    static_cast<int>(cols), partials);
+  else
+    colsum_partial_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(M), rows,
+                                                            static_cast<int>(cols), partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  colsum_final_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(
+      partials, static_cast<int>(chunks), static_cast<int>(cols), out);
   return cudaGetLastError();
 }
 

@@ -128,6 +128,7 @@ EpiParams epi(void* out, void* out2, const void* aux, int64_t ldo, tpmlp_gelu g)
   e.out = out;
   e.out2 = out2;
   e.aux = aux;
+  e.bias = nullptr;
   e.ldo = ldo;
   e.gelu = g == TPMLP_GELU_ERF ? kGeluErf : kGeluTanh;
   e.remap.enabled = 0;
@@ -139,58 +140,71 @@ EpiParams epi(void* out, void* out2, const void* aux, int64_t ldo, tpmlp_gelu g)
   return e;
 }
 
-// Forward GEMMs shared by tpmlp_forward and the sequence-parallel block.
+// Forward GEMMs shared by tpmlp_forward(_biased) and the sequence-parallel block. bias1 [m] is
+// the column-parallel layer's bias (each shard's slice is its column range), added before the
+// GeLU; bias2 [d] the row-parallel layer's, added once after the shard sum.
 tpmlp_status run_forward(const void* X, const void* A, const void* B, void* O, void* Z, void* Y, int64_t n, int64_t d,
                          int64_t m, tpmlp_gelu g, tpmlp_dtype dt, const RowRemap* remap, cudaStream_t s,
-                         const DeviceCtx& ctx) {
-  // FC1 (column-parallel, all shards at once): Z = X A, Y = gelu(Z).
-  TPMLP_CUDA(gemm(dt, n, m, d, Operand{X, n, d, d, false}, Operand{A, d, m, m, true}, kEpiGelu,
-                  epi(Z, Y, nullptr, m, g), s, ctx),
+                         const DeviceCtx& ctx, const void* bias1 = nullptr, const void* bias2 = nullptr) {
+  // FC1 (column-parallel, all shards at once): Z = X A (+ b1), Y = gelu(Z).
+  EpiParams e1 = epi(Z, Y, nullptr, m, g);
+  e1.bias = bias1;
+  TPMLP_CUDA(gemm(dt, n, m, d, Operand{X, n, d, d, false}, Operand{A, d, m, m, true}, kEpiGelu, e1, s, ctx),
              "FC1 GEMM");
-  // FC2 (row-parallel): O = Y B; the K-loop runs over every shard, which is the f-bar sum.
+  // FC2 (row-parallel): O = Y B (+ b2); the K-loop runs over every shard, which is the f-bar sum.
   EpiParams e2 = epi(O, nullptr, nullptr, d, g);
+  e2.bias = bias2;
   if (remap) e2.remap = *remap;
   TPMLP_CUDA(gemm(dt, n, d, m, Operand{Y, n, m, m, false}, Operand{B, m, d, d, true}, kEpiStore, e2, s, ctx),
              "FC2 GEMM");
   return TPMLP_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* tpmlp_last_error(void) { return g_last_error; }
-
-tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, void* O, void* Z_save, void* Y_save, int64_t n,
-                           int64_t d, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* stream) {
+tpmlp_status forward_impl(const void* X, const void* A, const void* B, const void* bias1, const void* bias2, void* O,
+                          void* Z_save, void* Y_save, int64_t n, int64_t d, int64_t m, int t, tpmlp_gelu gelu,
+                          tpmlp_dtype dt, void* stream) {
   TPMLP_TRY(check_common(gelu, dt));
   TPMLP_TRY(check_mlp_shape(n, d, m, t, dt));
   TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
+  if (bias1 && !aligned(bias1, dt == TPMLP_BF16 ? 16 : 4)) return fail(TPMLP_ERR_ALIGN, "bias1 is misaligned");
+  if (bias2 && !aligned(bias2, dt == TPMLP_BF16 ? 16 : 4)) return fail(TPMLP_ERR_ALIGN, "bias2 is misaligned");
   if (n == 0) return TPMLP_OK;  // token-sized buffers may be NULL when there are no tokens
   TPMLP_TRY(check_ptrs(dt, {{X, "X"}, {O, "O"}, {Y_save, "Y_save"}}));
   if (Z_save && !aligned(Z_save, dt == TPMLP_BF16 ? 16 : 4)) return fail(TPMLP_ERR_ALIGN, "Z_save is misaligned");
   DeviceCtx ctx;
   TPMLP_CUDA(get_device_ctx(&ctx), "device context");
-  return run_forward(X, A, B, O, Z_save, Y_save, n, d, m, gelu, dt, nullptr, static_cast<cudaStream_t>(stream), ctx);
+  return run_forward(X, A, B, O, Z_save, Y_save, n, d, m, gelu, dt, nullptr, static_cast<cudaStream_t>(stream), ctx,
+                     bias1, bias2);
 }
 
-size_t tpmlp_backward_workspace_size(int64_t n, int64_t m, tpmlp_dtype dt) {
+size_t d_bytes(int64_t n, int64_t m, tpmlp_dtype dt) {
   if (n <= 0 || m <= 0) return 0;
   return round_up(static_cast<size_t>(n) * static_cast<size_t>(m) * elt_size(dt), 256);
 }
 
-tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
-                            const void* Y_save, void* dX, float* dA, float* dB, int64_t n, int64_t d, int64_t m, int t,
-                            tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
+size_t colsum_bytes(int64_t n, int64_t d, int64_t m) {
+  if (n <= 0) return 0;
+  return round_up(colsum_partials_floats(n, m > d ? m : d) * sizeof(float), 256);
+}
+
+// Backward GEMMs; with dbias1/dbias2 non-null also the bias gradients (column sums of D and G),
+// whose partial sums use the workspace after D.
+tpmlp_status backward_impl(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
+                           const void* Y_save, void* dX, float* dA, float* dB, float* dbias1, float* dbias2, int64_t n,
+                           int64_t d, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace,
+                           size_t ws_bytes, void* stream) {
   TPMLP_TRY(check_common(gelu, dt));
   TPMLP_TRY(check_mlp_shape(n, d, m, t, dt));
   TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
   TPMLP_TRY(check_ptrs(dt, {{dA, "dA"}, {dB, "dB"}}));
+  const bool biases = dbias1 != nullptr || dbias2 != nullptr;
+  if (biases && !(dbias1 && dbias2)) return fail(TPMLP_ERR_INVALID, "pass both dbias1 and dbias2");
+  if (biases) TPMLP_TRY(check_ptrs(TPMLP_F32, {{dbias1, "dbias1"}, {dbias2, "dbias2"}}));
   if (n > 0)  // token-sized buffers may be NULL when there are no tokens
     TPMLP_TRY(check_ptrs(dt, {{X, "X"}, {G, "G"}, {Z_save, "Z_save"}, {Y_save, "Y_save"}, {dX, "dX"}}));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n > 0) {
-    const size_t need = tpmlp_backward_workspace_size(n, m, dt);
+    const size_t need = d_bytes(n, m, dt) + (biases ? colsum_bytes(n, d, m) : 0);
     if (!workspace || ws_bytes < need)
       return fail(TPMLP_ERR_WORKSPACE, "backward needs %zu workspace bytes, got %zu", need, workspace ? ws_bytes : 0);
     if (!aligned(workspace, 256)) return fail(TPMLP_ERR_ALIGN, "workspace is not 256-byte aligned");
@@ -200,6 +214,10 @@ tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const v
   if (n == 0) {
     TPMLP_CUDA(cudaMemsetAsync(dA, 0, sizeof(float) * d * m, s), "zero dA");
     TPMLP_CUDA(cudaMemsetAsync(dB, 0, sizeof(float) * m * d, s), "zero dB");
+    if (biases) {
+      TPMLP_CUDA(cudaMemsetAsync(dbias1, 0, sizeof(float) * m, s), "zero dbias1");
+      TPMLP_CUDA(cudaMemsetAsync(dbias2, 0, sizeof(float) * d, s), "zero dbias2");
+    }
     return TPMLP_OK;
   }
   void* D = workspace;
@@ -219,7 +237,54 @@ tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const v
   TPMLP_CUDA(gemm(dt, n, d, m, Operand{D, n, m, m, false}, Operand{A, d, m, m, false}, kEpiStore,
                   epi(dX, nullptr, nullptr, d, gelu), s, ctx),
              "dgrad-2 GEMM");
+  if (biases) {
+    // A broadcast bias collects the sum of its rows' gradients: db1 = 1^T D, db2 = 1^T G.
+    float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + d_bytes(n, m, dt));
+    const bool bf16 = dt == TPMLP_BF16;
+    TPMLP_CUDA(launch_column_sums(D, n, m, bf16, partials, dbias1, s), "dbias1 column sums");
+    TPMLP_CUDA(launch_column_sums(G, n, d, bf16, partials, dbias2, s), "dbias2 column sums");
+  }
   return TPMLP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tpmlp_last_error(void) { return g_last_error; }
+
+tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, void* O, void* Z_save, void* Y_save, int64_t n,
+                           int64_t d, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* stream) {
+  return forward_impl(X, A, B, nullptr, nullptr, O, Z_save, Y_save, n, d, m, t, gelu, dt, stream);
+}
+
+tpmlp_status tpmlp_forward_biased(const void* X, const void* A, const void* B, const void* bias1, const void* bias2,
+                                  void* O, void* Z_save, void* Y_save, int64_t n, int64_t d, int64_t m, int t,
+                                  tpmlp_gelu gelu, tpmlp_dtype dt, void* stream) {
+  if (!bias1 || !bias2) return fail(TPMLP_ERR_INVALID, "bias1 and bias2 must not be NULL");
+  return forward_impl(X, A, B, bias1, bias2, O, Z_save, Y_save, n, d, m, t, gelu, dt, stream);
+}
+
+size_t tpmlp_backward_workspace_size(int64_t n, int64_t m, tpmlp_dtype dt) { return d_bytes(n, m, dt); }
+
+tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
+                            const void* Y_save, void* dX, float* dA, float* dB, int64_t n, int64_t d, int64_t m, int t,
+                            tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
+  return backward_impl(X, A, B, G, Z_save, Y_save, dX, dA, dB, nullptr, nullptr, n, d, m, t, gelu, dt, workspace,
+                       ws_bytes, stream);
+}
+
+size_t tpmlp_backward_biased_workspace_size(int64_t n, int64_t d, int64_t m, tpmlp_dtype dt) {
+  return d_bytes(n, m, dt) + colsum_bytes(n, d, m);
+}
+
+tpmlp_status tpmlp_backward_biased(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
+                                   const void* Y_save, void* dX, float* dA, float* dB, float* dbias1, float* dbias2,
+                                   int64_t n, int64_t d, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+  if (!dbias1 || !dbias2) return fail(TPMLP_ERR_INVALID, "dbias1 and dbias2 must not be NULL");
+  return backward_impl(X, A, B, G, Z_save, Y_save, dX, dA, dB, dbias1, dbias2, n, d, m, t, gelu, dt, workspace,
+                       ws_bytes, stream);
 }
 
 namespace {

@@ -44,6 +44,7 @@ struct EpiParams {
   void* out;
   void* out2;
   const void* aux;
+  const void* bias;  // kEpiGelu, kEpiStore: per-column bias added to the accumulator (operand dtype), or null
   int64_t ldo;  // row stride of out/out2/aux, elements
   int gelu;
   RowRemap remap;
@@ -91,6 +92,16 @@ cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, 
                                     uint32_t* mask_bits, uint64_t threshold, float scale, uint64_t seed, int64_t b,
                                     int64_t s, int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms,
                                     unsigned int* status);
+
+// Column sums of a row-major [rows][cols] matrix into fp32 out[cols], in a fixed order:
+// CTAs sum chunks of kColSumRows rows into partials[chunk][cols], then partials are added in
+// chunk order. `partials` needs colsum_partials_floats(rows, cols) floats.
+constexpr int kColSumRows = 256;
+inline size_t colsum_partials_floats(int64_t rows, int64_t cols) {
+  return static_cast<size_t>((rows + kColSumRows - 1) / kColSumRows) * static_cast<size_t>(cols);
+}
+cudaError_t launch_column_sums(const void* M, int64_t rows, int64_t cols, bool bf16, float* partials, float* out,
+                               cudaStream_t stream);
 
 // Sequence-parallel backward: dropout backward fused with the gather into token order; LayerNorm
 // backward plus the residual with per-CTA dgamma/dbeta partials ([grid][2][h] fp32, at most

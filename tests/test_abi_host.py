@@ -58,6 +58,18 @@ def test_forward_validation(lib):
     assert fwd(lib, n=0) == OK                     # nothing to do, nothing launched
 
 
+def test_biased_validation(lib):
+    base = [FAKE] * 3
+    assert lib.tpmlp_forward_biased(*base, None, FAKE, *([FAKE] * 3), 8, 64, 64, 2, TANH, BF16, None) == INVALID
+    assert lib.tpmlp_forward_biased(*base, FAKE + 8, FAKE, *([FAKE] * 3), 8, 64, 64, 2, TANH, BF16, None) == ALIGN
+    args = [FAKE] * 9
+    assert lib.tpmlp_backward_biased(*args, None, FAKE, 8, 64, 64, 2, TANH, BF16, FAKE, 1 << 30, None) == INVALID
+    need = lib.tpmlp_backward_biased_workspace_size(1000, 64, 128, BF16)
+    assert need > lib.tpmlp_backward_workspace_size(1000, 128, BF16)
+    assert lib.tpmlp_backward_biased(*args, FAKE, FAKE, 1000, 64, 128, 2, TANH, BF16, FAKE, need - 1,
+                                     None) == WORKSPACE
+
+
 def test_backward_validation(lib):
     args = [FAKE] * 9 + [256, 512, 1024, 2, TANH, BF16]
     assert lib.tpmlp_backward(*args, None, 0, None) == WORKSPACE

@@ -140,3 +140,27 @@ def test_gpt_mlp_sampled():
 
 def test_large_mlp_sampled():
     sampled_parity(wl.LARGE_MLP)
+
+
+@pytest.mark.parametrize("dtype,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+@pytest.mark.parametrize("shape", [(512, 1024, 4096, 2), (300, 200, 392, 7), (37, 48, 72, 3)])
+def test_biased_block(shape, dtype, tol):
+    n, d, m, t = shape
+    cfg = wl.MLPConfig("biased", n, d, m, t, dtype, "tanh", 1.0, 0.05, 1.0, seed=n + 7)
+    inp = wl.mlp_inputs(cfg)
+    rng = np.random.default_rng(n)
+    b1 = (rng.standard_normal(m) * 0.5).astype(np.float32)
+    b2 = (rng.standard_normal(d) * 0.5).astype(np.float32)
+    if dtype == "bf16":
+        b1, b2 = wl.round_to_bf16(b1), wl.round_to_bf16(b2)
+    X, A, B, G = (dev(inp[k], dtype) for k in "XABG")
+    O, Z, Y = tp.forward(X, A, B, t, "tanh", bias1=dev(b1, dtype), bias2=dev(b2, dtype))
+    dX, dA, dB, db1, db2 = tp.backward(X, A, B, G, Z, Y, t, "tanh", with_bias=True)
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    ref = omlp.forward(inp["X"], inp["A"], inp["B"], "tanh", b1, b2)
+    ref.update(omlp.backward(inp["X"], inp["A"], inp["B"], inp["G"], "tanh", b1))
+    rep = {}
+    for k, got in (("Z", Z), ("O", O), ("dX", dX), ("dA", dA), ("dB", dB), ("db1", db1), ("db2", db2)):
+        assert_close(k, host(got), ref[k], tol, rep)
+    print(rep)
