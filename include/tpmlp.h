@@ -123,6 +123,20 @@ tpmlp_status tpmlp_backward_noalloc(const void* X, const void* A, const void* B,
                                     tpmlp_gelu gelu, tpmlp_dtype dt, void* stream);
 
 /*
+ * tpmlp_backward with fp32 gradient accumulation for dA and dB: dA += X^T D, dB += Y^T G, added
+ * by the weight-gradient GEMMs' epilogues into the caller's fp32 buffers (Megatron keeps fp32
+ * main_grad buffers and fuses the accumulation into the wgrad GEMM: "Megatron 训练" notes,
+ * gradient_accumulation_fusion and the mixed-precision section). dX is overwritten as in
+ * tpmlp_backward; workspace as for tpmlp_backward. n == 0 leaves dA and dB unchanged.
+ */
+tpmlp_status tpmlp_backward_accumulate(const void* X, const void* A, const void* B, const void* G,
+                                       const void* Z_save, const void* Y_save,
+                                       void* dX, float* dA, float* dB,
+                                       int64_t n, int64_t d, int64_t m, int t,
+                                       tpmlp_gelu gelu, tpmlp_dtype dt,
+                                       void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * The same block with Megatron's biases ("Megatron 训练" notes: ColumnParallelLinear keeps a
  * bias split like its output columns; RowParallelLinear keeps one full bias, added once after
  * the all-reduce):

@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     sp_block,
     sp_block_backward,
     tpmlp_backward,
+    tpmlp_backward_accumulate,
     tpmlp_backward_biased,
     tpmlp_backward_biased_workspace_size,
     tpmlp_backward_workspace_size,

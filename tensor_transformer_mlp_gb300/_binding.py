@@ -27,6 +27,7 @@ SIGNATURES = {
     "tpmlp_forward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_forward_biased": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_backward_workspace_size": (_SZ, [_I64, _I64, _I]),
+    "tpmlp_backward_accumulate": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_backward_biased_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
     "tpmlp_backward_biased": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ,
                                    _P]),
@@ -123,6 +124,20 @@ def tpmlp_forward_biased(X, A, B, bias1, bias2, O, Z_save, Y_save, t: int, gelu:
     _check(load_library().tpmlp_forward_biased(_ptr(X), _ptr(A), _ptr(B), _ptr(bias1), _ptr(bias2), _ptr(O),
                                                _ptr(Z_save), _ptr(Y_save), n, d, m, t, GELU[gelu], _dt(X),
                                                _stream(stream)))
+
+
+def tpmlp_backward_accumulate(X, A, B, G, Z_save, Y_save, dX, dA, dB, t: int, gelu: str = "tanh", workspace=None,
+                              stream=None) -> None:
+    """tpmlp_backward, but dA += X^T D and dB += Y^T G into the given fp32 buffers."""
+    n, d = X.shape
+    m = A.shape[1]
+    assert G.shape == (n, d) and Z_save.shape == (n, m) and Y_save.shape == (n, m) and dX.shape == (n, d)
+    assert dA.shape == (d, m) and dB.shape == (m, d) and dA.dtype == torch.float32 and dB.dtype == torch.float32
+    _cuda(X, A, B, G, Z_save, Y_save, dX, dA, dB, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().tpmlp_backward_accumulate(_ptr(X), _ptr(A), _ptr(B), _ptr(G), _ptr(Z_save), _ptr(Y_save),
+                                                    _ptr(dX), _ptr(dA), _ptr(dB), n, d, m, t, GELU[gelu], _dt(X),
+                                                    _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def tpmlp_backward_biased_workspace_size(n: int, d: int, m: int, dtype: torch.dtype) -> int:

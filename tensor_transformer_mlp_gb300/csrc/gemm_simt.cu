@@ -30,6 +30,8 @@ __device__ __forceinline__ void epilogue_elem(const EpiParams& ep, int64_t r, in
   } else if constexpr (EPI == kEpiGelu) {
     if (out) out[r * ep.ldo + c] = acc;
     static_cast<float*>(ep.out2)[r * ep.ldo + c] = gelu_f<true>(acc, ep.gelu);
+  } else if constexpr (EPI == kEpiAccumF32) {
+    out[r * ep.ldo + c] += acc;
   } else if constexpr (EPI == kEpiDGelu) {
     const float z = static_cast<const float*>(ep.aux)[r * ep.ldo + c];
     out[r * ep.ldo + c] = acc * gelu_grad_f<true>(z, ep.gelu);
@@ -114,6 +116,7 @@ cudaError_t gemm_f32_simt(int64_t M, int64_t N, int64_t K, const Operand& a, con
     case kEpiStoreF32: return launch_f32<kEpiStoreF32>(A, sam, sak, B, sbk, sbn, M, N, K, ep, stream);
     case kEpiGelu: return launch_f32<kEpiGelu>(A, sam, sak, B, sbk, sbn, M, N, K, ep, stream);
     case kEpiDGelu: return launch_f32<kEpiDGelu>(A, sam, sak, B, sbk, sbn, M, N, K, ep, stream);
+    case kEpiAccumF32: return launch_f32<kEpiAccumF32>(A, sam, sak, B, sbk, sbn, M, N, K, ep, stream);
   }
   return cudaErrorNotSupported;
 }

@@ -96,6 +96,11 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + prow * ep.ldo + col);
       dst[0] = make_float4(a[0], a[1], a[2], a[3]);
       dst[1] = make_float4(a[4], a[5], a[6], a[7]);
+    } else if constexpr (EPI == kEpiAccumF32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + row * ep.ldo + col);
+      const float4 o0 = dst[0], o1 = dst[1];
+      dst[0] = make_float4(o0.x + a[0], o0.y + a[1], o0.z + a[2], o0.w + a[3]);
+      dst[1] = make_float4(o1.x + a[4], o1.y + a[5], o1.z + a[6], o1.w + a[7]);
     } else if constexpr (EPI == kEpiStore) {
       const int64_t prow = remap_row(ep.remap, row);
       uint4 pk = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
@@ -400,6 +405,7 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
     if (epi == kEpiStoreF32) return launch<false, false, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
   } else if (a.mn_major && b.mn_major) {
     if (epi == kEpiStoreF32) return launch<true, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
+    if (epi == kEpiAccumF32) return launch<true, true, kEpiAccumF32>(ta, tb, m, n, k, ep, stream, ctx);
   }
   return cudaErrorNotSupported;
 }

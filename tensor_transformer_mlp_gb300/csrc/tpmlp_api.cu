@@ -192,7 +192,7 @@ size_t colsum_bytes(int64_t n, int64_t d, int64_t m) {
 tpmlp_status backward_impl(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
                            const void* Y_save, void* dX, float* dA, float* dB, float* dbias1, float* dbias2, int64_t n,
                            int64_t d, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace,
-                           size_t ws_bytes, void* stream) {
+                           size_t ws_bytes, void* stream, bool accumulate = false) {
   TPMLP_TRY(check_common(gelu, dt));
   TPMLP_TRY(check_mlp_shape(n, d, m, t, dt));
   TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
@@ -212,6 +212,7 @@ tpmlp_status backward_impl(const void* X, const void* A, const void* B, const vo
   DeviceCtx ctx;
   TPMLP_CUDA(get_device_ctx(&ctx), "device context");
   if (n == 0) {
+    if (accumulate) return TPMLP_OK;  // nothing to add
     TPMLP_CUDA(cudaMemsetAsync(dA, 0, sizeof(float) * d * m, s), "zero dA");
     TPMLP_CUDA(cudaMemsetAsync(dB, 0, sizeof(float) * m * d, s), "zero dB");
     if (biases) {
@@ -226,11 +227,12 @@ tpmlp_status backward_impl(const void* X, const void* A, const void* B, const vo
                   epi(D, nullptr, Z_save, m, gelu), s, ctx),
              "dgrad-1 GEMM");
   // wgrad-2: dB = Y^T G  (both operands MN-major, K = tokens)
-  TPMLP_CUDA(gemm(dt, m, d, n, Operand{Y_save, n, m, m, true}, Operand{G, n, d, d, true}, kEpiStoreF32,
+  const EpiKind wgrad_epi = accumulate ? kEpiAccumF32 : kEpiStoreF32;
+  TPMLP_CUDA(gemm(dt, m, d, n, Operand{Y_save, n, m, m, true}, Operand{G, n, d, d, true}, wgrad_epi,
                   epi(dB, nullptr, nullptr, d, gelu), s, ctx),
              "wgrad-2 GEMM");
-  // wgrad-1: dA = X^T D
-  TPMLP_CUDA(gemm(dt, d, m, n, Operand{X, n, d, d, true}, Operand{D, n, m, m, true}, kEpiStoreF32,
+  // wgrad-1: dA = X^T D (or dA += X^T D)
+  TPMLP_CUDA(gemm(dt, d, m, n, Operand{X, n, d, d, true}, Operand{D, n, m, m, true}, wgrad_epi,
                   epi(dA, nullptr, nullptr, m, gelu), s, ctx),
              "wgrad-1 GEMM");
   // dgrad-2: dX = D A^T; the K-loop over every shard is the f (backward all-reduce) sum.
@@ -272,6 +274,14 @@ tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const v
                             tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
   return backward_impl(X, A, B, G, Z_save, Y_save, dX, dA, dB, nullptr, nullptr, n, d, m, t, gelu, dt, workspace,
                        ws_bytes, stream);
+}
+
+tpmlp_status tpmlp_backward_accumulate(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
+                                       const void* Y_save, void* dX, float* dA, float* dB, int64_t n, int64_t d,
+                                       int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace,
+                                       size_t ws_bytes, void* stream) {
+  return backward_impl(X, A, B, G, Z_save, Y_save, dX, dA, dB, nullptr, nullptr, n, d, m, t, gelu, dt, workspace,
+                       ws_bytes, stream, true);
 }
 
 size_t tpmlp_backward_biased_workspace_size(int64_t n, int64_t d, int64_t m, tpmlp_dtype dt) {

@@ -20,7 +20,8 @@ enum EpiKind : int {
   kEpiStoreF32 = 1,  // out[r][c] = acc (fp32)
   kEpiGelu = 2,      // out[r][c] = acc (Z, may be null), out2[r][c] = gelu(acc) (Y)
   kEpiDGelu = 3,     // out[r][c] = acc * gelu'(aux[r][c])  (D = (G B^T) * gelu'(Z))
-  kEpiDropoutResidual = 4,  // out[R][c] = aux[R][c] + keep(r, c) * acc * scale, R = remap(r); mask bits
+  kEpiDropoutResidual = 4,
+  kEpiAccumF32 = 5,  // out[r][c] += acc (fp32): gradient accumulation into an fp32 main_grad  // out[R][c] = aux[R][c] + keep(r, c) * acc * scale, R = remap(r); mask bits
 };
 
 // Dropout of the sequence-parallel block applied in a GEMM epilogue: element (r, c) of the

@@ -164,3 +164,29 @@ def test_biased_block(shape, dtype, tol):
     for k, got in (("Z", Z), ("O", O), ("dX", dX), ("dA", dA), ("dB", dB), ("db1", db1), ("db2", db2)):
         assert_close(k, host(got), ref[k], tol, rep)
     print(rep)
+
+
+@pytest.mark.parametrize("dtype,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+def test_main_grad_accumulation_over_microbatches(dtype, tol):
+    """dA, dB accumulated over three micro-batches (one of them ragged) equal the oracle's
+    gradients of the concatenated batch added to the buffers' starting values."""
+    cfg = wl.MLPConfig("microbatches", 700, 256, 512, 4, dtype, "tanh", 1.0, 0.05, 1.0, seed=11)
+    inp = wl.mlp_inputs(cfg)
+    A, B = dev(inp["A"], dtype), dev(inp["B"], dtype)
+    rng = np.random.default_rng(12)
+    dA0 = rng.standard_normal((cfg.d, cfg.m)).astype(np.float32)
+    dB0 = rng.standard_normal((cfg.m, cfg.d)).astype(np.float32)
+    dA = torch.from_numpy(dA0).cuda()
+    dB = torch.from_numpy(dB0).cuda()
+    for lo, hi in ((0, 256), (256, 512), (512, 700)):
+        X = dev(inp["X"][lo:hi], dtype)
+        G = dev(inp["G"][lo:hi], dtype)
+        O, Z, Y = tp.forward(X, A, B, cfg.t, "tanh")
+        dX = torch.empty_like(X)
+        ws = torch.empty(tp.tpmlp_backward_workspace_size(hi - lo, cfg.m, X.dtype), dtype=torch.uint8, device="cuda")
+        tp.tpmlp_backward_accumulate(X, A, B, G, Z, Y, dX, dA, dB, cfg.t, "tanh", ws)
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    ref = omlp.backward(inp["X"], inp["A"], inp["B"], inp["G"], "tanh")
+    assert_close("dA", host(dA) - dA0, ref["dA"], tol)
+    assert_close("dB", host(dB) - dB0, ref["dB"], tol)

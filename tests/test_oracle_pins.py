@@ -382,3 +382,20 @@ def test_biased_shard_sum_adds_row_bias_once(t):
     if t > 1:  # adding b2 in every shard instead of once after the sum is the mistake this rules out
         wrong = mlp.forward_sharded(X, A, B, t, "tanh", b1, None)["O"] + t * b2
         assert np.abs(wrong - ref_f["O"]).max() > 0.1
+
+
+# ---------------------------------------------------------------- fp32 main_grad accumulation
+
+@pytest.mark.parametrize("chunks", [1, 2, 3])
+def test_microbatch_accumulation_equals_full_batch(chunks):
+    # Weight gradients are sums over tokens, so adding the gradients of micro-batches into an
+    # fp32 buffer (Megatron's main_grad with gradient_accumulation_fusion) gives the gradient of
+    # the concatenated batch; the activation gradient dX stays per micro-batch.
+    X, A, B, G = _rand((12, 16), 80), _rand((16, 32), 81, 0.3), _rand((32, 16), 82, 0.3), _rand((12, 16), 83)
+    full = mlp.backward(X, A, B, G, "erf")
+    acc_dA, acc_dB = np.zeros_like(full["dA"]), np.zeros_like(full["dB"])
+    for Xc, Gc in zip(np.array_split(X, chunks), np.array_split(G, chunks)):
+        g = mlp.backward(Xc, A, B, Gc, "erf")
+        acc_dA += g["dA"]
+        acc_dB += g["dB"]
+    assert np.abs(acc_dA - full["dA"]).max() < 1e-12 and np.abs(acc_dB - full["dB"]).max() < 1e-12
