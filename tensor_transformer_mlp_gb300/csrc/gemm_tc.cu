@@ -11,7 +11,8 @@
 //   warp 1      one thread issues tcgen05.mma (M=128, N=256, K=16) into a tensor-memory
 //               accumulator; two accumulators (2 x 256 columns) let the epilogue of one
 //               tile overlap the main loop of the next
-//   warps 2..5  epilogue: tcgen05.ld the fp32 tile, apply the fused op, store
+//   warps 2..9  epilogue: tcgen05.ld the fp32 tile, apply the fused op, store (two warps per
+//               tensor-memory lane quarter, each taking half of the 256 columns)
 // Operands are staged with 128-byte swizzle; K-major and MN-major layouts are both
 // read in place through the descriptors' major-ness bits, so no operand is transposed
 // in memory. Every mbarrier wait is bounded (kWaitLimitNs); on expiry the kernel
@@ -36,9 +37,10 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box of an MN-major operand
 constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = NUM_ACC * BN;  // 512: all of tensor memory
-constexpr int NUM_THREADS = 192;
-constexpr int NUM_EPI_THREADS = 128;
-constexpr int GROUP_M = 8;
+constexpr int NUM_EPI_WARPS = 8;  // two warps per tensor-memory lane quarter, each half the columns
+constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
+constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;
+constexpr int GROUP_M = 16;
 constexpr int BARRIER_BYTES = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BARRIER_BYTES + 1024;  // + alignment slack
 
@@ -297,6 +299,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
+    constexpr int kChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp
+    const int c_begin = ((warp - 2) / 4) * kChunks;
     int it = 0;
     for (int tile = blockIdx.x; tile < sched.num_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = c_begin; c < c_begin + kChunks; ++c) {
         const int col0 = nb * BN + c * 32;
         if (col0 >= N) break;  // uniform across the warp
         uint32_t v[32];
