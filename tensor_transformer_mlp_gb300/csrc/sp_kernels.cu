@@ -658,17 +658,19 @@ __global__ void __launch_bounds__(128) dropout_grad_gather_kernel(const T* __res
 // with the row statistics recomputed from x in one shifted pass and all four row sums
 // (sum d, sum d^2, sum g, sum g*d with d = x - x_0) reduced together. Each thread owns CH
 // vectors of columns and accumulates dgamma (dxn * x_hat) and dbeta (dxn) for them over its
-// CTA's rows in its own columns of a [2][h] shared-memory array (no two threads share a
-// column, so no atomics); the CTA writes them to partials[blockIdx][2][h] for a fixed-order sum.
+// CTA's rows in its own slots of a shared-memory array laid out [2][CH][8][threads] (no two
+// threads share a slot, so no atomics, and a warp's accesses hit 32 consecutive words, so no
+// bank conflicts); the CTA writes them to partials[blockIdx][2][h] for a fixed-order sum.
 constexpr int kLnBwdThreads = 128;
 
 template <typename T, int CH>
-__global__ void __launch_bounds__(kLnBwdThreads)
-    layernorm_backward_kernel(const T* __restrict__ x, const float* __restrict__ dxn, const T* __restrict__ dout,
+__global__ void __launch_bounds__(kLnBwdThreads, 4)
+    layernorm_backward_kernel(const T* __restrict__ x, const T* __restrict__ dxn, const T* __restrict__ dout,
                               const float* __restrict__ gamma, float eps, T* __restrict__ dx,
                               float* __restrict__ partials, int64_t rows, int h) {
   __shared__ float4 red[2][kLnBwdThreads / 32];
-  extern __shared__ float acc[];  // [2][h]: dgamma then dbeta partial sums
+  extern __shared__ float acc[];  // [2][CH][8][kLnBwdThreads]: dgamma then dbeta partial sums
+  constexpr int kHalf = CH * 8 * kLnBwdThreads;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   float gam[CH][8];
 #pragma unroll
@@ -677,26 +679,29 @@ __global__ void __launch_bounds__(kLnBwdThreads)
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       gam[c][e] = col < h ? gamma[col + e] : 0.f;
-      if (col < h) acc[col + e] = acc[h + col + e] = 0.f;
+      acc[(c * 8 + e) * kLnBwdThreads + tid] = 0.f;
+      acc[kHalf + (c * 8 + e) * kLnBwdThreads + tid] = 0.f;
     }
   }
   const float inv_h = 1.0f / static_cast<float>(h);
   int p = 0;
   for (int64_t R = blockIdx.x; R < rows; R += gridDim.x, p ^= 1) {
     const T* xr = x + R * h;
-    const float* dr = dxn + R * h;
+    const T* dr = dxn + R * h;
+    const T* gr = dout + R * h;
     const float shift = static_cast<float>(xr[0]);
     float f[CH][8], dn[CH][8];
+    Vec8<T> gv[CH];  // dout, loaded with x and dxn so that all of the row's reads are in flight at once
     float s_d = 0.f, s_dd = 0.f, s_g = 0.f, s_gd = 0.f;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int col = (tid + c * kLnBwdThreads) * 8;
       if (col < h) {
-        Vec8<T> xv;
+        Vec8<T> xv, dv;
         xv.load(xr + col);
-        xv.to_float(f[c]);
-        Vec8<float> dv;
         dv.load(dr + col);
+        gv[c].load(gr + col);
+        xv.to_float(f[c]);
         dv.to_float(dn[c]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -728,23 +733,21 @@ __global__ void __launch_bounds__(kLnBwdThreads)
     const float rstd = rsqrtf(fmaxf(t4.y * inv_h - md * md, 0.f) + eps);
     const float mean_g = t4.z * inv_h;
     const float mean_gxh = rstd * (t4.w * inv_h - md * mean_g);  // mean(g * x_hat)
-    const T* gr = dout + R * h;
     T* outr = dx + R * h;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int col = (tid + c * kLnBwdThreads) * 8;
       if (col < h) {
-        Vec8<T> gv;
-        gv.load(gr + col);
         float go[8], o[8];
-        gv.to_float(go);
+        gv[c].to_float(go);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float xh = (f[c][e] - shift - md) * rstd;
           const float g = dn[c][e] * gam[c][e];
           o[e] = go[e] + rstd * (g - mean_g - xh * mean_gxh);
-          acc[col + e] = fmaf(dn[c][e], xh, acc[col + e]);
-          acc[h + col + e] += dn[c][e];
+          const int slot = (c * 8 + e) * kLnBwdThreads + tid;
+          acc[slot] = fmaf(dn[c][e], xh, acc[slot]);
+          acc[kHalf + slot] += dn[c][e];
         }
         Vec8<T> ov;
         ov.from_float(o);
@@ -759,21 +762,32 @@ __global__ void __launch_bounds__(kLnBwdThreads)
     if (col < h) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        pg[col + e] = acc[col + e];
-        pg[h + col + e] = acc[h + col + e];
+        pg[col + e] = acc[(c * 8 + e) * kLnBwdThreads + tid];
+        pg[h + col + e] = acc[kHalf + (c * 8 + e) * kLnBwdThreads + tid];
       }
     }
   }
 }
 
-// dgamma[c] = sum over CTAs of partials[k][0][c], dbeta likewise, in CTA order.
+// dgamma[c] = sum over CTAs of partials[k][0][c], dbeta likewise. A CTA takes 32 of the 2h
+// columns; thread (g, c) adds partials g, g+8, g+16, ... of its column, and the 8 group sums are
+// then added in group order, so the result does not depend on scheduling.
 __global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restrict__ partials, int nparts, int h,
                                                            float* __restrict__ dgamma, float* __restrict__ dbeta) {
-  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < 2 * h; c += gridDim.x * blockDim.x) {
-    float acc = 0.f;
-    for (int k = 0; k < nparts; ++k) acc += partials[static_cast<int64_t>(k) * 2 * h + c];
-    if (c < h) dgamma[c] = acc;
-    else dbeta[c - h] = acc;
+  __shared__ float grp[8][32];
+  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
+  float acc = 0.f;
+  if (c < 2 * h)
+    for (int k = g; k < nparts; k += 8) acc += partials[static_cast<int64_t>(k) * 2 * h + c];
+  grp[g][lane] = acc;
+  __syncthreads();
+  if (g == 0 && c < 2 * h) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t += grp[k][lane];
+    if (c < h) dgamma[c] = t;
+    else dbeta[c - h] = t;
   }
 }
 
@@ -994,23 +1008,33 @@ cudaError_t launch_column_sums(const void* M, int64_t rows, int64_t cols, bool b
   return cudaGetLastError();
 }
 
-int layernorm_backward_grid(int64_t rows, int num_sms) {
-  const int g = rows_grid(rows, num_sms, 4);
+// One resident wave: as many CTAs as fit on the SMs at once (by registers and shared memory),
+// so no CTA waits for another to finish; at most kLnBwdMaxCtas (the partials' capacity).
+template <typename KERN>
+int layernorm_backward_grid(KERN kernel, size_t smem, int64_t rows, int num_sms) {
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kLnBwdThreads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int g = rows_grid(rows, num_sms, per_sm);
   return g < kLnBwdMaxCtas ? g : kLnBwdMaxCtas;
 }
 
-cudaError_t launch_layernorm_backward(const void* x, const float* dxn, const void* dout, const float* gamma, float eps,
+cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
                                       bool bf16, cudaStream_t stream, int num_sms) {
   if (rows <= 0) return cudaSuccess;
   if (h % 8 != 0 || h > kLnBwdThreads * 8 * 4) return cudaErrorInvalidValue;
-  const int grid = layernorm_backward_grid(rows, num_sms);
   const int ch = static_cast<int>((h / 8 + kLnBwdThreads - 1) / kLnBwdThreads);
-  const size_t acc_bytes = 2 * static_cast<size_t>(h) * sizeof(float);  // <= 32 KiB for h <= 4096
+  const size_t acc_bytes = 2 * static_cast<size_t>(ch) * 8 * kLnBwdThreads * sizeof(float);  // <= 32 KiB
+  int grid = 0;
 #define TPMLP_LNB(TYPE, CHN)                                                                                     \
-  layernorm_backward_kernel<TYPE, CHN><<<grid, kLnBwdThreads, acc_bytes, stream>>>(                              \
-      static_cast<const TYPE*>(x), dxn, static_cast<const TYPE*>(dout), gamma, eps, static_cast<TYPE*>(dx), partials, \
-      rows, static_cast<int>(h))
+  do {                                                                                                           \
+    auto k = layernorm_backward_kernel<TYPE, CHN>;                                                               \
+    grid = layernorm_backward_grid(k, acc_bytes, rows, num_sms);                                                 \
+    k<<<grid, kLnBwdThreads, acc_bytes, stream>>>(static_cast<const TYPE*>(x), static_cast<const TYPE*>(dxn),    \
+                                                  static_cast<const TYPE*>(dout), gamma, eps,                   \
+                                                  static_cast<TYPE*>(dx), partials, rows, static_cast<int>(h)); \
+  } while (0)
   if (bf16) {
     if (ch <= 1) TPMLP_LNB(__nv_bfloat16, 1);
     else if (ch <= 2) TPMLP_LNB(__nv_bfloat16, 2);
@@ -1023,7 +1047,7 @@ cudaError_t launch_layernorm_backward(const void* x, const float* dxn, const voi
 #undef TPMLP_LNB
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int hb = static_cast<int>((2 * h + 255) / 256);
+  const int hb = static_cast<int>((2 * h + 31) / 32);
   sum_partials_kernel<<<hb, 256, 0, stream>>>(partials, grid, static_cast<int>(h), dgamma, dbeta);
   return cudaGetLastError();
 }

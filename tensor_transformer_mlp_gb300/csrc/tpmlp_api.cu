@@ -439,7 +439,7 @@ size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, i
   if (b <= 0 || s <= 0 || h <= 0 || m <= 0 || t <= 0) return 0;
   const size_t e = elt_size(dt);
   const size_t tok = static_cast<size_t>(b) * static_cast<size_t>(s);
-  return 3 * round_up(tok * h * e, 256) + round_up(tok * m * e, 256) + round_up(tok * h * sizeof(float), 256) +
+  return 4 * round_up(tok * h * e, 256) + round_up(tok * m * e, 256) +
          round_up(static_cast<size_t>(kLnBwdMaxCtas) * 2 * h * sizeof(float), 256);
 }
 
@@ -485,8 +485,8 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
   void* xg = ws + round_up(tok * h * e, 256);
   void* dtok = ws + 2 * round_up(tok * h * e, 256);
   void* D = ws + 3 * round_up(tok * h * e, 256);
-  float* dxn = reinterpret_cast<float*>(static_cast<char*>(D) + round_up(tok * m * e, 256));
-  float* partials = reinterpret_cast<float*>(reinterpret_cast<char*>(dxn) + round_up(tok * h * sizeof(float), 256));
+  void* dxn = static_cast<char*>(D) + round_up(tok * m * e, 256);
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(dxn) + round_up(tok * h * e, 256));
   const bool bf16 = dt == TPMLP_BF16;
   // Recompute the LayerNorm output in token order (the forward's g), then the local dropout
   // gradient gathered into token order (g-bar's backward).
@@ -506,14 +506,14 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
   TPMLP_CUDA(gemm(dt, h, m, n, Operand{xg, n, h, h, true}, Operand{D, n, m, m, true}, kEpiStoreF32,
                   epi(dA, nullptr, nullptr, m, gelu), st, ctx),
              "wgrad-1 GEMM");
-  // dgrad-2: its K-loop sums every shard's D_i A_i^T and its epilogue writes fp32 rows back in
-  // shard layout (g's backward, the reduce-scatter).
+  // dgrad-2: its K-loop sums every shard's D_i A_i^T and its epilogue writes the rows back in
+  // shard layout (g's backward, the reduce-scatter), in the operand dtype like dX.
   EpiParams e5 = epi(dxn, nullptr, nullptr, h, gelu);
   e5.remap.enabled = 1;
   e5.remap.b = b;
   e5.remap.s = s;
   e5.remap.s_per_shard = s / t;
-  TPMLP_CUDA(gemm(dt, n, h, m, Operand{D, n, m, m, false}, Operand{A, h, m, m, false}, kEpiStoreF32, e5, st, ctx),
+  TPMLP_CUDA(gemm(dt, n, h, m, Operand{D, n, m, m, false}, Operand{A, h, m, m, false}, kEpiStore, e5, st, ctx),
              "dgrad-2 GEMM");
   // LayerNorm backward on the shards plus the residual path.
   TPMLP_CUDA(launch_layernorm_backward(x_shards, dxn, dout_shards, gamma, eps, dx_shards, partials, dgamma, dbeta, n,

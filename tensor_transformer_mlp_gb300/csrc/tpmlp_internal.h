@@ -111,7 +111,7 @@ constexpr int kLnBwdMaxCtas = 1024;
 cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint64_t threshold, float scale,
                                        uint64_t seed, int64_t b, int64_t s, int64_t h, int t, bool bf16,
                                        cudaStream_t stream, int num_sms);
-cudaError_t launch_layernorm_backward(const void* x, const float* dxn, const void* dout, const float* gamma, float eps,
+cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
                                       bool bf16, cudaStream_t stream, int num_sms);
 
