@@ -255,6 +255,15 @@ const char* tpmlp_last_error(void);
  */
 tpmlp_status tpmlp_device_status(void* stream, int clear);
 
+/*
+ * Exercises the failure path above on the GPU: launches a kernel whose one waiting thread waits
+ * on a barrier that nothing completes, gives up after limit_ns nanoseconds (1e3..1e9) and
+ * records a timeout in the device status word, exactly as a stalled GEMM or staged kernel would.
+ * A following tpmlp_device_status then returns TPMLP_ERR_TIMEOUT; the context stays usable.
+ * Nothing faults, traps or spins without a limit.
+ */
+tpmlp_status tpmlp_check_wait_timeout(uint64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     tpmlp_backward_biased,
     tpmlp_backward_biased_workspace_size,
     tpmlp_backward_workspace_size,
+    tpmlp_check_wait_timeout,
     tpmlp_device_status,
     tpmlp_forward,
     tpmlp_forward_biased,

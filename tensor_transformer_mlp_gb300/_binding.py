@@ -45,6 +45,7 @@ SIGNATURES = {
     "tpmlp_sp_dropout_residual": (_I, [_P, _P, _P, _P, _F, _U64, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_last_error": (ctypes.c_char_p, []),
     "tpmlp_device_status": (_I, [_P, _I]),
+    "tpmlp_check_wait_timeout": (_I, [_U64, _P]),
 }
 
 _lib = None
@@ -250,6 +251,10 @@ def tpmlp_sp_dropout_residual(x_shards, y_shards, out_shards, mask_bits, p_drop,
     _check(load_library().tpmlp_sp_dropout_residual(_ptr(x_shards), _ptr(y_shards), _ptr(out_shards),
                                                     _ptr(mask_bits), p_drop, seed, b, sl * t, h, t, _dt(x_shards),
                                                     _stream(stream)))
+
+
+def tpmlp_check_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load_library().tpmlp_check_wait_timeout(limit_ns, _stream(stream)))
 
 
 def tpmlp_device_status(stream=None, clear: bool = True) -> None:

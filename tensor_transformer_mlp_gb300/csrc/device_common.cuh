@@ -61,10 +61,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase with the given parity has completed, for at most kWaitLimitNs.
+// Waits until the phase with the given parity has completed, for at most limit_ns.
 // Returns false (and records a timeout in *status) if the limit expired.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
-                                          unsigned int where) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                              unsigned int where, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -72,11 +72,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(a, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       record_timeout(status, where);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          unsigned int where) {
+  return mbar_wait_for(bar, parity, status, where, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------------ TMA

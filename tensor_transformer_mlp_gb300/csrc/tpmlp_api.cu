@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/tpmlp.h"
+#include "device_common.cuh"
 #include "tpmlp_internal.h"
 
 namespace tpmlp {
@@ -72,6 +73,17 @@ cudaError_t get_device_ctx(DeviceCtx* ctx) {
 namespace tpmlp {
 // Lets other translation units of the library set the calling thread's last-error message.
 int report_error(int status, const char* msg) { return fail(static_cast<tpmlp_status>(status), "%s", msg); }
+// The library's failure path on demand: one thread waits on an mbarrier that nothing ever
+// completes, gives up after limit_ns like every in-kernel wait, and records the timeout.
+__global__ void wait_timeout_check_kernel(unsigned int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait_for(&bar, 0, status, 0xCC, limit_ns);
+  }
+}
+
 }  // namespace tpmlp
 
 using namespace tpmlp;
@@ -586,6 +598,16 @@ tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shard
                                      static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))), seed, b, s, h, t,
                                      dt == TPMLP_BF16, static_cast<cudaStream_t>(stream), ctx.num_sms, ctx.status),
              "dropout+residual");
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_check_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000ull)
+    return fail(TPMLP_ERR_INVALID, "limit_ns must lie in [1e3, 1e9], got %llu", (unsigned long long)limit_ns);
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  wait_timeout_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ctx.status, limit_ns);
+  TPMLP_CUDA(cudaGetLastError(), "wait-timeout check launch");
   return TPMLP_OK;
 }
 

@@ -128,5 +128,10 @@ def test_elementwise_validation(lib):
     assert lib.tpmlp_sp_layernorm(FAKE + 2, FAKE, FAKE, 1e-5, FAKE, 4, 256, BF16, None) == ALIGN
 
 
+def test_wait_timeout_check_validation(lib):
+    assert lib.tpmlp_check_wait_timeout(10, None) == INVALID
+    assert lib.tpmlp_check_wait_timeout(5_000_000_000, None) == INVALID
+
+
 def test_last_error_never_null(lib):
     assert isinstance(lib.tpmlp_last_error(), bytes)

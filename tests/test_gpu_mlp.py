@@ -190,3 +190,20 @@ def test_main_grad_accumulation_over_microbatches(dtype, tol):
     ref = omlp.backward(inp["X"], inp["A"], inp["B"], inp["G"], "tanh")
     assert_close("dA", host(dA) - dA0, ref["dA"], tol)
     assert_close("dB", host(dB) - dB0, ref["dB"], tol)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """Failure detection: a kernel waits on a barrier that nothing completes, gives up after
+    50 ms and records TPMLP_ERR_TIMEOUT; the status is read on the host, cleared, and the same
+    context then runs a forward pass correctly."""
+    tp.tpmlp_device_status(clear=True)
+    tp.tpmlp_check_wait_timeout(50_000_000)
+    with pytest.raises(tp.TpmlpError, match="TIMEOUT"):
+        tp.tpmlp_device_status(clear=True)
+    tp.tpmlp_device_status()  # cleared
+    cfg = wl.MLPConfig("after-timeout", 128, 256, 512, 2, "bf16", "tanh", 1.0, 0.05, 1.0)
+    inp = wl.mlp_inputs(cfg)
+    X, A, B = (dev(inp[k], "bf16") for k in "XAB")
+    O, _, _ = tp.forward(X, A, B, cfg.t, "tanh")
+    torch.cuda.synchronize()
+    assert_close("O", host(O), omlp.forward(inp["X"], inp["A"], inp["B"], "tanh")["O"], TOL_BF16)
