@@ -222,11 +222,19 @@ def run_reference(args, cfg):
     return 0
 
 
+def l2_note(cfg) -> str:
+    """Whether one step's operands exceed the 126 MiB L2 (no flush needed) or not."""
+    mib = 2 * (2 * cfg.n * cfg.d + 2 * cfg.d * cfg.m) / 2**20
+    if mib > 126:
+        return f"inputs larger than L2 ({mib:.0f} MiB of X, A, B, G per step), no flush"
+    return f"inputs ({mib:.0f} MiB) fit in L2; steps re-read them from L2"
+
+
 def config_dict(cfg):
     return {"workload": cfg.name, "n": cfg.n, "d": cfg.d, "m": cfg.m, "t": cfg.t, "gelu": cfg.gelu,
             "inputs": f"seed {cfg.seed}, X~N(0,{cfg.x_std}), A,B~N(0,{cfg.w_std}), G~N(0,{cfg.g_std}) (std), "
                       f"rounded to {cfg.dtype}",
-            "l2": "inputs larger than L2 (X, G 256+ MiB; A, B 512+ MiB per step), no flush",
+            "l2": l2_note(cfg),
             "parallelism": "replicas (t shards on one GPU per replica)"}
 
 
