@@ -17,6 +17,10 @@ What it computes, and which passage of the source pages it follows:
 * ``sp``: LayerNorm with torch semantics, the splitmix64 counter-hash dropout mask,
   and the sequence-parallel block (placement diagram of "Megatron-SP 机制",
   section "通信插在层内什么位置？").
+* ``attention``: the tensor-parallel self-attention block (column-parallel QKV with heads split
+  across shards, softmax(Q K^T / sqrt(head_dim)) V per head, row-parallel output projection) and
+  its gradients, from the SenseParrots note's parallel attention code (section 2.1.1) and the
+  "Attention 层" section of the "Megatron 训练" notes.
 * ``collectives``: host "ranks" for all-reduce, all-gather and reduce-scatter, to pin
   AllReduce = AllGather(ReduceScatter(x)) ("Megatron-SP 机制", section
   "f/g 算子怎么定义？").
@@ -28,4 +32,4 @@ closed forms, the block-matrix invariants and the ReLU counterexample. The
 worked example on the pages prints shapes only, so its absolute values are
 parity-unpinned; every other function here is pinned.
 """
-from . import collectives, mlp, sp  # noqa: F401
+from . import attention, collectives, mlp, sp  # noqa: F401

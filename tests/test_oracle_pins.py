@@ -399,3 +399,72 @@ def test_microbatch_accumulation_equals_full_batch(chunks):
         acc_dA += g["dA"]
         acc_dB += g["dB"]
     assert np.abs(acc_dA - full["dA"]).max() < 1e-12 and np.abs(acc_dB - full["dB"]).max() < 1e-12
+
+
+# ---------------------------------------------------------------- tensor-parallel attention
+
+from oracle import attention as oattn  # noqa: E402
+
+
+def _attn_small(seed=90, b=2, s=5, h=16, heads=4):
+    X = _rand((b, s, h), seed)
+    Wqkv, Wo = _rand((h, 3 * h), seed + 1, 0.3), _rand((h, h), seed + 2, 0.3)
+    G = _rand((b, s, h), seed + 3)
+    return X, Wqkv, Wo, heads, G
+
+
+def test_attention_matches_torch_autograd():
+    X, Wqkv, Wo, heads, G = _attn_small()
+    b, s, h = X.shape
+    dh = h // heads
+    tX, tW, tO = (torch.tensor(a, requires_grad=True) for a in (X, Wqkv, Wo))
+    qkv = (tX @ tW).reshape(b, s, heads, 3, dh).permute(3, 0, 2, 1, 4)   # the note's reshape/permute
+    q, k, v = qkv[0], qkv[1], qkv[2]
+    att = torch.softmax((q @ k.transpose(-2, -1)) * dh ** -0.5, dim=-1)
+    Y = (att @ v).transpose(1, 2).reshape(b, s, h) @ tO
+    Y.backward(torch.tensor(G))
+    f = oattn.forward(X, Wqkv, Wo, heads)
+    g = oattn.backward(X, Wqkv, Wo, heads, G)
+    assert np.abs(f["Y"] - Y.detach().numpy()).max() < 1e-12
+    for key, t in (("dX", tX), ("dWqkv", tW), ("dWo", tO)):
+        assert np.abs(g[key] - t.grad.numpy()).max() < 1e-11, key
+
+
+def test_attention_matches_library_sdpa():
+    X, Wqkv, Wo, heads, _ = _attn_small(95)
+    b, s, h = X.shape
+    dh = h // heads
+    qkv = torch.tensor(X @ Wqkv).reshape(b, s, heads, 3, dh).permute(3, 0, 2, 1, 4)
+    o = torch.nn.functional.scaled_dot_product_attention(qkv[0], qkv[1], qkv[2])
+    ref = o.transpose(1, 2).reshape(b, s, h).numpy() @ Wo
+    assert np.abs(oattn.forward(X, Wqkv, Wo, heads)["Y"] - ref).max() < 1e-12
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_attention_head_shards_sum_to_unsharded(t):
+    X, Wqkv, Wo, heads, _ = _attn_small(100)
+    assert np.abs(oattn.forward_sharded(X, Wqkv, Wo, heads, t) - oattn.forward(X, Wqkv, Wo, heads)["Y"]).max() < 1e-12
+
+
+def test_attention_backward_finite_differences():
+    X, Wqkv, Wo, heads, G = _attn_small(110, b=1, s=3, h=8, heads=2)
+    g = oattn.backward(X, Wqkv, Wo, heads, G)
+    loss = lambda X_, W_, O_: float((oattn.forward(X_, W_, O_, heads)["Y"] * G).sum())
+    for name, key in (("X", "dX"), ("W", "dWqkv"), ("O", "dWo")):
+        args = {"X": X, "W": Wqkv, "O": Wo}
+        arr = args[name]
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            ap, am = dict(args), dict(args)
+            ap[name], am[name] = arr.copy(), arr.copy()
+            ap[name][idx] += 1e-6
+            am[name][idx] -= 1e-6
+            fd[idx] = (loss(ap["X"], ap["W"], ap["O"]) - loss(am["X"], am["W"], am["O"])) / 2e-6
+        assert np.abs(fd - g[key]).max() / np.abs(g[key]).max() < 1e-6, name
+
+
+def test_softmax_rows_sum_to_one_and_shift_invariant():
+    S = _rand((3, 7, 9), 120) * 5
+    P = oattn.softmax(S)
+    assert np.abs(P.sum(-1) - 1).max() < 1e-14
+    assert np.abs(oattn.softmax(S + 100.0) - P).max() < 1e-14
