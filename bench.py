@@ -332,6 +332,47 @@ def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
             "kernels": res}
 
 
+# ----------------------------------------------------------------------------- attention
+
+def measure_attention(dev, peaks, reps: int = 10):
+    """Times the tensor-parallel attention block (forward, backward) on the GPT-style shape;
+    algorithmic FLOPs: forward 8*n*h^2 + 4*b*s^2*h, backward twice that."""
+    import torch
+
+    import tensor_transformer_mlp_gb300 as tp
+
+    cfg = wl.GPT_ATTENTION
+    inp = wl.attn_inputs(cfg)
+    bf = torch.bfloat16
+    X = torch.from_numpy(inp["X"]).to(dev).to(bf)
+    Wqkv = torch.from_numpy(inp["Wqkv"]).to(dev).to(bf)
+    Wo = torch.from_numpy(inp["Wo"]).to(dev).to(bf)
+    G = torch.from_numpy(inp["G"]).to(dev).to(bf)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps / 1e3
+
+    _, saves = tp.attention_forward(X, Wqkv, Wo, cfg.heads, cfg.t)
+    fwd = timed(lambda: tp.attention_forward(X, Wqkv, Wo, cfg.heads, cfg.t))
+    bwd = timed(lambda: tp.attention_backward(X, Wqkv, Wo, G, saves, cfg.heads, cfg.t))
+    tp.tpmlp_device_status(stream)
+    ff = cfg.flops_fwd
+    return {"workload": cfg.name, "forward_ms": fwd * 1e3, "forward_tflops": ff / fwd / 1e12,
+            "backward_ms": bwd * 1e3, "backward_tflops": 2 * ff / bwd / 1e12,
+            "note": "scores materialised in fp32 with a separate softmax kernel (Megatron's classic form); "
+                    "includes allocation of outputs and workspace by the convenience wrappers"}
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_ours(args, cfg):
@@ -478,6 +519,7 @@ def run_ours(args, cfg):
     }
     if not args.no_sp:
         line["sp"] = measure_sp(dev, peaks)
+        line["attention"] = measure_attention(dev, peaks)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp)
     print(json.dumps(line), flush=True)

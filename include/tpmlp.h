@@ -245,6 +245,39 @@ tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shard
                                        int64_t b, int64_t s, int64_t h, int t,
                                        tpmlp_dtype dt, void* stream);
 
+/*
+ * Tensor-parallel self-attention block (SenseParrots model-parallel note, section 2.1.1, its
+ * parallel multi-head attention code; "Megatron 训练" notes, section "Attention 层":
+ * S = Q K^T / sqrt(d), A = softmax(S)). bf16 only.
+ *   X [b*s][h]; W_qkv [h][3h] with head j's columns [q | k | v] at (3j .. 3j+3) * head_dim
+ *   (column-parallel: shard i owns heads i*heads/t .. (i+1)*heads/t - 1); W_o [h][h]
+ *   (row-parallel: shard i owns the rows of its heads).
+ *   Per head and sequence: P = softmax(Q K^T / sqrt(head_dim)) over the keys (no mask; no
+ *   attention dropout), O_head = P V; O [b*s][h] holds the heads side by side; Y = O W_o, the
+ *   K-loop over every head being the shard sum.
+ *   Saves (caller-owned, for the backward): QKV_save [b*s][3h], P_save [b][heads][s][s],
+ *   O_save [b*s][h]. workspace: the fp32 scores, tpmlp_attention_forward_workspace_size bytes.
+ *   Requires heads % t == 0, h % heads == 0, head_dim and s multiples of 8, s <= 8192.
+ */
+size_t tpmlp_attention_forward_workspace_size(int64_t b, int64_t s, int64_t h, int heads, tpmlp_dtype dt);
+tpmlp_status tpmlp_attention_forward(const void* X, const void* Wqkv, const void* Wo, void* Y,
+                                     void* QKV_save, void* P_save, void* O_save,
+                                     int64_t b, int64_t s, int64_t h, int heads, int t, tpmlp_dtype dt,
+                                     void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Backward of the attention block from G = dl/dY [b*s][h]: dX [b*s][h] (bf16), dWqkv [h][3h] and
+ * dWo [h][h] (fp32, overwritten). dO = G W_o^T, dW_o = O^T G; per head dV = P^T dO,
+ * dP = dO V^T, dS = P * (dP - rowsum(P * dP)) / sqrt(head_dim), dQ = dS K, dK = dS^T Q;
+ * dX = dQKV W_qkv^T, dW_qkv = X^T dQKV. Saves from tpmlp_attention_forward.
+ */
+size_t tpmlp_attention_backward_workspace_size(int64_t b, int64_t s, int64_t h, int heads, tpmlp_dtype dt);
+tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const void* Wo, const void* G,
+                                      const void* QKV_save, const void* P_save, const void* O_save,
+                                      void* dX, float* dWqkv, float* dWo,
+                                      int64_t b, int64_t s, int64_t h, int heads, int t, tpmlp_dtype dt,
+                                      void* workspace, size_t ws_bytes, void* stream);
+
 /* Message for the calling thread's last non-OK status ("" if none). Never NULL. */
 const char* tpmlp_last_error(void);
 

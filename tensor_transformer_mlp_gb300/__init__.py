@@ -8,6 +8,8 @@ from . import workloads  # noqa: F401
 from ._binding import (  # noqa: F401
     SIGNATURES,
     TpmlpError,
+    attention_backward,
+    attention_forward,
     backward,
     forward,
     load_library,

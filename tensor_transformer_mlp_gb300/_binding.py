@@ -43,6 +43,11 @@ SIGNATURES = {
     "tpmlp_sp_gather": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_reduce_scatter": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_dropout_residual": (_I, [_P, _P, _P, _P, _F, _U64, _I64, _I64, _I64, _I, _I, _P]),
+    "tpmlp_attention_forward_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "tpmlp_attention_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
+    "tpmlp_attention_backward_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "tpmlp_attention_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ,
+                                      _P]),
     "tpmlp_last_error": (ctypes.c_char_p, []),
     "tpmlp_device_status": (_I, [_P, _I]),
     "tpmlp_check_wait_timeout": (_I, [_U64, _P]),
@@ -332,3 +337,42 @@ def sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z, Y, dout
     tpmlp_sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z, Y, dout_shards, dx, dgamma, dbeta, dA,
                             dB, t, gelu, ws, stream)
     return dx, dgamma, dbeta, dA, dB
+
+
+# ----------------------------------------------------------------------- attention block
+
+def attention_forward(X, Wqkv, Wo, heads: int, t: int, stream=None):
+    """X [b, s, h] bf16; allocates Y, the saves and the workspace and runs tpmlp_attention_forward.
+    Returns (Y [b, s, h], (QKV, P, O))."""
+    b, s, h = X.shape
+    _cuda(X, Wqkv, Wo)
+    assert Wqkv.shape == (h, 3 * h) and Wo.shape == (h, h)
+    dev = X.device
+    Y = torch.empty_like(X)
+    QKV = torch.empty((b * s, 3 * h), dtype=X.dtype, device=dev)
+    P = torch.empty((b, heads, s, s), dtype=X.dtype, device=dev)
+    O = torch.empty((b * s, h), dtype=X.dtype, device=dev)
+    lib = load_library()
+    ws = torch.empty(max(1, lib.tpmlp_attention_forward_workspace_size(b, s, h, heads, _dt(X))), dtype=torch.uint8,
+                     device=dev)
+    _check(lib.tpmlp_attention_forward(_ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(Y), _ptr(QKV), _ptr(P), _ptr(O), b, s, h,
+                                       heads, t, _dt(X), _ptr(ws), ws.numel(), _stream(stream)))
+    return Y, (QKV, P, O)
+
+
+def attention_backward(X, Wqkv, Wo, G, saves, heads: int, t: int, stream=None):
+    """Runs tpmlp_attention_backward; returns (dX [b, s, h], dWqkv [h, 3h] fp32, dWo [h, h] fp32)."""
+    b, s, h = X.shape
+    QKV, P, O = saves
+    _cuda(X, Wqkv, Wo, G, QKV, P, O)
+    dev = X.device
+    dX = torch.empty_like(X)
+    dWqkv = torch.empty((h, 3 * h), dtype=torch.float32, device=dev)
+    dWo = torch.empty((h, h), dtype=torch.float32, device=dev)
+    lib = load_library()
+    ws = torch.empty(max(1, lib.tpmlp_attention_backward_workspace_size(b, s, h, heads, _dt(X))), dtype=torch.uint8,
+                     device=dev)
+    _check(lib.tpmlp_attention_backward(_ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(G), _ptr(QKV), _ptr(P), _ptr(O), _ptr(dX),
+                                        _ptr(dWqkv), _ptr(dWo), b, s, h, heads, t, _dt(X), _ptr(ws), ws.numel(),
+                                        _stream(stream)))
+    return dX, dWqkv, dWo

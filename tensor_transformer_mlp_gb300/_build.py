@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libtpmlp.so")
-SOURCES = ["tpmlp_api.cu", "gemm_tc.cu", "gemm_simt.cu", "sp_kernels.cu", "tpmlp_noalloc.cu"]
+SOURCES = ["tpmlp_api.cu", "gemm_tc.cu", "gemm_simt.cu", "sp_kernels.cu", "tpmlp_noalloc.cu", "tpmlp_attention.cu"]
 HEADERS = ["device_common.cuh", "tpmlp_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

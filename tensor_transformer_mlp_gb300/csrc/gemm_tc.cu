@@ -69,10 +69,22 @@ __device__ __forceinline__ int64_t remap_row(const RowRemap& rm, int64_t r) {
   return (j * rm.b + bi) * rm.s_per_shard + l;
 }
 
-// Applies the epilogue to 32 consecutive accumulator columns of one row.
-template <int EPI>
+// Device form of a batched launch: batch sizes, the tensor-map coordinate slot (1..3) that
+// takes each operand's row index and batch indices, the output offsets per batch index and
+// the accumulator scale.
+struct BatchDev {
+  int nz1, nz2;
+  int a_row, a_z1, a_z2;
+  int b_row, b_z1, b_z2;
+  int64_t out_z1, out_z2;
+  float alpha;
+};
+
+// Applies the epilogue to 32 consecutive accumulator columns of one row. Batched launches
+// (kEpiStore, kEpiStoreF32 only) scale by alpha and write at out + out_off.
+template <int EPI, bool BATCHED = false>
 __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row, int col0, int N,
-                                               const uint32_t (&v)[32]) {
+                                               const uint32_t (&v)[32], int64_t out_off = 0, float alpha = 1.f) {
   uint32_t drop_bits = 0;  // kEpiDropoutResidual: one mask word per 32 columns
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
@@ -81,6 +93,10 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
     float a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
+    if constexpr (BATCHED) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] *= alpha;
+    }
     if constexpr (EPI == kEpiGelu || EPI == kEpiStore) {
       if (ep.bias) {  // per-column bias (bf16), uniform across the warp
         const uint4 bv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.bias) + col);
@@ -95,7 +111,7 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
     }
     if constexpr (EPI == kEpiStoreF32) {
       const int64_t prow = remap_row(ep.remap, row);
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + prow * ep.ldo + col);
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + out_off + prow * ep.ldo + col);
       dst[0] = make_float4(a[0], a[1], a[2], a[3]);
       dst[1] = make_float4(a[4], a[5], a[6], a[7]);
     } else if constexpr (EPI == kEpiAccumF32) {
@@ -107,7 +123,7 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
       const int64_t prow = remap_row(ep.remap, row);
       uint4 pk = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
                             pack_bf16x2(a[6], a[7]));
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + prow * ep.ldo + col) = pk;
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + out_off + prow * ep.ldo + col) = pk;
     } else if constexpr (EPI == kEpiGelu) {
       const int64_t off = row * ep.ldo + col;
       if (ep.out) {
@@ -164,10 +180,26 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
   }
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+// One TMA tile load: 2-D map for plain launches; 4-D map (inner, then row and batch indices in
+// the slots recorded in BatchDev) for batched ones.
+template <bool BATCHED>
+__device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, uint64_t* bar, int inner, int row, int z1,
+                                          int z2, int s_row, int s_z1, int s_z2) {
+  if constexpr (!BATCHED) {
+    tma_load_2d(dst, map, bar, inner, row);
+  } else {
+    const int c1 = s_row == 1 ? row : (s_z1 == 1 ? z1 : z2);
+    const int c2 = s_row == 2 ? row : (s_z1 == 2 ? z1 : z2);
+    const int c3 = s_row == 3 ? row : (s_z1 == 3 ? z1 : z2);
+    (void)s_z2;
+    tma_load_4d(dst, map, bar, inner, c1, c2, c3);
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
-                     int N, int K, EpiParams ep, unsigned int* status) {
+                     int N, int K, EpiParams ep, unsigned int* status, BatchDev bd) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -184,6 +216,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   sched.num_mb = (M + BM - 1) / BM;
   sched.num_nb = (N + BN - 1) / BN;
   sched.num_tiles = sched.num_mb * sched.num_nb;
+  const int tiles_per_batch = sched.num_tiles;
+  const int total_tiles = BATCHED ? tiles_per_batch * bd.nz1 * bd.nz2 : tiles_per_batch;
+  // tile -> (batch index, M block, N block); batch-major so neighbouring tiles share a batch
+  auto tile_coords = [&](int tile, int& z1, int& z2, int& mb, int& nb) {
+    int z = 0;
+    if constexpr (BATCHED) {
+      z = tile / tiles_per_batch;
+      tile -= z * tiles_per_batch;
+    }
+    z1 = BATCHED ? z % bd.nz1 : 0;
+    z2 = BATCHED ? z / bd.nz1 : 0;
+    sched.coords(tile, mb, nb);
+  };
   const int num_kb = (K + BK - 1) / BK;
 
   if (warp == 0 && lane == 0) {
@@ -216,9 +261,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---------------------------------------------------------------- TMA producer
       int kiter = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < sched.num_tiles && ok; tile += gridDim.x) {
-        int mb, nb;
-        sched.coords(tile, mb, nb);
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        int z1, z2, mb, nb;
+        tile_coords(tile, z1, z2, mb, nb);
         for (int kb = 0; kb < num_kb; ++kb) {
           const int s = kiter % STAGES;
           const uint32_t parity = ((kiter / STAGES) & 1) ^ 1;
@@ -230,18 +275,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* sa = smem + s * STAGE_BYTES;
           uint8_t* sb = sa + A_STAGE_BYTES;
           if constexpr (!A_MN) {
-            tma_load_2d(sa, &tmap_a, &full_bar[s], kb * BK, mb * BM);
+            load_tile<BATCHED>(sa, &tmap_a, &full_bar[s], kb * BK, mb * BM, z1, z2, bd.a_row, bd.a_z1, bd.a_z2);
           } else {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d(sa + j * MN_BOX_BYTES, &tmap_a, &full_bar[s], mb * BM + j * 64, kb * BK);
+              load_tile<BATCHED>(sa + j * MN_BOX_BYTES, &tmap_a, &full_bar[s], mb * BM + j * 64, kb * BK, z1, z2,
+                                 bd.a_row, bd.a_z1, bd.a_z2);
           }
           if constexpr (!B_MN) {
-            tma_load_2d(sb, &tmap_b, &full_bar[s], kb * BK, nb * BN);
+            load_tile<BATCHED>(sb, &tmap_b, &full_bar[s], kb * BK, nb * BN, z1, z2, bd.b_row, bd.b_z1, bd.b_z2);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(sb + j * MN_BOX_BYTES, &tmap_b, &full_bar[s], nb * BN + j * 64, kb * BK);
+              load_tile<BATCHED>(sb + j * MN_BOX_BYTES, &tmap_b, &full_bar[s], nb * BN + j * 64, kb * BK, z1, z2,
+                                 bd.b_row, bd.b_z1, bd.b_z2);
           }
           ++kiter;
         }
@@ -258,7 +305,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
       int kiter = 0, it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < sched.num_tiles; tile += gridDim.x, ++it) {
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
         if (!mbar_wait(&tempty_bar[acc], (use & 1) ^ 1, status, 3)) {
@@ -302,14 +349,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int kChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp
     const int c_begin = ((warp - 2) / 4) * kChunks;
     int it = 0;
-    for (int tile = blockIdx.x; tile < sched.num_tiles; tile += gridDim.x, ++it) {
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
       const bool ok = mbar_wait(&tfull_bar[acc], use & 1, status, 6);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      int mb, nb;
-      sched.coords(tile, mb, nb);
+      int z1, z2, mb, nb;
+      tile_coords(tile, z1, z2, mb, nb);
+      const int64_t out_off = BATCHED ? z1 * bd.out_z1 + z2 * bd.out_z2 : 0;
       const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -319,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
         tmem_ld_wait();
-        if (row < M) epilogue_row32<EPI>(ep, row, col0, N, v);
+        if (row < M) epilogue_row32<EPI, BATCHED>(ep, row, col0, N, v, out_off, BATCHED ? bd.alpha : 1.f);
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
@@ -368,16 +416,53 @@ cudaError_t make_tmap(CUtensorMap* map, const Operand& op, uint32_t box_inner, u
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
-                   cudaStream_t stream, const DeviceCtx& ctx) {
-  auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI>;
+                   cudaStream_t stream, const DeviceCtx& ctx, const BatchDev& bd = BatchDev{}) {
+  auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI, BATCHED>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
-  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, M, N, K, ep, ctx.status);
+  int64_t tiles = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  if (BATCHED) tiles *= static_cast<int64_t>(bd.nz1) * bd.nz2;
+  if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+  const int grid = tiles < ctx.num_sms ? static_cast<int>(tiles) : ctx.num_sms;
+  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, M, N, K, ep, ctx.status, bd);
   return cudaGetLastError();
+}
+
+// 4-D bf16 tensor map over a batched operand: dimension 0 is the contiguous column index; the
+// row index and the two batch indices take dimensions 1..3 in order of increasing stride.
+// box_inner x box_row elements are copied per load (one row slab of one batch index).
+cudaError_t make_tmap_batched(CUtensorMap* map, const BatchedOperand& op, int64_t nz1, int64_t nz2,
+                              uint32_t box_inner, uint32_t box_row, int* slot_row, int* slot_z1, int* slot_z2) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+  cudaError_t e = get_encode(&encode);
+  if (e != cudaSuccess) return e;
+  struct D { int64_t extent, stride; int id; };
+  // extent-1 batch dimensions get a stride past everything else, so they sort last
+  int64_t far = (op.rows * op.ld + (nz1 - 1) * op.z1_stride + (nz2 - 1) * op.z2_stride + 1) * 2;
+  far = (far + 7) / 8 * 8;  // a multiple of 8 elements, i.e. of 16 bytes, like every TMA stride
+  D d[3] = {{op.rows, op.ld, 0}, {nz1, nz1 > 1 ? op.z1_stride : far, 1}, {nz2, nz2 > 1 ? op.z2_stride : far, 2}};
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (d[j].stride < d[i].stride || (d[j].stride == d[i].stride && d[j].id < d[i].id)) {
+        D t = d[i]; d[i] = d[j]; d[j] = t;
+      }
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(op.cols), 0, 0, 0};
+  cuuint64_t strides[3];
+  cuuint32_t box[4] = {box_inner, 1, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 3; ++i) {
+    dims[i + 1] = static_cast<cuuint64_t>(d[i].extent);
+    strides[i] = static_cast<cuuint64_t>(d[i].stride) * 2;
+    if (d[i].id == 0) { box[i + 1] = box_row; *slot_row = i + 1; }
+    if (d[i].id == 1) *slot_z1 = i + 1;
+    if (d[i].id == 2) *slot_z2 = i + 1;
+  }
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(op.ptr), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -411,6 +496,35 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
     if (epi == kEpiStoreF32) return launch<true, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
     if (epi == kEpiAccumF32) return launch<true, true, kEpiAccumF32>(ta, tb, m, n, k, ep, stream, ctx);
   }
+  return cudaErrorNotSupported;
+}
+
+cudaError_t gemm_bf16_tc_batched(int64_t M, int64_t N, int64_t K, const BatchedOperand& a, const BatchedOperand& b,
+                                 const BatchSpec& bs, EpiKind epi, const EpiParams& ep, cudaStream_t stream,
+                                 const DeviceCtx& ctx) {
+  if (M <= 0 || N <= 0 || K <= 0 || bs.nz1 <= 0 || bs.nz2 <= 0) return cudaErrorInvalidValue;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || bs.nz1 > INT32_MAX || bs.nz2 > INT32_MAX)
+    return cudaErrorInvalidValue;
+  if (a.mn_major ? (a.rows != K || a.cols != M) : (a.rows != M || a.cols != K)) return cudaErrorInvalidValue;
+  if (b.mn_major ? (b.rows != K || b.cols != N) : (b.rows != N || b.cols != K)) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  BatchDev bd{};
+  bd.nz1 = static_cast<int>(bs.nz1);
+  bd.nz2 = static_cast<int>(bs.nz2);
+  bd.out_z1 = bs.out_z1;
+  bd.out_z2 = bs.out_z2;
+  bd.alpha = bs.alpha;
+  cudaError_t e = make_tmap_batched(&ta, a, bs.nz1, bs.nz2, 64, a.mn_major ? BK : BM, &bd.a_row, &bd.a_z1, &bd.a_z2);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_batched(&tb, b, bs.nz1, bs.nz2, 64, b.mn_major ? BK : BN, &bd.b_row, &bd.b_z1, &bd.b_z2);
+  if (e != cudaSuccess) return e;
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (!a.mn_major && !b.mn_major && epi == kEpiStoreF32)
+    return launch<false, false, kEpiStoreF32, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
+  if (!a.mn_major && b.mn_major && epi == kEpiStore)
+    return launch<false, true, kEpiStore, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
+  if (a.mn_major && b.mn_major && epi == kEpiStore)
+    return launch<true, true, kEpiStore, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
   return cudaErrorNotSupported;
 }
 

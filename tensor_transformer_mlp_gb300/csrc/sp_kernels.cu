@@ -830,6 +830,118 @@ __global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restri
   }
 }
 
+// ------------------------------------------------------------------ attention softmax
+// Row softmax of fp32 scores into bf16 probabilities, one CTA per row (persistent over rows):
+// max, then sum of exp(s - max), then p = exp(s - max) / sum, the row held in registers.
+template <int CH>
+__global__ void __launch_bounds__(256) softmax_rows_kernel(const float* __restrict__ S, __nv_bfloat16* __restrict__ P,
+                                                           int64_t rows, int L) {
+  __shared__ float red[2][8];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int p = 0;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, p ^= 1) {
+    const float* sr = S + r * L;
+    float f[CH][8];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * 256) * 8;
+      if (col < L) {
+        Vec8<float> v;
+        v.load(sr + col);
+        v.to_float(f[c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, f[c][e]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[p][w] = mx;
+    __syncthreads();
+    mx = red[p][0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) mx = fmaxf(mx, red[p][k]);
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      if ((tid + c * 256) * 8 < L) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          f[c][e] = __expf(f[c][e] - mx);
+          sum += f[c][e];
+        }
+      }
+    }
+    sum = warp_sum(sum);
+    __syncthreads();  // everyone has read red[p] for the max
+    if (lane == 0) red[p][w] = sum;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tot += red[p][k];
+    const float inv = 1.0f / tot;
+    __nv_bfloat16* pr = P + r * L;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * 256) * 8;
+      if (col < L) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = f[c][e] * inv;
+        Vec8<__nv_bfloat16> ov;
+        ov.from_float(o);
+        ov.store(pr + col);
+      }
+    }
+  }
+}
+
+// Softmax backward with the score scale: dS = scale * P * (dP - sum_k P dP), bf16 out.
+template <int CH>
+__global__ void __launch_bounds__(256) softmax_backward_kernel(const __nv_bfloat16* __restrict__ P,
+                                                               const float* __restrict__ dP, float scale,
+                                                               __nv_bfloat16* __restrict__ dS, int64_t rows, int L) {
+  __shared__ float red[2][8];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int p = 0;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, p ^= 1) {
+    float pv[CH][8], dv[CH][8];
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * 256) * 8;
+      if (col < L) {
+        Vec8<__nv_bfloat16> a;
+        a.load(P + r * L + col);
+        a.to_float(pv[c]);
+        Vec8<float> b;
+        b.load(dP + r * L + col);
+        b.to_float(dv[c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dot = fmaf(pv[c][e], dv[c][e], dot);
+      }
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) red[p][w] = dot;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tot += red[p][k];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * 256) * 8;
+      if (col < L) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = scale * pv[c][e] * (dv[c][e] - tot);
+        Vec8<__nv_bfloat16> ov;
+        ov.from_float(o);
+        ov.store(dS + r * L + col);
+      }
+    }
+  }
+}
+
 int rows_grid(int64_t rows, int num_sms, int per_sm) {
   const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
   return static_cast<int>(rows < cap ? (rows > 0 ? rows : 1) : cap);
@@ -1049,6 +1161,32 @@ cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void
   if (e != cudaSuccess) return e;
   const int hb = static_cast<int>((2 * h + 31) / 32);
   sum_partials_kernel<<<hb, 256, 0, stream>>>(partials, grid, static_cast<int>(h), dgamma, dbeta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_rows(const float* S, void* P, int64_t rows, int64_t L, cudaStream_t stream, int num_sms) {
+  if (rows <= 0) return cudaSuccess;
+  if (L % 8 != 0 || L > 256 * 8 * 4) return cudaErrorInvalidValue;
+  const int grid = rows_grid(rows, num_sms, 8);
+  const int ch = static_cast<int>((L / 8 + 255) / 256);
+  auto* Pp = static_cast<__nv_bfloat16*>(P);
+  if (ch <= 1) softmax_rows_kernel<1><<<grid, 256, 0, stream>>>(S, Pp, rows, static_cast<int>(L));
+  else if (ch <= 2) softmax_rows_kernel<2><<<grid, 256, 0, stream>>>(S, Pp, rows, static_cast<int>(L));
+  else softmax_rows_kernel<4><<<grid, 256, 0, stream>>>(S, Pp, rows, static_cast<int>(L));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_backward(const void* P, const float* dP, float scale, void* dS, int64_t rows, int64_t L,
+                                    cudaStream_t stream, int num_sms) {
+  if (rows <= 0) return cudaSuccess;
+  if (L % 8 != 0 || L > 256 * 8 * 4) return cudaErrorInvalidValue;
+  const int grid = rows_grid(rows, num_sms, 8);
+  const int ch = static_cast<int>((L / 8 + 255) / 256);
+  auto* Pp = static_cast<const __nv_bfloat16*>(P);
+  auto* dSp = static_cast<__nv_bfloat16*>(dS);
+  if (ch <= 1) softmax_backward_kernel<1><<<grid, 256, 0, stream>>>(Pp, dP, scale, dSp, rows, static_cast<int>(L));
+  else if (ch <= 2) softmax_backward_kernel<2><<<grid, 256, 0, stream>>>(Pp, dP, scale, dSp, rows, static_cast<int>(L));
+  else softmax_backward_kernel<4><<<grid, 256, 0, stream>>>(Pp, dP, scale, dSp, rows, static_cast<int>(L));
   return cudaGetLastError();
 }
 

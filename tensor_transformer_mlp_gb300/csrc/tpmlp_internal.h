@@ -61,6 +61,22 @@ struct Operand {
   bool mn_major;
 };
 
+// Batched GEMM: batch index z = z2 * nz1 + z1 (e.g. z1 = attention head, z2 = sequence in the
+// batch). A batched operand is a stored matrix per batch index, placed at
+// ptr + z1 * z1_stride + z2 * z2_stride (elements) with row stride ld.
+struct BatchedOperand {
+  const void* ptr;
+  int64_t rows, cols, ld;
+  int64_t z1_stride, z2_stride;
+  bool mn_major;
+};
+
+struct BatchSpec {
+  int64_t nz1, nz2;
+  int64_t out_z1, out_z2;  // element offsets of the output block of batch index (z1, z2)
+  float alpha;             // scale applied to the accumulator before the epilogue
+};
+
 // Per-device context: SM count and the address of the device status word.
 struct DeviceCtx {
   int device;
@@ -76,6 +92,12 @@ int report_error(int status, const char* msg);
 // bf16 tensor-core GEMM (tcgen05 + TMA). C = Aop(M x K) * Bop(K x N), fp32 accumulation.
 cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
                          const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx);
+
+// Batched bf16 tensor-core GEMM: C_z = alpha * Aop_z(M x K) * Bop_z(K x N) for every batch index;
+// epilogues kEpiStore (bf16) and kEpiStoreF32, written at ep.out + out offsets of z.
+cudaError_t gemm_bf16_tc_batched(int64_t M, int64_t N, int64_t K, const BatchedOperand& a, const BatchedOperand& b,
+                                 const BatchSpec& bs, EpiKind epi, const EpiParams& ep, cudaStream_t stream,
+                                 const DeviceCtx& ctx);
 
 // fp32 FMA GEMM for the fp32 dtype, same semantics and epilogues (outputs in fp32).
 cudaError_t gemm_f32_simt(int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
@@ -114,5 +136,11 @@ cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint
 cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
                                       bool bf16, cudaStream_t stream, int num_sms);
+
+// Attention softmax: fp32 scores -> bf16 probabilities per row of length L (L % 8 == 0, L <= 8192),
+// and its backward dS = scale * P * (dP - rowsum(P * dP)) in bf16.
+cudaError_t launch_softmax_rows(const float* S, void* P, int64_t rows, int64_t L, cudaStream_t stream, int num_sms);
+cudaError_t launch_softmax_backward(const void* P, const float* dP, float scale, void* dS, int64_t rows, int64_t L,
+                                    cudaStream_t stream, int num_sms);
 
 }  // namespace tpmlp

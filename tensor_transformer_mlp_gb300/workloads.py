@@ -80,6 +80,33 @@ GPT_MLP = MLPConfig("gpt_mlp_n8192_h4096_m16384_t8_bf16", 8192, 4096, 16384, 8, 
 SP_BLOCK = SPConfig("sp_block_b2_s4096_h4096_m16384_t8_bf16", 2, 4096, 4096, 16384, 8, "tanh", 1.0, 0.02)
 LARGE_MLP = MLPConfig("large_mlp_n16384_h8192_m32768_t8_bf16", 16384, 8192, 32768, 8, "bf16", "tanh", 1.0, 0.01, 0.01)
 
+@dataclass(frozen=True)
+class AttnConfig:
+    """One tensor-parallel self-attention workload (heads split across t shards)."""
+    name: str
+    b: int
+    s: int
+    h: int
+    heads: int
+    t: int
+    x_std: float
+    w_std: float
+    g_std: float
+    seed: int = 0
+    dtype: str = "bf16"
+
+    @property
+    def n(self) -> int:
+        return self.b * self.s
+
+    @property
+    def flops_fwd(self) -> int:
+        """QKV (6nh^2) + scores and PV (4 b s^2 h) + output projection (2nh^2)."""
+        return 8 * self.n * self.h * self.h + 4 * self.b * self.s * self.s * self.h
+
+
+GPT_ATTENTION = AttnConfig("gpt_attention_b2_s2048_h4096_a32_t8_bf16", 2, 2048, 4096, 32, 8, 1.0, 0.02, 0.01)
+
 MLP_CONFIGS = {c.name: c for c in (WORKED_EXAMPLE, SINGLE_BLOCK, GPT_MLP, LARGE_MLP)}
 SP_CONFIGS = {SP_BLOCK.name: SP_BLOCK}
 
@@ -147,3 +174,13 @@ def sample_indices(count: int, total: int, seed: int) -> np.ndarray:
     """Sorted distinct indices for sampled parity checks at full size."""
     rng = np.random.default_rng(seed)
     return np.sort(rng.choice(total, size=min(count, total), replace=False))
+
+
+def attn_inputs(cfg: AttnConfig, seed: int | None = None) -> dict[str, np.ndarray]:
+    """X [b, s, h], W_qkv [h, 3h], W_o [h, h], G [b, s, h] (same recipe as the MLP workloads)."""
+    rng = np.random.default_rng(cfg.seed if seed is None else seed)
+    X = _draw(rng, (cfg.b * cfg.s, cfg.h), cfg.x_std, cfg.dtype).reshape(cfg.b, cfg.s, cfg.h)
+    Wqkv = _draw(rng, (cfg.h, 3 * cfg.h), cfg.w_std, cfg.dtype)
+    Wo = _draw(rng, (cfg.h, cfg.h), cfg.w_std, cfg.dtype)
+    G = _draw(rng, (cfg.b * cfg.s, cfg.h), cfg.g_std, cfg.dtype).reshape(cfg.b, cfg.s, cfg.h)
+    return {"X": X, "Wqkv": Wqkv, "Wo": Wo, "G": G}

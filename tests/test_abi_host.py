@@ -133,5 +133,15 @@ def test_wait_timeout_check_validation(lib):
     assert lib.tpmlp_check_wait_timeout(5_000_000_000, None) == INVALID
 
 
+def test_attention_validation(lib):
+    P = [FAKE] * 7
+    assert lib.tpmlp_attention_forward(*P, 2, 64, 256, 4, 3, BF16, FAKE, 1 << 30, None) == SHAPE   # heads % t
+    assert lib.tpmlp_attention_forward(*P, 2, 64, 256, 4, 2, F32, FAKE, 1 << 30, None) == DTYPE
+    assert lib.tpmlp_attention_forward(*P, 2, 60, 256, 4, 2, BF16, FAKE, 1 << 30, None) == SHAPE   # s % 8
+    assert lib.tpmlp_attention_forward(*P, 2, 64, 256, 4, 2, BF16, None, 0, None) == WORKSPACE
+    need = lib.tpmlp_attention_backward_workspace_size(2, 64, 256, 4, BF16)
+    assert lib.tpmlp_attention_backward(*([FAKE] * 10), 2, 64, 256, 4, 2, BF16, FAKE, need - 1, None) == WORKSPACE
+
+
 def test_last_error_never_null(lib):
     assert isinstance(lib.tpmlp_last_error(), bytes)
