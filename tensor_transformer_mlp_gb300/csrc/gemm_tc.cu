@@ -42,7 +42,10 @@ constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
 constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;
 constexpr int GROUP_M = 16;
 constexpr int BARRIER_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BARRIER_BYTES + 1024;  // + alignment slack
+// Per epilogue warp: 32 rows x 128 bytes, used to turn the one-row-per-thread layout of
+// tcgen05.ld into line-wide global stores (kEpiStore, kEpiStoreF32).
+constexpr int EPI_STAGE_BYTES = 32 * 128;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;  // + slack
 
 static_assert(A_STAGE_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -180,6 +183,58 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
   }
 }
 
+// Store path for kEpiStore (bf16, 64 columns) and kEpiStoreF32 (fp32, 32 columns): each thread
+// holds 128 bytes of its own row in seg[]; they go through the warp's shared-memory buffer
+// (16-byte segments XOR-swizzled by row, so both phases are free of bank conflicts) and leave
+// as 8 rows x 128 contiguous bytes per store instruction instead of 32 rows x 16 bytes.
+// prow is this lane's destination row (-1 past M); every lane of the warp must call this.
+template <bool F32OUT>
+__device__ __forceinline__ void store_staged(uint8_t* buf, const uint4 (&seg)[8], int lane, int64_t prow, void* out,
+                                             int64_t ldo, int col0, int N) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = seg[j];
+  __syncwarp();
+  constexpr int kElemsPerSeg = F32OUT ? 4 : 8;
+  const int j = lane & 7;
+  const int col = col0 + j * kElemsPerSeg;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const uint4 val = *reinterpret_cast<const uint4*>(buf + r * 128 + ((j ^ (r & 7)) << 4));
+    const int64_t pr = __shfl_sync(0xffffffffu, prow, r);
+    if (pr >= 0 && col < N) {
+      if constexpr (F32OUT) {
+        *reinterpret_cast<uint4*>(static_cast<float*>(out) + pr * ldo + col) = val;
+      } else {
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + pr * ldo + col) = val;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// Scale (batched) and bias (bf16 per column) for the store kinds, 8 columns at a time.
+template <int EPI, bool BATCHED>
+__device__ __forceinline__ void store_prologue8(const EpiParams& ep, int col, bool col_ok, float (&a)[8],
+                                                float alpha) {
+  if constexpr (BATCHED) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] *= alpha;
+  }
+  if constexpr (EPI == kEpiStore) {
+    if (ep.bias && col_ok) {
+      const uint4 bv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.bias) + col);
+      const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 bf = unpack_bf16x2(bw[i]);
+        a[2 * i] += bf.x;
+        a[2 * i + 1] += bf.y;
+      }
+    }
+  }
+}
+
 // One TMA tile load: 2-D map for plain launches; 4-D map (inner, then row and batch indices in
 // the slots recorded in BatchDev) for batched ones.
 template <bool BATCHED>
@@ -203,7 +258,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_stage + NUM_EPI_WARPS * EPI_STAGE_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;
   uint64_t* tempty_bar = tfull_bar + NUM_ACC;
@@ -360,14 +416,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t out_off = BATCHED ? z1 * bd.out_z1 + z2 * bd.out_z2 : 0;
       const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (EPI == kEpiStore || EPI == kEpiStoreF32) {
+        constexpr bool kF32 = EPI == kEpiStoreF32;
+        constexpr int kCols = kF32 ? 32 : 64;  // 128 bytes of output per row per pass
+        uint8_t* buf = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
+        const int64_t prow = row < M ? remap_row(ep.remap, row) : -1;
+        void* out = kF32 ? static_cast<void*>(static_cast<float*>(ep.out) + out_off)
+                         : static_cast<void*>(static_cast<__nv_bfloat16*>(ep.out) + out_off);
+        const float alpha = BATCHED ? bd.alpha : 1.f;
 #pragma unroll 1
-      for (int c = c_begin; c < c_begin + kChunks; ++c) {
-        const int col0 = nb * BN + c * 32;
-        if (col0 >= N) break;  // uniform across the warp
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
-        tmem_ld_wait();
-        if (row < M) epilogue_row32<EPI, BATCHED>(ep, row, col0, N, v, out_off, BATCHED ? bd.alpha : 1.f);
+        for (int c = c_begin; c < c_begin + kChunks; c += kCols / 32) {
+          const int col0 = nb * BN + c * 32;
+          if (col0 >= N) break;  // uniform across the warp
+          uint32_t v[kCols];
+          if constexpr (!kF32)
+            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+          tmem_ld_wait();
+          uint4 seg[8];
+#pragma unroll
+          for (int g = 0; g < kCols / 8; ++g) {
+            float a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
+            store_prologue8<EPI, BATCHED>(ep, col0 + g * 8, col0 + g * 8 < N, a, alpha);
+            if constexpr (kF32) {
+              seg[2 * g] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                      __float_as_uint(a[3]));
+              seg[2 * g + 1] = make_uint4(__float_as_uint(a[4]), __float_as_uint(a[5]), __float_as_uint(a[6]),
+                                          __float_as_uint(a[7]));
+            } else {
+              seg[g] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                                  pack_bf16x2(a[6], a[7]));
+            }
+          }
+          store_staged<kF32>(buf, seg, lane, prow, out, ep.ldo, col0, N);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = c_begin; c < c_begin + kChunks; ++c) {
+          const int col0 = nb * BN + c * 32;
+          if (col0 >= N) break;  // uniform across the warp
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
+          tmem_ld_wait();
+          if (row < M) epilogue_row32<EPI, BATCHED>(ep, row, col0, N, v, out_off, BATCHED ? bd.alpha : 1.f);
+        }
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
