@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 GEMM_LAUNCHES_PER_STEP = 6
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the
 # committed ncu summary named below; None until a capture of the current kernel exists.
-DOMINANT_KERNEL_TRAFFIC = 9439155797  # average over the six GEMM launches of one step
-DOMINANT_KERNEL_PROFILE = "profiles/gemm_bf16_kernel_large_mlp_dram.md"
+DOMINANT_KERNEL_TRAFFIC = 9754046592  # average over the six GEMM launches of one step
+DOMINANT_KERNEL_PROFILE = "profiles/gemm_bf16_pair_kernel_large_mlp_dram.md"
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -508,7 +508,8 @@ def run_ours(args, cfg):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "traffic": DOMINANT_KERNEL_TRAFFIC if cfg is wl.LARGE_MLP else None,
-                     "kernel": "gemm_bf16_kernel (tcgen05; 6 launches per step, 2*n*d*m FLOP each)",
+                     "kernel": "gemm_bf16_pair_kernel (tcgen05 cta_group::2, 256x256 tiles on SM pairs; "
+                               "6 launches per step, 2*n*d*m FLOP each)",
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
                      "traffic_profile": DOMINANT_KERNEL_PROFILE if cfg is wl.LARGE_MLP else None},
         "e2e": {"value": e2e_flops / e2e_elapsed / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -6,12 +6,18 @@
 //   wgrad    dB = Y^T G, dA = X^T D                 (fp32 out, K = tokens)
 //   dgrad-2  dX = D A^T         K-loop over all t shards = the f sum
 //
-// Design (one CTA per SM, persistent):
-//   warp 0      one thread issues TMA tile loads into a 4-stage shared-memory ring
-//   warp 1      one thread issues tcgen05.mma (M=128, N=256, K=16) into a tensor-memory
+// Two persistent kernels, one CTA per SM, sharing the epilogue code:
+//   gemm_bf16_pair_kernel (plain GEMMs): 256 x 256 tiles on clusters of two SMs
+//               (tcgen05 cta_group::2), 6-stage ring of 32 KB per SM, paced pairs
+//   gemm_bf16_kernel (batched GEMMs, or all of them with TPMLP_GEMM_PAIR=0): 128 x 256
+//               tiles on one SM, 4-stage ring of 48 KB
+// Warp roles in both:
+//   warp 0      one thread issues TMA tile loads into the shared-memory ring
+//   warp 1      one thread issues tcgen05.mma (K=16 steps) into a tensor-memory
 //               accumulator; two accumulators (2 x 256 columns) let the epilogue of one
 //               tile overlap the main loop of the next
-//   warps 2..9  epilogue: tcgen05.ld the fp32 tile, apply the fused op, store (two warps per
+//   warps 2..9  epilogue: tcgen05.ld the fp32 tile, apply the fused op, store through a
+//               per-warp shared-memory transpose in whole 128-byte lines (two warps per
 //               tensor-memory lane quarter, each taking half of the 256 columns)
 // Operands are staged with 128-byte swizzle; K-major and MN-major layouts are both
 // read in place through the descriptors' major-ness bits, so no operand is transposed
@@ -19,6 +25,8 @@
 // records a timeout, drains its own copies and MMAs, frees tensor memory and returns.
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -83,11 +91,12 @@ struct BatchDev {
   float alpha;
 };
 
-// Applies the epilogue to 32 consecutive accumulator columns of one row. Batched launches
-// (kEpiStore, kEpiStoreF32 only) scale by alpha and write at out + out_off.
-template <int EPI, bool BATCHED = false>
+// Applies the epilogues that read as well as write (kEpiAccumF32, kEpiDropoutResidual) to
+// 32 consecutive accumulator columns of one row.
+template <int EPI>
 __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row, int col0, int N,
-                                               const uint32_t (&v)[32], int64_t out_off = 0, float alpha = 1.f) {
+                                               const uint32_t (&v)[32]) {
+  static_assert(EPI == kEpiAccumF32 || EPI == kEpiDropoutResidual, "the other kinds are staged");
   uint32_t drop_bits = 0;  // kEpiDropoutResidual: one mask word per 32 columns
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
@@ -96,50 +105,11 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
     float a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
-    if constexpr (BATCHED) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] *= alpha;
-    }
-    if constexpr (EPI == kEpiGelu || EPI == kEpiStore) {
-      if (ep.bias) {  // per-column bias (bf16), uniform across the warp
-        const uint4 bv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.bias) + col);
-        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 bf = unpack_bf16x2(bw[i]);
-          a[2 * i] += bf.x;
-          a[2 * i + 1] += bf.y;
-        }
-      }
-    }
-    if constexpr (EPI == kEpiStoreF32) {
-      const int64_t prow = remap_row(ep.remap, row);
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + out_off + prow * ep.ldo + col);
-      dst[0] = make_float4(a[0], a[1], a[2], a[3]);
-      dst[1] = make_float4(a[4], a[5], a[6], a[7]);
-    } else if constexpr (EPI == kEpiAccumF32) {
+    if constexpr (EPI == kEpiAccumF32) {
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ep.out) + row * ep.ldo + col);
       const float4 o0 = dst[0], o1 = dst[1];
       dst[0] = make_float4(o0.x + a[0], o0.y + a[1], o0.z + a[2], o0.w + a[3]);
       dst[1] = make_float4(o1.x + a[4], o1.y + a[5], o1.z + a[6], o1.w + a[7]);
-    } else if constexpr (EPI == kEpiStore) {
-      const int64_t prow = remap_row(ep.remap, row);
-      uint4 pk = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                            pack_bf16x2(a[6], a[7]));
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + out_off + prow * ep.ldo + col) = pk;
-    } else if constexpr (EPI == kEpiGelu) {
-      const int64_t off = row * ep.ldo + col;
-      if (ep.out) {
-        uint4 z = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                             pack_bf16x2(a[6], a[7]));
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + off) = z;
-      }
-      float y[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = gelu_f<false>(a[i], ep.gelu);
-      uint4 yy = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                            pack_bf16x2(y[6], y[7]));
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out2) + off) = yy;
     } else if constexpr (EPI == kEpiDropoutResidual) {
       const int64_t prow = remap_row(ep.remap, row);
       const int64_t off = prow * ep.ldo + col;
@@ -160,20 +130,6 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
       }
       uint4 pk = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                             pack_bf16x2(o[6], o[7]));
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + off) = pk;
-    } else if constexpr (EPI == kEpiDGelu) {
-      const int64_t off = row * ep.ldo + col;
-      const uint4 z = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.aux) + off);
-      const uint32_t zw[4] = {z.x, z.y, z.z, z.w};
-      float d[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 zf = unpack_bf16x2(zw[i]);
-        d[2 * i] = a[2 * i] * gelu_grad_f<false>(zf.x, ep.gelu);
-        d[2 * i + 1] = a[2 * i + 1] * gelu_grad_f<false>(zf.y, ep.gelu);
-      }
-      uint4 pk = make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]), pack_bf16x2(d[4], d[5]),
-                            pack_bf16x2(d[6], d[7]));
       *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ep.out) + off) = pk;
     }
   }
@@ -213,6 +169,27 @@ __device__ __forceinline__ void store_staged(uint8_t* buf, const uint4 (&seg)[8]
   __syncwarp();
 }
 
+// The inverse of store_staged for bf16: the warp reads 32 rows x 64 columns of src with
+// line-wide loads (8 rows x 128 bytes per instruction) and each thread receives its own row's
+// 128 bytes in seg[] (zeros past M or N).
+__device__ __forceinline__ void load_staged_bf16(uint8_t* buf, uint4 (&seg)[8], int lane, int64_t prow,
+                                                 const void* src, int64_t ldo, int col0, int N) {
+  const int j = lane & 7;
+  const int col = col0 + j * 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const int64_t pr = __shfl_sync(0xffffffffu, prow, r);
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (pr >= 0 && col < N) val = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + pr * ldo + col);
+    *reinterpret_cast<uint4*>(buf + r * 128 + ((j ^ (r & 7)) << 4)) = val;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) seg[jj] = *reinterpret_cast<const uint4*>(buf + lane * 128 + ((jj ^ (lane & 7)) << 4));
+  __syncwarp();
+}
+
 // Scale (batched) and bias (bf16 per column) for the store kinds, 8 columns at a time.
 template <int EPI, bool BATCHED>
 __device__ __forceinline__ void store_prologue8(const EpiParams& ep, int col, bool col_ok, float (&a)[8],
@@ -231,6 +208,116 @@ __device__ __forceinline__ void store_prologue8(const EpiParams& ep, int col, bo
         a[2 * i] += bf.x;
         a[2 * i + 1] += bf.y;
       }
+    }
+  }
+}
+
+// The epilogue of one accumulator tile for one epilogue warp: its 32 tensor-memory lanes
+// (rows row - lane .. row - lane + 31 of the output) and its kEpiChunks 32-column chunks from
+// c_begin, starting at output column col_tile0. buf is the warp's staging buffer.
+constexpr int kEpiChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp
+
+template <int EPI, bool BATCHED>
+__device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf, int lane, int64_t row, int M, int N,
+                                              int col_tile0, int c_begin, uint32_t t_row, int64_t out_off,
+                                              float alpha) {
+  if constexpr (EPI == kEpiStore || EPI == kEpiStoreF32) {
+    constexpr bool kF32 = EPI == kEpiStoreF32;
+    constexpr int kCols = kF32 ? 32 : 64;  // 128 bytes of output per row per pass
+    const int64_t prow = row < M ? remap_row(ep.remap, row) : -1;
+    void* out = kF32 ? static_cast<void*>(static_cast<float*>(ep.out) + out_off)
+                     : static_cast<void*>(static_cast<__nv_bfloat16*>(ep.out) + out_off);
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kEpiChunks; c += kCols / 32) {
+      const int col0 = col_tile0 + c * 32;
+      if (col0 >= N) break;  // uniform across the warp
+      uint32_t v[kCols];
+      if constexpr (!kF32)
+        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_wait();
+      uint4 seg[8];
+#pragma unroll
+      for (int g = 0; g < kCols / 8; ++g) {
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
+        store_prologue8<EPI, BATCHED>(ep, col0 + g * 8, col0 + g * 8 < N, a, alpha);
+        if constexpr (kF32) {
+          seg[2 * g] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                  __float_as_uint(a[3]));
+          seg[2 * g + 1] = make_uint4(__float_as_uint(a[4]), __float_as_uint(a[5]), __float_as_uint(a[6]),
+                                      __float_as_uint(a[7]));
+        } else {
+          seg[g] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                              pack_bf16x2(a[6], a[7]));
+        }
+      }
+      store_staged<kF32>(buf, seg, lane, prow, out, ep.ldo, col0, N);
+    }
+  } else if constexpr (EPI == kEpiGelu) {
+    // Z (optional) and Y = gelu(Z), 64 columns per pass, both through the staging buffer.
+    const int64_t prow = row < M ? row : -1;
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kEpiChunks; c += 2) {
+      const int col0 = col_tile0 + c * 32;
+      if (col0 >= N) break;  // uniform across the warp
+      uint32_t v[64];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait();
+      uint4 zs[8], ys[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
+        store_prologue8<kEpiStore, false>(ep, col0 + g * 8, col0 + g * 8 < N, a, 1.f);  // bias1
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = gelu_f<false>(a[i], ep.gelu);
+        zs[g] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                           pack_bf16x2(a[6], a[7]));
+        ys[g] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                           pack_bf16x2(y[6], y[7]));
+      }
+      if (ep.out) store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
+      store_staged<false>(buf, ys, lane, prow, ep.out2, ep.ldo, col0, N);
+    }
+  } else if constexpr (EPI == kEpiDGelu) {
+    // D = acc * gelu'(Z): Z read and D written 64 columns at a time through the staging buffer.
+    const int64_t prow = row < M ? row : -1;
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kEpiChunks; c += 2) {
+      const int col0 = col_tile0 + c * 32;
+      if (col0 >= N) break;  // uniform across the warp
+      uint32_t v[64];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      uint4 zs[8];
+      load_staged_bf16(buf, zs, lane, prow, ep.aux, ep.ldo, col0, N);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {  // D overwrites Z in place
+        uint32_t* w = reinterpret_cast<uint32_t*>(&zs[g]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 zf = unpack_bf16x2(w[i]);
+          w[i] = pack_bf16x2(__uint_as_float(v[g * 8 + 2 * i]) * gelu_grad_f<false>(zf.x, ep.gelu),
+                             __uint_as_float(v[g * 8 + 2 * i + 1]) * gelu_grad_f<false>(zf.y, ep.gelu));
+        }
+      }
+      store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
+    }
+  } else {
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kEpiChunks; ++c) {
+      const int col0 = col_tile0 + c * 32;
+      if (col0 >= N) break;  // uniform across the warp
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
+      tmem_ld_wait();
+      if (row < M) epilogue_row32<EPI>(ep, row, col0, N, v);
     }
   }
 }
@@ -402,8 +489,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
-    constexpr int kChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp
-    const int c_begin = ((warp - 2) / 4) * kChunks;
+    const int c_begin = ((warp - 2) / 4) * kEpiChunks;
     int it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -416,53 +502,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t out_off = BATCHED ? z1 * bd.out_z1 + z2 * bd.out_z2 : 0;
       const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if constexpr (EPI == kEpiStore || EPI == kEpiStoreF32) {
-        constexpr bool kF32 = EPI == kEpiStoreF32;
-        constexpr int kCols = kF32 ? 32 : 64;  // 128 bytes of output per row per pass
-        uint8_t* buf = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
-        const int64_t prow = row < M ? remap_row(ep.remap, row) : -1;
-        void* out = kF32 ? static_cast<void*>(static_cast<float*>(ep.out) + out_off)
-                         : static_cast<void*>(static_cast<__nv_bfloat16*>(ep.out) + out_off);
-        const float alpha = BATCHED ? bd.alpha : 1.f;
-#pragma unroll 1
-        for (int c = c_begin; c < c_begin + kChunks; c += kCols / 32) {
-          const int col0 = nb * BN + c * 32;
-          if (col0 >= N) break;  // uniform across the warp
-          uint32_t v[kCols];
-          if constexpr (!kF32)
-            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
-          tmem_ld_wait();
-          uint4 seg[8];
-#pragma unroll
-          for (int g = 0; g < kCols / 8; ++g) {
-            float a[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
-            store_prologue8<EPI, BATCHED>(ep, col0 + g * 8, col0 + g * 8 < N, a, alpha);
-            if constexpr (kF32) {
-              seg[2 * g] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
-                                      __float_as_uint(a[3]));
-              seg[2 * g + 1] = make_uint4(__float_as_uint(a[4]), __float_as_uint(a[5]), __float_as_uint(a[6]),
-                                          __float_as_uint(a[7]));
-            } else {
-              seg[g] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                                  pack_bf16x2(a[6], a[7]));
-            }
-          }
-          store_staged<kF32>(buf, seg, lane, prow, out, ep.ldo, col0, N);
-        }
-      } else {
-#pragma unroll 1
-        for (int c = c_begin; c < c_begin + kChunks; ++c) {
-          const int col0 = nb * BN + c * 32;
-          if (col0 >= N) break;  // uniform across the warp
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
-          tmem_ld_wait();
-          if (row < M) epilogue_row32<EPI, BATCHED>(ep, row, col0, N, v, out_off, BATCHED ? bd.alpha : 1.f);
-        }
-      }
+      epilogue_tile<EPI, BATCHED>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N, nb * BN, c_begin,
+                                  t_row, out_off, BATCHED ? bd.alpha : 1.f);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
@@ -474,6 +515,245 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------- CTA-pair kernel
+// The same GEMM on 256 x 256 tiles computed by a cluster of two CTAs on two SMs
+// (tcgen05 cta_group::2): each CTA loads its 128 rows of A and 128 of the tile's 256 B
+// columns, so each SM fills 32 KB of shared memory per 64-deep k-block instead of 48 KB and
+// six stages fit where four did; one thread of the even CTA issues M256 N256 K16 MMAs that
+// read both CTAs' operands and write 128 accumulator rows into each CTA's tensor memory.
+//   barriers: full[s] (even CTA; both CTAs' copies complete on it), empty[s] (each CTA;
+//   the MMA commit arrives on both), tfull[acc] (each CTA; multicast commit), tempty[acc]
+//   (even CTA; all epilogue threads of both CTAs arrive), drain (even CTA).
+constexpr int PAIR_STAGES = 6;
+constexpr int BN_HALF = BN / 2;                               // B columns loaded per CTA
+constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + BN_HALF * BK * 2;  // 32 KiB
+constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;
+constexpr int PAIR_GROUP_M = GROUP_M / 2;                     // in 256-row pair blocks
+static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory budget (pair kernel)");
+static_assert((2 * PAIR_STAGES + 2 * NUM_ACC + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area");
+
+constexpr int kPaceKb = 32;                 // k-blocks between pacing points
+constexpr uint64_t kPaceWaitNs = 50000;     // longest pause at one pacing point
+
+// Spins (bounded by limit_ns) until *ctr >= target; a pacing hint, so expiry is not an error.
+__device__ __forceinline__ void pace_wait(const unsigned int* ctr, unsigned int target, uint64_t limit_ns) {
+  auto read = [&] {
+    unsigned int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    return v;
+  };
+  if (read() >= target) return;
+  const uint64_t t0 = global_timer_ns();
+  while (read() < target) {
+    if (global_timer_ns() - t0 > limit_ns) return;
+    __nanosleep(64);
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                          int M, int N, int K, EpiParams ep, unsigned int* status, int group,
+                          unsigned int* pace) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* epi_stage = smem + PAIR_STAGES * PAIR_STAGE_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_stage + NUM_EPI_WARPS * EPI_STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + PAIR_STAGES;
+  uint64_t* tfull_bar = empty_bar + PAIR_STAGES;
+  uint64_t* tempty_bar = tfull_bar + NUM_ACC;
+  uint64_t* drain_bar = tempty_bar + NUM_ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+  const int num_mb = (M + 2 * BM - 1) / (2 * BM);
+  const int num_nb = (N + BN - 1) / BN;
+  const int num_tiles = num_mb * num_nb;
+  // group > 0: bands of `group` pair-rows, each walked N-block by N-block (M fastest);
+  // group < 0: bands of -group N-blocks, walked pair-row by pair-row (N fastest).
+  auto coords = [&](int tile, int& mb, int& nb) {
+    if (group > 0) {
+      const int group_size = group * num_nb;
+      const int g = tile / group_size;
+      const int first_mb = g * group;
+      const int gsz = min(num_mb - first_mb, group);
+      const int in_group = tile - g * group_size;
+      mb = first_mb + in_group % gsz;
+      nb = in_group / gsz;
+    } else {
+      const int gn = -group;
+      const int group_size = gn * num_mb;
+      const int g = tile / group_size;
+      const int first_nb = g * gn;
+      const int gsz = min(num_nb - first_nb, gn);
+      const int in_group = tile - g * group_size;
+      nb = first_nb + in_group % gsz;
+      mb = in_group / gsz;
+    }
+  };
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (warp == 0 && lane == 0) {
+#pragma unroll
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+#pragma unroll
+    for (int a = 0; a < NUM_ACC; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 2 * NUM_EPI_THREADS);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers initialised in both CTAs before either signals the other
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer (both CTAs)
+      int kiter = 0;
+      bool ok = true;
+      // Pacing (even CTAs, when pace != null): every kPaceKb k-blocks a pair announces itself on
+      // *pace and first waits, for at most kPaceWaitNs, until every pair with a tile in the
+      // same round has announced the previous point. Pairs that share operand panels then stay
+      // within a few dozen k-blocks of each other and find the panels in L2 instead of
+      // re-reading them from DRAM. The wait only delays loads; it is never an error. The host
+      // zeroes the counter before the launch.
+      const bool pacer = pace != nullptr && rank == 0;
+      unsigned int pace_target = 0;  // announcements of all earlier points
+      for (int tile = pair, round = 0; tile < num_tiles && ok; tile += num_pairs, ++round) {
+        int mb, nb;
+        coords(tile, mb, nb);
+        const int a_row = mb * 2 * BM + static_cast<int>(rank) * BM;
+        const int b_col = nb * BN + static_cast<int>(rank) * BN_HALF;
+        const unsigned int active = static_cast<unsigned int>(min(num_pairs, num_tiles - round * num_pairs));
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (pacer && kb % kPaceKb == 0) {
+            pace_wait(pace, pace_target, kPaceWaitNs);
+            atomicAdd(pace, 1u);
+            pace_target += active;
+          }
+          const int s = kiter % PAIR_STAGES;
+          const uint32_t parity = ((kiter / PAIR_STAGES) & 1) ^ 1;
+          if (!mbar_wait_cluster(&empty_bar[s], parity, status, 11)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * PAIR_STAGE_BYTES);
+          const uint32_t full0 = map_to_cta(&full_bar[s], 0);
+          uint8_t* sa = smem + s * PAIR_STAGE_BYTES;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          if constexpr (!A_MN) {
+            tma_load_2d_pair(sa, &tmap_a, full0, kb * BK, a_row);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * MN_BOX_BYTES, &tmap_a, full0, a_row + j * 64, kb * BK);
+          }
+          if constexpr (!B_MN) {
+            tma_load_2d_pair(sb, &tmap_b, full0, kb * BK, b_col);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN_HALF / 64; ++j)
+              tma_load_2d_pair(sb + j * MN_BOX_BYTES, &tmap_b, full0, b_col + j * 64, kb * BK);
+          }
+          ++kiter;
+        }
+      }
+      // The even CTA's full barriers count both CTAs' copies: once its last phases have
+      // completed (at once on the normal path), no copy of the pair is still in flight.
+      if (rank == 0)
+        for (int k = max(0, kiter - PAIR_STAGES); k < kiter; ++k)
+          mbar_wait_cluster(&full_bar[k % PAIR_STAGES], (k / PAIR_STAGES) & 1, status, 12);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA issuer (even CTA)
+      constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+      int kiter = 0, it = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        if (!mbar_wait_cluster(&tempty_bar[acc], (use & 1) ^ 1, status, 13)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          const int s = kiter % PAIR_STAGES;
+          if (!mbar_wait_cluster(&full_bar[s], (kiter / PAIR_STAGES) & 1, status, 14)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + s * PAIR_STAGE_BYTES);
+          const uint32_t b_base = a_base + A_STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t adesc = A_MN ? smem_desc_sw128(a_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                        : smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? smem_desc_sw128(b_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                        : smem_desc_sw128(b_base + kk * 32, 16, 1024);
+            umma_bf16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair_mc(&empty_bar[s], 0x3);  // frees stage s in both CTAs
+          ++kiter;
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(&tfull_bar[acc], 0x3);  // both halves of the accumulator ready
+      }
+      umma_commit_pair(drain_bar);
+      mbar_wait_cluster(drain_bar, 0, status, 15);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int c_begin = ((warp - 2) / 4) * kEpiChunks;
+    int it = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      const bool ok = mbar_wait_cluster(&tfull_bar[acc], use & 1, status, 16);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      int mb, nb;
+      coords(tile, mb, nb);
+      const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      epilogue_tile<EPI, false>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N, nb * BN, c_begin,
+                                t_row, 0, 1.f);
+      tc_fence_before();
+      mbar_arrive_cluster(map_to_cta(&tempty_bar[acc], 0));
+    }
+  }
+
+  // Neither CTA frees tensor memory or leaves (its barriers are targets of the other's
+  // arrivals) before both are done.
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -524,6 +804,81 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, i
   return cudaGetLastError();
 }
 
+// Pacing counters of the pair kernel: a small pool handed out round-robin so that launches
+// in flight on different streams use different counters; each is zeroed on the launch's
+// stream before the launch. TPMLP_PAIR_PACE=0 turns pacing off.
+__device__ unsigned int g_pace_counters[64];
+
+unsigned int* next_pace_counter() {
+  static const bool on = [] {
+    const char* v = std::getenv("TPMLP_PAIR_PACE");
+    return !(v && v[0] == '0');
+  }();
+  if (!on) return nullptr;
+  static std::atomic<unsigned int> next{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return nullptr;
+  static unsigned int* base[16] = {};
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!base[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_pace_counters) != cudaSuccess) return nullptr;
+      base[dev] = static_cast<unsigned int*>(p);
+    }
+  }
+  return base[dev] + (next.fetch_add(1) % 64);
+}
+
+// Tile-order band of the pair kernel (see gemm_bf16_pair_kernel); TPMLP_PAIR_GROUP overrides.
+int pair_group() {
+  static const int g = [] {
+    const char* v = std::getenv("TPMLP_PAIR_GROUP");
+    const int x = v ? std::atoi(v) : 0;
+    return x != 0 ? x : PAIR_GROUP_M;
+  }();
+  return g;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
+                        cudaStream_t stream, const DeviceCtx& ctx) {
+  auto kernel = gemm_bf16_pair_kernel<A_MN, B_MN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = static_cast<int64_t>((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
+  const int64_t max_pairs = ctx.num_sms / 2;
+  const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  unsigned int* pace = next_pace_counter();
+  if (pace) {
+    e = cudaMemsetAsync(pace, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, ep, ctx.status, pair_group(), pace);
+}
+
+// Pair kernel unless TPMLP_GEMM_PAIR=0 (the single-SM kernel then runs every plain GEMM).
+bool use_pair_kernel() {
+  static const bool on = [] {
+    const char* v = std::getenv("TPMLP_GEMM_PAIR");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 // 4-D bf16 tensor map over a batched operand: dimension 0 is the contiguous column index; the
 // row index and the two batch indices take dimensions 1..3 in order of increasing stride.
 // box_inner x box_row elements are copied per load (one row slab of one batch index).
@@ -568,12 +923,32 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
   // The stored shapes must match the contraction.
   if (a.mn_major ? (a.rows != K || a.cols != M) : (a.rows != M || a.cols != K)) return cudaErrorInvalidValue;
   if (b.mn_major ? (b.rows != K || b.cols != N) : (b.rows != N || b.cols != K)) return cudaErrorInvalidValue;
+  const bool pair = use_pair_kernel() && ctx.num_sms >= 2;
   CUtensorMap ta, tb;
   cudaError_t e = make_tmap(&ta, a, 64, a.mn_major ? BK : BM);
   if (e != cudaSuccess) return e;
-  e = make_tmap(&tb, b, 64, b.mn_major ? BK : BN);
+  e = make_tmap(&tb, b, 64, b.mn_major ? BK : (pair ? BN_HALF : BN));
   if (e != cudaSuccess) return e;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (pair) {
+    if (!a.mn_major && b.mn_major) {
+      if (epi == kEpiGelu) return launch_pair<false, true, kEpiGelu>(ta, tb, m, n, k, ep, stream, ctx);
+      if (epi == kEpiStore) return launch_pair<false, true, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
+      if (epi == kEpiStoreF32) return launch_pair<false, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
+      if (epi == kEpiDropoutResidual) {
+        if (N % 32 != 0) return cudaErrorInvalidValue;
+        return launch_pair<false, true, kEpiDropoutResidual>(ta, tb, m, n, k, ep, stream, ctx);
+      }
+    } else if (!a.mn_major && !b.mn_major) {
+      if (epi == kEpiDGelu) return launch_pair<false, false, kEpiDGelu>(ta, tb, m, n, k, ep, stream, ctx);
+      if (epi == kEpiStore) return launch_pair<false, false, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
+      if (epi == kEpiStoreF32) return launch_pair<false, false, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
+    } else if (a.mn_major && b.mn_major) {
+      if (epi == kEpiStoreF32) return launch_pair<true, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
+      if (epi == kEpiAccumF32) return launch_pair<true, true, kEpiAccumF32>(ta, tb, m, n, k, ep, stream, ctx);
+    }
+    return cudaErrorNotSupported;
+  }
   if (!a.mn_major && b.mn_major) {
     if (epi == kEpiGelu) return launch<false, true, kEpiGelu>(ta, tb, m, n, k, ep, stream, ctx);
     if (epi == kEpiStore) return launch<false, true, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);

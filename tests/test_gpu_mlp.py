@@ -2,6 +2,8 @@
 the float64 oracle, element by element on seeded inputs; sampled rows and columns at the
 full sizes the benchmark runs."""
 import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -207,3 +209,15 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     O, _, _ = tp.forward(X, A, B, cfg.t, "tanh")
     torch.cuda.synchronize()
     assert_close("O", host(O), omlp.forward(inp["X"], inp["A"], inp["B"], "tanh")["O"], TOL_BF16)
+
+
+@pytest.mark.parametrize("env", [{"TPMLP_GEMM_PAIR": "0"}, {"TPMLP_PAIR_PACE": "0"}])
+def test_alternative_gemm_paths(env):
+    """The same parity cases on the one-SM GEMM kernel and on the SM-pair kernel without pacing
+    (both chosen once per process, so they run in a child pytest)."""
+    repo = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    child_env = dict(os.environ, **env)
+    cmd = [sys.executable, "-m", "pytest", os.path.join(repo, "tests", "test_gpu_mlp.py"), "-m", "gpu", "-q", "-x",
+           "-k", "ragged_bf16 or single_block or biased or accumulation or shard_count or gpt_mlp_sampled"]
+    r = subprocess.run(cmd, cwd=repo, env=child_env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
