@@ -435,59 +435,69 @@ def run_ours(args, cfg):
     flops_step = cfg.flops_fwd_bwd
     max_elapsed, total_flops = aggregate(elapsed, flops_step * args.steps, world, dev)
 
-    # End to end through the public API with host buffers: every step copies X, A, B, G from
-    # pinned host memory and reads O, dX, dA, dB back. The copies of neighbouring steps overlap
-    # the compute: step k+1's inputs go up on one stream and step k-1's results come down on
-    # another while step k runs, with two device buffer sets and events ordering the reuse.
-    hX, hA, hB, hG = (x.cpu().pin_memory() for x in (X, A, B, G))
-    hO, hdX = torch.empty_like(O, device="cpu").pin_memory(), torch.empty_like(dX, device="cpu").pin_memory()
-    hdA, hdB = torch.empty_like(dA, device="cpu").pin_memory(), torch.empty_like(dB, device="cpu").pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hX, hA, hB, hG))
-    d2h = sum(x.numel() * x.element_size() for x in (hO, hdX, hdA, hdB))
-    ins = [(X, A, B, G), tuple(torch.empty_like(x) for x in (X, A, B, G))]
-    outs = [(O, dX, dA, dB), tuple(torch.empty_like(x) for x in (O, dX, dA, dB))]
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()  # noqa: E731
-    in_ready, in_free = [ev(), ev()], [ev(), ev()]
-    done, out_free = [ev(), ev()], [ev(), ev()]
-    for e in in_free + out_free:
-        e.record(stream)
+    # End to end through the public API with host buffers, two ways. "layer": what one MLP layer
+    # of a training step moves, with its weights A, B and its fp32 gradient accumulators dA, dB
+    # resident on the device (uploaded once, read by the optimizer there): each step uploads the
+    # activations X and the upstream gradient G from pinned host memory and reads the output O
+    # and the input gradient dX back. "all": every tensor crosses every step (X, A, B, G up;
+    # O, dX, dA, dB down). In both, step k+1's uploads and step k-1's downloads overlap step k
+    # (two device buffer sets, one stream each way, events ordering the reuse).
+    def e2e_run(up_names, down_names, k_steps):
+        dev_in = {"X": X, "A": A, "B": B, "G": G}
+        dev_out = {"O": O, "dX": dX, "dA": dA, "dB": dB}
+        host_in = {k: dev_in[k].cpu().pin_memory() for k in up_names}
+        host_out = {k: torch.empty_like(dev_out[k], device="cpu").pin_memory() for k in down_names}
+        ins = [dict(dev_in), {k: (torch.empty_like(v) if k in up_names else v) for k, v in dev_in.items()}]
+        outs = [dict(dev_out), {k: (torch.empty_like(v) if k in down_names else v) for k, v in dev_out.items()}]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_ready, in_free = [ev(), ev()], [ev(), ev()]
+        done, out_free = [ev(), ev()], [ev(), ev()]
+        for e in in_free + out_free:
+            e.record(stream)
 
-    def e2e_steps_run(k_steps):
-        for k in range(k_steps):
-            j = k % 2
-            xi, ai, bi, gi = ins[j]
-            oi, dxi, dai, dbi = outs[j]
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(in_free[j])
-                for dst, src in ((xi, hX), (ai, hA), (bi, hB), (gi, hG)):
-                    dst.copy_(src, non_blocking=True)
-                in_ready[j].record(s_in)
-            stream.wait_event(in_ready[j])
-            stream.wait_event(out_free[j])
-            tp.tpmlp_forward(xi, ai, bi, oi, Z, Y, t, cfg.gelu, stream)
-            tp.tpmlp_backward(xi, ai, bi, gi, Z, Y, dxi, dai, dbi, t, cfg.gelu, ws, stream)
-            done[j].record(stream)
-            in_free[j].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(done[j])
-                for dst, src in ((hO, oi), (hdX, dxi), (hdA, dai), (hdB, dbi)):
-                    dst.copy_(src, non_blocking=True)
-                out_free[j].record(s_out)
+        def steps(k_n):
+            for k in range(k_n):
+                j = k % 2
+                xi, oi = ins[j], outs[j]
+                with torch.cuda.stream(s_in):
+                    s_in.wait_event(in_free[j])
+                    for name in up_names:
+                        xi[name].copy_(host_in[name], non_blocking=True)
+                    in_ready[j].record(s_in)
+                stream.wait_event(in_ready[j])
+                stream.wait_event(out_free[j])
+                tp.tpmlp_forward(xi["X"], xi["A"], xi["B"], oi["O"], Z, Y, t, cfg.gelu, stream)
+                tp.tpmlp_backward(xi["X"], xi["A"], xi["B"], xi["G"], Z, Y, oi["dX"], oi["dA"], oi["dB"], t,
+                                  cfg.gelu, ws, stream)
+                done[j].record(stream)
+                in_free[j].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done[j])
+                    for name in down_names:
+                        host_out[name].copy_(oi[name], non_blocking=True)
+                    out_free[j].record(s_out)
+
+        steps(2)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        stream.wait_event(e0)
+        s_out.wait_event(e0)
+        steps(k_steps)
+        e1.record(s_out)  # the last step's results are on the host once s_out reaches here
+        torch.cuda.synchronize()
+        el, fl = aggregate(e0.elapsed_time(e1) / 1e3, flops_step * k_steps, world, dev)
+        h2d = sum(host_in[k].numel() * host_in[k].element_size() for k in up_names)
+        d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in down_names)
+        del ins, outs, host_in, host_out
+        return fl / el / 1e12, h2d, d2h
 
     e2e_steps = max(4, args.steps // 2)
-    e2e_steps_run(2)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    stream.wait_event(e0)
-    s_out.wait_event(e0)
-    e2e_steps_run(e2e_steps)
-    e1.record(s_out)  # the last step's results are on the host once s_out reaches here
-    torch.cuda.synchronize()
-    e2e_elapsed, e2e_flops = aggregate(e0.elapsed_time(e1) / 1e3, flops_step * e2e_steps, world, dev)
+    e2e_layer, h2d, d2h = e2e_run(("X", "G"), ("O", "dX"), e2e_steps)
+    e2e_all, h2d_all, d2h_all = e2e_run(("X", "A", "B", "G"), ("O", "dX", "dA", "dB"), e2e_steps)
 
     if rank != 0:
         return 0
@@ -512,9 +522,14 @@ def run_ours(args, cfg):
                                "6 launches per step, 2*n*d*m FLOP each)",
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
                      "traffic_profile": DOMINANT_KERNEL_PROFILE if cfg is wl.LARGE_MLP else None},
-        "e2e": {"value": e2e_flops / e2e_elapsed / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "note": "pinned host buffers; step k+1's uploads and step k-1's downloads overlap step k"},
+        "e2e": {"value": e2e_layer, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps,
+                "note": "one training layer's traffic: X, G up and O, dX down every step from/to pinned host "
+                        "memory; weights A, B and fp32 gradient accumulators dA, dB resident on the device; "
+                        "step k+1's uploads and step k-1's downloads overlap step k"},
+        "e2e_all_tensors": {"value": e2e_all, "unit": UNIT, "h2d_bytes_per_step": h2d_all,
+                            "d2h_bytes_per_step": d2h_all, "steps": e2e_steps,
+                            "note": "every tensor crosses every step: X, A, B, G up; O, dX, dA, dB down"},
         "gpu_launches": GEMM_LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks,
     }
