@@ -8,7 +8,7 @@ import pytest
 import torch
 from scipy.integrate import quad
 
-from oracle import collectives, mlp, sp
+from oracle import collectives, mlp, rmsnorm, sp
 from tensor_transformer_mlp_gb300 import workloads as wl
 
 KINDS = ("erf", "tanh")
@@ -468,3 +468,71 @@ def test_softmax_rows_sum_to_one_and_shift_invariant():
     P = oattn.softmax(S)
     assert np.abs(P.sum(-1) - 1).max() < 1e-14
     assert np.abs(oattn.softmax(S + 100.0) - P).max() < 1e-14
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_unit_mean_square():
+    # With gamma = 1 and eps = 0 every output row has mean square exactly 1; a row scaled by
+    # any positive factor gives the same output (scale control), a shifted row does not.
+    x = _rand((32, 96), 80) * 4 + 2
+    y = rmsnorm.rmsnorm(x, np.ones(96), 0.0)
+    assert np.abs((y * y).mean(axis=1) - 1.0).max() < 1e-12
+    assert np.abs(rmsnorm.rmsnorm(7.5 * x, np.ones(96), 0.0) - y).max() < 1e-12
+    assert np.abs(rmsnorm.rmsnorm(x + 1.0, np.ones(96), 0.0) - y).max() > 1e-3
+
+
+def test_rmsnorm_matches_torch():
+    x = _rand((24, 128), 81)
+    g = _rand(128, 82)
+    for eps in (1e-6, 1e-2):
+        ref = torch.nn.functional.rms_norm(torch.tensor(x), (128,), torch.tensor(g), eps).numpy()
+        assert np.abs(rmsnorm.rmsnorm(x, g, eps) - ref).max() < 1e-12
+
+
+def test_rmsnorm_is_not_layernorm():
+    # Dropping the mean matters: on rows with a non-zero mean the two norms differ, and they
+    # agree on rows whose mean is zero (then mean(x^2) is the variance).
+    x = _rand((8, 64), 83) + 3.0
+    g, z = np.ones(64), np.zeros(64)
+    assert np.abs(rmsnorm.rmsnorm(x, g, 1e-5) - sp.layernorm(x, g, z, 1e-5)).max() > 0.1
+    xc = x - x.mean(axis=1, keepdims=True)
+    assert np.abs(rmsnorm.rmsnorm(xc, g, 1e-5) - sp.layernorm(xc, g, z, 1e-5)).max() < 1e-12
+
+
+def test_rmsnorm_backward_matches_torch_autograd():
+    x = _rand((12, 80), 84) * 2 + 0.5
+    g = _rand(80, 85)
+    dy = _rand((12, 80), 86)
+    tx, tg = torch.tensor(x, requires_grad=True), torch.tensor(g, requires_grad=True)
+    torch.nn.functional.rms_norm(tx, (80,), tg, 1e-5).backward(torch.tensor(dy))
+    dx, dg = rmsnorm.rmsnorm_backward(x, g, 1e-5, dy)
+    assert np.abs(dx - tx.grad.numpy()).max() < 1e-12
+    assert np.abs(dg - tg.grad.numpy()).max() < 1e-12
+
+
+def test_rmsnorm_backward_finite_differences():
+    x = _rand((3, 16), 87) + 0.3
+    g = _rand(16, 88)
+    dy = _rand((3, 16), 89)
+    eps, h = 1e-3, 1e-6
+    dx, dg = rmsnorm.rmsnorm_backward(x, g, eps, dy)
+    f = lambda xx, gg: float((rmsnorm.rmsnorm(xx, gg, eps) * dy).sum())  # noqa: E731
+    for idx in [(0, 0), (1, 7), (2, 15)]:
+        e = np.zeros_like(x)
+        e[idx] = h
+        assert abs((f(x + e, g) - f(x - e, g)) / (2 * h) - dx[idx]) < 1e-7
+    for j in (0, 9):
+        e = np.zeros_like(g)
+        e[j] = h
+        assert abs((f(x, g + e) - f(x, g - e)) / (2 * h) - dg[j]) < 1e-7
+
+
+def test_rmsnorm_gradient_orthogonal_to_x_only():
+    # Scale invariance (eps = 0): the gradient has no component along x (x_hat); unlike
+    # LayerNorm's it keeps its component along 1.
+    x = _rand((16, 64), 90) * 3 + 1
+    dy = _rand((16, 64), 91)
+    dx, _ = rmsnorm.rmsnorm_backward(x, np.ones(64), 0.0, dy)
+    assert np.abs((dx * x).sum(1)).max() < 1e-11
+    assert np.abs(dx.sum(1)).max() > 1e-3
