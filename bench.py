@@ -294,7 +294,15 @@ def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
     sec = timed(lambda i: tp.tpmlp_sp_dropout_residual(xs[i % sets], ys[i % sets], outs[i % sets], masks[i % sets],
                                                        cfg.p_drop, cfg.seed, stream), reps)
     entry("dropout_residual", sec, 3 * N * elt + N // 8, "read x, y + write out (bf16) + mask bits")
-    del full
+    sec = timed(lambda i: tp.tpmlp_rmsnorm(xs[i % sets], gamma, cfg.eps, ys[i % sets], stream), reps)
+    entry("rmsnorm", sec, 2 * N * elt, "read x + write RMSNorm(x), bf16")
+    dgs = [torch.empty(h, dtype=torch.float32, device=dev) for _ in range(sets)]
+    wsr = [torch.empty(tp.tpmlp_rmsnorm_backward_workspace_size(b * s, h), dtype=torch.uint8, device=dev)
+           for _ in range(sets)]
+    sec = timed(lambda i: tp.tpmlp_rmsnorm_backward(xs[i % sets], gamma, cfg.eps, ys[i % sets],
+                                                    outs[i % sets], dgs[i % sets], wsr[i % sets], stream), reps)
+    entry("rmsnorm_backward", sec, 3 * N * elt, "read x, dy + write dx (bf16); dgamma partials are small")
+    del full, wsr
     parts = torch.randn((t, b * s, h), dtype=torch.float32, device=dev)  # 1 GiB > L2
     sec = timed(lambda i: tp.tpmlp_sp_reduce_scatter(parts, outs[i % sets], stream), max(10, reps // 4))
     entry("reduce_scatter_splitk", sec, t * N * 4 + N * elt, "read t fp32 partials + write shards (bf16)")

@@ -227,6 +227,30 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
 tpmlp_status tpmlp_sp_layernorm(const void* x, const float* gamma, const float* beta, float eps,
                                 void* y, int64_t rows, int64_t h, tpmlp_dtype dt, void* stream);
 
+/*
+ * RMSNorm of `rows` rows of width h ("Megatron 训练" notes, section "RMSNorm": LayerNorm with
+ * the mean computation removed), for use in front of either block:
+ *   y = x / sqrt(mean(x^2) + eps) * gamma      (mean over the h elements of a row; no bias).
+ * x, y: [rows][h] in dt (may alias); gamma: [h] fp32 device. Statistics in fp32.
+ * Requires h % 8 == 0 and h <= 8192 (bf16) or 4096 (f32), eps > 0, 16-byte aligned pointers.
+ * Errors: TPMLP_ERR_SHAPE, TPMLP_ERR_INVALID (null pointer, eps), TPMLP_ERR_ALIGN, TPMLP_ERR_DTYPE.
+ */
+tpmlp_status tpmlp_rmsnorm(const void* x, const float* gamma, float eps, void* y, int64_t rows, int64_t h,
+                           tpmlp_dtype dt, void* stream);
+
+/*
+ * Backward of tpmlp_rmsnorm from dy = dl/dy ([rows][h], dt): with r = 1/sqrt(mean(x^2) + eps),
+ * x_hat = x r and g = dy gamma,
+ *   dx = r * (g - x_hat * mean(g * x_hat))     ([rows][h], dt, overwritten)
+ *   dgamma = sum over rows of dy * x_hat       ([h] fp32, overwritten; summed in a fixed order).
+ * workspace: device memory of tpmlp_rmsnorm_backward_workspace_size(rows, h) bytes (per-CTA
+ * partial sums), 16-byte aligned. Requires h % 8 == 0 and h <= 4096; rows == 0 zeroes dgamma.
+ */
+size_t tpmlp_rmsnorm_backward_workspace_size(int64_t rows, int64_t h);
+tpmlp_status tpmlp_rmsnorm_backward(const void* x, const float* gamma, float eps, const void* dy, void* dx,
+                                    float* dgamma, int64_t rows, int64_t h, tpmlp_dtype dt, void* workspace,
+                                    size_t ws_bytes, void* stream);
+
 /* g forward, all-gather ("Megatron-SP 机制", f/g operator table): [t][b][s/t][h] -> [b][s][h]. */
 tpmlp_status tpmlp_sp_gather(const void* x_shards, void* x_full,
                              int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype dt, void* stream);

@@ -13,6 +13,8 @@ from ._binding import (  # noqa: F401
     backward,
     forward,
     load_library,
+    rmsnorm,
+    rmsnorm_backward,
     sp_block,
     sp_block_backward,
     tpmlp_backward,
@@ -24,6 +26,9 @@ from ._binding import (  # noqa: F401
     tpmlp_device_status,
     tpmlp_forward,
     tpmlp_forward_biased,
+    tpmlp_rmsnorm,
+    tpmlp_rmsnorm_backward,
+    tpmlp_rmsnorm_backward_workspace_size,
     tpmlp_sp_block,
     tpmlp_sp_block_backward,
     tpmlp_sp_block_backward_workspace_size,

@@ -40,6 +40,9 @@ SIGNATURES = {
     "tpmlp_sp_block_backward": (_I, [_P, _P, _P, _F, _P, _P, _F, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                                      _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_sp_layernorm": (_I, [_P, _P, _P, _F, _P, _I64, _I64, _I, _P]),
+    "tpmlp_rmsnorm": (_I, [_P, _P, _F, _P, _I64, _I64, _I, _P]),
+    "tpmlp_rmsnorm_backward_workspace_size": (_SZ, [_I64, _I64]),
+    "tpmlp_rmsnorm_backward": (_I, [_P, _P, _F, _P, _P, _P, _I64, _I64, _I, _P, _SZ, _P]),
     "tpmlp_sp_gather": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_reduce_scatter": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_dropout_residual": (_I, [_P, _P, _P, _P, _F, _U64, _I64, _I64, _I64, _I, _I, _P]),
@@ -233,6 +236,28 @@ def tpmlp_sp_layernorm(x, gamma, beta, eps, y, stream=None) -> None:
                                              _stream(stream)))
 
 
+def tpmlp_rmsnorm(x, gamma, eps, y, stream=None) -> None:
+    h = x.shape[-1]
+    rows = x.numel() // h
+    assert y.shape == x.shape and gamma.shape == (h,) and gamma.dtype == torch.float32
+    _cuda(x, gamma, y)
+    _check(load_library().tpmlp_rmsnorm(_ptr(x), _ptr(gamma), eps, _ptr(y), rows, h, _dt(x), _stream(stream)))
+
+
+def tpmlp_rmsnorm_backward_workspace_size(rows: int, h: int) -> int:
+    return load_library().tpmlp_rmsnorm_backward_workspace_size(rows, h)
+
+
+def tpmlp_rmsnorm_backward(x, gamma, eps, dy, dx, dgamma, workspace, stream=None) -> None:
+    h = x.shape[-1]
+    rows = x.numel() // h
+    assert dy.shape == x.shape and dx.shape == x.shape and gamma.shape == (h,) and dgamma.shape == (h,)
+    assert dgamma.dtype == torch.float32 and workspace.dtype == torch.uint8
+    _cuda(x, gamma, dy, dx, dgamma, workspace)
+    _check(load_library().tpmlp_rmsnorm_backward(_ptr(x), _ptr(gamma), eps, _ptr(dy), _ptr(dx), _ptr(dgamma), rows, h,
+                                                 _dt(x), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
 def tpmlp_sp_gather(x_shards, x_full, stream=None) -> None:
     t, b, sl, h = x_shards.shape
     assert x_full.shape == (b, sl * t, h) and x_full.dtype == x_shards.dtype
@@ -340,6 +365,23 @@ def sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z, Y, dout
 
 
 # ----------------------------------------------------------------------- attention block
+
+def rmsnorm(x, gamma, eps: float = 1e-5, stream=None):
+    """Allocates y and runs tpmlp_rmsnorm."""
+    y = torch.empty_like(x)
+    tpmlp_rmsnorm(x, gamma, eps, y, stream)
+    return y
+
+
+def rmsnorm_backward(x, gamma, dy, eps: float = 1e-5, stream=None):
+    """Allocates dx, dgamma and the workspace and runs tpmlp_rmsnorm_backward; returns (dx, dgamma)."""
+    h = x.shape[-1]
+    dx = torch.empty_like(x)
+    dgamma = torch.empty(h, dtype=torch.float32, device=x.device)
+    ws = torch.empty(tpmlp_rmsnorm_backward_workspace_size(x.numel() // h, h), dtype=torch.uint8, device=x.device)
+    tpmlp_rmsnorm_backward(x, gamma, eps, dy, dx, dgamma, ws, stream)
+    return dx, dgamma
+
 
 def attention_forward(X, Wqkv, Wo, heads: int, t: int, stream=None):
     """X [b, s, h] bf16; allocates Y, the saves and the workspace and runs tpmlp_attention_forward.

@@ -396,7 +396,9 @@ __global__ void __launch_bounds__(kRowThreads)
 // one-pass variance E[d^2] - E[d]^2 free of cancellation for rows with a large mean), the
 // warps' partial sums go to per-warp shared-memory slots that every thread adds in a fixed
 // order after a single barrier (deterministic). Slots alternate between rows.
-template <typename T, int CH, int kRowThreads, int kRowStages, bool kAffineInRegs>
+// kRms: RMSNorm ("Megatron 训练" notes, section "RMSNorm": LayerNorm without the mean):
+// no shift, no mean, rstd = 1 / sqrt(mean(x^2) + eps), y = x * rstd * gamma (beta unused).
+template <typename T, int CH, int kRowThreads, int kRowStages, bool kAffineInRegs, bool kRms = false>
 __global__ void __launch_bounds__(kRowThreads)
     layernorm_staged_kernel(const T* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ beta,
                             float eps, T* __restrict__ y, int64_t rows, int h, unsigned int* status) {
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(kRowThreads)
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         greg[c][e] = col < h ? gamma[col + e] : 0.f;
-        breg[c][e] = col < h ? beta[col + e] : 0.f;
+        breg[c][e] = (!kRms && col < h) ? beta[col + e] : 0.f;
       }
     }
   }
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kRowThreads)
       break;
     }
     const T* xs = reinterpret_cast<const T*>(smem + st * row_bytes);
-    const float shift = static_cast<float>(xs[0]);
+    const float shift = kRms ? 0.f : static_cast<float>(xs[0]);
     float f[CH][8];
     float sum = 0.f, sq = 0.f;
 #pragma unroll
@@ -475,10 +477,10 @@ __global__ void __launch_bounds__(kRowThreads)
       tsum += ps.x;
       tsq += ps.y;
     }
-    const float md = tsum * inv_h;  // mean of x - shift
-    const float var = fmaxf(tsq * inv_h - md * md, 0.f);
+    const float md = kRms ? 0.f : tsum * inv_h;  // mean of x - shift
+    const float var = kRms ? tsq * inv_h : fmaxf(tsq * inv_h - md * md, 0.f);  // RMS: mean square
     const float rstd = rsqrtf(var + eps);
-    const float a0 = -(md + shift) * rstd;  // (x - mean) * rstd = x * rstd + a0
+    const float a0 = kRms ? 0.f : -(md + shift) * rstd;  // (x - mean) * rstd = x * rstd + a0
     const int64_t R = blockIdx.x + i * gridDim.x;
     T* yr = y + R * h;
 #pragma unroll
@@ -492,7 +494,11 @@ __global__ void __launch_bounds__(kRowThreads)
           for (int e = 0; e < 8; ++e) o[e] = fmaf(fmaf(f[c][e], rstd, a0), greg[c][e], breg[c][e]);
         } else {
           const float4 g0 = reinterpret_cast<const float4*>(gamma + col)[0], g1 = reinterpret_cast<const float4*>(gamma + col)[1];
-          const float4 b0 = reinterpret_cast<const float4*>(beta + col)[0], b1 = reinterpret_cast<const float4*>(beta + col)[1];
+          float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+          if constexpr (!kRms) {
+            b0 = reinterpret_cast<const float4*>(beta + col)[0];
+            b1 = reinterpret_cast<const float4*>(beta + col)[1];
+          }
           const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
           const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -663,7 +669,9 @@ __global__ void __launch_bounds__(128) dropout_grad_gather_kernel(const T* __res
 // bank conflicts); the CTA writes them to partials[blockIdx][2][h] for a fixed-order sum.
 constexpr int kLnBwdThreads = 128;
 
-template <typename T, int CH>
+// kRms: RMSNorm's backward, dx = [dout +] rstd * (g - x_hat * mean(g * x_hat)) with
+// x_hat = x * rstd (no shift, no mean, no mean(g) term). dout may be null (no residual).
+template <typename T, int CH, bool kRms = false>
 __global__ void __launch_bounds__(kLnBwdThreads, 4)
     layernorm_backward_kernel(const T* __restrict__ x, const T* __restrict__ dxn, const T* __restrict__ dout,
                               const float* __restrict__ gamma, float eps, T* __restrict__ dx,
@@ -688,8 +696,8 @@ __global__ void __launch_bounds__(kLnBwdThreads, 4)
   for (int64_t R = blockIdx.x; R < rows; R += gridDim.x, p ^= 1) {
     const T* xr = x + R * h;
     const T* dr = dxn + R * h;
-    const T* gr = dout + R * h;
-    const float shift = static_cast<float>(xr[0]);
+    const T* gr = dout ? dout + R * h : nullptr;
+    const float shift = kRms ? 0.f : static_cast<float>(xr[0]);
     float f[CH][8], dn[CH][8];
     Vec8<T> gv[CH];  // dout, loaded with x and dxn so that all of the row's reads are in flight at once
     float s_d = 0.f, s_dd = 0.f, s_g = 0.f, s_gd = 0.f;
@@ -700,23 +708,27 @@ __global__ void __launch_bounds__(kLnBwdThreads, 4)
         Vec8<T> xv, dv;
         xv.load(xr + col);
         dv.load(dr + col);
-        gv[c].load(gr + col);
+        if (gr) gv[c].load(gr + col);
         xv.to_float(f[c]);
         dv.to_float(dn[c]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float d = f[c][e] - shift;
           const float g = dn[c][e] * gam[c][e];
-          s_d += d;
+          if constexpr (!kRms) {
+            s_d += d;
+            s_g += g;
+          }
           s_dd = fmaf(d, d, s_dd);
-          s_g += g;
           s_gd = fmaf(g, d, s_gd);
         }
       }
     }
-    s_d = warp_sum(s_d);
+    if constexpr (!kRms) {
+      s_d = warp_sum(s_d);
+      s_g = warp_sum(s_g);
+    }
     s_dd = warp_sum(s_dd);
-    s_g = warp_sum(s_g);
     s_gd = warp_sum(s_gd);
     if (lane == 0) red[p][w] = make_float4(s_d, s_dd, s_g, s_gd);
     __syncthreads();
@@ -729,17 +741,17 @@ __global__ void __launch_bounds__(kLnBwdThreads, 4)
       t4.z += v.z;
       t4.w += v.w;
     }
-    const float md = t4.x * inv_h;
-    const float rstd = rsqrtf(fmaxf(t4.y * inv_h - md * md, 0.f) + eps);
-    const float mean_g = t4.z * inv_h;
+    const float md = kRms ? 0.f : t4.x * inv_h;
+    const float rstd = rsqrtf((kRms ? t4.y * inv_h : fmaxf(t4.y * inv_h - md * md, 0.f)) + eps);
+    const float mean_g = kRms ? 0.f : t4.z * inv_h;
     const float mean_gxh = rstd * (t4.w * inv_h - md * mean_g);  // mean(g * x_hat)
     T* outr = dx + R * h;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int col = (tid + c * kLnBwdThreads) * 8;
       if (col < h) {
-        float go[8], o[8];
-        gv[c].to_float(go);
+        float go[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, o[8];
+        if (gr) gv[c].to_float(go);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float xh = (f[c][e] - shift - md) * rstd;
@@ -787,7 +799,7 @@ __global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restri
 #pragma unroll
     for (int k = 0; k < 8; ++k) t += grp[k][lane];
     if (c < h) dgamma[c] = t;
-    else dbeta[c - h] = t;
+    else if (dbeta) dbeta[c - h] = t;
   }
 }
 
@@ -950,11 +962,13 @@ int rows_grid(int64_t rows, int num_sms, int per_sm) {
 }  // namespace
 
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, float eps, void* y, int64_t rows,
-                             int64_t h, bool bf16, cudaStream_t stream, int num_sms, unsigned int* status) {
+                             int64_t h, bool bf16, cudaStream_t stream, int num_sms, unsigned int* status, bool rms) {
   if (rows <= 0) return cudaSuccess;
   const size_t elt = bf16 ? 2 : 4;
   const size_t ln_smem = staged_smem(static_cast<size_t>(h) * elt, kLnStages);
-  if (h % 8 == 0 && h <= kLnStagedThreads * 8 * 8 && ln_smem <= kStagedSmemMax) {
+  const bool staged = h % 8 == 0 && h <= kLnStagedThreads * 8 * 8 && ln_smem <= kStagedSmemMax;
+  if (rms && !staged) return cudaErrorNotSupported;  // RMSNorm runs on the staged kernel only
+  if (staged) {
     const int by_smem = static_cast<int>((220 * 1024) / ln_smem);
     const int by_threads = 2048 / kLnStagedThreads;
     const int per_sm = by_smem < by_threads ? (by_smem > 0 ? by_smem : 1) : by_threads;
@@ -962,7 +976,8 @@ cudaError_t launch_layernorm(const void* x, const float* gamma, const float* bet
     const int ch = static_cast<int>((h / 8 + kLnStagedThreads - 1) / kLnStagedThreads);
 #define TPMLP_LN_STAGED(TYPE, CHN)                                                                              \
   do {                                                                                                          \
-    auto k = layernorm_staged_kernel<TYPE, CHN, kLnStagedThreads, kLnStages, kLnAffineInRegs>;                                   \
+    auto k = rms ? layernorm_staged_kernel<TYPE, CHN, kLnStagedThreads, kLnStages, kLnAffineInRegs, true>       \
+                 : layernorm_staged_kernel<TYPE, CHN, kLnStagedThreads, kLnStages, kLnAffineInRegs, false>;     \
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ln_smem);         \
     if (e != cudaSuccess) return e;                                                                             \
     k<<<grid, kLnStagedThreads, ln_smem, stream>>>(static_cast<const TYPE*>(x), gamma, beta, eps,               \
@@ -1133,7 +1148,7 @@ int layernorm_backward_grid(KERN kernel, size_t smem, int64_t rows, int num_sms)
 
 cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
-                                      bool bf16, cudaStream_t stream, int num_sms) {
+                                      bool bf16, cudaStream_t stream, int num_sms, bool rms) {
   if (rows <= 0) return cudaSuccess;
   if (h % 8 != 0 || h > kLnBwdThreads * 8 * 4) return cudaErrorInvalidValue;
   const int ch = static_cast<int>((h / 8 + kLnBwdThreads - 1) / kLnBwdThreads);
@@ -1141,7 +1156,7 @@ cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void
   int grid = 0;
 #define TPMLP_LNB(TYPE, CHN)                                                                                     \
   do {                                                                                                           \
-    auto k = layernorm_backward_kernel<TYPE, CHN>;                                                               \
+    auto k = rms ? layernorm_backward_kernel<TYPE, CHN, true> : layernorm_backward_kernel<TYPE, CHN, false>;    \
     grid = layernorm_backward_grid(k, acc_bytes, rows, num_sms);                                                 \
     k<<<grid, kLnBwdThreads, acc_bytes, stream>>>(static_cast<const TYPE*>(x), static_cast<const TYPE*>(dxn),    \
                                                   static_cast<const TYPE*>(dout), gamma, eps,                   \

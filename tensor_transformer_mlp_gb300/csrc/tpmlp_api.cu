@@ -554,6 +554,61 @@ tpmlp_status tpmlp_sp_layernorm(const void* x, const float* gamma, const float* 
   return TPMLP_OK;
 }
 
+tpmlp_status tpmlp_rmsnorm(const void* x, const float* gamma, float eps, void* y, int64_t rows, int64_t h,
+                           tpmlp_dtype dt, void* stream) {
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  if (rows < 0 || h < 1) return fail(TPMLP_ERR_SHAPE, "need rows >= 0 and h >= 1");
+  const int64_t h_max = dt == TPMLP_BF16 ? 8192 : 4096;
+  if (h % 8 != 0 || h > h_max)
+    return fail(TPMLP_ERR_SHAPE, "rmsnorm needs h %% 8 == 0 and h <= %lld (h=%lld)", (long long)h_max, (long long)h);
+  if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
+  if (rows > 0 && (!x || !y)) return fail(TPMLP_ERR_INVALID, "null pointer");
+  if (!gamma) return fail(TPMLP_ERR_INVALID, "null pointer");
+  if (rows > 0) TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x, "x"}, {y, "y"}}));
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{gamma, "gamma"}}));
+  if (rows == 0) return TPMLP_OK;
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  TPMLP_CUDA(launch_layernorm(x, gamma, nullptr, eps, y, rows, h, dt == TPMLP_BF16, static_cast<cudaStream_t>(stream),
+                              ctx.num_sms, ctx.status, true),
+             "rmsnorm");
+  return TPMLP_OK;
+}
+
+size_t tpmlp_rmsnorm_backward_workspace_size(int64_t rows, int64_t h) {
+  if (rows < 0 || h <= 0) return 0;
+  return round_up(static_cast<size_t>(kLnBwdMaxCtas) * 2 * static_cast<size_t>(h) * sizeof(float), 256);
+}
+
+tpmlp_status tpmlp_rmsnorm_backward(const void* x, const float* gamma, float eps, const void* dy, void* dx,
+                                    float* dgamma, int64_t rows, int64_t h, tpmlp_dtype dt, void* workspace,
+                                    size_t ws_bytes, void* stream) {
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  if (rows < 0 || h < 1) return fail(TPMLP_ERR_SHAPE, "need rows >= 0 and h >= 1");
+  if (h % 8 != 0 || h > 4096)
+    return fail(TPMLP_ERR_SHAPE, "rmsnorm_backward needs h %% 8 == 0 and h <= 4096 (h=%lld)", (long long)h);
+  if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
+  if (!gamma || !dgamma) return fail(TPMLP_ERR_INVALID, "null pointer");
+  if (rows > 0 && (!x || !dy || !dx)) return fail(TPMLP_ERR_INVALID, "null pointer");
+  if (rows > 0) TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x, "x"}, {dy, "dy"}, {dx, "dx"}}));
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{gamma, "gamma"}, {dgamma, "dgamma"}}));
+  const size_t need = tpmlp_rmsnorm_backward_workspace_size(rows, h);
+  if (rows > 0 && (!workspace || ws_bytes < need))
+    return fail(TPMLP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+  if (rows > 0) TPMLP_TRY(check_ptrs(TPMLP_BF16, {{workspace, "workspace"}}));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {  // no rows: dgamma is an empty sum
+    TPMLP_CUDA(cudaMemsetAsync(dgamma, 0, static_cast<size_t>(h) * sizeof(float), st), "zero dgamma");
+    return TPMLP_OK;
+  }
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  TPMLP_CUDA(launch_layernorm_backward(x, dy, nullptr, gamma, eps, dx, static_cast<float*>(workspace), dgamma, nullptr,
+                                       rows, h, dt == TPMLP_BF16, st, ctx.num_sms, true),
+             "rmsnorm backward");
+  return TPMLP_OK;
+}
+
 tpmlp_status tpmlp_sp_gather(const void* x_shards, void* x_full, int64_t b, int64_t s, int64_t h, int t,
                              tpmlp_dtype dt, void* stream) {
   if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);

@@ -104,9 +104,10 @@ cudaError_t gemm_f32_simt(int64_t M, int64_t N, int64_t K, const Operand& a, con
                           const EpiParams& ep, cudaStream_t stream);
 
 // Sequence-parallel memory-bound kernels. `bf16` selects the element type (else fp32).
+// rms: RMSNorm instead (beta unused; staged widths only, else cudaErrorNotSupported).
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, float eps, void* y,
                              int64_t rows, int64_t h, bool bf16, cudaStream_t stream, int num_sms,
-                             unsigned int* status);
+                             unsigned int* status, bool rms = false);
 cudaError_t launch_gather(const void* x_shards, void* x_full, int64_t b, int64_t s, int64_t h, int t, bool bf16,
                           cudaStream_t stream, int num_sms);
 cudaError_t launch_reduce_scatter(const float* partials, void* out_shards, int64_t b, int64_t s, int64_t h, int t,
@@ -133,9 +134,10 @@ constexpr int kLnBwdMaxCtas = 1024;
 cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint64_t threshold, float scale,
                                        uint64_t seed, int64_t b, int64_t s, int64_t h, int t, bool bf16,
                                        cudaStream_t stream, int num_sms);
+// rms: RMSNorm's backward (dbeta may be null); dout may be null (no residual term).
 cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
-                                      bool bf16, cudaStream_t stream, int num_sms);
+                                      bool bf16, cudaStream_t stream, int num_sms, bool rms = false);
 
 // Attention softmax: fp32 scores -> bf16 probabilities per row of length L (L % 8 == 0, L <= 8192),
 // and its backward dS = scale * P * (dP - rowsum(P * dP)) in bf16.

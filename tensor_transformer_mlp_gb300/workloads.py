@@ -184,3 +184,16 @@ def attn_inputs(cfg: AttnConfig, seed: int | None = None) -> dict[str, np.ndarra
     Wo = _draw(rng, (cfg.h, cfg.h), cfg.w_std, cfg.dtype)
     G = _draw(rng, (cfg.b * cfg.s, cfg.h), cfg.g_std, cfg.dtype).reshape(cfg.b, cfg.s, cfg.h)
     return {"X": X, "Wqkv": Wqkv, "Wo": Wo, "G": G}
+
+
+def norm_inputs(rows: int, h: int, dtype: str = "bf16", seed: int = 0, x_std: float = 1.0, x_mean: float = 0.5):
+    """RMSNorm inputs: x [rows, h] ~ N(x_mean, x_std), gamma [h] ~ 1 + 0.1 N(0, 1) (fp32), dy
+    [rows, h] ~ N(0, 1); x and dy hold values exact in `dtype`."""
+    rng = np.random.default_rng(seed)
+    x = _draw(rng, (rows, h), x_std, dtype) + np.float32(x_mean)
+    if dtype == "bf16":
+        x = round_to_bf16(x)
+    gamma = (1.0 + 0.1 * rng.standard_normal(h)).astype(np.float32)
+    dy = _draw(rng, (rows, h), 1.0, dtype)
+    return {"x": x, "gamma": gamma, "dy": dy}
+

@@ -143,5 +143,22 @@ def test_attention_validation(lib):
     assert lib.tpmlp_attention_backward(*([FAKE] * 10), 2, 64, 256, 4, 2, BF16, FAKE, need - 1, None) == WORKSPACE
 
 
+def test_rmsnorm_validation(lib):
+    assert lib.tpmlp_rmsnorm(FAKE, FAKE, 1e-5, FAKE, 4, 256, 9, None) == DTYPE
+    assert lib.tpmlp_rmsnorm(FAKE, FAKE, 1e-5, FAKE, 4, 260, BF16, None) == SHAPE      # h % 8
+    assert lib.tpmlp_rmsnorm(FAKE, FAKE, 1e-5, FAKE, 4, 8200, BF16, None) == SHAPE     # h > 8192
+    assert lib.tpmlp_rmsnorm(FAKE, FAKE, 1e-5, FAKE, 4, 8192, F32, None) == SHAPE      # h > 4096 (fp32)
+    assert lib.tpmlp_rmsnorm(FAKE, FAKE, 0.0, FAKE, 4, 256, BF16, None) == INVALID     # eps
+    assert lib.tpmlp_rmsnorm(None, FAKE, 1e-5, FAKE, 4, 256, BF16, None) == INVALID
+    assert lib.tpmlp_rmsnorm(FAKE + 8, FAKE, 1e-5, FAKE, 4, 256, BF16, None) == ALIGN
+    need = lib.tpmlp_rmsnorm_backward_workspace_size(4, 256)
+    assert need >= 2 * 256 * 4
+    P = [FAKE] * 2
+    assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 8192, BF16, FAKE, 1 << 30, None) == SHAPE
+    assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, None, 4, 256, BF16, FAKE, need, None) == INVALID
+    assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 256, BF16, FAKE, need - 1, None) == WORKSPACE
+    assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 256, 7, FAKE, need, None) == DTYPE
+
+
 def test_last_error_never_null(lib):
     assert isinstance(lib.tpmlp_last_error(), bytes)
