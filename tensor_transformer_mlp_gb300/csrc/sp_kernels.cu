@@ -781,6 +781,159 @@ __global__ void __launch_bounds__(kLnBwdThreads, 4)
   }
 }
 
+// The same backward (LayerNorm, or RMSNorm with kRms) with the row streamed through the
+// bulk-copy ring: thread 0 keeps `stages` rows of x, dxn (and dout when given) in flight, so
+// loads never wait behind the reductions. 256 threads, CH vectors of 8 columns per thread;
+// dgamma / dbeta accumulate in registers and go to partials[blockIdx][2][h] at the end.
+// Needs 16-byte aligned row starts (bulk copies).
+constexpr int kLnBwdStagedThreads = 256;
+
+template <typename T, int CH, bool kRms>
+__global__ void __launch_bounds__(kLnBwdStagedThreads)
+    norm_backward_staged_kernel(const T* __restrict__ x, const T* __restrict__ dxn, const T* __restrict__ dout,
+                                const float* __restrict__ gamma, float eps, T* __restrict__ dx,
+                                float* __restrict__ partials, int64_t rows, int h, int stages,
+                                unsigned int* status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float4 red[2][kLnBwdStagedThreads / 32];
+  const uint32_t row_bytes = static_cast<uint32_t>(h) * sizeof(T);
+  const uint32_t stage_bytes = (dout ? 3u : 2u) * row_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(stages) * stage_bytes);
+  const int64_t nloc = rows_for_cta(rows);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) {
+    for (int st = 0; st < stages; ++st) mbar_init(&full[st], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int64_t i) {
+    const int64_t R = blockIdx.x + i * gridDim.x;
+    const int st = static_cast<int>(i % stages);
+    uint8_t* dst = smem + static_cast<size_t>(st) * stage_bytes;
+    mbar_arrive_expect_tx(&full[st], stage_bytes);
+    bulk_load(dst, x + R * h, row_bytes, &full[st]);
+    bulk_load(dst + row_bytes, dxn + R * h, row_bytes, &full[st]);
+    if (dout) bulk_load(dst + 2 * row_bytes, dout + R * h, row_bytes, &full[st]);
+  };
+  if (tid == 0)
+    for (int64_t i = 0; i < nloc && i < stages; ++i) issue(i);
+  float gam[CH][8], accg[CH][8], accb[kRms ? 1 : CH][8];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int col = (tid + c * kLnBwdStagedThreads) * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      gam[c][e] = col < h ? gamma[col + e] : 0.f;
+      accg[c][e] = 0.f;
+      if constexpr (!kRms) accb[c][e] = 0.f;
+    }
+  }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  int64_t i = 0;
+  bool aborted = false;
+  for (; i < nloc; ++i) {
+    const int st = static_cast<int>(i % stages);
+    const int p = static_cast<int>(i & 1);
+    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1), status, 23);
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    const T* xs = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes);
+    const T* ds = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes + row_bytes);
+    const T* gs = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes + 2 * row_bytes);
+    const float shift = kRms ? 0.f : static_cast<float>(xs[0]);
+    float f[CH][8], dn[CH][8], go[CH][8];
+    float s_d = 0.f, s_dd = 0.f, s_g = 0.f, s_gd = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * kLnBwdStagedThreads) * 8;
+      if (col < h) {
+        Vec8<T> xv, dv;
+        xv.load(xs + col);
+        dv.load(ds + col);
+        xv.to_float(f[c]);
+        dv.to_float(dn[c]);
+        if (dout) {
+          Vec8<T> gv;
+          gv.load(gs + col);
+          gv.to_float(go[c]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) go[c][e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = f[c][e] - shift;
+          const float g = dn[c][e] * gam[c][e];
+          if constexpr (!kRms) {
+            s_d += d;
+            s_g += g;
+          }
+          s_dd = fmaf(d, d, s_dd);
+          s_gd = fmaf(g, d, s_gd);
+        }
+      }
+    }
+    if constexpr (!kRms) {
+      s_d = warp_sum(s_d);
+      s_g = warp_sum(s_g);
+    }
+    s_dd = warp_sum(s_dd);
+    s_gd = warp_sum(s_gd);
+    if (lane == 0) red[p][w] = make_float4(s_d, s_dd, s_g, s_gd);
+    __syncthreads();  // the row's sums are published, and every thread has read stage st
+    if (tid == 0 && i + stages < nloc) issue(i + stages);
+    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kLnBwdStagedThreads / 32; ++k) {
+      const float4 v = red[p][k];
+      t4.x += v.x;
+      t4.y += v.y;
+      t4.z += v.z;
+      t4.w += v.w;
+    }
+    const float md = kRms ? 0.f : t4.x * inv_h;
+    const float rstd = rsqrtf((kRms ? t4.y * inv_h : fmaxf(t4.y * inv_h - md * md, 0.f)) + eps);
+    const float mean_g = kRms ? 0.f : t4.z * inv_h;
+    const float mean_gxh = rstd * (t4.w * inv_h - md * mean_g);  // mean(g * x_hat)
+    const int64_t R = blockIdx.x + i * gridDim.x;
+    T* outr = dx + R * h;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (tid + c * kLnBwdStagedThreads) * 8;
+      if (col < h) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xh = (f[c][e] - shift - md) * rstd;
+          const float g = dn[c][e] * gam[c][e];
+          o[e] = go[c][e] + rstd * (g - mean_g - xh * mean_gxh);
+          accg[c][e] = fmaf(dn[c][e], xh, accg[c][e]);
+          if constexpr (!kRms) accb[c][e] += dn[c][e];
+        }
+        Vec8<T> ov;
+        ov.from_float(o);
+        ov.store(outr + col);
+      }
+    }
+  }
+  if (aborted && tid == 0)
+    for (int64_t k = i; k < nloc && k < i + stages; ++k) mbar_wait(&full[k % stages], (k / stages) & 1, status, 21);
+  float* pg = partials + static_cast<int64_t>(blockIdx.x) * 2 * h;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int col = (tid + c * kLnBwdStagedThreads) * 8;
+    if (col < h) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        pg[col + e] = accg[c][e];
+        pg[h + col + e] = kRms ? 0.f : accb[kRms ? 0 : c][e];
+      }
+    }
+  }
+}
+
 // dgamma[c] = sum over CTAs of partials[k][0][c], dbeta likewise. A CTA takes 32 of the 2h
 // columns; thread (g, c) adds partials g, g+8, g+16, ... of its column, and the 8 group sums are
 // then added in group order, so the result does not depend on scheduling.
@@ -1146,10 +1299,51 @@ int layernorm_backward_grid(KERN kernel, size_t smem, int64_t rows, int num_sms)
   return g < kLnBwdMaxCtas ? g : kLnBwdMaxCtas;
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
-                                      bool bf16, cudaStream_t stream, int num_sms, bool rms) {
+                                      bool bf16, cudaStream_t stream, int num_sms, bool rms, unsigned int* status) {
   if (rows <= 0) return cudaSuccess;
+  const size_t elt = bf16 ? 2 : 4;
+  const size_t stage_bytes = (dout ? 3 : 2) * static_cast<size_t>(h) * elt;
+  const bool staged = h % 8 == 0 && h <= kLnBwdStagedThreads * 8 * 2 && aligned16(x) && aligned16(dxn) &&
+                      (!dout || aligned16(dout)) && 2 * stage_bytes + 16 <= kStagedSmemMax;
+  if (staged) {
+    int stages = static_cast<int>(kStagedSmemMax / (stage_bytes + sizeof(uint64_t)));
+    stages = stages > 4 ? 4 : stages;
+    const size_t smem = staged_smem(stage_bytes, stages);
+    const int ch = static_cast<int>((h / 8 + kLnBwdStagedThreads - 1) / kLnBwdStagedThreads);
+    int grid = 0;
+#define TPMLP_NBS(TYPE, CHN)                                                                                       \
+  do {                                                                                                             \
+    auto k = rms ? norm_backward_staged_kernel<TYPE, CHN, true> : norm_backward_staged_kernel<TYPE, CHN, false>;   \
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
+    if (e != cudaSuccess) return e;                                                                                \
+    int per_sm = 1;                                                                                                \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kLnBwdStagedThreads, smem) != cudaSuccess ||     \
+        per_sm < 1)                                                                                                \
+      per_sm = 1;                                                                                                  \
+    grid = rows_grid(rows, num_sms, per_sm);                                                                       \
+    grid = grid < kLnBwdMaxCtas ? grid : kLnBwdMaxCtas;                                                            \
+    k<<<grid, kLnBwdStagedThreads, smem, stream>>>(static_cast<const TYPE*>(x), static_cast<const TYPE*>(dxn),     \
+                                                   static_cast<const TYPE*>(dout), gamma, eps, static_cast<TYPE*>(dx), \
+                                                   partials, rows, static_cast<int>(h), stages, status);          \
+  } while (0)
+    if (bf16) {
+      if (ch <= 1) TPMLP_NBS(__nv_bfloat16, 1);
+      else TPMLP_NBS(__nv_bfloat16, 2);
+    } else {
+      if (ch <= 1) TPMLP_NBS(float, 1);
+      else TPMLP_NBS(float, 2);
+    }
+#undef TPMLP_NBS
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int hb = static_cast<int>((2 * h + 31) / 32);
+    sum_partials_kernel<<<hb, 256, 0, stream>>>(partials, grid, static_cast<int>(h), dgamma, dbeta);
+    return cudaGetLastError();
+  }
   if (h % 8 != 0 || h > kLnBwdThreads * 8 * 4) return cudaErrorInvalidValue;
   const int ch = static_cast<int>((h / 8 + kLnBwdThreads - 1) / kLnBwdThreads);
   const size_t acc_bytes = 2 * static_cast<size_t>(ch) * 8 * kLnBwdThreads * sizeof(float);  // <= 32 KiB

@@ -529,7 +529,7 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
              "dgrad-2 GEMM");
   // LayerNorm backward on the shards plus the residual path.
   TPMLP_CUDA(launch_layernorm_backward(x_shards, dxn, dout_shards, gamma, eps, dx_shards, partials, dgamma, dbeta, n,
-                                       h, bf16, st, ctx.num_sms),
+                                       h, bf16, st, ctx.num_sms, false, ctx.status),
              "layernorm backward");
   return TPMLP_OK;
 }
@@ -604,7 +604,7 @@ tpmlp_status tpmlp_rmsnorm_backward(const void* x, const float* gamma, float eps
   DeviceCtx ctx;
   TPMLP_CUDA(get_device_ctx(&ctx), "device context");
   TPMLP_CUDA(launch_layernorm_backward(x, dy, nullptr, gamma, eps, dx, static_cast<float*>(workspace), dgamma, nullptr,
-                                       rows, h, dt == TPMLP_BF16, st, ctx.num_sms, true),
+                                       rows, h, dt == TPMLP_BF16, st, ctx.num_sms, true, ctx.status),
              "rmsnorm backward");
   return TPMLP_OK;
 }

@@ -137,7 +137,8 @@ cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint
 // rms: RMSNorm's backward (dbeta may be null); dout may be null (no residual term).
 cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
-                                      bool bf16, cudaStream_t stream, int num_sms, bool rms = false);
+                                      bool bf16, cudaStream_t stream, int num_sms, bool rms = false,
+                                      unsigned int* status = nullptr);
 
 // Attention softmax: fp32 scores -> bf16 probabilities per row of length L (L % 8 == 0, L <= 8192),
 // and its backward dS = scale * P * (dP - rowsum(P * dP)) in bf16.
