@@ -198,8 +198,41 @@ __global__ void __launch_bounds__(256) layernorm_generic_kernel(const T* __restr
 
 // ------------------------------------------------------------------ gather (g forward)
 // Destination row r (token order) <- source shard-major row; rows are copied as 16-byte vectors.
+// Each CTA moves kRowsPer rows per iteration and every thread issues all its loads (up to
+// kRowsPer * V vectors) before its stores, so enough bytes are in flight to cover HBM latency.
+template <int V, int kRowsPer>
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                      int64_t rows, int64_t b, int64_t s, int64_t sl, int row_vecs) {
+  for (int64_t R0 = static_cast<int64_t>(blockIdx.x) * kRowsPer; R0 < rows;
+       R0 += static_cast<int64_t>(gridDim.x) * kRowsPer) {
+    uint4 v[kRowsPer][V];
+#pragma unroll
+    for (int k = 0; k < kRowsPer; ++k) {
+      const int64_t R = R0 + k;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int c = threadIdx.x + j * 256;
+        if (R < rows && c < row_vecs) v[k][j] = src[R * row_vecs + c];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRowsPer; ++k) {
+      const int64_t R = R0 + k;
+      if (R >= rows) break;
+      uint4* dr = dst + shard_row_to_token(R, b, s, sl) * row_vecs;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int c = threadIdx.x + j * 256;
+        if (c < row_vecs) dr[c] = v[k][j];
+      }
+    }
+  }
+}
+
+// Any row width: one row per CTA iteration.
+__global__ void __launch_bounds__(256) gather_generic_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                             int64_t rows, int64_t b, int64_t s, int64_t sl,
+                                                             int row_vecs) {
   for (int64_t R = blockIdx.x; R < rows; R += gridDim.x) {
     const int64_t r = shard_row_to_token(R, b, s, sl);
     const uint4* sr = src + R * row_vecs;
@@ -1184,9 +1217,18 @@ cudaError_t launch_gather(const void* x_shards, void* x_full, int64_t b, int64_t
   if (rows <= 0) return cudaSuccess;
   const int64_t row_bytes = h * (bf16 ? 2 : 4);
   if (row_bytes % 16 != 0) return cudaErrorInvalidValue;
-  gather_kernel<<<rows_grid(rows, num_sms, 8), 256, 0, stream>>>(static_cast<const uint4*>(x_shards),
-                                                                   static_cast<uint4*>(x_full), rows, b, s, s / t,
-                                                                   static_cast<int>(row_bytes / 16));
+  const int row_vecs = static_cast<int>(row_bytes / 16);
+  const auto* src = static_cast<const uint4*>(x_shards);
+  auto* dst = static_cast<uint4*>(x_full);
+  if (row_vecs <= 256) {
+    gather_kernel<1, 4><<<rows_grid((rows + 3) / 4, num_sms, 8), 256, 0, stream>>>(src, dst, rows, b, s, s / t, row_vecs);
+  } else if (row_vecs <= 512) {
+    gather_kernel<2, 2><<<rows_grid((rows + 1) / 2, num_sms, 8), 256, 0, stream>>>(src, dst, rows, b, s, s / t, row_vecs);
+  } else if (row_vecs <= 1024) {
+    gather_kernel<4, 1><<<rows_grid(rows, num_sms, 8), 256, 0, stream>>>(src, dst, rows, b, s, s / t, row_vecs);
+  } else {
+    gather_generic_kernel<<<rows_grid(rows, num_sms, 8), 256, 0, stream>>>(src, dst, rows, b, s, s / t, row_vecs);
+  }
   return cudaGetLastError();
 }
 
