@@ -503,7 +503,7 @@ def run_ours(args, cfg):
         del ins, outs, host_in, host_out
         return fl / el / 1e12, h2d, d2h
 
-    e2e_steps = max(4, args.steps // 2)
+    e2e_steps = max(4, args.steps)
     e2e_layer, h2d, d2h = e2e_run(("X", "G"), ("O", "dX"), e2e_steps)
     e2e_all, h2d_all, d2h_all = e2e_run(("X", "A", "B", "G"), ("O", "dX", "dA", "dB"), e2e_steps)
 
