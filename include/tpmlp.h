@@ -281,7 +281,8 @@ tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shard
  *   K-loop over every head being the shard sum.
  *   Saves (caller-owned, for the backward): QKV_save [b*s][3h], P_save [b][heads][s][s],
  *   O_save [b*s][h]. workspace: the fp32 scores, tpmlp_attention_forward_workspace_size bytes.
- *   Requires heads % t == 0, h % heads == 0, head_dim and s multiples of 8, s <= 8192.
+ *   Requires heads % t == 0, h % heads == 0, head_dim and s multiples of 8, s <= 8192. b == 0
+ *   is an empty batch: nothing is computed and the token buffers may be NULL.
  */
 size_t tpmlp_attention_forward_workspace_size(int64_t b, int64_t s, int64_t h, int heads, tpmlp_dtype dt);
 tpmlp_status tpmlp_attention_forward(const void* X, const void* Wqkv, const void* Wo, void* Y,
@@ -293,7 +294,8 @@ tpmlp_status tpmlp_attention_forward(const void* X, const void* Wqkv, const void
  * Backward of the attention block from G = dl/dY [b*s][h]: dX [b*s][h] (bf16), dWqkv [h][3h] and
  * dWo [h][h] (fp32, overwritten). dO = G W_o^T, dW_o = O^T G; per head dV = P^T dO,
  * dP = dO V^T, dS = P * (dP - rowsum(P * dP)) / sqrt(head_dim), dQ = dS K, dK = dS^T Q;
- * dX = dQKV W_qkv^T, dW_qkv = X^T dQKV. Saves from tpmlp_attention_forward.
+ * dX = dQKV W_qkv^T, dW_qkv = X^T dQKV. Saves from tpmlp_attention_forward. With b == 0 the
+ * weight gradients are zeroed (empty sums) and the token buffers may be NULL.
  */
 size_t tpmlp_attention_backward_workspace_size(int64_t b, int64_t s, int64_t h, int heads, tpmlp_dtype dt);
 tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const void* Wo, const void* G,

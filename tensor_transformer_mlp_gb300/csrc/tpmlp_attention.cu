@@ -48,7 +48,8 @@ EpiParams plain_epi(void* out, int64_t ldo) {
 
 tpmlp_status check_shape(int64_t b, int64_t s, int64_t h, int heads, int t, tpmlp_dtype dt) {
   if (dt != TPMLP_BF16) return err(TPMLP_ERR_DTYPE, "the attention block runs on the bf16 tensor-core path only");
-  if (b < 1 || s < 1 || h < 1 || heads < 1 || t < 1) return err(TPMLP_ERR_SHAPE, "need b, s, h, heads, t >= 1");
+  if (b < 0 || s < 1 || h < 1 || heads < 1 || t < 1)
+    return err(TPMLP_ERR_SHAPE, "need b >= 0 and s, h, heads, t >= 1");
   if (heads % t != 0) return err(TPMLP_ERR_SHAPE, "heads must split evenly over the t shards");
   if (h % heads != 0) return err(TPMLP_ERR_SHAPE, "h must be a multiple of heads");
   const int64_t dh = h / heads;
@@ -95,7 +96,12 @@ tpmlp_status tpmlp_attention_forward(const void* X, const void* Wqkv, const void
                                      tpmlp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
   tpmlp_status st = check_shape(b, s, h, heads, t, dt);
   if (st != TPMLP_OK) return st;
-  for (const void* p : {X, Wqkv, Wo, static_cast<const void*>(Y), static_cast<const void*>(QKV_save),
+  for (const void* p : {Wqkv, Wo}) {
+    if (!p) return err(TPMLP_ERR_INVALID, "null pointer");
+    if (!aligned16(p)) return err(TPMLP_ERR_ALIGN, "pointers must be 16-byte aligned");
+  }
+  if (b == 0) return TPMLP_OK;  // no tokens: nothing to compute
+  for (const void* p : {X, static_cast<const void*>(Y), static_cast<const void*>(QKV_save),
                         static_cast<const void*>(P_save), static_cast<const void*>(O_save)}) {
     if (!p) return err(TPMLP_ERR_INVALID, "null pointer");
     if (!aligned16(p)) return err(TPMLP_ERR_ALIGN, "pointers must be 16-byte aligned");
@@ -145,8 +151,17 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
                                       tpmlp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
   tpmlp_status st = check_shape(b, s, h, heads, t, dt);
   if (st != TPMLP_OK) return st;
-  for (const void* p : {X, Wqkv, Wo, G, QKV_save, P_save, O_save, static_cast<const void*>(dX),
-                        static_cast<const void*>(dWqkv), static_cast<const void*>(dWo)}) {
+  for (const void* p : {Wqkv, Wo, static_cast<const void*>(dWqkv), static_cast<const void*>(dWo)}) {
+    if (!p) return err(TPMLP_ERR_INVALID, "null pointer");
+    if (!aligned16(p)) return err(TPMLP_ERR_ALIGN, "pointers must be 16-byte aligned");
+  }
+  if (b == 0) {  // no tokens: the weight gradients are empty sums
+    cudaStream_t stm = static_cast<cudaStream_t>(stream);
+    ATT_CUDA(cudaMemsetAsync(dWqkv, 0, static_cast<size_t>(h) * 3 * h * sizeof(float), stm), "zero dWqkv");
+    ATT_CUDA(cudaMemsetAsync(dWo, 0, static_cast<size_t>(h) * h * sizeof(float), stm), "zero dWo");
+    return TPMLP_OK;
+  }
+  for (const void* p : {X, G, QKV_save, P_save, O_save, static_cast<const void*>(dX)}) {
     if (!p) return err(TPMLP_ERR_INVALID, "null pointer");
     if (!aligned16(p)) return err(TPMLP_ERR_ALIGN, "pointers must be 16-byte aligned");
   }

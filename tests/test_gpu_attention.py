@@ -43,3 +43,25 @@ def test_attention_small(shape):
 
 def test_attention_gpt_size():
     run_case(wl.GPT_ATTENTION)
+
+
+def test_attention_empty_batch():
+    h, heads = 128, 2
+    X = torch.empty((0, 64, h), dtype=torch.bfloat16, device="cuda")
+    Wqkv = torch.ones((h, 3 * h), dtype=torch.bfloat16, device="cuda")
+    Wo = torch.ones((h, h), dtype=torch.bfloat16, device="cuda")
+    Y, saves = tp.attention_forward(X, Wqkv, Wo, heads, 2)
+    dX, dWqkv, dWo = tp.attention_backward(X, Wqkv, Wo, torch.empty_like(X), saves, heads, 2)
+    torch.cuda.synchronize()
+    assert Y.shape == (0, 64, h) and dX.shape == (0, 64, h)
+    assert torch.count_nonzero(dWqkv) == 0 and torch.count_nonzero(dWo) == 0
+
+
+def test_attention_smallest_head_dim_and_sequence():
+    # head_dim 8 and s 8: the operand tiles are mostly fill, one row of a softmax is 8 wide
+    run_case(wl.AttnConfig("attn-min", 3, 8, 32, 4, 2, 1.0, 0.2, 1.0, seed=5))
+
+
+def test_attention_longest_sequence():
+    # s = 8192, the largest the softmax kernels take (one row per CTA, 8 vectors per thread)
+    run_case(wl.AttnConfig("attn-s8192", 1, 8192, 256, 2, 2, 1.0, 0.05, 1.0, seed=9))
