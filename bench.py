@@ -377,8 +377,9 @@ def measure_attention(dev, peaks, reps: int = 10):
     ff = cfg.flops_fwd
     return {"workload": cfg.name, "forward_ms": fwd * 1e3, "forward_tflops": ff / fwd / 1e12,
             "backward_ms": bwd * 1e3, "backward_tflops": 2 * ff / bwd / 1e12,
-            "note": "scores materialised in fp32 with a separate softmax kernel (Megatron's classic form); "
-                    "includes allocation of outputs and workspace by the convenience wrappers"}
+            "note": "P materialised and saved (Megatron's form); softmax in the epilogues of two passes of the "
+                    "scores GEMM, dS in the dP GEMM's epilogue; includes allocation of outputs and workspace by "
+                    "the convenience wrappers"}
 
 
 # ----------------------------------------------------------------------------- GPU arm

@@ -280,7 +280,9 @@ tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shard
  *   attention dropout), O_head = P V; O [b*s][h] holds the heads side by side; Y = O W_o, the
  *   K-loop over every head being the shard sum.
  *   Saves (caller-owned, for the backward): QKV_save [b*s][3h], P_save [b][heads][s][s],
- *   O_save [b*s][h]. workspace: the fp32 scores, tpmlp_attention_forward_workspace_size bytes.
+ *   O_save [b*s][h]. workspace: per-row softmax statistics (the scores go through two GEMM
+ *   passes: row max and sum of exp, then P; no score matrix is stored),
+ *   tpmlp_attention_forward_workspace_size bytes, 256-byte aligned.
  *   Requires heads % t == 0, h % heads == 0, head_dim and s multiples of 8, s <= 8192. b == 0
  *   is an empty batch: nothing is computed and the token buffers may be NULL.
  */
@@ -294,8 +296,11 @@ tpmlp_status tpmlp_attention_forward(const void* X, const void* Wqkv, const void
  * Backward of the attention block from G = dl/dY [b*s][h]: dX [b*s][h] (bf16), dWqkv [h][3h] and
  * dWo [h][h] (fp32, overwritten). dO = G W_o^T, dW_o = O^T G; per head dV = P^T dO,
  * dP = dO V^T, dS = P * (dP - rowsum(P * dP)) / sqrt(head_dim), dQ = dS K, dK = dS^T Q;
- * dX = dQKV W_qkv^T, dW_qkv = X^T dQKV. Saves from tpmlp_attention_forward. With b == 0 the
- * weight gradients are zeroed (empty sums) and the token buffers may be NULL.
+ * dX = dQKV W_qkv^T, dW_qkv = X^T dQKV. Saves from tpmlp_attention_forward. rowsum(P * dP) is
+ * taken as rowsum(dO * O) per head (equal, since O = P V), so dS comes out of the dP GEMM's
+ * epilogue and dP is never stored. workspace: tpmlp_attention_backward_workspace_size bytes
+ * (dO, that row sum, dS, dQKV), 256-byte aligned. With b == 0 the weight gradients are zeroed
+ * (empty sums) and the token buffers may be NULL.
  */
 size_t tpmlp_attention_backward_workspace_size(int64_t b, int64_t s, int64_t h, int heads, tpmlp_dtype dt);
 tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const void* Wo, const void* G,

@@ -169,25 +169,41 @@ __device__ __forceinline__ void store_staged(uint8_t* buf, const uint4 (&seg)[8]
   __syncwarp();
 }
 
-// The inverse of store_staged for bf16: the warp reads 32 rows x 64 columns of src with
-// line-wide loads (8 rows x 128 bytes per instruction) and each thread receives its own row's
-// 128 bytes in seg[] (zeros past M or N).
-__device__ __forceinline__ void load_staged_bf16(uint8_t* buf, uint4 (&seg)[8], int lane, int64_t prow,
-                                                 const void* src, int64_t ldo, int col0, int N) {
-  const int j = lane & 7;
-  const int col = col0 + j * 8;
+// The inverse of store_staged for bf16, in two steps so that a warp can keep several blocks'
+// loads in flight. issue_block_loads: the warp reads 32 rows x 64 columns of src with line-wide
+// loads (8 rows x 128 bytes per instruction; lane gets rows i*4 + lane/8, segment lane%8; zeros
+// past M or N). transpose_block: through the warp's staging buffer, each thread receives its
+// own row's 128 bytes in seg[].
+__device__ __forceinline__ void issue_block_loads(uint4 (&r8)[8], int lane, int64_t prow, const void* src, int64_t ldo,
+                                                  int col0, int N) {
+  const int col = col0 + (lane & 7) * 8;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = i * 4 + (lane >> 3);
     const int64_t pr = __shfl_sync(0xffffffffu, prow, r);
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (pr >= 0 && col < N) val = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + pr * ldo + col);
-    *reinterpret_cast<uint4*>(buf + r * 128 + ((j ^ (r & 7)) << 4)) = val;
+    r8[i] = make_uint4(0, 0, 0, 0);
+    if (pr >= 0 && col < N) r8[i] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + pr * ldo + col);
+  }
+}
+
+__device__ __forceinline__ void transpose_block(uint8_t* buf, const uint4 (&r8)[8], uint4 (&seg)[8], int lane) {
+  const int j = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    *reinterpret_cast<uint4*>(buf + r * 128 + ((j ^ (r & 7)) << 4)) = r8[i];
   }
   __syncwarp();
 #pragma unroll
   for (int jj = 0; jj < 8; ++jj) seg[jj] = *reinterpret_cast<const uint4*>(buf + lane * 128 + ((jj ^ (lane & 7)) << 4));
   __syncwarp();
+}
+
+__device__ __forceinline__ void load_staged_bf16(uint8_t* buf, uint4 (&seg)[8], int lane, int64_t prow,
+                                                 const void* src, int64_t ldo, int col0, int N) {
+  uint4 r8[8];
+  issue_block_loads(r8, lane, prow, src, ldo, col0, N);
+  transpose_block(buf, r8, seg, lane);
 }
 
 // Scale (batched) and bias (bf16 per column) for the store kinds, 8 columns at a time.
@@ -220,7 +236,7 @@ constexpr int kEpiChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks p
 template <int EPI, bool BATCHED>
 __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf, int lane, int64_t row, int M, int N,
                                               int col_tile0, int c_begin, uint32_t t_row, int64_t out_off,
-                                              float alpha) {
+                                              float alpha, int64_t srow, int nb, int num_nb) {
   if constexpr (EPI == kEpiStore || EPI == kEpiStoreF32) {
     constexpr bool kF32 = EPI == kEpiStoreF32;
     constexpr int kCols = kF32 ? 32 : 64;  // 128 bytes of output per row per pass
@@ -283,6 +299,88 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       }
       if (ep.out) store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
       store_staged<false>(buf, ys, lane, prow, ep.out2, ep.ldo, col0, N);
+    }
+  } else if constexpr (EPI == kEpiRowStats) {
+    // Online max / sum of exp over the warp's 128 columns of the row: per 32-column chunk the
+    // running sum is rescaled to the new maximum. Columns past N do not count.
+    float m = -INFINITY, l = 0.f;
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kEpiChunks; ++c) {
+      const int col0 = col_tile0 + c * 32;
+      if (col0 >= N) break;  // uniform across the warp
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
+      tmem_ld_wait();
+      float x[32];
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] = col0 + i < N ? __uint_as_float(v[i]) * alpha : -INFINITY;
+        cmax = fmaxf(cmax, x[i]);
+      }
+      const float mn = fmaxf(m, cmax);
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sum += __expf(x[i] - mn);
+      l = l * __expf(m - mn) + sum;
+      m = mn;
+    }
+    if (row < M) {
+      const int half = c_begin / kEpiChunks;
+      static_cast<float2*>(ep.stats)[srow * (2 * num_nb) + 2 * nb + half] = make_float2(m, l);
+    }
+  } else if constexpr (EPI == kEpiSoftmax) {
+    // P = exp(x - M) / L with the row's combined statistics, 64 columns per pass, staged.
+    const float2 st = row < M ? static_cast<const float2*>(ep.rowvec)[srow] : make_float2(0.f, 0.f);
+    const int64_t prow = row < M ? row : -1;
+    void* out = static_cast<__nv_bfloat16*>(ep.out) + out_off;
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kEpiChunks; c += 2) {
+      const int col0 = col_tile0 + c * 32;
+      if (col0 >= N) break;  // uniform across the warp
+      uint32_t v[64];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait();
+      uint4 seg[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = __expf(__uint_as_float(v[g * 8 + i]) * alpha - st.x) * st.y;
+        seg[g] = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                            pack_bf16x2(p[6], p[7]));
+      }
+      store_staged<false>(buf, seg, lane, prow, out, ep.ldo, col0, N);
+    }
+  } else if constexpr (EPI == kEpiSoftmaxGrad) {
+    // dS = escale * P * (dP - D): P read and dS written 64 columns at a time through the staging buffer.
+    const float d = row < M ? static_cast<const float*>(ep.rowvec)[srow] : 0.f;
+    const int64_t prow = row < M ? row : -1;
+    const void* pin = static_cast<const __nv_bfloat16*>(ep.aux) + out_off;
+    void* out = static_cast<__nv_bfloat16*>(ep.out) + out_off;
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kEpiChunks; c += 2) {
+      const int col0 = col_tile0 + c * 32;
+      if (col0 >= N) break;  // uniform across the warp
+      uint32_t v[64];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      uint4 ps[8];
+      load_staged_bf16(buf, ps, lane, prow, pin, ep.ldo, col0, N);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {  // dS overwrites P in place
+        uint32_t* w = reinterpret_cast<uint32_t*>(&ps[g]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 pf = unpack_bf16x2(w[i]);
+          const float x0 = __uint_as_float(v[g * 8 + 2 * i]) * alpha;
+          const float x1 = __uint_as_float(v[g * 8 + 2 * i + 1]) * alpha;
+          w[i] = pack_bf16x2(ep.escale * pf.x * (x0 - d), ep.escale * pf.y * (x1 - d));
+        }
+      }
+      store_staged<false>(buf, ps, lane, prow, out, ep.ldo, col0, N);
     }
   } else if constexpr (EPI == kEpiDGelu) {
     // D = acc * gelu'(Z): Z read and D written 64 columns at a time through the staging buffer.
@@ -502,8 +600,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t out_off = BATCHED ? z1 * bd.out_z1 + z2 * bd.out_z2 : 0;
       const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const int64_t srow = BATCHED ? (static_cast<int64_t>(z2) * bd.nz1 + z1) * M + row : row;
       epilogue_tile<EPI, BATCHED>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N, nb * BN, c_begin,
-                                  t_row, out_off, BATCHED ? bd.alpha : 1.f);
+                                  t_row, out_off, BATCHED ? bd.alpha : 1.f, srow, nb, sched.num_nb);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
@@ -740,7 +839,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       epilogue_tile<EPI, false>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N, nb * BN, c_begin,
-                                t_row, 0, 1.f);
+                                t_row, 0, 1.f, row, nb, num_nb);
       tc_fence_before();
       mbar_arrive_cluster(map_to_cta(&tempty_bar[acc], 0));
     }
@@ -990,6 +1089,12 @@ cudaError_t gemm_bf16_tc_batched(int64_t M, int64_t N, int64_t K, const BatchedO
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   if (!a.mn_major && !b.mn_major && epi == kEpiStoreF32)
     return launch<false, false, kEpiStoreF32, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
+  if (!a.mn_major && !b.mn_major && epi == kEpiRowStats)
+    return launch<false, false, kEpiRowStats, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
+  if (!a.mn_major && !b.mn_major && epi == kEpiSoftmax)
+    return launch<false, false, kEpiSoftmax, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
+  if (!a.mn_major && !b.mn_major && epi == kEpiSoftmaxGrad)
+    return launch<false, false, kEpiSoftmaxGrad, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
   if (!a.mn_major && b.mn_major && epi == kEpiStore)
     return launch<false, true, kEpiStore, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
   if (a.mn_major && b.mn_major && epi == kEpiStore)

@@ -1028,116 +1028,46 @@ __global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restri
   }
 }
 
-// ------------------------------------------------------------------ attention softmax
-// Row softmax of fp32 scores into bf16 probabilities, one CTA per row (persistent over rows):
-// max, then sum of exp(s - max), then p = exp(s - max) / sum, the row held in registers.
-template <int CH>
-__global__ void __launch_bounds__(256) softmax_rows_kernel(const float* __restrict__ S, __nv_bfloat16* __restrict__ P,
-                                                           int64_t rows, int L) {
-  __shared__ float red[2][8];
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  int p = 0;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, p ^= 1) {
-    const float* sr = S + r * L;
-    float f[CH][8];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (tid + c * 256) * 8;
-      if (col < L) {
-        Vec8<float> v;
-        v.load(sr + col);
-        v.to_float(f[c]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, f[c][e]);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[p][w] = mx;
-    __syncthreads();
-    mx = red[p][0];
-#pragma unroll
-    for (int k = 1; k < 8; ++k) mx = fmaxf(mx, red[p][k]);
-    float sum = 0.f;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      if ((tid + c * 256) * 8 < L) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          f[c][e] = __expf(f[c][e] - mx);
-          sum += f[c][e];
-        }
-      }
-    }
-    sum = warp_sum(sum);
-    __syncthreads();  // everyone has read red[p] for the max
-    if (lane == 0) red[p][w] = sum;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) tot += red[p][k];
-    const float inv = 1.0f / tot;
-    __nv_bfloat16* pr = P + r * L;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (tid + c * 256) * 8;
-      if (col < L) {
-        float o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = f[c][e] * inv;
-        Vec8<__nv_bfloat16> ov;
-        ov.from_float(o);
-        ov.store(pr + col);
-      }
-    }
-  }
+// ------------------------------------------------------------------ attention softmax (fused form)
+// Row r's partial statistics (m_j, l_j) from the scores GEMM's kEpiRowStats epilogue become
+// M = max_j m_j and 1/L with L = sum_j l_j * exp(m_j - M); one thread per row.
+__global__ void __launch_bounds__(256) softmax_combine_kernel(const float2* __restrict__ stats, int nparts,
+                                                              float2* __restrict__ rowstats, int64_t rows) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  const float2* st = stats + r * nparts;
+  float M = -INFINITY;
+  for (int j = 0; j < nparts; ++j) M = fmaxf(M, st[j].x);
+  float L = 0.f;
+  for (int j = 0; j < nparts; ++j) L += st[j].y * __expf(st[j].x - M);
+  rowstats[r] = make_float2(M, 1.0f / L);
 }
 
-// Softmax backward with the score scale: dS = scale * P * (dP - sum_k P dP), bf16 out.
-template <int CH>
-__global__ void __launch_bounds__(256) softmax_backward_kernel(const __nv_bfloat16* __restrict__ P,
-                                                               const float* __restrict__ dP, float scale,
-                                                               __nv_bfloat16* __restrict__ dS, int64_t rows, int L) {
-  __shared__ float red[2][8];
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  int p = 0;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, p ^= 1) {
-    float pv[CH][8], dv[CH][8];
-    float dot = 0.f;
+// D[(bi*heads + j)*s + si] = sum over head j's dh columns of dO * O in token row bi*s + si
+// (= rowsum(P * dP) for that query row); one thread per (token row, head), 16-byte loads.
+__global__ void __launch_bounds__(256) row_dot_kernel(const __nv_bfloat16* __restrict__ dO,
+                                                      const __nv_bfloat16* __restrict__ O, float* __restrict__ D,
+                                                      int64_t b, int64_t s, int64_t h, int heads) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= b * s * heads) return;
+  const int64_t tok = idx / heads;
+  const int j = static_cast<int>(idx - tok * heads);
+  const int64_t dh = h / heads;
+  const __nv_bfloat16* a = dO + tok * h + j * dh;
+  const __nv_bfloat16* c = O + tok * h + j * dh;
+  float acc = 0.f;
+  for (int64_t e = 0; e < dh; e += 8) {
+    Vec8<__nv_bfloat16> va, vc;
+    va.load(a + e);
+    vc.load(c + e);
+    float fa[8], fc[8];
+    va.to_float(fa);
+    vc.to_float(fc);
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (tid + c * 256) * 8;
-      if (col < L) {
-        Vec8<__nv_bfloat16> a;
-        a.load(P + r * L + col);
-        a.to_float(pv[c]);
-        Vec8<float> b;
-        b.load(dP + r * L + col);
-        b.to_float(dv[c]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dot = fmaf(pv[c][e], dv[c][e], dot);
-      }
-    }
-    dot = warp_sum(dot);
-    if (lane == 0) red[p][w] = dot;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) tot += red[p][k];
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (tid + c * 256) * 8;
-      if (col < L) {
-        float o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = scale * pv[c][e] * (dv[c][e] - tot);
-        Vec8<__nv_bfloat16> ov;
-        ov.from_float(o);
-        ov.store(dS + r * L + col);
-      }
-    }
+    for (int k = 0; k < 8; ++k) acc = fmaf(fa[k], fc[k], acc);
   }
+  const int64_t bi = tok / s, si = tok - bi * s;
+  D[(bi * heads + j) * s + si] = acc;
 }
 
 int rows_grid(int64_t rows, int num_sms, int per_sm) {
@@ -1415,30 +1345,25 @@ cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void
   return cudaGetLastError();
 }
 
-cudaError_t launch_softmax_rows(const float* S, void* P, int64_t rows, int64_t L, cudaStream_t stream, int num_sms) {
+cudaError_t launch_softmax_combine(const void* stats, int nparts, void* rowstats, int64_t rows, cudaStream_t stream,
+                                   int num_sms) {
+  (void)num_sms;
   if (rows <= 0) return cudaSuccess;
-  if (L % 8 != 0 || L > 256 * 8 * 4) return cudaErrorInvalidValue;
-  const int grid = rows_grid(rows, num_sms, 8);
-  const int ch = static_cast<int>((L / 8 + 255) / 256);
-  auto* Pp = static_cast<__nv_bfloat16*>(P);
-  if (ch <= 1) softmax_rows_kernel<1><<<grid, 256, 0, stream>>>(S, Pp, rows, static_cast<int>(L));
-  else if (ch <= 2) softmax_rows_kernel<2><<<grid, 256, 0, stream>>>(S, Pp, rows, static_cast<int>(L));
-  else softmax_rows_kernel<4><<<grid, 256, 0, stream>>>(S, Pp, rows, static_cast<int>(L));
+  softmax_combine_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
+      static_cast<const float2*>(stats), nparts, static_cast<float2*>(rowstats), rows);
   return cudaGetLastError();
 }
 
-cudaError_t launch_softmax_backward(const void* P, const float* dP, float scale, void* dS, int64_t rows, int64_t L,
-                                    cudaStream_t stream, int num_sms) {
-  if (rows <= 0) return cudaSuccess;
-  if (L % 8 != 0 || L > 256 * 8 * 4) return cudaErrorInvalidValue;
-  const int grid = rows_grid(rows, num_sms, 8);
-  const int ch = static_cast<int>((L / 8 + 255) / 256);
-  auto* Pp = static_cast<const __nv_bfloat16*>(P);
-  auto* dSp = static_cast<__nv_bfloat16*>(dS);
-  if (ch <= 1) softmax_backward_kernel<1><<<grid, 256, 0, stream>>>(Pp, dP, scale, dSp, rows, static_cast<int>(L));
-  else if (ch <= 2) softmax_backward_kernel<2><<<grid, 256, 0, stream>>>(Pp, dP, scale, dSp, rows, static_cast<int>(L));
-  else softmax_backward_kernel<4><<<grid, 256, 0, stream>>>(Pp, dP, scale, dSp, rows, static_cast<int>(L));
+cudaError_t launch_row_dot(const void* dO, const void* O, float* D, int64_t b, int64_t s, int64_t h, int heads,
+                           cudaStream_t stream, int num_sms) {
+  (void)num_sms;
+  const int64_t n = b * s * heads;
+  if (n <= 0) return cudaSuccess;
+  if ((h / heads) % 8 != 0) return cudaErrorInvalidValue;
+  row_dot_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), D, b, s, h, heads);
   return cudaGetLastError();
 }
+
 
 }  // namespace tpmlp

@@ -1,7 +1,7 @@
 // C ABI of the tensor-parallel self-attention block (SenseParrots model-parallel note, section
 // 2.1.1; "Megatron 训练" notes, section "Attention 层"): column-parallel QKV projection with the
 // heads split across the t shards, per head softmax(Q K^T / sqrt(head_dim)) V in the classic
-// Megatron form (scores materialised, a softmax kernel, two batched GEMMs), and a row-parallel
+// Megatron form (P materialised and saved), and a row-parallel
 // output projection whose K-loop over every head is the shard sum. All GEMMs run on the tcgen05
 // kernel; the per-head GEMMs are batched over (head, sequence) through 4-D tensor maps.
 #include <cuda_bf16.h>
@@ -80,6 +80,9 @@ BatchedOperand heads_view(const void* O, int64_t s, int64_t h, int64_t dh, bool 
   return BatchedOperand{O, s, dh, h, dh, s * h, mn_major};
 }
 
+// Partial row statistics of the scores GEMM: two per 256-column N-block of a row.
+int64_t stat_parts(int64_t s) { return 2 * ((s + 255) / 256); }
+
 }  // namespace
 
 extern "C" {
@@ -88,7 +91,8 @@ size_t tpmlp_attention_forward_workspace_size(int64_t b, int64_t s, int64_t h, i
   (void)h;
   (void)dt;
   if (b <= 0 || s <= 0 || heads <= 0) return 0;
-  return round_up(scores_elems(b, s, heads) * sizeof(float), 256);
+  const size_t rows = static_cast<size_t>(b) * static_cast<size_t>(heads) * static_cast<size_t>(s);
+  return round_up(rows * static_cast<size_t>(stat_parts(s)) * 8, 256) + round_up(rows * 8, 256);
 }
 
 tpmlp_status tpmlp_attention_forward(const void* X, const void* Wqkv, const void* Wo, void* Y, void* QKV_save,
@@ -113,17 +117,29 @@ tpmlp_status tpmlp_attention_forward(const void* X, const void* Wqkv, const void
   ATT_CUDA(get_device_ctx(&ctx), "device context");
   cudaStream_t stm = static_cast<cudaStream_t>(stream);
   const int64_t n = b * s, dh = h / heads;
-  float* S = static_cast<float*>(workspace);
+  const int64_t rows = b * heads * s;
+  void* stats = workspace;
+  void* rowstats = static_cast<char*>(workspace) + round_up(static_cast<size_t>(rows * stat_parts(s)) * 8, 256);
   // QKV = X W_qkv (column-parallel: every shard's heads at once)
   ATT_CUDA(gemm_bf16_tc(n, 3 * h, h, Operand{X, n, h, h, false}, Operand{Wqkv, h, 3 * h, 3 * h, true}, kEpiStore,
                         plain_epi(QKV_save, 3 * h), stm, ctx),
            "QKV GEMM");
-  // S = Q K^T / sqrt(dh) per (head, sequence)
+  // P = softmax(Q K^T / sqrt(dh)) per (head, sequence) in two passes over the same scores: the
+  // first keeps only each row's running max and sum of exp per N-block, the second recomputes
+  // the scores (bit-identical accumulators) and writes exp(x - M) / L; no fp32 score matrix.
   BatchSpec bs_s{heads, b, s * s, heads * s * s, static_cast<float>(1.0 / std::sqrt(static_cast<double>(dh)))};
+  EpiParams ep_stats = plain_epi(nullptr, s);
+  ep_stats.stats = stats;
   ATT_CUDA(gemm_bf16_tc_batched(s, s, dh, qkv_view(QKV_save, 0, s, h, dh, false), qkv_view(QKV_save, 1, s, h, dh, false),
-                                bs_s, kEpiStoreF32, plain_epi(S, s), stm, ctx),
-           "scores GEMM");
-  ATT_CUDA(launch_softmax_rows(S, P_save, b * heads * s, s, stm, ctx.num_sms), "softmax");
+                                bs_s, kEpiRowStats, ep_stats, stm, ctx),
+           "scores GEMM (row statistics)");
+  ATT_CUDA(launch_softmax_combine(stats, static_cast<int>(stat_parts(s)), rowstats, rows, stm, ctx.num_sms),
+           "softmax statistics");
+  EpiParams ep_p = plain_epi(P_save, s);
+  ep_p.rowvec = rowstats;
+  ATT_CUDA(gemm_bf16_tc_batched(s, s, dh, qkv_view(QKV_save, 0, s, h, dh, false), qkv_view(QKV_save, 1, s, h, dh, false),
+                                bs_s, kEpiSoftmax, ep_p, stm, ctx),
+           "scores GEMM (softmax)");
   // O_head = P V, written into the head's columns of O [b*s][h]
   BatchSpec bs_o{heads, b, dh, s * h, 1.0f};
   ATT_CUDA(gemm_bf16_tc_batched(s, dh, s, scores_view(P_save, s, heads, false), qkv_view(QKV_save, 2, s, h, dh, true),
@@ -141,7 +157,7 @@ size_t tpmlp_attention_backward_workspace_size(int64_t b, int64_t s, int64_t h, 
   if (b <= 0 || s <= 0 || h <= 0 || heads <= 0) return 0;
   const size_t n = static_cast<size_t>(b) * static_cast<size_t>(s);
   const size_t sc = scores_elems(b, s, heads);
-  return round_up(n * h * 2, 256) + round_up(sc * sizeof(float), 256) + round_up(sc * 2, 256) +
+  return round_up(n * h * 2, 256) + round_up(n * heads * sizeof(float), 256) + round_up(sc * 2, 256) +
          round_up(n * 3 * h * 2, 256);
 }
 
@@ -175,8 +191,8 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
   const size_t sc = scores_elems(b, s, heads);
   char* ws = static_cast<char*>(workspace);
   void* dO = ws;
-  float* dP = reinterpret_cast<float*>(ws + round_up(static_cast<size_t>(n) * h * 2, 256));
-  void* dS = reinterpret_cast<char*>(dP) + round_up(sc * sizeof(float), 256);
+  float* D = reinterpret_cast<float*>(ws + round_up(static_cast<size_t>(n) * h * 2, 256));
+  void* dS = reinterpret_cast<char*>(D) + round_up(static_cast<size_t>(n) * heads * sizeof(float), 256);
   void* dQKV = static_cast<char*>(dS) + round_up(sc * 2, 256);
   // output projection: dO = G W_o^T, dW_o = O^T G
   ATT_CUDA(gemm_bf16_tc(n, h, h, Operand{G, n, h, h, false}, Operand{Wo, h, h, h, false}, kEpiStore,
@@ -191,13 +207,17 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
   ATT_CUDA(gemm_bf16_tc_batched(s, dh, s, scores_view(P_save, s, heads, true), heads_view(dO, s, h, dh, true), bs_qkv,
                                 kEpiStore, plain_epi(dq + 2 * dh * 2, 3 * h), stm, ctx),
            "dV GEMM");
+  // dS = P * (dP - D) / sqrt(dh) with dP = dO V^T computed and consumed in the same GEMM's
+  // epilogue; D = rowsum(P * dP) = rowsum(dO * O) per (head, query row), from dO and O alone.
+  ATT_CUDA(launch_row_dot(dO, O_save, D, b, s, h, heads, stm, ctx.num_sms), "rowsum(dO * O)");
   const BatchSpec bs_p{heads, b, s * s, heads * s * s, 1.0f};
+  EpiParams ep_ds = plain_epi(dS, s);
+  ep_ds.aux = P_save;
+  ep_ds.rowvec = D;
+  ep_ds.escale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(dh)));
   ATT_CUDA(gemm_bf16_tc_batched(s, s, dh, heads_view(dO, s, h, dh, false), qkv_view(QKV_save, 2, s, h, dh, false),
-                                bs_p, kEpiStoreF32, plain_epi(dP, s), stm, ctx),
-           "dP GEMM");
-  ATT_CUDA(launch_softmax_backward(P_save, dP, static_cast<float>(1.0 / std::sqrt(static_cast<double>(dh))), dS,
-                                   b * heads * s, s, stm, ctx.num_sms),
-           "softmax backward");
+                                bs_p, kEpiSoftmaxGrad, ep_ds, stm, ctx),
+           "dP GEMM (softmax backward)");
   ATT_CUDA(gemm_bf16_tc_batched(s, dh, s, scores_view(dS, s, heads, false), qkv_view(QKV_save, 1, s, h, dh, true),
                                 bs_qkv, kEpiStore, plain_epi(dq, 3 * h), stm, ctx),
            "dQ GEMM");

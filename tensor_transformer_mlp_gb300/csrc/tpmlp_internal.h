@@ -20,8 +20,12 @@ enum EpiKind : int {
   kEpiStoreF32 = 1,  // out[r][c] = acc (fp32)
   kEpiGelu = 2,      // out[r][c] = acc (Z, may be null), out2[r][c] = gelu(acc) (Y)
   kEpiDGelu = 3,     // out[r][c] = acc * gelu'(aux[r][c])  (D = (G B^T) * gelu'(Z))
-  kEpiDropoutResidual = 4,
-  kEpiAccumF32 = 5,  // out[r][c] += acc (fp32): gradient accumulation into an fp32 main_grad  // out[R][c] = aux[R][c] + keep(r, c) * acc * scale, R = remap(r); mask bits
+  kEpiDropoutResidual = 4,  // out[R][c] = aux[R][c] + keep(r, c) * acc * scale, R = remap(r); mask bits
+  kEpiAccumF32 = 5,  // out[r][c] += acc (fp32): gradient accumulation into an fp32 main_grad
+  // Attention softmax in two GEMM passes over the same scores x = alpha * acc (batched only):
+  kEpiRowStats = 6,     // stats[srow][2*nb + half] = (max x, sum exp(x - max)) over the warp's columns
+  kEpiSoftmax = 7,      // out[r][c] = exp(x - rowvec[srow].M) * rowvec[srow].invL  (P, operand dtype)
+  kEpiSoftmaxGrad = 8,  // out[r][c] = escale * aux[r][c] * (x - rowvec[srow])  (dS from dP, P and D)
 };
 
 // Dropout of the sequence-parallel block applied in a GEMM epilogue: element (r, c) of the
@@ -50,6 +54,12 @@ struct EpiParams {
   int gelu;
   RowRemap remap;
   DropoutParams drop;
+  // kEpiRowStats: float2 partial row statistics [rows][2 * N-blocks]; kEpiSoftmax: float2 (M, 1/L)
+  // per row; kEpiSoftmaxGrad: float D per row. Rows of a batched launch are numbered
+  // srow = (z2 * nz1 + z1) * M + r.
+  void* stats;
+  const void* rowvec;
+  float escale;
 };
 
 // A stored operand matrix [rows][cols] with row stride `ld` elements.
@@ -140,10 +150,11 @@ cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void
                                       bool bf16, cudaStream_t stream, int num_sms, bool rms = false,
                                       unsigned int* status = nullptr);
 
-// Attention softmax: fp32 scores -> bf16 probabilities per row of length L (L % 8 == 0, L <= 8192),
-// and its backward dS = scale * P * (dP - rowsum(P * dP)) in bf16.
-cudaError_t launch_softmax_rows(const float* S, void* P, int64_t rows, int64_t L, cudaStream_t stream, int num_sms);
-cudaError_t launch_softmax_backward(const void* P, const float* dP, float scale, void* dS, int64_t rows, int64_t L,
-                                    cudaStream_t stream, int num_sms);
+// Attention helpers: combine the kEpiRowStats partials of each row into (M, 1/L); and
+// D[(bi*heads + j)*s + si] = dot(dO, O) over head j's columns of token row bi*s + si.
+cudaError_t launch_softmax_combine(const void* stats, int nparts, void* rowstats, int64_t rows, cudaStream_t stream,
+                                   int num_sms);
+cudaError_t launch_row_dot(const void* dO, const void* O, float* D, int64_t b, int64_t s, int64_t h, int heads,
+                           cudaStream_t stream, int num_sms);
 
 }  // namespace tpmlp
