@@ -1030,17 +1030,28 @@ __global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restri
 
 // ------------------------------------------------------------------ attention softmax (fused form)
 // Row r's partial statistics (m_j, l_j) from the scores GEMM's kEpiRowStats epilogue become
-// M = max_j m_j and 1/L with L = sum_j l_j * exp(m_j - M); one thread per row.
+// M = max_j m_j and 1/L with L = sum_j l_j * exp(m_j - M); one warp per row, lanes over j.
 __global__ void __launch_bounds__(256) softmax_combine_kernel(const float2* __restrict__ stats, int nparts,
                                                               float2* __restrict__ rowstats, int64_t rows) {
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (r >= rows) return;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;  // uniform across the warp
   const float2* st = stats + r * nparts;
+  float2 v[2];
   float M = -INFINITY;
-  for (int j = 0; j < nparts; ++j) M = fmaxf(M, st[j].x);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int j = lane + 32 * k;
+    v[k] = j < nparts ? st[j] : make_float2(-INFINITY, 0.f);
+    M = fmaxf(M, v[k].x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float L = 0.f;
-  for (int j = 0; j < nparts; ++j) L += st[j].y * __expf(st[j].x - M);
-  rowstats[r] = make_float2(M, 1.0f / L);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) L += v[k].y > 0.f ? v[k].y * __expf(v[k].x - M) : 0.f;
+  L = warp_sum(L);
+  if (lane == 0) rowstats[r] = make_float2(M, 1.0f / L);
 }
 
 // D[(bi*heads + j)*s + si] = sum over head j's dh columns of dO * O in token row bi*s + si
@@ -1349,7 +1360,8 @@ cudaError_t launch_softmax_combine(const void* stats, int nparts, void* rowstats
                                    int num_sms) {
   (void)num_sms;
   if (rows <= 0) return cudaSuccess;
-  softmax_combine_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
+  if (nparts > 64) return cudaErrorInvalidValue;  // s <= 8192: at most 2 * 32 parts
+  softmax_combine_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const float2*>(stats), nparts, static_cast<float2*>(rowstats), rows);
   return cudaGetLastError();
 }
