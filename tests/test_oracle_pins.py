@@ -536,3 +536,22 @@ def test_rmsnorm_gradient_orthogonal_to_x_only():
     dx, _ = rmsnorm.rmsnorm_backward(x, np.ones(64), 0.0, dy)
     assert np.abs((dx * x).sum(1)).max() < 1e-11
     assert np.abs(dx.sum(1)).max() > 1e-3
+
+
+def test_attention_softmax_gradient_rowsum_identity():
+    # The kernels take rowsum(P * dP) as rowsum(dO * O) per head and query row: with O = P V and
+    # dP = dO V^T the two are the same sum, sum_j P_ij (dO_i . V_j) = dO_i . (sum_j P_ij V_j).
+    # Checked on the oracle's own P, dO and V (the oracle itself uses the first form).
+    X, Wqkv, Wo, heads, G = _attn_small(120)
+    b, s, h = X.shape
+    dh = h // heads
+    f = oattn.forward(X, Wqkv, Wo, heads)
+    g = oattn.backward(X, Wqkv, Wo, heads, G)
+    v = np.transpose(f["QKV"].reshape(b, s, heads, 3, dh)[:, :, :, 2, :], (0, 2, 1, 3))
+    dOh = np.transpose(g["dO"].reshape(b, s, heads, dh), (0, 2, 1, 3))
+    Oh = np.transpose(f["O"].reshape(b, s, heads, dh), (0, 2, 1, 3))
+    dP = dOh @ np.swapaxes(v, -1, -2)
+    lhs = (f["P"] * dP).sum(axis=-1)
+    rhs = (dOh * Oh).sum(axis=-1)
+    assert np.abs(lhs - rhs).max() < 1e-12 * max(1.0, np.abs(lhs).max())
+    assert np.abs(lhs).max() > 1e-3  # not a vacuous zero
