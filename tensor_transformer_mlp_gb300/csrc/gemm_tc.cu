@@ -301,8 +301,12 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       store_staged<false>(buf, ys, lane, prow, ep.out2, ep.ldo, col0, N);
     }
   } else if constexpr (EPI == kEpiRowStats) {
-    // Online max / sum of exp over the warp's 128 columns of the row: per 32-column chunk the
-    // running sum is rescaled to the new maximum. Columns past N do not count.
+    // Online max / sum of exp over the warp's 128 columns of the row, in base 2: with
+    // c = alpha * log2(e) > 0, y = acc * c, the running (m, l) are max y and sum 2^(y - m); per
+    // 32-column chunk the sum is rescaled to the new maximum. max(acc) * c = max(acc * c) since
+    // c > 0, so the max is taken on the raw accumulators; 2^(y - m) is ex2(fma(acc, c, -m)).
+    // Columns past N do not count (only a ragged last chunk checks them).
+    const float c2 = alpha * kLog2e;
     float m = -INFINITY, l = 0.f;
 #pragma unroll 1
     for (int c = c_begin; c < c_begin + kEpiChunks; ++c) {
@@ -312,17 +316,21 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), v);
       tmem_ld_wait();
       float x[32];
-      float cmax = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] = col0 + i < N ? __uint_as_float(v[i]) * alpha : -INFINITY;
-        cmax = fmaxf(cmax, x[i]);
+      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
+      if (col0 + 32 > N) {  // uniform across the warp
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i >= N) x[i] = -INFINITY;
       }
-      const float mn = fmaxf(m, cmax);
-      float sum = 0.f;
+      float c4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sum += __expf(x[i] - mn);
-      l = l * __expf(m - mn) + sum;
+      for (int i = 4; i < 32; ++i) c4[i & 3] = fmaxf(c4[i & 3], x[i]);
+      const float mn = fmaxf(m, fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3])) * c2);
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s4[i & 3] += ex2_approx(fmaf(x[i], c2, -mn));
+      l = l * ex2_approx(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
       m = mn;
     }
     if (row < M) {
@@ -330,7 +338,9 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       static_cast<float2*>(ep.stats)[srow * (2 * num_nb) + 2 * nb + half] = make_float2(m, l);
     }
   } else if constexpr (EPI == kEpiSoftmax) {
-    // P = exp(x - M) / L with the row's combined statistics, 64 columns per pass, staged.
+    // P = 2^(acc * c - M) / L with the row's combined base-2 statistics (M, 1/L), 64 columns
+    // per pass, staged.
+    const float c2 = alpha * kLog2e;
     const float2 st = row < M ? static_cast<const float2*>(ep.rowvec)[srow] : make_float2(0.f, 0.f);
     const int64_t prow = row < M ? row : -1;
     void* out = static_cast<__nv_bfloat16*>(ep.out) + out_off;
@@ -347,7 +357,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       for (int g = 0; g < 8; ++g) {
         float p[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) p[i] = __expf(__uint_as_float(v[g * 8 + i]) * alpha - st.x) * st.y;
+        for (int i = 0; i < 8; ++i) p[i] = ex2_approx(fmaf(__uint_as_float(v[g * 8 + i]), c2, -st.x)) * st.y;
         seg[g] = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
                             pack_bf16x2(p[6], p[7]));
       }
@@ -355,7 +365,9 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
     }
   } else if constexpr (EPI == kEpiSoftmaxGrad) {
     // dS = escale * P * (dP - D): P read and dS written 64 columns at a time through the staging buffer.
-    const float d = row < M ? static_cast<const float*>(ep.rowvec)[srow] : 0.f;
+    // escale * (acc * alpha - D) = acc * a2 - d2: one FFMA and one FMUL per element.
+    const float a2 = alpha * ep.escale;
+    const float d2 = (row < M ? static_cast<const float*>(ep.rowvec)[srow] : 0.f) * ep.escale;
     const int64_t prow = row < M ? row : -1;
     const void* pin = static_cast<const __nv_bfloat16*>(ep.aux) + out_off;
     void* out = static_cast<__nv_bfloat16*>(ep.out) + out_off;
@@ -375,9 +387,8 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 pf = unpack_bf16x2(w[i]);
-          const float x0 = __uint_as_float(v[g * 8 + 2 * i]) * alpha;
-          const float x1 = __uint_as_float(v[g * 8 + 2 * i + 1]) * alpha;
-          w[i] = pack_bf16x2(ep.escale * pf.x * (x0 - d), ep.escale * pf.y * (x1 - d));
+          w[i] = pack_bf16x2(pf.x * fmaf(__uint_as_float(v[g * 8 + 2 * i]), a2, -d2),
+                             pf.y * fmaf(__uint_as_float(v[g * 8 + 2 * i + 1]), a2, -d2));
         }
       }
       store_staged<false>(buf, ps, lane, prow, out, ep.ldo, col0, N);

@@ -23,8 +23,9 @@ enum EpiKind : int {
   kEpiDropoutResidual = 4,  // out[R][c] = aux[R][c] + keep(r, c) * acc * scale, R = remap(r); mask bits
   kEpiAccumF32 = 5,  // out[r][c] += acc (fp32): gradient accumulation into an fp32 main_grad
   // Attention softmax in two GEMM passes over the same scores x = alpha * acc (batched only):
-  kEpiRowStats = 6,     // stats[srow][2*nb + half] = (max x, sum exp(x - max)) over the warp's columns
-  kEpiSoftmax = 7,      // out[r][c] = exp(x - rowvec[srow].M) * rowvec[srow].invL  (P, operand dtype)
+  // (statistics in base 2: y = x * log2(e), so exp(x - max x) = 2^(y - max y))
+  kEpiRowStats = 6,     // stats[srow][2*nb + half] = (max y, sum 2^(y - max y)) over the warp's columns
+  kEpiSoftmax = 7,      // out[r][c] = 2^(y - rowvec[srow].M) * rowvec[srow].invL  (P, operand dtype)
   kEpiSoftmaxGrad = 8,  // out[r][c] = escale * aux[r][c] * (x - rowvec[srow])  (dS from dP, P and D)
 };
 
