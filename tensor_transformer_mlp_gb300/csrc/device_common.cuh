@@ -328,12 +328,23 @@ constexpr float kInvSqrt2 = 0.7071067811865476f;
 constexpr float kInvSqrt2Pi = 0.3989422804014327f;
 
 // GeLU and its derivative in fp32. `precise` selects tanhf over the hardware tanh.approx.
+// Tanh form with a = sqrt(2/pi), b = a * 0.044715: u = x (a + b x^2), phi = x/2 (1 + tanh u),
+// phi' = (1 + tanh u) / 2 + x/2 (1 - tanh^2 u) (a + 3 b x^2); the fast path is arranged as
+// FMAs (five FP operations and one tanh.approx for phi).
+constexpr float kTanhA = kSqrt2OverPi;
+constexpr float kTanhB = kSqrt2OverPi * kTanhC;
+
 template <bool precise>
 __device__ __forceinline__ float gelu_f(float x, int kind) {
   if (kind == kGeluErf) return 0.5f * x * (1.0f + erff(x * kInvSqrt2));
-  const float u = kSqrt2OverPi * fmaf(kTanhC * x * x, x, x);
-  const float th = precise ? tanhf(u) : tanh_fast(u);
-  return 0.5f * x * (1.0f + th);
+  if constexpr (precise) {
+    const float u = kSqrt2OverPi * fmaf(kTanhC * x * x, x, x);
+    return 0.5f * x * (1.0f + tanhf(u));
+  } else {
+    const float th = tanh_fast(x * fmaf(kTanhB, x * x, kTanhA));
+    const float hx = 0.5f * x;
+    return fmaf(hx, th, hx);
+  }
 }
 
 template <bool precise>
@@ -342,9 +353,16 @@ __device__ __forceinline__ float gelu_grad_f(float x, int kind) {
     const float cdf = 0.5f * (1.0f + erff(x * kInvSqrt2));
     return cdf + x * kInvSqrt2Pi * expf(-0.5f * x * x);
   }
-  const float u = kSqrt2OverPi * fmaf(kTanhC * x * x, x, x);
-  const float th = precise ? tanhf(u) : tanh_fast(u);
-  return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * kSqrt2OverPi * fmaf(3.0f * kTanhC, x * x, 1.0f);
+  if constexpr (precise) {
+    const float u = kSqrt2OverPi * fmaf(kTanhC * x * x, x, x);
+    const float th = tanhf(u);
+    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * kSqrt2OverPi * fmaf(3.0f * kTanhC, x * x, 1.0f);
+  } else {
+    const float x2 = x * x;
+    const float th = tanh_fast(x * fmaf(kTanhB, x2, kTanhA));
+    const float dudx = fmaf(3.0f * kTanhB, x2, kTanhA);
+    return fmaf(0.5f, th, 0.5f) + (0.5f * x * dudx) * fmaf(-th, th, 1.0f);
+  }
 }
 
 // Drop decision for one element: splitmix64(key) < threshold, with SplitMix64 as published by
