@@ -221,3 +221,38 @@ def test_alternative_gemm_paths(env):
            "-k", "ragged_bf16 or single_block or biased or accumulation or shard_count or gpt_mlp_sampled"]
     r = subprocess.run(cmd, cwd=repo, env=child_env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+
+
+def test_step_replays_from_a_cuda_graph():
+    """Forward + backward captured once in a CUDA graph and replayed: bit-identical to eager
+    launches (no host synchronisation or allocation inside the calls; the pair GEMM's cluster
+    launches and pacing-counter resets are captured like any other stream work)."""
+    cfg = wl.MLPConfig("graph", 1024, 512, 2048, 4, "bf16", "tanh", 1.0, 0.05, 1.0, seed=21)
+    inp = wl.mlp_inputs(cfg)
+    X, A, B, G = (dev(inp[k], "bf16") for k in "XABG")
+    n, d, m, t = cfg.n, cfg.d, cfg.m, cfg.t
+    outs = {k: torch.empty(s, dtype=dt, device="cuda") for k, s, dt in
+            (("O", (n, d), torch.bfloat16), ("Z", (n, m), torch.bfloat16), ("Y", (n, m), torch.bfloat16),
+             ("dX", (n, d), torch.bfloat16), ("dA", (d, m), torch.float32), ("dB", (m, d), torch.float32))}
+    ws = torch.empty(tp.tpmlp_backward_workspace_size(n, m, torch.bfloat16), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        tp.tpmlp_forward(X, A, B, outs["O"], outs["Z"], outs["Y"], t, "tanh", s)
+        tp.tpmlp_backward(X, A, B, G, outs["Z"], outs["Y"], outs["dX"], outs["dA"], outs["dB"], t, "tanh", ws, s)
+
+    with torch.cuda.stream(s):
+        step()  # eager, also initialises the library's per-device state outside the capture
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in outs.items()}
+    for v in outs.values():
+        v.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    for k in outs:
+        assert torch.equal(outs[k], eager[k]), k
