@@ -58,6 +58,22 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTE
 static_assert(A_STAGE_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
+// One-SM kernel configurations by tile width: 128 x 256 tiles with a 4-stage ring, or 128 x 128
+// tiles (for N <= 128, e.g. N = head_dim) with a 6-stage ring and half the tensor memory.
+template <int BN_T>
+struct OneSm {
+  static constexpr int kBN = BN_T;
+  static constexpr int kStages = BN_T == 256 ? 4 : 6;
+  static constexpr int kStageBytes = A_STAGE_BYTES + BN_T * BK * 2;
+  static constexpr int kSmemBytes = kStages * kStageBytes + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;
+  static constexpr int kTmemCols = NUM_ACC * BN_T;  // a power of two, >= 32
+  static constexpr int kEpiChunks = BN_T / 32 / (NUM_EPI_WARPS / 4);
+  static_assert(BN_T == 256 || BN_T == 128, "tile widths");
+  static_assert(kStageBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert((2 * kStages + 2 * NUM_ACC + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area");
+};
+
 struct TileSched {
   int num_mb, num_nb, num_tiles;
   __device__ __forceinline__ void coords(int tile, int& mb, int& nb) const {
@@ -233,7 +249,7 @@ __device__ __forceinline__ void store_prologue8(const EpiParams& ep, int col, bo
 // c_begin, starting at output column col_tile0. buf is the warp's staging buffer.
 constexpr int kEpiChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp
 
-template <int EPI, bool BATCHED>
+template <int EPI, bool BATCHED, int kChunks = kEpiChunks>
 __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf, int lane, int64_t row, int M, int N,
                                               int col_tile0, int c_begin, uint32_t t_row, int64_t out_off,
                                               float alpha, int64_t srow, int nb, int num_nb) {
@@ -244,7 +260,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
     void* out = kF32 ? static_cast<void*>(static_cast<float*>(ep.out) + out_off)
                      : static_cast<void*>(static_cast<__nv_bfloat16*>(ep.out) + out_off);
 #pragma unroll 1
-    for (int c = c_begin; c < c_begin + kEpiChunks; c += kCols / 32) {
+    for (int c = c_begin; c < c_begin + kChunks; c += kCols / 32) {
       const int col0 = col_tile0 + c * 32;
       if (col0 >= N) break;  // uniform across the warp
       uint32_t v[kCols];
@@ -275,7 +291,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
     // Z (optional) and Y = gelu(Z), 64 columns per pass, both through the staging buffer.
     const int64_t prow = row < M ? row : -1;
 #pragma unroll 1
-    for (int c = c_begin; c < c_begin + kEpiChunks; c += 2) {
+    for (int c = c_begin; c < c_begin + kChunks; c += 2) {
       const int col0 = col_tile0 + c * 32;
       if (col0 >= N) break;  // uniform across the warp
       uint32_t v[64];
@@ -309,7 +325,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
     const float c2 = alpha * kLog2e;
     float m = -INFINITY, l = 0.f;
 #pragma unroll 1
-    for (int c = c_begin; c < c_begin + kEpiChunks; ++c) {
+    for (int c = c_begin; c < c_begin + kChunks; ++c) {
       const int col0 = col_tile0 + c * 32;
       if (col0 >= N) break;  // uniform across the warp
       uint32_t v[32];
@@ -334,7 +350,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       m = mn;
     }
     if (row < M) {
-      const int half = c_begin / kEpiChunks;
+      const int half = c_begin / kChunks;
       static_cast<float2*>(ep.stats)[srow * (2 * num_nb) + 2 * nb + half] = make_float2(m, l);
     }
   } else if constexpr (EPI == kEpiSoftmax) {
@@ -345,7 +361,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
     const int64_t prow = row < M ? row : -1;
     void* out = static_cast<__nv_bfloat16*>(ep.out) + out_off;
 #pragma unroll 1
-    for (int c = c_begin; c < c_begin + kEpiChunks; c += 2) {
+    for (int c = c_begin; c < c_begin + kChunks; c += 2) {
       const int col0 = col_tile0 + c * 32;
       if (col0 >= N) break;  // uniform across the warp
       uint32_t v[64];
@@ -372,7 +388,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
     const void* pin = static_cast<const __nv_bfloat16*>(ep.aux) + out_off;
     void* out = static_cast<__nv_bfloat16*>(ep.out) + out_off;
 #pragma unroll 1
-    for (int c = c_begin; c < c_begin + kEpiChunks; c += 2) {
+    for (int c = c_begin; c < c_begin + kChunks; c += 2) {
       const int col0 = col_tile0 + c * 32;
       if (col0 >= N) break;  // uniform across the warp
       uint32_t v[64];
@@ -397,7 +413,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
     // D = acc * gelu'(Z): Z read and D written 64 columns at a time through the staging buffer.
     const int64_t prow = row < M ? row : -1;
 #pragma unroll 1
-    for (int c = c_begin; c < c_begin + kEpiChunks; c += 2) {
+    for (int c = c_begin; c < c_begin + kChunks; c += 2) {
       const int col0 = col_tile0 + c * 32;
       if (col0 >= N) break;  // uniform across the warp
       uint32_t v[64];
@@ -420,7 +436,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
     }
   } else {
 #pragma unroll 1
-    for (int c = c_begin; c < c_begin + kEpiChunks; ++c) {
+    for (int c = c_begin; c < c_begin + kChunks; ++c) {
       const int col0 = col_tile0 + c * 32;
       if (col0 >= N) break;  // uniform across the warp
       uint32_t v[32];
@@ -447,10 +463,13 @@ __device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, uin
   }
 }
 
-template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false>
+template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false, int BN_T = 256>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
                      int N, int K, EpiParams ep, unsigned int* status, BatchDev bd) {
+  using Cfg = OneSm<BN_T>;
+  constexpr int BN = Cfg::kBN, STAGES = Cfg::kStages, STAGE_BYTES = Cfg::kStageBytes, TMEM_COLS = Cfg::kTmemCols;
+  constexpr int kChunks = Cfg::kEpiChunks;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -598,7 +617,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
-    const int c_begin = ((warp - 2) / 4) * kEpiChunks;
+    const int c_begin = ((warp - 2) / 4) * kChunks;
     int it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -612,7 +631,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       const int64_t srow = BATCHED ? (static_cast<int64_t>(z2) * bd.nz1 + z1) * M + row : row;
-      epilogue_tile<EPI, BATCHED>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N, nb * BN, c_begin,
+      epilogue_tile<EPI, BATCHED, kChunks>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N, nb * BN, c_begin,
                                   t_row, out_off, BATCHED ? bd.alpha : 1.f, srow, nb, sched.num_nb);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
@@ -900,17 +919,18 @@ cudaError_t make_tmap(CUtensorMap* map, const Operand& op, uint32_t box_inner, u
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false>
+template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false, int BN_T = 256>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
                    cudaStream_t stream, const DeviceCtx& ctx, const BatchDev& bd = BatchDev{}) {
-  auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI, BATCHED>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI, BATCHED, BN_T>;
+  constexpr int kSmem = OneSm<BN_T>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  int64_t tiles = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  int64_t tiles = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN_T - 1) / BN_T);
   if (BATCHED) tiles *= static_cast<int64_t>(bd.nz1) * bd.nz2;
   if (tiles > INT32_MAX) return cudaErrorInvalidValue;
   const int grid = tiles < ctx.num_sms ? static_cast<int>(tiles) : ctx.num_sms;
-  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, M, N, K, ep, ctx.status, bd);
+  kernel<<<grid, NUM_THREADS, kSmem, stream>>>(ta, tb, M, N, K, ep, ctx.status, bd);
   return cudaGetLastError();
 }
 
@@ -1098,6 +1118,12 @@ cudaError_t gemm_bf16_tc_batched(int64_t M, int64_t N, int64_t K, const BatchedO
   e = make_tmap_batched(&tb, b, bs.nz1, bs.nz2, 64, b.mn_major ? BK : BN, &bd.b_row, &bd.b_z1, &bd.b_z2);
   if (e != cudaSuccess) return e;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  // N <= 128 with B stored MN-major (the head_dim-wide P V, P^T dO, dS K, dS^T Q): 128-wide tiles,
+  // no padded half. An MN-major B is loaded in 64-column boxes, so its tensor map is the same.
+  if (N <= 128 && b.mn_major && epi == kEpiStore) {
+    if (!a.mn_major) return launch<false, true, kEpiStore, true, 128>(ta, tb, m, n, k, ep, stream, ctx, bd);
+    return launch<true, true, kEpiStore, true, 128>(ta, tb, m, n, k, ep, stream, ctx, bd);
+  }
   if (!a.mn_major && !b.mn_major && epi == kEpiStoreF32)
     return launch<false, false, kEpiStoreF32, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
   if (!a.mn_major && !b.mn_major && epi == kEpiRowStats)
