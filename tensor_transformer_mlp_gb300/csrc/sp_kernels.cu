@@ -1056,30 +1056,57 @@ __global__ void __launch_bounds__(256) softmax_combine_kernel(const float2* __re
 }
 
 // D[(bi*heads + j)*s + si] = sum over head j's dh columns of dO * O in token row bi*s + si
-// (= rowsum(P * dP) for that query row); one thread per (token row, head), 16-byte loads.
+// (= rowsum(P * dP) for that query row). One warp per token row; the lanes read a head's dh/8
+// 16-byte vectors of dO and O (coalesced), several heads at once when dh/8 divides 32, and the
+// products are summed across the lanes of each head.
 __global__ void __launch_bounds__(256) row_dot_kernel(const __nv_bfloat16* __restrict__ dO,
                                                       const __nv_bfloat16* __restrict__ O, float* __restrict__ D,
                                                       int64_t b, int64_t s, int64_t h, int heads) {
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= b * s * heads) return;
-  const int64_t tok = idx / heads;
-  const int j = static_cast<int>(idx - tok * heads);
+  const int64_t tok = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (tok >= b * s) return;  // uniform across the warp
   const int64_t dh = h / heads;
-  const __nv_bfloat16* a = dO + tok * h + j * dh;
-  const __nv_bfloat16* c = O + tok * h + j * dh;
-  float acc = 0.f;
-  for (int64_t e = 0; e < dh; e += 8) {
-    Vec8<__nv_bfloat16> va, vc;
-    va.load(a + e);
-    vc.load(c + e);
-    float fa[8], fc[8];
-    va.to_float(fa);
-    vc.to_float(fc);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc = fmaf(fa[k], fc[k], acc);
-  }
+  const int vh = static_cast<int>(dh / 8);
   const int64_t bi = tok / s, si = tok - bi * s;
-  D[(bi * heads + j) * s + si] = acc;
+  const __nv_bfloat16* a = dO + tok * h;
+  const __nv_bfloat16* c = O + tok * h;
+  if (vh <= 32 && (32 % vh) == 0) {
+    // 32 / vh heads at a time: lane l takes vector l % vh of head j0 + l / vh; segments of vh
+    // lanes are summed by xor shuffles that stay inside the segment.
+    const int hpw = 32 / vh, seg = lane / vh, v = lane % vh;
+    for (int j0 = 0; j0 < heads; j0 += hpw) {
+      const int j = j0 + seg;
+      float acc = 0.f;
+      if (j < heads) {
+        Vec8<__nv_bfloat16> va, vc;
+        va.load(a + j * dh + v * 8);
+        vc.load(c + j * dh + v * 8);
+        float fa[8], fc[8];
+        va.to_float(fa);
+        vc.to_float(fc);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = fmaf(fa[k], fc[k], acc);
+      }
+      for (int o = vh / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (v == 0 && j < heads) D[(bi * heads + j) * s + si] = acc;
+    }
+    return;
+  }
+  for (int j = 0; j < heads; ++j) {
+    float acc = 0.f;
+    for (int v = lane; v < vh; v += 32) {
+      Vec8<__nv_bfloat16> va, vc;
+      va.load(a + j * dh + v * 8);
+      vc.load(c + j * dh + v * 8);
+      float fa[8], fc[8];
+      va.to_float(fa);
+      vc.to_float(fc);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc = fmaf(fa[k], fc[k], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) D[(bi * heads + j) * s + si] = acc;
+  }
 }
 
 int rows_grid(int64_t rows, int num_sms, int per_sm) {
@@ -1370,10 +1397,10 @@ cudaError_t launch_softmax_combine(const void* stats, int nparts, void* rowstats
 cudaError_t launch_row_dot(const void* dO, const void* O, float* D, int64_t b, int64_t s, int64_t h, int heads,
                            cudaStream_t stream, int num_sms) {
   (void)num_sms;
-  const int64_t n = b * s * heads;
+  const int64_t n = b * s;  // token rows, one warp each
   if (n <= 0) return cudaSuccess;
   if ((h / heads) % 8 != 0) return cudaErrorInvalidValue;
-  row_dot_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+  row_dot_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), D, b, s, h, heads);
   return cudaGetLastError();
 }
