@@ -10,7 +10,12 @@
 //   gemm_bf16_pair_kernel (plain GEMMs): 256 x 256 tiles on clusters of two SMs
 //               (tcgen05 cta_group::2), 6-stage ring of 32 KB per SM, paced pairs
 //   gemm_bf16_kernel (batched GEMMs, or all of them with TPMLP_GEMM_PAIR=0): 128 x 256
-//               tiles on one SM, 4-stage ring of 48 KB
+//               tiles on one SM with a 4-stage ring of 48 KB, or 128 x 128 tiles with a
+//               6-stage ring of 32 KB for the batched GEMMs whose N is at most 128
+// The batched launches serve the attention block ("SenseParrots" model-parallel note, section
+// 2.1.1): per (batch, head) the score GEMM Q K^T, whose epilogues compute the softmax in two
+// passes (row statistics, then P), the dP GEMM, whose epilogue forms dS, and P V, P^T dO, dS K,
+// dS^T Q.
 // Warp roles in both:
 //   warp 0      one thread issues TMA tile loads into the shared-memory ring
 //   warp 1      one thread issues tcgen05.mma (K=16 steps) into a tensor-memory
@@ -35,16 +40,13 @@ namespace tpmlp {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // one 128-byte swizzle span of bf16
+constexpr int BN = 256;  // tile width of the pair kernel and the one-SM kernel's wide variant
+constexpr int BK = 64;   // one 128-byte swizzle span of bf16
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box of an MN-major operand
 constexpr int NUM_ACC = 2;
-constexpr int TMEM_COLS = NUM_ACC * BN;  // 512: all of tensor memory
+constexpr int TMEM_COLS = NUM_ACC * BN;  // 512: all of tensor memory (pair kernel)
 constexpr int NUM_EPI_WARPS = 8;  // two warps per tensor-memory lane quarter, each half the columns
 constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
 constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;
@@ -53,10 +55,6 @@ constexpr int BARRIER_BYTES = 256;
 // Per epilogue warp: 32 rows x 128 bytes, used to turn the one-row-per-thread layout of
 // tcgen05.ld into line-wide global stores (kEpiStore, kEpiStoreF32).
 constexpr int EPI_STAGE_BYTES = 32 * 128;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;  // + slack
-
-static_assert(A_STAGE_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 // One-SM kernel configurations by tile width: 128 x 256 tiles with a 4-stage ring, or 128 x 128
 // tiles (for N <= 128, e.g. N = head_dim) with a 6-stage ring and half the tensor memory.
@@ -65,7 +63,8 @@ struct OneSm {
   static constexpr int kBN = BN_T;
   static constexpr int kStages = BN_T == 256 ? 4 : 6;
   static constexpr int kStageBytes = A_STAGE_BYTES + BN_T * BK * 2;
-  static constexpr int kSmemBytes = kStages * kStageBytes + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;
+  static constexpr int kSmemBytes =
+      kStages * kStageBytes + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;  // + alignment slack
   static constexpr int kTmemCols = NUM_ACC * BN_T;  // a power of two, >= 32
   static constexpr int kEpiChunks = BN_T / 32 / (NUM_EPI_WARPS / 4);
   static_assert(BN_T == 256 || BN_T == 128, "tile widths");
@@ -155,7 +154,7 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
   }
 }
 
-// Store path for kEpiStore (bf16, 64 columns) and kEpiStoreF32 (fp32, 32 columns): each thread
+// Store path of the staged epilogues (bf16: 64 columns, fp32: 32 columns per call): each thread
 // holds 128 bytes of its own row in seg[]; they go through the warp's shared-memory buffer
 // (16-byte segments XOR-swizzled by row, so both phases are free of bank conflicts) and leave
 // as 8 rows x 128 contiguous bytes per store instruction instead of 32 rows x 16 bytes.
@@ -185,11 +184,11 @@ __device__ __forceinline__ void store_staged(uint8_t* buf, const uint4 (&seg)[8]
   __syncwarp();
 }
 
-// The inverse of store_staged for bf16, in two steps so that a warp can keep several blocks'
-// loads in flight. issue_block_loads: the warp reads 32 rows x 64 columns of src with line-wide
-// loads (8 rows x 128 bytes per instruction; lane gets rows i*4 + lane/8, segment lane%8; zeros
-// past M or N). transpose_block: through the warp's staging buffer, each thread receives its
-// own row's 128 bytes in seg[].
+// The inverse of store_staged for bf16 (load_staged_bf16), in two steps. issue_block_loads: the
+// warp reads 32 rows x 64 columns of src with line-wide loads (8 rows x 128 bytes per
+// instruction; lane gets rows i*4 + lane/8, segment lane%8; zeros past M or N).
+// transpose_block: through the warp's staging buffer, each thread receives its own row's 128
+// bytes in seg[].
 __device__ __forceinline__ void issue_block_loads(uint4 (&r8)[8], int lane, int64_t prow, const void* src, int64_t ldo,
                                                   int col0, int N) {
   const int col = col0 + (lane & 7) * 8;
@@ -245,9 +244,10 @@ __device__ __forceinline__ void store_prologue8(const EpiParams& ep, int col, bo
 }
 
 // The epilogue of one accumulator tile for one epilogue warp: its 32 tensor-memory lanes
-// (rows row - lane .. row - lane + 31 of the output) and its kEpiChunks 32-column chunks from
-// c_begin, starting at output column col_tile0. buf is the warp's staging buffer.
-constexpr int kEpiChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp
+// (rows row - lane .. row - lane + 31 of the output) and its kChunks 32-column chunks from
+// c_begin, starting at output column col_tile0. buf is the warp's staging buffer; srow numbers
+// the row across the batch (row statistics), nb / num_nb give the tile's N-block.
+constexpr int kEpiChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp, 256-wide tiles
 
 template <int EPI, bool BATCHED, int kChunks = kEpiChunks>
 __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf, int lane, int64_t row, int M, int N,
