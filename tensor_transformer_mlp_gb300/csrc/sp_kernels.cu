@@ -1,10 +1,13 @@
 // Memory-bound kernels of the sequence-parallel MLP block ("Megatron-SP 机制", section
 // "通信插在层内什么位置？"): LayerNorm on [b, s/t, h] shards, the all-gather g that turns
 // shard-major rows into token order, the reduce-scatter g-bar that sums t fp32 partials
-// and writes shard-major rows, and dropout + residual add with a counter-hash mask.
-// All shards live in one HBM buffer [t][b][s/t][h], so g and g-bar are row permutations
-// (plus the t-way sum for g-bar). Every kernel moves 16-byte vectors, one row per CTA
-// iteration, with the shard <-> token mapping computed once per row.
+// and writes shard-major rows, and dropout + residual add with a counter-hash mask; their
+// backward (LayerNorm backward, dropout backward fused with the gather, fixed-order column
+// and partial sums); RMSNorm ("Megatron 训练" notes, section "RMSNorm") through the LayerNorm
+// kernels; and the attention block's two small helpers (softmax statistics combine, per-head
+// row dot product of dO and O). All shards live in one HBM buffer [t][b][s/t][h], so g and
+// g-bar are row permutations (plus the t-way sum for g-bar). Kernels move 16-byte vectors,
+// with the shard <-> token mapping computed once per row.
 #include "device_common.cuh"
 
 namespace tpmlp {
