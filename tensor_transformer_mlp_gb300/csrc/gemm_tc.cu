@@ -978,10 +978,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, int M, int
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int64_t tiles = static_cast<int64_t>((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
-  const int64_t max_pairs = ctx.num_sms / 2;
-  const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
   cfg.stream = stream;
@@ -992,6 +989,24 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, int M, int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // The persistent grid (and the pacing, which waits for every pair of a round) assumes all
+  // pairs are resident at once: no more pairs than the device runs concurrently. Every pair
+  // instantiation has the same threads and shared memory, so one query per device serves all.
+  static int resident_pairs[16] = {};
+  static std::mutex mu;
+  int max_pairs = ctx.num_sms / 2;
+  if (ctx.device >= 0 && ctx.device < 16) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (resident_pairs[ctx.device] == 0) {
+      cfg.gridDim = dim3(2, 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) n = ctx.num_sms / 2;
+      resident_pairs[ctx.device] = n < ctx.num_sms / 2 ? n : ctx.num_sms / 2;
+    }
+    max_pairs = resident_pairs[ctx.device];
+  }
+  const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
   unsigned int* pace = next_pace_counter();
   if (pace) {
     e = cudaMemsetAsync(pace, 0, sizeof(unsigned int), stream);
