@@ -210,3 +210,24 @@ def test_sp_block_backward_full_size():
     assert_close("dA", host(dA), ref["dA"], TOL_BF16, rep)
     assert_close("dB", host(dB), ref["dB"], TOL_BF16, rep)
     print(rep)
+
+
+@pytest.mark.parametrize("rs", ["fused", "splitk"])
+@pytest.mark.parametrize("p", [0.0, 0.9])
+def test_sp_block_dropout_extremes(p, rs):
+    # p = 0: nothing is dropped, out = x + MLP(...) with an all-zero mask; p = 0.9: most of the
+    # MLP output is dropped and the kept part is scaled by 10. Both through the block's own path
+    # (the FC2 epilogue when fused, the separate dropout kernel after split-K).
+    b, s, h, m, t = 2, 128, 256, 512, 4
+    cfg = wl.SPConfig("sp-p", b, s, h, m, t, "tanh", 1.0, 0.05, p_drop=p, seed=77)
+    inp, out, mask = sp_case(cfg, rs)
+    ref = osp.sp_block(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop, cfg.seed, cfg.gelu)
+    got = wl.from_shards(host(out).reshape(t, b, s // t, h))
+    assert_close("out", got, ref["out"], TOL_BF16)
+    words = mask_words(mask)
+    assert np.array_equal(words, osp.pack_mask_bits(ref["dropped"]))
+    if p == 0.0:
+        assert not words.any()
+    else:
+        frac = ref["dropped"].mean()
+        assert 0.85 < frac < 0.95
