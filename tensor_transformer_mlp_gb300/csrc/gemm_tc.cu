@@ -58,19 +58,25 @@ constexpr int EPI_STAGE_BYTES = 32 * 128;
 
 // One-SM kernel configurations by tile width: 128 x 256 tiles with a 4-stage ring, or 128 x 128
 // tiles (for N <= 128, e.g. N = head_dim) with a 6-stage ring and half the tensor memory.
-template <int BN_T>
+// kAux (the dS epilogue, which reads P): each epilogue warp also owns two 4 KB buffers that its
+// lane 0 fills with TMA loads of P one pass ahead, and the ring shrinks to 2 stages to make room
+// (the score-shaped GEMMs have K = head_dim = two k-blocks).
+constexpr int AUX_BUF_BYTES = 32 * 128;  // one 32-row x 64-column bf16 block
+template <int BN_T, bool kAux = false>
 struct OneSm {
   static constexpr int kBN = BN_T;
-  static constexpr int kStages = BN_T == 256 ? 4 : 6;
+  static constexpr int kStages = kAux ? 2 : (BN_T == 256 ? 4 : 6);
   static constexpr int kStageBytes = A_STAGE_BYTES + BN_T * BK * 2;
-  static constexpr int kSmemBytes =
-      kStages * kStageBytes + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;  // + alignment slack
+  static constexpr int kAuxBytes = kAux ? NUM_EPI_WARPS * 2 * AUX_BUF_BYTES : 0;
+  static constexpr int kSmemBytes = kStages * kStageBytes + NUM_EPI_WARPS * EPI_STAGE_BYTES + kAuxBytes +
+                                    BARRIER_BYTES + 1024;  // + alignment slack
   static constexpr int kTmemCols = NUM_ACC * BN_T;  // a power of two, >= 32
   static constexpr int kEpiChunks = BN_T / 32 / (NUM_EPI_WARPS / 4);
   static_assert(BN_T == 256 || BN_T == 128, "tile widths");
   static_assert(kStageBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static_assert((2 * kStages + 2 * NUM_ACC + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area");
+  static_assert((2 * kStages + 2 * NUM_ACC + 1 + (kAux ? 2 * NUM_EPI_WARPS : 0)) * 8 + 4 <= BARRIER_BYTES,
+                "barrier area");
 };
 
 struct TileSched {
@@ -102,6 +108,7 @@ struct BatchDev {
   int nz1, nz2;
   int a_row, a_z1, a_z2;
   int b_row, b_z1, b_z2;
+  int x_row, x_z1, x_z2;  // slots of the aux (P) tensor map, kEpiSoftmaxGrad
   int64_t out_z1, out_z2;
   float alpha;
 };
@@ -465,21 +472,25 @@ __device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, uin
 
 template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false, int BN_T = 256>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
-                     int N, int K, EpiParams ep, unsigned int* status, BatchDev bd) {
-  using Cfg = OneSm<BN_T>;
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_aux, int M, int N, int K, EpiParams ep,
+                     unsigned int* status, BatchDev bd) {
+  constexpr bool kAux = EPI == kEpiSoftmaxGrad && BATCHED;
+  using Cfg = OneSm<BN_T, kAux>;
   constexpr int BN = Cfg::kBN, STAGES = Cfg::kStages, STAGE_BYTES = Cfg::kStageBytes, TMEM_COLS = Cfg::kTmemCols;
   constexpr int kChunks = Cfg::kEpiChunks;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_stage + NUM_EPI_WARPS * EPI_STAGE_BYTES);
+  uint8_t* aux_buf = epi_stage + NUM_EPI_WARPS * EPI_STAGE_BYTES;  // 1024-byte aligned (128-byte swizzle)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(aux_buf + Cfg::kAuxBytes);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;
   uint64_t* tempty_bar = tfull_bar + NUM_ACC;
   uint64_t* drain_bar = tempty_bar + NUM_ACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* aux_bar = drain_bar + 1;  // kAux: two per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + (kAux ? 2 * NUM_EPI_WARPS : 0));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -514,9 +525,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&tempty_bar[a], NUM_EPI_THREADS);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (kAux)
+      for (int i = 0; i < 2 * NUM_EPI_WARPS; ++i) mbar_init(&aux_bar[i], 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
+    if constexpr (kAux) tma_prefetch_desc(&tmap_aux);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -618,6 +632,94 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
     const int c_begin = ((warp - 2) / 4) * kChunks;
+    if constexpr (kAux) {
+      // dS = escale * P * (dP - D) with P arriving by TMA: pass k (64 columns) of a tile reads
+      // buffer k, which lane 0 refills with the next tile's pass k as soon as the warp has read it.
+      static_assert(kChunks == 4, "two 64-column passes per warp");
+      uint8_t* pb = aux_buf + (warp - 2) * 2 * AUX_BUF_BYTES;
+      uint64_t* pbar = aux_bar + (warp - 2) * 2;
+      uint32_t pphase[2] = {0u, 0u};
+      bool pending[2] = {false, false};
+      auto issue_p = [&](int tl, int k) {  // uniform across the warp
+        if (tl >= total_tiles) return;
+        int z1, z2, mb, nb;
+        tile_coords(tl, z1, z2, mb, nb);
+        const int col = nb * BN + (c_begin + 2 * k) * 32;
+        if (col >= N) return;
+        if (lane == 0) {
+          fence_proxy_async_smem();  // the warp's reads of this buffer come before the TMA refill
+          mbar_arrive_expect_tx(&pbar[k], AUX_BUF_BYTES);
+          load_tile<true>(pb + k * AUX_BUF_BYTES, &tmap_aux, &pbar[k], col, mb * BM + q * 32, z1, z2, bd.x_row,
+                          bd.x_z1, bd.x_z2);
+        }
+        pending[k] = true;
+      };
+      issue_p(blockIdx.x, 0);
+      issue_p(blockIdx.x, 1);
+      int it = 0;
+      bool fail = false;
+      for (int tile = blockIdx.x; tile < total_tiles && !fail; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        const bool ok = mbar_wait(&tfull_bar[acc], use & 1, status, 6);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        int z1, z2, mb, nb;
+        tile_coords(tile, z1, z2, mb, nb);
+        const int64_t out_off = z1 * bd.out_z1 + z2 * bd.out_z2;
+        const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+        const int64_t srow = (static_cast<int64_t>(z2) * bd.nz1 + z1) * M + row;
+        const float a2 = bd.alpha * ep.escale;
+        const float d2 = (row < M ? static_cast<const float*>(ep.rowvec)[srow] : 0.f) * ep.escale;
+        const int64_t prow = row < M ? row : -1;
+        void* out = static_cast<__nv_bfloat16*>(ep.out) + out_off;
+        uint8_t* sbuf = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+          const int c = c_begin + 2 * k;
+          const int col0 = nb * BN + c * 32;
+          if (col0 < N) {  // uniform across the warp
+            uint32_t v[64];
+            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32),
+                               *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            const bool okp = mbar_wait(&pbar[k], pphase[k], status, 7);
+            pphase[k] ^= 1u;
+            pending[k] = false;
+            if (!__all_sync(0xffffffffu, okp)) fail = true;
+            // The TMA wrote the block with the 128-byte swizzle: row r's 16-byte segment j sits
+            // at r * 128 + ((j ^ (r & 7)) << 4), so each thread reads its own row without conflicts.
+            uint4 ps[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+              ps[jj] = *reinterpret_cast<const uint4*>(pb + k * AUX_BUF_BYTES + lane * 128 + ((jj ^ (lane & 7)) << 4));
+            __syncwarp();
+            if (!fail) issue_p(tile + static_cast<int>(gridDim.x), k);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {  // dS overwrites P in place
+              uint32_t* w = reinterpret_cast<uint32_t*>(&ps[g]);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 pf = unpack_bf16x2(w[i]);
+                w[i] = pack_bf16x2(pf.x * fmaf(__uint_as_float(v[g * 8 + 2 * i]), a2, -d2),
+                                   pf.y * fmaf(__uint_as_float(v[g * 8 + 2 * i + 1]), a2, -d2));
+              }
+            }
+            store_staged<false>(sbuf, ps, lane, prow, out, ep.ldo, col0, N);
+          } else if (!fail) {
+            issue_p(tile + static_cast<int>(gridDim.x), k);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[acc]);
+      }
+      // Copies still in flight land before the CTA's shared memory goes away (bounded).
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (pending[k]) mbar_wait(&pbar[k], pphase[k], status, 8);
+    } else {
     int it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -635,6 +737,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                   t_row, out_off, BATCHED ? bd.alpha : 1.f, srow, nb, sched.num_nb);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
+    }
     }
   }
 
@@ -921,16 +1024,17 @@ cudaError_t make_tmap(CUtensorMap* map, const Operand& op, uint32_t box_inner, u
 
 template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false, int BN_T = 256>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
-                   cudaStream_t stream, const DeviceCtx& ctx, const BatchDev& bd = BatchDev{}) {
+                   cudaStream_t stream, const DeviceCtx& ctx, const BatchDev& bd = BatchDev{},
+                   const CUtensorMap* taux = nullptr) {
   auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI, BATCHED, BN_T>;
-  constexpr int kSmem = OneSm<BN_T>::kSmemBytes;
+  constexpr int kSmem = OneSm<BN_T, EPI == kEpiSoftmaxGrad && BATCHED>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   int64_t tiles = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN_T - 1) / BN_T);
   if (BATCHED) tiles *= static_cast<int64_t>(bd.nz1) * bd.nz2;
   if (tiles > INT32_MAX) return cudaErrorInvalidValue;
   const int grid = tiles < ctx.num_sms ? static_cast<int>(tiles) : ctx.num_sms;
-  kernel<<<grid, NUM_THREADS, kSmem, stream>>>(ta, tb, M, N, K, ep, ctx.status, bd);
+  kernel<<<grid, NUM_THREADS, kSmem, stream>>>(ta, tb, taux ? *taux : ta, M, N, K, ep, ctx.status, bd);
   return cudaGetLastError();
 }
 
@@ -1145,8 +1249,14 @@ cudaError_t gemm_bf16_tc_batched(int64_t M, int64_t N, int64_t K, const BatchedO
     return launch<false, false, kEpiRowStats, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
   if (!a.mn_major && !b.mn_major && epi == kEpiSoftmax)
     return launch<false, false, kEpiSoftmax, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
-  if (!a.mn_major && !b.mn_major && epi == kEpiSoftmaxGrad)
-    return launch<false, false, kEpiSoftmaxGrad, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
+  if (!a.mn_major && !b.mn_major && epi == kEpiSoftmaxGrad) {
+    // P (the aux operand, laid out like the output) is read by TMA in 64-column x 32-row blocks.
+    CUtensorMap taux;
+    const BatchedOperand pa{ep.aux, M, N, ep.ldo, bs.out_z1, bs.out_z2, false};
+    e = make_tmap_batched(&taux, pa, bs.nz1, bs.nz2, 64, 32, &bd.x_row, &bd.x_z1, &bd.x_z2);
+    if (e != cudaSuccess) return e;
+    return launch<false, false, kEpiSoftmaxGrad, true>(ta, tb, m, n, k, ep, stream, ctx, bd, &taux);
+  }
   if (!a.mn_major && b.mn_major && epi == kEpiStore)
     return launch<false, true, kEpiStore, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
   if (a.mn_major && b.mn_major && epi == kEpiStore)
