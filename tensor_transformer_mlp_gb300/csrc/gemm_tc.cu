@@ -58,18 +58,20 @@ constexpr int EPI_STAGE_BYTES = 32 * 128;
 
 // One-SM kernel configurations by tile width: 128 x 256 tiles with a 4-stage ring, or 128 x 128
 // tiles (for N <= 128, e.g. N = head_dim) with a 6-stage ring and half the tensor memory.
-// kAux (the dS epilogue, which reads P): each epilogue warp also owns two 4 KB buffers that its
-// lane 0 fills with TMA loads of P one pass ahead, and the ring shrinks to 2 stages to make room
-// (the score-shaped GEMMs have K = head_dim = two k-blocks).
 constexpr int AUX_BUF_BYTES = 32 * 128;  // one 32-row x 64-column bf16 block
-template <int BN_T, bool kAux = false>
+// kAuxBufs > 0 (the batched softmax and dS epilogues): each epilogue warp owns that many 4 KB
+// buffers for TMA loads of P and TMA stores of its output instead of the generic staging buffer,
+// and the ring shrinks to 2 stages (the score-shaped GEMMs have K = head_dim = two k-blocks).
+template <int BN_T, int kAuxBufs = 0>
 struct OneSm {
+  static constexpr bool kAux = kAuxBufs > 0;
   static constexpr int kBN = BN_T;
   static constexpr int kStages = kAux ? 2 : (BN_T == 256 ? 4 : 6);
   static constexpr int kStageBytes = A_STAGE_BYTES + BN_T * BK * 2;
-  static constexpr int kAuxBytes = kAux ? NUM_EPI_WARPS * 2 * AUX_BUF_BYTES : 0;
-  static constexpr int kSmemBytes = kStages * kStageBytes + NUM_EPI_WARPS * EPI_STAGE_BYTES + kAuxBytes +
-                                    BARRIER_BYTES + 1024;  // + alignment slack
+  static constexpr int kEpiStageBytes = kAux ? 0 : NUM_EPI_WARPS * EPI_STAGE_BYTES;
+  static constexpr int kAuxBytes = NUM_EPI_WARPS * kAuxBufs * AUX_BUF_BYTES;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kEpiStageBytes + kAuxBytes + BARRIER_BYTES +
+                                    1024;  // + alignment slack
   static constexpr int kTmemCols = NUM_ACC * BN_T;  // a power of two, >= 32
   static constexpr int kEpiChunks = BN_T / 32 / (NUM_EPI_WARPS / 4);
   static_assert(BN_T == 256 || BN_T == 128, "tile widths");
@@ -454,6 +456,13 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
   }
 }
 
+// Per-warp TMA buffers of the batched epilogues: kEpiSoftmax stores P through two; kEpiSoftmaxGrad
+// loads P through two and stores dS through two more.
+template <int EPI, bool BATCHED>
+__host__ __device__ constexpr int aux_bufs() {
+  return !BATCHED ? 0 : (EPI == kEpiSoftmax ? 2 : (EPI == kEpiSoftmaxGrad ? 4 : 0));
+}
+
 // One TMA tile load: 2-D map for plain launches; 4-D map (inner, then row and batch indices in
 // the slots recorded in BatchDev) for batched ones.
 template <bool BATCHED>
@@ -473,17 +482,20 @@ __device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, uin
 template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false, int BN_T = 256>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const __grid_constant__ CUtensorMap tmap_aux, int M, int N, int K, EpiParams ep,
-                     unsigned int* status, BatchDev bd) {
-  constexpr bool kAux = EPI == kEpiSoftmaxGrad && BATCHED;
-  using Cfg = OneSm<BN_T, kAux>;
+                     const __grid_constant__ CUtensorMap tmap_aux, const __grid_constant__ CUtensorMap tmap_out,
+                     int M, int N, int K, EpiParams ep, unsigned int* status, BatchDev bd) {
+  // The batched softmax and dS epilogues move P and dS by TMA through per-warp buffers
+  // (tmap_aux: P to load, tmap_out: the output to store).
+  constexpr int kAuxBufs = aux_bufs<EPI, BATCHED>();
+  constexpr bool kAux = kAuxBufs > 0;
+  using Cfg = OneSm<BN_T, kAuxBufs>;
   constexpr int BN = Cfg::kBN, STAGES = Cfg::kStages, STAGE_BYTES = Cfg::kStageBytes, TMEM_COLS = Cfg::kTmemCols;
   constexpr int kChunks = Cfg::kEpiChunks;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
-  uint8_t* aux_buf = epi_stage + NUM_EPI_WARPS * EPI_STAGE_BYTES;  // 1024-byte aligned (128-byte swizzle)
+  uint8_t* aux_buf = epi_stage + Cfg::kEpiStageBytes;  // 1024-byte aligned (128-byte swizzle)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(aux_buf + Cfg::kAuxBytes);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;
@@ -530,7 +542,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    if constexpr (kAux) tma_prefetch_desc(&tmap_aux);
+    if constexpr (kAux) {
+      tma_prefetch_desc(&tmap_aux);
+      tma_prefetch_desc(&tmap_out);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -632,12 +647,79 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
     const int c_begin = ((warp - 2) / 4) * kChunks;
-    if constexpr (kAux) {
+    // Coordinates of a batched tensor map for (inner, row, z1, z2), slots as recorded in bd.
+  auto aux_coords = [&](int inner, int row, int z1, int z2, int (&cc)[4]) {
+    cc[0] = inner;
+    cc[bd.x_row] = row;
+    cc[bd.x_z1] = z1;
+    cc[bd.x_z2] = z2;
+  };
+  if constexpr (kAux && EPI == kEpiSoftmax) {
+      // P = 2^(acc * c - M) / L written by TMA stores: each 64-column pass of the warp's 32 rows
+      // goes into one of its two 4 KB buffers in the 128-byte-swizzled layout the store expects,
+      // and lane 0 issues the store; a buffer is reused once the store two passes back has read it.
+      uint8_t* sb = aux_buf + (warp - 2) * kAuxBufs * AUX_BUF_BYTES;
+      int nstore = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        const bool ok = mbar_wait(&tfull_bar[acc], use & 1, status, 6);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        int z1, z2, mb, nb;
+        tile_coords(tile, z1, z2, mb, nb);
+        const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+        const int64_t srow = (static_cast<int64_t>(z2) * bd.nz1 + z1) * M + row;
+        const float c2 = bd.alpha * kLog2e;
+        const float2 st = row < M ? static_cast<const float2*>(ep.rowvec)[srow] : make_float2(0.f, 0.f);
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+          const int c = c_begin + 2 * k;
+          const int col0 = nb * BN + c * 32;
+          if (col0 >= N) break;  // uniform across the warp
+          uint32_t v[64];
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+          tmem_ld_wait();
+          uint4 seg[8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float pv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(v[g * 8 + i]), c2, -st.x)) * st.y;
+            seg[g] = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                                pack_bf16x2(pv[6], pv[7]));
+          }
+          uint8_t* buf = sb + (nstore & 1) * AUX_BUF_BYTES;
+          if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = seg[j];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            int cc[4];
+            aux_coords(col0, mb * BM + q * 32, z1, z2, cc);
+            tma_store_4d(&tmap_out, buf, cc[0], cc[1], cc[2], cc[3]);
+            bulk_commit_group();
+          }
+          ++nstore;
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[acc]);
+      }
+      if (lane == 0) bulk_wait_group_all();
+      __syncwarp();
+  } else if constexpr (kAux) {
       // dS = escale * P * (dP - D) with P arriving by TMA: pass k (64 columns) of a tile reads
       // buffer k, which lane 0 refills with the next tile's pass k as soon as the warp has read it.
       static_assert(kChunks == 4, "two 64-column passes per warp");
-      uint8_t* pb = aux_buf + (warp - 2) * 2 * AUX_BUF_BYTES;
+      uint8_t* pb = aux_buf + (warp - 2) * kAuxBufs * AUX_BUF_BYTES;  // buffers 0, 1: P loads
+      uint8_t* sb = pb + 2 * AUX_BUF_BYTES;                             // buffers 2, 3: dS stores
       uint64_t* pbar = aux_bar + (warp - 2) * 2;
+      int nstore = 0;
       uint32_t pphase[2] = {0u, 0u};
       bool pending[2] = {false, false};
       auto issue_p = [&](int tl, int k) {  // uniform across the warp
@@ -666,15 +748,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         int z1, z2, mb, nb;
         tile_coords(tile, z1, z2, mb, nb);
-        const int64_t out_off = z1 * bd.out_z1 + z2 * bd.out_z2;
         const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
         const int64_t srow = (static_cast<int64_t>(z2) * bd.nz1 + z1) * M + row;
         const float a2 = bd.alpha * ep.escale;
         const float d2 = (row < M ? static_cast<const float*>(ep.rowvec)[srow] : 0.f) * ep.escale;
-        const int64_t prow = row < M ? row : -1;
-        void* out = static_cast<__nv_bfloat16*>(ep.out) + out_off;
-        uint8_t* sbuf = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
 #pragma unroll 1
         for (int k = 0; k < 2; ++k) {
           const int c = c_begin + 2 * k;
@@ -707,7 +785,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                    pf.y * fmaf(__uint_as_float(v[g * 8 + 2 * i + 1]), a2, -d2));
               }
             }
-            store_staged<false>(sbuf, ps, lane, prow, out, ep.ldo, col0, N);
+            uint8_t* buf = sb + (nstore & 1) * AUX_BUF_BYTES;
+            if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = ps[j];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              int cc[4];
+              aux_coords(col0, mb * BM + q * 32, z1, z2, cc);
+              tma_store_4d(&tmap_out, buf, cc[0], cc[1], cc[2], cc[3]);
+              bulk_commit_group();
+            }
+            ++nstore;
           } else if (!fail) {
             issue_p(tile + static_cast<int>(gridDim.x), k);
           }
@@ -715,10 +806,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(&tempty_bar[acc]);
       }
-      // Copies still in flight land before the CTA's shared memory goes away (bounded).
+      // Copies still in flight finish before the CTA's shared memory goes away (the loads' waits
+      // are bounded).
 #pragma unroll
       for (int k = 0; k < 2; ++k)
         if (pending[k]) mbar_wait(&pbar[k], pphase[k], status, 8);
+      if (lane == 0) bulk_wait_group_all();
+      __syncwarp();
     } else {
     int it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
@@ -1025,16 +1119,17 @@ cudaError_t make_tmap(CUtensorMap* map, const Operand& op, uint32_t box_inner, u
 template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false, int BN_T = 256>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
                    cudaStream_t stream, const DeviceCtx& ctx, const BatchDev& bd = BatchDev{},
-                   const CUtensorMap* taux = nullptr) {
+                   const CUtensorMap* taux = nullptr, const CUtensorMap* tout = nullptr) {
   auto kernel = gemm_bf16_kernel<A_MN, B_MN, EPI, BATCHED, BN_T>;
-  constexpr int kSmem = OneSm<BN_T, EPI == kEpiSoftmaxGrad && BATCHED>::kSmemBytes;
+  constexpr int kSmem = OneSm<BN_T, aux_bufs<EPI, BATCHED>()>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   int64_t tiles = static_cast<int64_t>((M + BM - 1) / BM) * ((N + BN_T - 1) / BN_T);
   if (BATCHED) tiles *= static_cast<int64_t>(bd.nz1) * bd.nz2;
   if (tiles > INT32_MAX) return cudaErrorInvalidValue;
   const int grid = tiles < ctx.num_sms ? static_cast<int>(tiles) : ctx.num_sms;
-  kernel<<<grid, NUM_THREADS, kSmem, stream>>>(ta, tb, taux ? *taux : ta, M, N, K, ep, ctx.status, bd);
+  kernel<<<grid, NUM_THREADS, kSmem, stream>>>(ta, tb, taux ? *taux : ta, tout ? *tout : ta, M, N, K, ep, ctx.status,
+                                               bd);
   return cudaGetLastError();
 }
 
@@ -1247,15 +1342,25 @@ cudaError_t gemm_bf16_tc_batched(int64_t M, int64_t N, int64_t K, const BatchedO
     return launch<false, false, kEpiStoreF32, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
   if (!a.mn_major && !b.mn_major && epi == kEpiRowStats)
     return launch<false, false, kEpiRowStats, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
-  if (!a.mn_major && !b.mn_major && epi == kEpiSoftmax)
-    return launch<false, false, kEpiSoftmax, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
+  if (!a.mn_major && !b.mn_major && epi == kEpiSoftmax) {
+    // P is written by TMA stores in 64-column x 32-row blocks.
+    CUtensorMap tout;
+    const BatchedOperand po{ep.out, M, N, ep.ldo, bs.out_z1, bs.out_z2, false};
+    e = make_tmap_batched(&tout, po, bs.nz1, bs.nz2, 64, 32, &bd.x_row, &bd.x_z1, &bd.x_z2);
+    if (e != cudaSuccess) return e;
+    return launch<false, false, kEpiSoftmax, true>(ta, tb, m, n, k, ep, stream, ctx, bd, nullptr, &tout);
+  }
   if (!a.mn_major && !b.mn_major && epi == kEpiSoftmaxGrad) {
     // P (the aux operand, laid out like the output) is read by TMA in 64-column x 32-row blocks.
-    CUtensorMap taux;
+    // dS, laid out like P, is written by TMA stores through the same block shape.
+    CUtensorMap taux, tout;
     const BatchedOperand pa{ep.aux, M, N, ep.ldo, bs.out_z1, bs.out_z2, false};
     e = make_tmap_batched(&taux, pa, bs.nz1, bs.nz2, 64, 32, &bd.x_row, &bd.x_z1, &bd.x_z2);
     if (e != cudaSuccess) return e;
-    return launch<false, false, kEpiSoftmaxGrad, true>(ta, tb, m, n, k, ep, stream, ctx, bd, &taux);
+    const BatchedOperand po{ep.out, M, N, ep.ldo, bs.out_z1, bs.out_z2, false};
+    e = make_tmap_batched(&tout, po, bs.nz1, bs.nz2, 64, 32, &bd.x_row, &bd.x_z1, &bd.x_z2);
+    if (e != cudaSuccess) return e;
+    return launch<false, false, kEpiSoftmaxGrad, true>(ta, tb, m, n, k, ep, stream, ctx, bd, &taux, &tout);
   }
   if (!a.mn_major && b.mn_major && epi == kEpiStore)
     return launch<false, true, kEpiStore, true>(ta, tb, m, n, k, ep, stream, ctx, bd);
