@@ -648,11 +648,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
     const int c_begin = ((warp - 2) / 4) * kChunks;
     // Coordinates of a batched tensor map for (inner, row, z1, z2), slots as recorded in bd.
-  auto aux_coords = [&](int inner, int row, int z1, int z2, int (&cc)[4]) {
+  auto aux_coords = [&](int inner, int row, int z1, int z2, int (&cc)[4]) {  // selects, no local memory
     cc[0] = inner;
-    cc[bd.x_row] = row;
-    cc[bd.x_z1] = z1;
-    cc[bd.x_z2] = z2;
+    cc[1] = bd.x_row == 1 ? row : (bd.x_z1 == 1 ? z1 : z2);
+    cc[2] = bd.x_row == 2 ? row : (bd.x_z1 == 2 ? z1 : z2);
+    cc[3] = bd.x_row == 3 ? row : (bd.x_z1 == 3 ? z1 : z2);
   };
   if constexpr (kAux && EPI == kEpiSoftmax) {
       // P = 2^(acc * c - M) / L written by TMA stores: each 64-column pass of the warp's 32 rows
@@ -753,7 +753,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int64_t srow = (static_cast<int64_t>(z2) * bd.nz1 + z1) * M + row;
         const float a2 = bd.alpha * ep.escale;
         const float d2 = (row < M ? static_cast<const float*>(ep.rowvec)[srow] : 0.f) * ep.escale;
-#pragma unroll 1
+#pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int c = c_begin + 2 * k;
           const int col0 = nb * BN + c * 32;
