@@ -72,3 +72,12 @@ def test_cli_contract():
         bench.main(["--warmup", "2"])      # the contract wants at least 3 warm-up steps
     with pytest.raises(SystemExit):
         bench.main(["--workload", "nope"])
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
+    # Under torchrun only rank 0 runs the CPU reference and prints its line; others return 0.
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out.strip() == ""
