@@ -61,27 +61,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, with cluster-scope acquire: for barriers that the peer CTA of a pair
-// (or the pair's MMAs) arrive on.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits until the phase with the given parity has completed, for at most limit_ns.
 // Returns false (and records a timeout in *status) if the limit expired.
-template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* status,
                                               unsigned int where, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
-  auto try_once = [&] { return kClusterScope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+  auto try_once = [&] { return mbar_try_wait(a, parity); };
   if (try_once()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -98,11 +83,6 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, un
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
                                           unsigned int where) {
   return mbar_wait_for(bar, parity, status, where, kWaitLimitNs);
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, unsigned int* status,
-                                                  unsigned int where) {
-  return mbar_wait_for<true>(bar, parity, status, where, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------------ CTA pairs (clusters of two)

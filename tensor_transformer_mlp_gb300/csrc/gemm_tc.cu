@@ -853,6 +853,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //   barriers: full[s] (even CTA; both CTAs' copies complete on it), empty[s] (each CTA;
 //   the MMA commit arrives on both), tfull[acc] (each CTA; multicast commit), tempty[acc]
 //   (even CTA; all epilogue threads of both CTAs arrive), drain (even CTA).
+//   Every wait is the ordinary CTA-scope try_wait, also on barriers the peer arrives on: what
+//   a waiter touches next is shared memory written by TMA and read by the tensor core (async
+//   proxy) or tensor memory ordered by the tcgen05 fences around the barrier, never data the
+//   peer wrote through the generic proxy. Waits with cluster-scope acquire cost a quarter of
+//   the throughput on some GB300s (the 256 epilogue threads spin on one for most of a launch).
 constexpr int PAIR_STAGES = 6;
 constexpr int BN_HALF = BN / 2;                               // B columns loaded per CTA
 constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + BN_HALF * BK * 2;  // 32 KiB
@@ -979,7 +984,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const int s = kiter % PAIR_STAGES;
           const uint32_t parity = ((kiter / PAIR_STAGES) & 1) ^ 1;
-          if (!mbar_wait_cluster(&empty_bar[s], parity, status, 11)) {
+          if (!mbar_wait(&empty_bar[s], parity, status, 11)) {
             ok = false;
             break;
           }
@@ -1007,7 +1012,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // completed (at once on the normal path), no copy of the pair is still in flight.
       if (rank == 0)
         for (int k = max(0, kiter - PAIR_STAGES); k < kiter; ++k)
-          mbar_wait_cluster(&full_bar[k % PAIR_STAGES], (k / PAIR_STAGES) & 1, status, 12);
+          mbar_wait(&full_bar[k % PAIR_STAGES], (k / PAIR_STAGES) & 1, status, 12);
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -1018,7 +1023,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
-        if (!mbar_wait_cluster(&tempty_bar[acc], (use & 1) ^ 1, status, 13)) {
+        if (!mbar_wait(&tempty_bar[acc], (use & 1) ^ 1, status, 13)) {
           ok = false;
           break;
         }
@@ -1026,7 +1031,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
           const int s = kiter % PAIR_STAGES;
-          if (!mbar_wait_cluster(&full_bar[s], (kiter / PAIR_STAGES) & 1, status, 14)) {
+          if (!mbar_wait(&full_bar[s], (kiter / PAIR_STAGES) & 1, status, 14)) {
             ok = false;
             break;
           }
@@ -1048,7 +1053,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_commit_pair_mc(&tfull_bar[acc], 0x3);  // both halves of the accumulator ready
       }
       umma_commit_pair(drain_bar);
-      mbar_wait_cluster(drain_bar, 0, status, 15);
+      mbar_wait(drain_bar, 0, status, 15);
     }
   } else {
     // ------------------------------------------------------------------ epilogue (both CTAs)
@@ -1058,7 +1063,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
-      const bool ok = mbar_wait_cluster(&tfull_bar[acc], use & 1, status, 16);
+      const bool ok = mbar_wait(&tfull_bar[acc], use & 1, status, 16);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       int mb, nb;
