@@ -856,8 +856,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //   Every wait is the ordinary CTA-scope try_wait, also on barriers the peer arrives on: what
 //   a waiter touches next is shared memory written by TMA and read by the tensor core (async
 //   proxy) or tensor memory ordered by the tcgen05 fences around the barrier, never data the
-//   peer wrote through the generic proxy. Waits with cluster-scope acquire cost a quarter of
-//   the throughput on some GB300s (the 256 epilogue threads spin on one for most of a launch).
+//   peer wrote through the generic proxy. (The 256 epilogue threads spin on a wait for most
+//   of a launch; with cluster-scope acquire the step measured 0.5-1 % slower.)
 constexpr int PAIR_STAGES = 6;
 constexpr int BN_HALF = BN / 2;                               // B columns loaded per CTA
 constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + BN_HALF * BK * 2;  // 32 KiB
