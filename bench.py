@@ -384,6 +384,47 @@ def measure_attention(dev, peaks, reps: int = 10):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def measure_library_gemms(X, A, B, G, Z, Y, stream, steps: int, warmup: int):
+    """The step's six GEMMs by torch.matmul (cuBLAS), as a library reference point.
+
+    Same shapes and operand layouts as the library's step (transposed operands are views,
+    which cuBLAS reads in place); bf16 outputs and no GeLU / GeLU' epilogues, so it does
+    strictly less work than the step. Z stands in for D (same shape and dtype). Timed
+    back to back like the step, with CUDA events on the launching stream.
+    """
+    import torch
+
+    n, d = X.shape
+    m = A.shape[1]
+    nm = torch.empty((n, m), dtype=X.dtype, device=X.device)
+    nd = torch.empty((n, d), dtype=X.dtype, device=X.device)
+    md = torch.empty((m, d), dtype=X.dtype, device=X.device)
+    dm = torch.empty((d, m), dtype=X.dtype, device=X.device)
+
+    def six():
+        torch.matmul(X, A, out=nm)          # FC1
+        torch.matmul(Y, B, out=nd)          # FC2
+        torch.matmul(G, B.t(), out=nm)      # dgrad-1
+        torch.matmul(Y.t(), G, out=md)      # wgrad dB
+        torch.matmul(X.t(), Z, out=dm)      # wgrad dA
+        torch.matmul(Z, A.t(), out=nd)      # dgrad-2
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            six()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            six()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del nm, nd, md, dm
+    return ms
+
+
 def run_ours(args, cfg):
     import torch
 
@@ -542,6 +583,14 @@ def run_ours(args, cfg):
         "gpu_launches": GEMM_LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks,
     }
+    if world == 1:
+        lib_ms = measure_library_gemms(X, A, B, G, Z, Y, stream, args.steps, args.warmup)
+        line["library_reference"] = {
+            "what": "torch.matmul (cuBLAS) of the step's six GEMMs: same shapes and operand layouts, bf16 "
+                    "outputs, no GeLU / GeLU' epilogues (less work than the step); run and timed after the "
+                    "step, back to back, CUDA events",
+            "ms_per_step": lib_ms, "tflops": flops_step / (lib_ms / 1e3) / 1e12,
+            "ours_ms_per_step": max_elapsed / args.steps * 1e3}
     if not args.no_sp:
         line["sp"] = measure_sp(dev, peaks)
         line["attention"] = measure_attention(dev, peaks)
