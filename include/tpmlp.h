@@ -178,9 +178,11 @@ size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m,
  *   x_shards, out_shards: [t][b][s/t][h] in dt (shard j holds sequence positions j*s/t .. (j+1)*s/t-1)
  *   gamma, beta: [h] fp32; eps > 0. LayerNorm uses the biased variance and fp32 statistics.
  *   A [h][m], B [m][h] (dt), gelu as for tpmlp_forward.
- *   Dropout: p_drop in [0, 1) is the drop probability. Element k of the logical [b][s][h]
- *   tensor (row-major flat index) is dropped iff splitmix64(seed ^ k) < floor(p_drop * 2^64)
- *   (product in double); kept elements are scaled by 1/(1-p_drop); the residual is x.
+ *   Dropout: p_drop in [0, 1) is the drop probability, a double, so that the threshold
+ *   T = floor(p_drop * 2^64) (product in double) is the one a caller computes from the same
+ *   value (p = 0.1 gives T = 0x1999999999999A00). Element k of the logical [b][s][h] tensor
+ *   (row-major flat index) is dropped iff splitmix64(seed ^ k) < T; kept elements are scaled
+ *   by 1/(1-p_drop), computed in double and applied in fp32; the residual is x.
  *   mask_bits: NULL, or [ceil(b*s*h/32)] uint32 words; bit i of word w is 1 iff element
  *   32*w+i (global flat index) was dropped. Needs h % 32 == 0.
  *   Z_save, Y_save: NULL, or [b*s][m] in dt (token order): FC1's pre- and post-GeLU activations,
@@ -189,7 +191,7 @@ size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m,
  *   "Megatron-SP 机制", section "工程约束与实测收益是什么？"), s % t == 0, m % t == 0.
  */
 tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const float* beta, float eps,
-                            const void* A, const void* B, float p_drop, uint64_t seed,
+                            const void* A, const void* B, double p_drop, uint64_t seed,
                             void* out_shards, uint32_t* mask_bits, void* Z_save, void* Y_save,
                             int64_t b, int64_t s, int64_t h, int64_t m, int t,
                             tpmlp_gelu gelu, tpmlp_dtype dt, tpmlp_rs_mode rs,
@@ -211,7 +213,7 @@ size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, i
  * Requires h <= 4096 and h % 8 == 0 in addition to tpmlp_sp_block's rules.
  */
 tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, const float* beta, float eps,
-                                     const void* A, const void* B, float p_drop, uint64_t seed,
+                                     const void* A, const void* B, double p_drop, uint64_t seed,
                                      const void* Z_save, const void* Y_save, const void* dout_shards,
                                      void* dx_shards, float* dgamma, float* dbeta, float* dA, float* dB,
                                      int64_t b, int64_t s, int64_t h, int64_t m, int t,
@@ -265,7 +267,7 @@ tpmlp_status tpmlp_sp_reduce_scatter(const float* partials, void* out_shards,
  * out = x + keep * y / (1 - p_drop), mask definition and mask_bits as for tpmlp_sp_block.
  * x_shards, y_shards, out_shards: [t][b][s/t][h] in dt. */
 tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shards, void* out_shards,
-                                       uint32_t* mask_bits, float p_drop, uint64_t seed,
+                                       uint32_t* mask_bits, double p_drop, uint64_t seed,
                                        int64_t b, int64_t s, int64_t h, int t,
                                        tpmlp_dtype dt, void* stream);
 

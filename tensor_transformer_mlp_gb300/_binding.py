@@ -23,6 +23,7 @@ STATUS = {0: "TPMLP_OK", 1: "TPMLP_ERR_INVALID", 2: "TPMLP_ERR_SHAPE", 3: "TPMLP
 
 # Every entry point declared in include/tpmlp.h, with its ctypes signature.
 _P, _I64, _I, _F, _U64, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
+_D = ctypes.c_double
 SIGNATURES = {
     "tpmlp_forward": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_forward_biased": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
@@ -34,10 +35,10 @@ SIGNATURES = {
     "tpmlp_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P]),
     "tpmlp_sp_block_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I, _I, _I]),
-    "tpmlp_sp_block": (_I, [_P, _P, _P, _F, _P, _P, _F, _U64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I,
+    "tpmlp_sp_block": (_I, [_P, _P, _P, _F, _P, _P, _D, _U64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I,
                             _P, _SZ, _P]),
     "tpmlp_sp_block_backward_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I, _I]),
-    "tpmlp_sp_block_backward": (_I, [_P, _P, _P, _F, _P, _P, _F, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+    "tpmlp_sp_block_backward": (_I, [_P, _P, _P, _F, _P, _P, _D, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                                      _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_sp_layernorm": (_I, [_P, _P, _P, _F, _P, _I64, _I64, _I, _P]),
     "tpmlp_rmsnorm": (_I, [_P, _P, _F, _P, _I64, _I64, _I, _P]),
@@ -45,7 +46,7 @@ SIGNATURES = {
     "tpmlp_rmsnorm_backward": (_I, [_P, _P, _F, _P, _P, _P, _I64, _I64, _I, _P, _SZ, _P]),
     "tpmlp_sp_gather": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_reduce_scatter": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
-    "tpmlp_sp_dropout_residual": (_I, [_P, _P, _P, _P, _F, _U64, _I64, _I64, _I64, _I, _I, _P]),
+    "tpmlp_sp_dropout_residual": (_I, [_P, _P, _P, _P, _D, _U64, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_attention_forward_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),
     "tpmlp_attention_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_attention_backward_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),

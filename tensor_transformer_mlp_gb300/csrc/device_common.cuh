@@ -377,12 +377,86 @@ __device__ __forceinline__ float gelu_grad_f(float x, int kind) {
 // Drop decision for one element: splitmix64(key) < threshold, with SplitMix64 as published by
 // Steele, Lea and Flood (2014) / Vigna's splitmix64.c: add the golden-gamma increment, then the
 // variant-13 mixer (xor-shift 30, multiply, xor-shift 27, multiply, xor-shift 31), mod 2^64.
-// Straight-line code: a data-dependent early exit here costs more than the full compare.
-__device__ __forceinline__ bool hash_below(uint64_t key, uint64_t threshold) {
-  uint64_t z = key + 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+constexpr uint64_t kSplitMixGamma = 0x9E3779B97F4A7C15ull;
+constexpr uint64_t kSplitMixMul1 = 0xBF58476D1CE4E5B9ull;
+constexpr uint64_t kSplitMixMul2 = 0x94D049BB133111EBull;
+
+__host__ __device__ __forceinline__ bool hash_below(uint64_t key, uint64_t threshold) {
+  uint64_t z = key + kSplitMixGamma;
+  z = (z ^ (z >> 30)) * kSplitMixMul1;
+  z = (z ^ (z >> 27)) * kSplitMixMul2;
   return (z ^ (z >> 31)) < threshold;
+}
+
+// drop_bits8 on keys whose shortcut below does not apply: eight full hashes.
+static __host__ __device__ __noinline__ uint32_t drop_bits8_full(uint64_t base, uint64_t threshold) {
+  uint32_t bits = 0;
+  for (uint32_t e = 0; e < 8; ++e) bits |= (hash_below(base ^ e, threshold) ? 1u : 0u) << e;
+  return bits;
+}
+
+// SplitMix64 of the eight keys base ^ e, e = 0..7, where base = seed ^ k0 with k0 a multiple of 8
+// (so the keys are seed ^ (k0 + e)), with the work the eight keys share done once, in 32-bit
+// halves:
+//  * (base ^ e) + gamma = ((base & ~7) + gamma) + ((base & 7) ^ e), the last term in [0, 7].
+//    Unless the low word of the first sum lies within 7 of 2^32, no key carries into the high
+//    word, so the eight high words are equal, and so are the high word after the first
+//    xor-shift and its share (high word x low word of the multiplier) of the first product.
+//  * The final xor-shift changes the high word only by flipping its bit 0 when its bit 31 is
+//    set. For a threshold below 2^63 (p < 1/2) that changes neither "high word < threshold's
+//    high word" nor equality with it, so high(e), the last product's high word, decides key e:
+//    dropped iff high(e) < thi, unless high(e) == thi (probability 2^-32 per key), when only the
+//    full hash decides.
+// shortcut is false in the carry case and for thresholds of 2^63 and above; a caller then uses
+// hash_below (or drop_bits8_full) for all eight keys, and it does the same on a tie.
+// kLow3 >= 0 promises base & 7 == kLow3 (the seed's low three bits), which makes each key's low
+// word one addition of a constant.
+template <int kLow3 = -1>
+struct DropHash8 {
+  uint32_t klo, low3, hi_in, thi;
+  uint64_t hi_product;
+  bool shortcut;
+
+  __host__ __device__ __forceinline__ DropHash8(uint64_t base, uint64_t threshold) {
+    const uint64_t k = (base & ~7ull) + kSplitMixGamma;
+    const uint32_t khi = static_cast<uint32_t>(k >> 32);
+    klo = static_cast<uint32_t>(k);
+    thi = static_cast<uint32_t>(threshold >> 32);
+    shortcut = klo <= 0xFFFFFFF8u && thi < 0x80000000u;
+    low3 = kLow3 >= 0 ? static_cast<uint32_t>(kLow3) : static_cast<uint32_t>(base) & 7u;
+    hi_in = khi << 2;  // bits the high word sends down by >> 30
+    hi_product = static_cast<uint64_t>((khi ^ (khi >> 30)) * static_cast<uint32_t>(kSplitMixMul1)) << 32;
+  }
+
+  __host__ __device__ __forceinline__ uint32_t high(uint32_t e) const {
+    const uint32_t m1lo = static_cast<uint32_t>(kSplitMixMul1), m1hi = static_cast<uint32_t>(kSplitMixMul1 >> 32);
+    const uint32_t m2lo = static_cast<uint32_t>(kSplitMixMul2), m2hi = static_cast<uint32_t>(kSplitMixMul2 >> 32);
+    const uint32_t z0 = klo + (low3 ^ e);
+    const uint32_t l1 = z0 ^ (z0 >> 30) ^ hi_in;                        // low word after xor-shift 30
+    const uint64_t p1 = static_cast<uint64_t>(l1) * m1lo + hi_product;  // first product, minus l1 * m1hi
+    const uint32_t a_lo = static_cast<uint32_t>(p1);
+    const uint32_t a_hi = static_cast<uint32_t>(p1 >> 32) + l1 * m1hi;
+    const uint32_t b_lo = a_lo ^ ((a_lo >> 27) | (a_hi << 5));         // xor-shift 27
+    const uint32_t b_hi = a_hi ^ (a_hi >> 27);
+    return static_cast<uint32_t>((static_cast<uint64_t>(b_lo) * m2lo) >> 32) + b_lo * m2hi + b_hi * m2lo;
+  }
+};
+
+// The drop decisions of the eight keys base ^ e as bit e of the result (see DropHash8),
+// identical to hash_below on each key.
+template <int kLow3 = -1>
+__host__ __device__ __forceinline__ uint32_t drop_bits8(uint64_t base, uint64_t threshold) {
+  const DropHash8<kLow3> hs(base, threshold);
+  if (!hs.shortcut) return drop_bits8_full(base, threshold);
+  uint32_t bits = 0;
+  bool tie = false;
+#pragma unroll
+  for (uint32_t e = 0; e < 8; ++e) {
+    const uint32_t c = hs.high(e);
+    bits |= (c < hs.thi ? 1u : 0u) << e;
+    tie |= c == hs.thi;
+  }
+  return tie ? drop_bits8_full(base, threshold) : bits;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -139,18 +139,15 @@ __device__ __forceinline__ void epilogue_row32(const EpiParams& ep, int64_t row,
       const int64_t off = prow * ep.ldo + col;
       const uint4 xr = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.aux) + off);
       const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
-      // (seed ^ k0) ^ e = seed ^ (k0 + e) because k0 = row * ldo + col is a multiple of 8
-      const uint64_t base = ep.drop.seed ^ static_cast<uint64_t>(row * ep.ldo + col);
+      // k0 = row * ldo + col is a multiple of 8, so the eight keys are (seed ^ k0) ^ e
+      const uint32_t bits = drop_bits8(ep.drop.seed ^ static_cast<uint64_t>(row * ep.ldo + col), ep.drop.threshold);
+      drop_bits |= bits << (g * 8);
       float o[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 xf = unpack_bf16x2(xw[i]);
-        const bool d0 = hash_below(base ^ static_cast<uint64_t>(2 * i), ep.drop.threshold);
-        const bool d1 = hash_below(base ^ static_cast<uint64_t>(2 * i + 1), ep.drop.threshold);
-        drop_bits |= (d0 ? 1u : 0u) << (g * 8 + 2 * i);
-        drop_bits |= (d1 ? 1u : 0u) << (g * 8 + 2 * i + 1);
-        o[2 * i] = d0 ? xf.x : fmaf(a[2 * i], ep.drop.scale, xf.x);
-        o[2 * i + 1] = d1 ? xf.y : fmaf(a[2 * i + 1], ep.drop.scale, xf.y);
+        o[2 * i] = (bits >> (2 * i)) & 1u ? xf.x : fmaf(a[2 * i], ep.drop.scale, xf.x);
+        o[2 * i + 1] = (bits >> (2 * i + 1)) & 1u ? xf.y : fmaf(a[2 * i + 1], ep.drop.scale, xf.y);
       }
       uint4 pk = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                             pack_bf16x2(o[6], o[7]));

@@ -9,6 +9,7 @@
 // g-bar are row permutations (plus the t-way sum for g-bar). Kernels move 16-byte vectors,
 // with the shard <-> token mapping computed once per row.
 #include "device_common.cuh"
+#include <type_traits>
 
 namespace tpmlp {
 namespace {
@@ -276,16 +277,49 @@ __global__ void __launch_bounds__(256) reduce_scatter_kernel(const float* __rest
 
 // ------------------------------------------------------------------ dropout + residual
 
+// Rare path of the dropout kernels (a key carrying into the hash's high word, a threshold of
+// 2^63 or more, or a tie with the threshold's high word): the vector of 8 elements at k0 redone
+// from global memory with eight full hashes, overwriting what the shortcut stored. y == nullptr
+// selects the dropout gradient (out = keep * x * scale) instead of out = x + keep * y * scale.
+template <typename T>
+__device__ __noinline__ uint32_t dropout_vector_full(const T* xp, const T* yp, T* op, uint64_t base,
+                                                     uint64_t threshold, float scale) {
+  const uint32_t bits = drop_bits8_full(base, threshold);
+  Vec8<T> xv;
+  xv.load(xp);
+  float xf[8], yf[8] = {}, o[8];
+  xv.to_float(xf);
+  if (yp != nullptr) {
+    Vec8<T> yv;
+    yv.load(yp);
+    yv.to_float(yf);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const bool dropped = (bits >> e) & 1u;
+    o[e] = yp != nullptr ? (dropped ? xf[e] : fmaf(yf[e], scale, xf[e])) : (dropped ? 0.f : xf[e] * scale);
+  }
+  Vec8<T> ov;
+  ov.from_float(o);
+  ov.store(op);
+  return bits;
+}
+
+// Resident CTAs per SM of the dropout kernels: 16 x 128 threads, at most 32 registers a thread
+// for bf16 (rows move through the memory system by occupancy, not by registers).
+template <typename T>
+constexpr int dropout_min_blocks() { return sizeof(T) == 2 ? 16 : 8; }
+
 // out = x + keep * y * scale for shard-major rows; element k of the logical token-order
-// tensor is dropped iff splitmix64(seed ^ k) < threshold. Each thread handles VPT vectors of
-// 8 consecutive elements and issues all their loads before hashing; 4 neighbouring lanes OR
-// their bits into one 32-bit mask word.
-template <typename T, int VPT>
-__global__ void __launch_bounds__(128) dropout_residual_kernel(const T* __restrict__ x, const T* __restrict__ y,
-                                                               T* __restrict__ out, uint32_t* __restrict__ mask_bits,
-                                                               uint64_t threshold, float scale, uint64_t seed,
-                                                               int64_t rows, int64_t b, int64_t s, int64_t sl,
-                                                               int h) {
+// tensor is dropped iff splitmix64(seed ^ k) < threshold. One thread per vector of 8
+// consecutive elements, one row per CTA (grid = rows, so the block scheduler balances the
+// tail); each element is decided by the high word of the last product (DropHash8) and the
+// rare cases redo the vector in full. 4 neighbouring lanes OR their bits into one 32-bit
+// mask word. kLow3 = seed & 7.
+template <typename T, int kLow3>
+__global__ void __launch_bounds__(128, dropout_min_blocks<T>()) dropout_residual_kernel(
+    const T* __restrict__ x, const T* __restrict__ y, T* __restrict__ out, uint32_t* __restrict__ mask_bits,
+    uint64_t threshold, float scale, uint64_t seed, int64_t rows, int64_t b, int64_t s, int64_t sl, int h) {
   const int nvec = h >> 3;
   for (int64_t R = blockIdx.x; R < rows; R += gridDim.x) {
     const int64_t r = shard_row_to_token(R, b, s, sl);
@@ -293,41 +327,39 @@ __global__ void __launch_bounds__(128) dropout_residual_kernel(const T* __restri
     const T* xr = x + R * h;
     const T* yr = y + R * h;
     T* orow = out + R * h;
-    for (int v0 = 0; v0 < nvec; v0 += blockDim.x * VPT) {  // uniform trip count across the CTA
-      Vec8<T> xv[VPT], yv[VPT];
-#pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const int v = v0 + j * blockDim.x + threadIdx.x;
-        if (v < nvec) {
-          xv[j].load(xr + v * 8);
-          yv[j].load(yr + v * 8);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const int v = v0 + j * blockDim.x + threadIdx.x;
-        uint32_t bits = 0;
-        if (v < nvec) {
-          const uint64_t base = seed ^ (flat_row + static_cast<uint64_t>(v) * 8);  // (seed^k0)^e = seed^(k0+e)
+    for (int v0 = 0; v0 < nvec; v0 += blockDim.x) {  // uniform trip count across the CTA
+      const int v = v0 + threadIdx.x;
+      uint32_t bits = 0;
+      if (v < nvec) {
+        const uint64_t base = seed ^ (flat_row + static_cast<uint64_t>(v) * 8);  // (seed^k0)^e = seed^(k0+e)
+        const DropHash8<kLow3> hs(base, threshold);
+        bool redo = !hs.shortcut;
+        if (hs.shortcut) {
+          Vec8<T> xv, yv;
+          xv.load(xr + v * 8);
+          yv.load(yr + v * 8);
           float xf[8], yf[8], o[8];
-          xv[j].to_float(xf);
-          yv[j].to_float(yf);
+          xv.to_float(xf);
+          yv.to_float(yf);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const bool drop = hash_below(base ^ static_cast<uint64_t>(e), threshold);
-            bits |= (drop ? 1u : 0u) << e;
-            o[e] = drop ? xf[e] : fmaf(yf[e], scale, xf[e]);
+          for (uint32_t e = 0; e < 8; ++e) {
+            const uint32_t c = hs.high(e);
+            const bool dropped = c < hs.thi;
+            redo |= c == hs.thi;
+            bits |= (dropped ? 1u : 0u) << e;
+            o[e] = dropped ? xf[e] : fmaf(yf[e], scale, xf[e]);
           }
           Vec8<T> ov;
           ov.from_float(o);
           ov.store(orow + v * 8);
         }
-        if (mask_bits != nullptr) {
-          bits <<= 8 * (threadIdx.x & 3);
-          bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
-          bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
-          if (v < nvec && (threadIdx.x & 3) == 0) mask_bits[(flat_row + static_cast<uint64_t>(v) * 8) >> 5] = bits;
-        }
+        if (redo) bits = dropout_vector_full(xr + v * 8, yr + v * 8, orow + v * 8, base, threshold, scale);
+      }
+      if (mask_bits != nullptr) {
+        bits <<= 8 * (threadIdx.x & 3);
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
+        if (v < nvec && (threadIdx.x & 3) == 0) mask_bits[(flat_row + static_cast<uint64_t>(v) * 8) >> 5] = bits;
       }
     }
   }
@@ -349,82 +381,6 @@ __device__ __forceinline__ void drain_rows(uint64_t* full, int64_t from, int64_t
   for (int64_t k = from; k < to; ++k) mbar_wait(&full[k % STAGES], (k / STAGES) & 1, status, 21);
 }
 
-
-template <typename T, int kRowThreads, int kRowStages>
-__global__ void __launch_bounds__(kRowThreads)
-    dropout_residual_staged_kernel(const T* __restrict__ x, const T* __restrict__ y, T* __restrict__ out,
-                                   uint32_t* __restrict__ mask_bits, uint64_t threshold, float scale, uint64_t seed,
-                                   int64_t rows, int64_t b, int64_t s, int64_t sl, int h, unsigned int* status) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t row_bytes = static_cast<uint32_t>(h) * sizeof(T);
-  const uint32_t stage_bytes = 2 * row_bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRowStages * stage_bytes);
-  const int64_t nloc = rows_for_cta(rows);
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int st = 0; st < kRowStages; ++st) mbar_init(&full[st], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  auto issue = [&](int64_t i) {
-    const int64_t R = blockIdx.x + i * gridDim.x;
-    const int st = static_cast<int>(i % kRowStages);
-    uint8_t* dst = smem + st * stage_bytes;
-    mbar_arrive_expect_tx(&full[st], stage_bytes);
-    bulk_load(dst, x + R * h, row_bytes, &full[st]);
-    bulk_load(dst + row_bytes, y + R * h, row_bytes, &full[st]);
-  };
-  if (threadIdx.x == 0)
-    for (int64_t i = 0; i < nloc && i < kRowStages; ++i) issue(i);
-  const int nvec = h >> 3;
-  int64_t i = 0;
-  bool aborted = false;
-  for (; i < nloc; ++i) {
-    const int st = static_cast<int>(i % kRowStages);
-    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / kRowStages) & 1), status, 20);
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    const int64_t R = blockIdx.x + i * gridDim.x;
-    const uint64_t flat_row = static_cast<uint64_t>(shard_row_to_token(R, b, s, sl)) * static_cast<uint64_t>(h);
-    const T* xs = reinterpret_cast<const T*>(smem + st * stage_bytes);
-    const T* ys = reinterpret_cast<const T*>(smem + st * stage_bytes + row_bytes);
-    T* orow = out + R * h;
-    for (int v0 = 0; v0 < nvec; v0 += kRowThreads) {  // uniform trip count across the CTA
-      const int v = v0 + threadIdx.x;
-      uint32_t bits = 0;
-      if (v < nvec) {
-        Vec8<T> xv, yv;
-        xv.load(xs + v * 8);
-        yv.load(ys + v * 8);
-        float xf[8], yf[8], o[8];
-        xv.to_float(xf);
-        yv.to_float(yf);
-        // k0 is a multiple of 8, so seed ^ (k0 + e) = (seed ^ k0) ^ e.
-        const uint64_t base = seed ^ (flat_row + static_cast<uint64_t>(v) * 8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const bool drop = hash_below(base ^ static_cast<uint64_t>(e), threshold);
-          bits |= (drop ? 1u : 0u) << e;
-          o[e] = drop ? xf[e] : fmaf(yf[e], scale, xf[e]);
-        }
-        Vec8<T> ov;
-        ov.from_float(o);
-        ov.store(orow + v * 8);
-      }
-      if (mask_bits != nullptr) {
-        bits <<= 8 * (threadIdx.x & 3);
-        bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
-        bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
-        if (v < nvec && (threadIdx.x & 3) == 0) mask_bits[(flat_row + static_cast<uint64_t>(v) * 8) >> 5] = bits;
-      }
-    }
-    __syncthreads();  // every thread has read stage st
-    if (threadIdx.x == 0 && i + kRowStages < nloc) issue(i + kRowStages);
-  }
-  if (aborted && threadIdx.x == 0) drain_rows<kRowStages>(full, i, i + kRowStages < nloc ? i + kRowStages : nloc, status);
-}
 
 // LayerNorm with rows staged through the shared-memory ring; one CTA per row at a time, each
 // thread holding CH vectors of 8 elements in registers. The statistics take one pass: every
@@ -644,8 +600,6 @@ size_t staged_smem(size_t stage_bytes, int stages) { return stages * stage_bytes
 
 constexpr int kLnStagedThreads = 128, kLnStages = 6;
 constexpr bool kLnAffineInRegs = true;  // gamma, beta read once per CTA
-constexpr bool kUseStagedDropout = false;  // the register kernel issues fewer instructions per element
-constexpr int kDoStagedThreads = 256, kDoStages = 4;
 
 constexpr size_t kStagedSmemMax = 100 * 1024;  // at least two CTAs per SM
 
@@ -659,38 +613,37 @@ __device__ __forceinline__ int64_t token_to_shard_row(int64_t r, int64_t b, int6
 }
 
 // Dropout backward fused with g-bar's backward (all-gather): token row r of the result is
-// dout[shard row of r] * keep / (1 - p), with the mask recomputed from the hash.
-template <typename T, int VPT>
-__global__ void __launch_bounds__(128) dropout_grad_gather_kernel(const T* __restrict__ dout, T* __restrict__ dtok,
-                                                                  uint64_t threshold, float scale, uint64_t seed,
-                                                                  int64_t rows, int64_t b, int64_t s, int64_t sl,
-                                                                  int h) {
+// dout[shard row of r] * keep / (1 - p), with the mask recomputed from the hash; one thread
+// per vector of 8 elements, one token row per CTA, as dropout_residual_kernel. kLow3 = seed & 7.
+template <typename T, int kLow3>
+__global__ void __launch_bounds__(128, dropout_min_blocks<T>()) dropout_grad_gather_kernel(
+    const T* __restrict__ dout, T* __restrict__ dtok, uint64_t threshold, float scale, uint64_t seed, int64_t rows,
+    int64_t b, int64_t s, int64_t sl, int h) {
   const int nvec = h >> 3;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const T* src = dout + token_to_shard_row(r, b, s, sl) * h;
     T* dst = dtok + r * h;
     const uint64_t flat_row = static_cast<uint64_t>(r) * static_cast<uint64_t>(h);
-    for (int v0 = 0; v0 < nvec; v0 += blockDim.x * VPT) {
-      Vec8<T> gv[VPT];
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const uint64_t base = seed ^ (flat_row + static_cast<uint64_t>(v) * 8);
+      const DropHash8<kLow3> hs(base, threshold);
+      bool redo = !hs.shortcut;
+      if (hs.shortcut) {
+        Vec8<T> gv;
+        gv.load(src + v * 8);
+        float gf[8], o[8];
+        gv.to_float(gf);
 #pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const int v = v0 + j * blockDim.x + threadIdx.x;
-        if (v < nvec) gv[j].load(src + v * 8);
-      }
-#pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const int v = v0 + j * blockDim.x + threadIdx.x;
-        if (v < nvec) {
-          const uint64_t base = seed ^ (flat_row + static_cast<uint64_t>(v) * 8);
-          float gf[8], o[8];
-          gv[j].to_float(gf);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = hash_below(base ^ static_cast<uint64_t>(e), threshold) ? 0.f : gf[e] * scale;
-          Vec8<T> ov;
-          ov.from_float(o);
-          ov.store(dst + v * 8);
+        for (uint32_t e = 0; e < 8; ++e) {
+          const uint32_t c = hs.high(e);
+          redo |= c == hs.thi;
+          o[e] = c < hs.thi ? 0.f : gf[e] * scale;
         }
+        Vec8<T> ov;
+        ov.from_float(o);
+        ov.store(dst + v * 8);
       }
+      if (redo) dropout_vector_full<T>(src + v * 8, nullptr, dst + v * 8, base, threshold, scale);
     }
   }
 }
@@ -1219,6 +1172,23 @@ cudaError_t launch_reduce_scatter(const float* partials, void* out_shards, int64
   return cudaGetLastError();
 }
 
+// Calls launch(std::integral_constant<int, seed & 7>{}): the dropout kernels take the seed's low
+// three bits as a template argument.
+template <class L>
+cudaError_t with_seed_low3(uint64_t seed, L&& launch) {
+  switch (static_cast<int>(seed & 7)) {
+    case 0: launch(std::integral_constant<int, 0>{}); break;
+    case 1: launch(std::integral_constant<int, 1>{}); break;
+    case 2: launch(std::integral_constant<int, 2>{}); break;
+    case 3: launch(std::integral_constant<int, 3>{}); break;
+    case 4: launch(std::integral_constant<int, 4>{}); break;
+    case 5: launch(std::integral_constant<int, 5>{}); break;
+    case 6: launch(std::integral_constant<int, 6>{}); break;
+    default: launch(std::integral_constant<int, 7>{}); break;
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, void* out_shards,
                                     uint32_t* mask_bits, uint64_t threshold, float scale, uint64_t seed, int64_t b,
                                     int64_t s, int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms,
@@ -1226,42 +1196,19 @@ cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, 
   const int64_t rows = b * s;
   if (rows <= 0) return cudaSuccess;
   if (h % 8 != 0 || (mask_bits && h % 32 != 0)) return cudaErrorInvalidValue;
-  const size_t elt = bf16 ? 2 : 4;
-  const size_t do_smem = staged_smem(2 * static_cast<size_t>(h) * elt, kDoStages);
-  if (kUseStagedDropout && do_smem <= kStagedSmemMax) {
-    const int per_sm = static_cast<int>((220 * 1024) / do_smem);
-    const int grid = rows_grid(rows, num_sms, per_sm > 0 ? per_sm : 1);
-    if (bf16) {
-      auto k = dropout_residual_staged_kernel<__nv_bfloat16, kDoStagedThreads, kDoStages>;
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)do_smem);
-      if (e != cudaSuccess) return e;
-      k<<<grid, kDoStagedThreads, do_smem, stream>>>(static_cast<const __nv_bfloat16*>(x_shards),
-                                                static_cast<const __nv_bfloat16*>(y_shards),
-                                                static_cast<__nv_bfloat16*>(out_shards), mask_bits, threshold, scale,
-                                                seed, rows, b, s, s / t, static_cast<int>(h), status);
-    } else {
-      auto k = dropout_residual_staged_kernel<float, kDoStagedThreads, kDoStages>;
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)do_smem);
-      if (e != cudaSuccess) return e;
-      k<<<grid, kDoStagedThreads, do_smem, stream>>>(static_cast<const float*>(x_shards),
-                                                static_cast<const float*>(y_shards), static_cast<float*>(out_shards),
-                                                mask_bits, threshold, scale, seed, rows, b, s, s / t,
-                                                static_cast<int>(h), status);
-    }
-    return cudaGetLastError();
-  }
-  const int grid = rows_grid(rows, num_sms, 16);
-  if (bf16)
-    dropout_residual_kernel<__nv_bfloat16, 4><<<grid, 128, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x_shards), static_cast<const __nv_bfloat16*>(y_shards),
-        static_cast<__nv_bfloat16*>(out_shards), mask_bits, threshold, scale, seed, rows, b, s, s / t,
-        static_cast<int>(h));
-  else
-    dropout_residual_kernel<float, 4><<<grid, 128, 0, stream>>>(static_cast<const float*>(x_shards),
-                                                                 static_cast<const float*>(y_shards),
-                                                                 static_cast<float*>(out_shards), mask_bits, threshold,
-                                                                 scale, seed, rows, b, s, s / t, static_cast<int>(h));
-  return cudaGetLastError();
+  const int grid = rows_grid(rows, num_sms, 64);  // one row per CTA up to 64 CTAs per SM
+  return with_seed_low3(seed, [&](auto low3) {
+    constexpr int kLow3 = decltype(low3)::value;
+    if (bf16)
+      dropout_residual_kernel<__nv_bfloat16, kLow3><<<grid, 128, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(x_shards), static_cast<const __nv_bfloat16*>(y_shards),
+          static_cast<__nv_bfloat16*>(out_shards), mask_bits, threshold, scale, seed, rows, b, s, s / t,
+          static_cast<int>(h));
+    else
+      dropout_residual_kernel<float, kLow3><<<grid, 128, 0, stream>>>(
+          static_cast<const float*>(x_shards), static_cast<const float*>(y_shards), static_cast<float*>(out_shards),
+          mask_bits, threshold, scale, seed, rows, b, s, s / t, static_cast<int>(h));
+  });
 }
 
 cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint64_t threshold, float scale,
@@ -1270,16 +1217,18 @@ cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint
   const int64_t rows = b * s;
   if (rows <= 0) return cudaSuccess;
   if (h % 8 != 0) return cudaErrorInvalidValue;
-  const int grid = rows_grid(rows, num_sms, 16);
-  if (bf16)
-    dropout_grad_gather_kernel<__nv_bfloat16, 4><<<grid, 128, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(dout_shards), static_cast<__nv_bfloat16*>(dtok), threshold, scale, seed,
-        rows, b, s, s / t, static_cast<int>(h));
-  else
-    dropout_grad_gather_kernel<float, 4><<<grid, 128, 0, stream>>>(static_cast<const float*>(dout_shards),
-                                                                    static_cast<float*>(dtok), threshold, scale, seed,
-                                                                    rows, b, s, s / t, static_cast<int>(h));
-  return cudaGetLastError();
+  const int grid = rows_grid(rows, num_sms, 64);  // one row per CTA up to 64 CTAs per SM
+  return with_seed_low3(seed, [&](auto low3) {
+    constexpr int kLow3 = decltype(low3)::value;
+    if (bf16)
+      dropout_grad_gather_kernel<__nv_bfloat16, kLow3><<<grid, 128, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(dout_shards), static_cast<__nv_bfloat16*>(dtok), threshold, scale, seed,
+          rows, b, s, s / t, static_cast<int>(h));
+    else
+      dropout_grad_gather_kernel<float, kLow3><<<grid, 128, 0, stream>>>(
+          static_cast<const float*>(dout_shards), static_cast<float*>(dtok), threshold, scale, seed, rows, b, s,
+          s / t, static_cast<int>(h));
+  });
 }
 
 cudaError_t launch_column_sums(const void* M, int64_t rows, int64_t cols, bool bf16, float* partials, float* out,

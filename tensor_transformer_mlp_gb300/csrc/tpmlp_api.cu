@@ -339,14 +339,14 @@ tpmlp_status check_sp_shape(int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype 
   return TPMLP_OK;
 }
 
-tpmlp_status check_dropout(float p) {
-  if (!(p >= 0.0f && p < 1.0f)) return fail(TPMLP_ERR_INVALID, "p_drop must lie in [0, 1), got %g", (double)p);
+tpmlp_status check_dropout(double p) {
+  if (!(p >= 0.0 && p < 1.0)) return fail(TPMLP_ERR_INVALID, "p_drop must lie in [0, 1), got %g", p);
   return TPMLP_OK;
 }
 
 // T = floor(p * 2^64) with the product in double; p in [0, 1).
-uint64_t drop_threshold(float p) {
-  const double v = static_cast<double>(p) * 18446744073709551616.0;
+uint64_t drop_threshold(double p) {
+  const double v = p * 18446744073709551616.0;
   return static_cast<uint64_t>(v);
 }
 
@@ -359,7 +359,7 @@ size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m,
 }
 
 tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const float* beta, float eps, const void* A,
-                            const void* B, float p_drop, uint64_t seed, void* out_shards, uint32_t* mask_bits,
+                            const void* B, double p_drop, uint64_t seed, void* out_shards, uint32_t* mask_bits,
                             void* Z_save, void* Y_save, int64_t b, int64_t s, int64_t h, int64_t m, int t,
                             tpmlp_gelu gelu, tpmlp_dtype dt, tpmlp_rs_mode rs, void* workspace, size_t ws_bytes,
                             void* stream) {
@@ -397,7 +397,7 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
   TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms, ctx.status), "layernorm");
   TPMLP_CUDA(launch_gather(xn, xg, b, s, h, t, bf16, st, ctx.num_sms), "gather");
   const uint64_t threshold = drop_threshold(p_drop);
-  const float scale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop)));
+  const float scale = static_cast<float>(1.0 / (1.0 - p_drop));
   RowRemap rm;
   rm.enabled = 1;
   rm.b = b;
@@ -456,7 +456,7 @@ size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, i
 }
 
 tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, const float* beta, float eps,
-                                     const void* A, const void* B, float p_drop, uint64_t seed, const void* Z_save,
+                                     const void* A, const void* B, double p_drop, uint64_t seed, const void* Z_save,
                                      const void* Y_save, const void* dout_shards, void* dx_shards, float* dgamma,
                                      float* dbeta, float* dA, float* dB, int64_t b, int64_t s, int64_t h, int64_t m,
                                      int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace, size_t ws_bytes,
@@ -505,7 +505,7 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
   TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms, ctx.status), "layernorm");
   TPMLP_CUDA(launch_gather(xn, xg, b, s, h, t, bf16, st, ctx.num_sms), "gather");
   TPMLP_CUDA(launch_dropout_grad_gather(dout_shards, dtok, drop_threshold(p_drop),
-                                        static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))), seed, b, s, h,
+                                        static_cast<float>(1.0 / (1.0 - p_drop)), seed, b, s, h,
                                         t, bf16, st, ctx.num_sms),
              "dropout backward + gather");
   // Row-GEMM backward with the GeLU' mask, the two weight gradients, column-GEMM backward.
@@ -638,7 +638,7 @@ tpmlp_status tpmlp_sp_reduce_scatter(const float* partials, void* out_shards, in
 }
 
 tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shards, void* out_shards,
-                                       uint32_t* mask_bits, float p_drop, uint64_t seed, int64_t b, int64_t s,
+                                       uint32_t* mask_bits, double p_drop, uint64_t seed, int64_t b, int64_t s,
                                        int64_t h, int t, tpmlp_dtype dt, void* stream) {
   if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
   TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
@@ -650,7 +650,7 @@ tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shard
   DeviceCtx ctx;
   TPMLP_CUDA(get_device_ctx(&ctx), "device context");
   TPMLP_CUDA(launch_dropout_residual(x_shards, y_shards, out_shards, mask_bits, drop_threshold(p_drop),
-                                     static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))), seed, b, s, h, t,
+                                     static_cast<float>(1.0 / (1.0 - p_drop)), seed, b, s, h, t,
                                      dt == TPMLP_BF16, static_cast<cudaStream_t>(stream), ctx.num_sms, ctx.status),
              "dropout+residual");
   return TPMLP_OK;

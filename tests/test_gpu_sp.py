@@ -231,3 +231,79 @@ def test_sp_block_dropout_extremes(p, rs):
     else:
         frac = ref["dropped"].mean()
         assert 0.85 < frac < 0.95
+
+
+# ---------------------------------------------------------------- seeds that reach the hash's rare cases
+
+_M64 = (1 << 64) - 1
+
+
+def _unxorshift(y: int, s: int) -> int:
+    x = y
+    for _ in range(64 // s + 1):
+        x = y ^ (x >> s)
+    return x
+
+
+def splitmix64_preimage(h: int) -> int:
+    """The state x with splitmix64(x) = h: each step of the mixer (add, xor-shift, multiply by
+    an odd constant) is invertible mod 2^64."""
+    z = _unxorshift(h, 31)
+    z = (z * pow(0x94D049BB133111EB, -1, 1 << 64)) & _M64
+    z = _unxorshift(z, 27)
+    z = (z * pow(0xBF58476D1CE4E5B9, -1, 1 << 64)) & _M64
+    z = _unxorshift(z, 30)
+    return (z - 0x9E3779B97F4A7C15) & _M64
+
+
+K_AT, K_BELOW, K_CARRY = 12345, 40001, 8 * 777
+
+
+def crafted_seeds():
+    """Seeds for p = 0.1 that steer single elements onto the hash's rare cases:
+    'at': element K_AT hashes to exactly T = floor(0.1 * 2^64) = 0x1999999999999A00, so it is
+    kept (a threshold taken from p in single precision, 0x199999A000000000, would drop it);
+    'below': element K_BELOW hashes to T - 1 and is dropped; both tie T's high word;
+    'carry': the eight keys of the vector at K_CARRY carry out of the low word when gamma is added."""
+    T = osp.drop_threshold(0.1)
+    seeds = {"at": splitmix64_preimage(T) ^ K_AT, "below": splitmix64_preimage(T - 1) ^ K_BELOW,
+             "carry": (0x1234_5678 << 32) | ((0x80B583E8 | 5) ^ K_CARRY)}
+    assert osp.splitmix64_scalar(seeds["at"] ^ K_AT) == T
+    assert osp.splitmix64_scalar(seeds["below"] ^ K_BELOW) == T - 1
+    assert (((seeds["carry"] ^ K_CARRY) & ~7) + 0x9E3779B97F4A7C15) & 0xFFFFFFFF > 0xFFFFFFF8
+    return seeds
+
+
+@pytest.mark.parametrize("which", ["at", "below", "carry"])
+def test_dropout_residual_crafted_seeds(which):
+    seed = crafted_seeds()[which]
+    t, b, sl, h = 4, 2, 32, 256
+    rng = np.random.default_rng(9)
+    x = wl.round_to_bf16(rng.standard_normal((t, b, sl, h)).astype(np.float32))
+    y = wl.round_to_bf16(rng.standard_normal((t, b, sl, h)).astype(np.float32))
+    xd, yd = dev(x, "bf16"), dev(y, "bf16")
+    out = torch.empty_like(xd)
+    mask = torch.zeros((b * sl * t * h) // 32, dtype=torch.int32, device="cuda")
+    tp.tpmlp_sp_dropout_residual(xd, yd, out, mask, 0.1, seed)
+    torch.cuda.synchronize()
+    xl, yl = wl.from_shards(x), wl.from_shards(y)
+    flat = np.arange(b * sl * t * h, dtype=np.uint64).reshape(xl.shape)
+    dropped = osp.drop_mask(flat, seed, 0.1)
+    if which == "at":
+        assert not dropped.reshape(-1)[K_AT]
+    if which == "below":
+        assert dropped.reshape(-1)[K_BELOW]
+    assert np.array_equal(mask_words(mask), osp.pack_mask_bits(dropped))
+    assert_close("out", wl.from_shards(host(out).reshape(t, b, sl, h)), osp.dropout_residual(xl, yl, seed, 0.1, flat),
+                 8e-3)
+
+
+@pytest.mark.parametrize("which", ["at", "below", "carry"])
+def test_sp_block_crafted_seeds(which):
+    # The same seeds through the SP block, whose dropout runs in the FC2 epilogue.
+    b, s, h, m, t = 2, 256, 256, 512, 4
+    cfg = wl.SPConfig("sp-seed", b, s, h, m, t, "tanh", 1.0, 0.05, p_drop=0.1, seed=crafted_seeds()[which])
+    inp, out, mask = sp_case(cfg, "fused")
+    ref = osp.sp_block(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop, cfg.seed, cfg.gelu)
+    assert np.array_equal(mask_words(mask), osp.pack_mask_bits(ref["dropped"]))
+    assert_close("out", wl.from_shards(host(out).reshape(t, b, s // t, h)), ref["out"], TOL_BF16)
