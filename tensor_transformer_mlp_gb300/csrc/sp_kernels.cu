@@ -1148,7 +1148,8 @@ cudaError_t launch_gather(const void* x_shards, void* x_full, int64_t b, int64_t
   if (row_vecs <= 256) {
     gather_kernel<1, 4><<<rows_grid((rows + 3) / 4, num_sms, 8), 256, 0, stream>>>(src, dst, rows, b, s, s / t, row_vecs);
   } else if (row_vecs <= 512) {
-    gather_kernel<2, 2><<<rows_grid((rows + 1) / 2, num_sms, 8), 256, 0, stream>>>(src, dst, rows, b, s, s / t, row_vecs);
+    // one row per CTA up to 64 CTAs per SM: the block scheduler balances the tail
+    gather_kernel<2, 1><<<rows_grid(rows, num_sms, 64), 256, 0, stream>>>(src, dst, rows, b, s, s / t, row_vecs);
   } else if (row_vecs <= 1024) {
     gather_kernel<4, 1><<<rows_grid(rows, num_sms, 8), 256, 0, stream>>>(src, dst, rows, b, s, s / t, row_vecs);
   } else {
