@@ -1,6 +1,7 @@
 """Host-side checks of the C ABI that need no GPU: the library builds and loads, it
 exports every entry point include/tpmlp.h declares, and bad arguments are rejected
 with the documented status before anything touches the device."""
+import ctypes
 import os
 import re
 import subprocess
@@ -30,6 +31,41 @@ def lib():
 
 def test_header_and_binding_agree():
     assert declared_functions() == set(_binding.SIGNATURES)
+
+
+# C parameter and return types of include/tpmlp.h -> the ctypes type the binding must declare.
+_CTYPE = {"const void*": ctypes.c_void_p, "void*": ctypes.c_void_p, "const float*": ctypes.c_void_p,
+          "float*": ctypes.c_void_p, "uint32_t*": ctypes.c_void_p, "int64_t": ctypes.c_int64, "int": ctypes.c_int,
+          "tpmlp_gelu": ctypes.c_int, "tpmlp_dtype": ctypes.c_int, "tpmlp_rs_mode": ctypes.c_int,
+          "float": ctypes.c_float, "double": ctypes.c_double, "uint64_t": ctypes.c_uint64, "size_t": ctypes.c_size_t,
+          "tpmlp_status": ctypes.c_int, "const char*": ctypes.c_char_p}
+
+
+def declared_signatures():
+    """{name: (return type, [parameter types])} parsed from the header's prototypes."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for ret, name, params in re.findall(r"(const\s+char\s*\*|size_t|tpmlp_status)\s+(tpmlp_\w+)\s*\(([^)]*)\)\s*;",
+                                        text, re.S):
+        types = []
+        for p in params.split(","):
+            p = " ".join(p.split())
+            if p and p != "void":
+                types.append(p.rsplit(" ", 1)[0].replace(" *", "*") if not p.endswith("*") else p)
+        out[name] = (" ".join(ret.split()).replace(" *", "*"), types)
+    return out
+
+
+def test_binding_argument_types_match_header():
+    # A float declared where the library takes a double (or an int where it takes int64_t)
+    # passes the wrong bits without any error, so every parameter is checked.
+    decl = declared_signatures()
+    assert set(decl) == declared_functions()
+    for name, (ret, params) in decl.items():
+        restype, argtypes = _binding.SIGNATURES[name]
+        assert restype is _CTYPE[ret], name
+        assert [_CTYPE[p] for p in params] == list(argtypes), name
 
 
 def test_library_exports_every_declared_symbol(lib):
