@@ -185,11 +185,30 @@ def calibrate_rows(cfg, inp, target_s: float, max_rows: int) -> int:
     return max(16, min(int(rows * target_s / max(t, 1e-3)), max_rows, cfg.n))
 
 
+def host_cpu() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo) and architecture, for the CPU-baseline record."""
+    import platform
+    import subprocess
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        model = next((ln.split(":", 1)[1].strip() for ln in out.splitlines() if ln.startswith("Model name:")), "")
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                model = next((ln.split(":", 1)[1].strip() for ln in f if ln.startswith("model name")), "")
+        except OSError:
+            pass
+    return f"{model or 'unknown'} ({platform.machine()})"
+
+
 def cpu_baseline(cfg, inp, target_s=15.0):
     rows = calibrate_rows(cfg, inp, target_s, 8192)
     secs = time_oracle(cfg, inp, rows)
     return {"value": oracle_rows_flops(cfg, rows) / secs / 1e12, "unit": UNIT, "cores": os.cpu_count(),
-            "kind": "oracle",
+            "cpu": host_cpu(), "kind": "oracle",
             "sample": f"float64 numpy oracle, forward+backward of {rows} of {cfg.n} token rows with full "
                       f"A [{cfg.d}x{cfg.m}] and B [{cfg.m}x{cfg.d}] (12*rows*d*m FLOP), {secs:.1f} s, "
                       f"BLAS on all host threads"}
@@ -215,8 +234,8 @@ def run_reference(args, cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_dict(cfg),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "cpu": host_cpu(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
