@@ -453,11 +453,13 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
   }
 }
 
-// Per-warp TMA buffers of the batched epilogues: kEpiSoftmax stores P through two; kEpiSoftmaxGrad
-// loads P through two and stores dS through two more.
+// Per-warp TMA buffers of the batched epilogues: kEpiSoftmax stores P through four (up to three
+// stores in flight while the next pass is computed); kEpiSoftmaxGrad loads P through two and
+// stores dS through two more.
+constexpr int kSoftmaxStoreBufs = 4;
 template <int EPI, bool BATCHED>
 __host__ __device__ constexpr int aux_bufs() {
-  return !BATCHED ? 0 : (EPI == kEpiSoftmax ? 2 : (EPI == kEpiSoftmaxGrad ? 4 : 0));
+  return !BATCHED ? 0 : (EPI == kEpiSoftmax ? kSoftmaxStoreBufs : (EPI == kEpiSoftmaxGrad ? 4 : 0));
 }
 
 // One TMA tile load: 2-D map for plain launches; 4-D map (inner, then row and batch indices in
@@ -653,8 +655,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   };
   if constexpr (kAux && EPI == kEpiSoftmax) {
       // P = 2^(acc * c - M) / L written by TMA stores: each 64-column pass of the warp's 32 rows
-      // goes into one of its two 4 KB buffers in the 128-byte-swizzled layout the store expects,
-      // and lane 0 issues the store; a buffer is reused once the store two passes back has read it.
+      // goes into one of its kSoftmaxStoreBufs 4 KB buffers in the 128-byte-swizzled layout the
+      // store expects, and lane 0 issues the store; a buffer is reused once the store
+      // kSoftmaxStoreBufs passes back has read it.
       uint8_t* sb = aux_buf + (warp - 2) * kAuxBufs * AUX_BUF_BYTES;
       int nstore = 0;
       int it = 0;
@@ -689,8 +692,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             seg[g] = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
                                 pack_bf16x2(pv[6], pv[7]));
           }
-          uint8_t* buf = sb + (nstore & 1) * AUX_BUF_BYTES;
-          if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
+          uint8_t* buf = sb + (nstore % kSoftmaxStoreBufs) * AUX_BUF_BYTES;
+          if (lane == 0 && nstore >= kSoftmaxStoreBufs) bulk_wait_group_read<kSoftmaxStoreBufs - 1>();
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = seg[j];
