@@ -188,7 +188,6 @@ def calibrate_rows(cfg, inp, target_s: float, max_rows: int) -> int:
 def host_cpu() -> str:
     """The host CPU's model name (lscpu, else /proc/cpuinfo) and architecture, for the CPU-baseline record."""
     import platform
-    import subprocess
     model = ""
     try:
         out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
@@ -204,11 +203,35 @@ def host_cpu() -> str:
     return f"{model or 'unknown'} ({platform.machine()})"
 
 
+_ONE_THREAD_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                   "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS")
+
+
+def single_thread_oracle(timeout_s: float = 120.0):
+    """The oracle's full forward + backward on the single MLP block (n512 d1024 m4096), timed in a
+    child process whose BLAS runs on one thread (the thread count is fixed when numpy loads its
+    BLAS, hence the child). Returns a small record, or None if the child fails."""
+    env = dict(os.environ)
+    env.update({k: "1" for k in _ONE_THREAD_ENV})
+    code = ("import json, bench; from tensor_transformer_mlp_gb300 import workloads as wl; "
+            "cfg = wl.SINGLE_BLOCK; inp = wl.mlp_inputs(cfg); bench.time_oracle(cfg, inp, 16); "
+            "s = bench.time_oracle(cfg, inp, cfg.n); "
+            "print(json.dumps({'workload': cfg.name, 'seconds': s, 'value': bench.oracle_rows_flops(cfg, cfg.n) / s / 1e12}))")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=timeout_s,
+                             cwd=os.path.dirname(os.path.abspath(__file__)))
+        rec = json.loads(out.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
+    rec.update({"unit": UNIT, "threads": 1, "sample": "full forward + backward of every token row, float64"})
+    return rec
+
+
 def cpu_baseline(cfg, inp, target_s=15.0):
     rows = calibrate_rows(cfg, inp, target_s, 8192)
     secs = time_oracle(cfg, inp, rows)
     return {"value": oracle_rows_flops(cfg, rows) / secs / 1e12, "unit": UNIT, "cores": os.cpu_count(),
-            "cpu": host_cpu(), "kind": "oracle",
+            "cpu": host_cpu(), "kind": "oracle", "single_thread": single_thread_oracle(),
             "sample": f"float64 numpy oracle, forward+backward of {rows} of {cfg.n} token rows with full "
                       f"A [{cfg.d}x{cfg.m}] and B [{cfg.m}x{cfg.d}] (12*rows*d*m FLOP), {secs:.1f} s, "
                       f"BLAS on all host threads"}
