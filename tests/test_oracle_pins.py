@@ -235,6 +235,23 @@ def test_dropout_p0_is_plain_residual():
     assert np.array_equal(out, x + y)
 
 
+@pytest.mark.parametrize("p", [0.1, 0.25, 0.5])
+def test_inverted_dropout_preserves_the_mean(p):
+    # Dropout scales kept elements so that the expected output equals the input ("Megatron 训练"
+    # notes, Dropout section: torch.nn.Dropout semantics). With x = 0 and y = 1 the output is
+    # keep / (1 - p), whose mean over N elements is 1 within 5 sigma, sigma^2 = p / ((1 - p) N);
+    # dropped elements are exactly the residual and kept ones all carry one common value.
+    N = 1 << 22
+    flat = np.arange(N, dtype=np.uint64)
+    x, y = np.zeros(N), np.ones(N)
+    out = sp.dropout_residual(x, y, 5, p, flat)
+    dropped = sp.drop_mask(flat, 5, p)
+    assert abs(out.mean() - 1.0) < 5 * math.sqrt(p / ((1.0 - p) * N))
+    assert np.array_equal(out[dropped], x[dropped])
+    kept = out[~dropped]
+    assert kept.min() == kept.max() > 1.0
+
+
 def test_pack_mask_bits():
     m = np.random.default_rng(19).random(200) < 0.3
     words = sp.pack_mask_bits(m)
