@@ -81,3 +81,33 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]) == 0
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_host_cpu_names_a_model_and_falls_back_without_lscpu(monkeypatch):
+    import platform
+    import subprocess
+
+    assert bench.host_cpu().endswith(f"({platform.machine()})")
+
+    def no_lscpu(*args, **kwargs):
+        raise FileNotFoundError("lscpu")
+
+    monkeypatch.setattr(subprocess, "run", no_lscpu)
+    got = bench.host_cpu()  # /proc/cpuinfo, else "unknown"
+    assert got.endswith(f"({platform.machine()})") and len(got) > len(platform.machine()) + 3
+
+
+def test_single_thread_oracle_is_null_when_its_child_fails(monkeypatch):
+    import subprocess
+
+    class Done:
+        stdout, stderr, returncode = "Traceback: no json here", "", 1
+
+    monkeypatch.setattr(subprocess, "run", lambda *a, **k: Done())
+    assert bench.single_thread_oracle() is None
+
+    def timeout(*a, **k):
+        raise subprocess.TimeoutExpired("python", 1.0)
+
+    monkeypatch.setattr(subprocess, "run", timeout)
+    assert bench.single_thread_oracle() is None
