@@ -214,6 +214,29 @@ def test_splitmix64_zero_state_closed_form():
     assert sp.splitmix64_scalar(0) != 0
 
 
+# Published SplitMix64 output streams. A generator seeded with s advances its state by the golden
+# gamma and returns the mix of the new state, so its k-th output (k = 0, 1, ...) is the oracle's
+# splitmix64 of s + k * gamma. The values are the ones printed for the published generator
+# (Vigna's splitmix64.c seeded with 0, and the Rosetta Code "Pseudo-random numbers/Splitmix64"
+# task seeded with 1234567), typed here by hand. A wrong multiplier, shift or increment in the
+# oracle changes every one of them.
+_SPLITMIX64_KNOWN = {
+    0: [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F, 0xF88BB8A8724C81EC,
+        0x1B39896A51A8749B],
+    1234567: [6457827717110365317, 3203168211198807973, 9817491932198370423, 4593380528125082431,
+              16408922859458223821],
+}
+
+
+@pytest.mark.parametrize("seed", sorted(_SPLITMIX64_KNOWN))
+def test_splitmix64_published_output_stream(seed):
+    gamma, mask = 0x9E3779B97F4A7C15, (1 << 64) - 1
+    states = [(seed + k * gamma) & mask for k in range(5)]
+    want = _SPLITMIX64_KNOWN[seed]
+    assert [sp.splitmix64_scalar(s) for s in states] == want
+    assert [int(v) for v in sp.splitmix64(np.array(states, dtype=np.uint64))] == want
+
+
 def test_drop_threshold():
     assert sp.drop_threshold(0.1) == 0x1999999999999A00
     assert sp.drop_threshold(0.0) == 0
