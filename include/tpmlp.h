@@ -34,6 +34,10 @@
  *  - Kernels that wait on in-kernel barriers give every wait a time limit; on
  *    expiry they record TPMLP_ERR_TIMEOUT in a device status word, release what
  *    they hold and return. tpmlp_device_status() reads that word.
+ *  - The library keeps a little state per device (the status word's address, the SM
+ *    count, the GEMM's pacing counters), set up by the first call on that device and
+ *    kept for the life of the process: calls run in the device's primary context, and
+ *    a cudaDeviceReset while the library is in use is not supported.
  */
 #ifndef TPMLP_H
 #define TPMLP_H
@@ -107,11 +111,16 @@ tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const v
  * state has begun). It computes exactly what tpmlp_backward computes, with the same arguments
  * minus the workspace, and keeps D in a static device array of 64 MiB (67,108,864 bytes)
  * inside the library, which every GPU that loads the library holds until the process exits.
- *   - n * m * element size above 64 MiB is rejected with TPMLP_ERR_WORKSPACE before anything
- *     runs; use tpmlp_backward with a workspace for larger problems.
+ *   - Arguments are checked exactly as tpmlp_backward checks them, with the same statuses;
+ *     then n * m * element size above 64 MiB is rejected with TPMLP_ERR_WORKSPACE before
+ *     anything runs (bf16: n * m <= 33,554,432, e.g. n = 8192 with m = 4096; fp32: half that).
+ *     Use tpmlp_backward with a workspace for larger problems.
+ *   - The result is bit-identical to tpmlp_backward's on the same inputs.
  *   - It allocates nothing (no cudaMalloc, cudaFree or allocating library call).
  *   - The first call on a device looks up the array's device address on that device (once);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture. The address is kept for the life of the
+ *     process, so a cudaDeviceReset between calls, or a context other than the device's
+ *     primary context, is not supported.
  *   - Every call on a device shares the one array: calls that may overlap on the GPU (on
  *     different streams, or from several threads) race on it and must be serialised by the
  *     caller. D is fully rewritten by each call, so no clearing is needed between calls.
@@ -310,6 +319,20 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
                                       void* dX, float* dWqkv, float* dWo,
                                       int64_t b, int64_t s, int64_t h, int heads, int t, tpmlp_dtype dt,
                                       void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Kernel choice for the plain bf16 GEMMs of every later call in this process, for comparing
+ * kernels and testing each one; a user of the library never needs it, and nothing else
+ * (no environment variable) changes the choice. The defaults, 1, 1, 0, are the fast path:
+ *   pair_kernel 1: 256 x 256 tiles on clusters of two SMs; 0: 128 x 256 tiles on one SM.
+ *   pair_pacing 1: pairs wait at intervals of 32 k-blocks for the pairs of the same round of
+ *                  tiles, which keeps shared operand panels in L2; 0: no pacing.
+ *   pair_group  0: the default tile band (8 pair-rows walked along N); g > 0: g pair-rows
+ *                  walked along N; g < 0: -g N-blocks walked along M. |g| <= 4096.
+ * The choice is read when a GEMM is launched, so a CUDA graph keeps the one it captured.
+ * Every variant computes the same contractions with fp32 accumulation. Errors: TPMLP_ERR_INVALID.
+ */
+tpmlp_status tpmlp_set_gemm_variant(int pair_kernel, int pair_pacing, int pair_group);
 
 /* Message for the calling thread's last non-OK status ("" if none). Never NULL. */
 const char* tpmlp_last_error(void);

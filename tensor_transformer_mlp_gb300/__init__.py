@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     tpmlp_rmsnorm,
     tpmlp_rmsnorm_backward,
     tpmlp_rmsnorm_backward_workspace_size,
+    tpmlp_set_gemm_variant,
     tpmlp_sp_block,
     tpmlp_sp_block_backward,
     tpmlp_sp_block_backward_workspace_size,

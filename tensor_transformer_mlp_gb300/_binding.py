@@ -55,6 +55,7 @@ SIGNATURES = {
     "tpmlp_last_error": (ctypes.c_char_p, []),
     "tpmlp_device_status": (_I, [_P, _I]),
     "tpmlp_check_wait_timeout": (_I, [_U64, _P]),
+    "tpmlp_set_gemm_variant": (_I, [_I, _I, _I]),
 }
 
 _lib = None
@@ -290,6 +291,10 @@ def tpmlp_check_wait_timeout(limit_ns: int, stream=None) -> None:
 
 def tpmlp_device_status(stream=None, clear: bool = True) -> None:
     _check(load_library().tpmlp_device_status(_stream(stream), 1 if clear else 0))
+
+
+def tpmlp_set_gemm_variant(pair_kernel: int = 1, pair_pacing: int = 1, pair_group: int = 0) -> None:
+    _check(load_library().tpmlp_set_gemm_variant(pair_kernel, pair_pacing, pair_group))
 
 
 # ----------------------------------------------------------------------- conveniences

@@ -9,7 +9,7 @@
 // Two persistent kernels, one CTA per SM, sharing the epilogue code:
 //   gemm_bf16_pair_kernel (plain GEMMs): 256 x 256 tiles on clusters of two SMs
 //               (tcgen05 cta_group::2), 6-stage ring of 32 KB per SM, paced pairs
-//   gemm_bf16_kernel (batched GEMMs, or all of them with TPMLP_GEMM_PAIR=0): 128 x 256
+//   gemm_bf16_kernel (batched GEMMs, or all of them when tpmlp_set_gemm_variant asks): 128 x 256
 //               tiles on one SM with a 4-stage ring of 48 KB, or 128 x 128 tiles with a
 //               6-stage ring of 32 KB for the batched GEMMs whose N is at most 128
 // The batched launches serve the attention block ("SenseParrots" model-parallel note, section
@@ -31,13 +31,18 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
-#include <cstdlib>
 #include <mutex>
 
 #include "device_common.cuh"
 
 namespace tpmlp {
 namespace {
+
+// GEMM variant for the plain (non-batched) GEMMs, process-wide; set only through
+// tpmlp_set_gemm_variant (comparison and testing). Defaults: SM-pair kernel, paced, default band.
+std::atomic<int> g_pair_kernel{1};
+std::atomic<int> g_pair_pacing{1};
+std::atomic<int> g_pair_group{0};
 
 constexpr int BM = 128;
 constexpr int BN = 256;  // tile width of the pair kernel and the one-SM kernel's wide variant
@@ -1140,15 +1145,11 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, i
 
 // Pacing counters of the pair kernel: a small pool handed out round-robin so that launches
 // in flight on different streams use different counters; each is zeroed on the launch's
-// stream before the launch. TPMLP_PAIR_PACE=0 turns pacing off.
+// stream before the launch. Pacing is on unless tpmlp_set_gemm_variant turned it off.
 __device__ unsigned int g_pace_counters[64];
 
 unsigned int* next_pace_counter() {
-  static const bool on = [] {
-    const char* v = std::getenv("TPMLP_PAIR_PACE");
-    return !(v && v[0] == '0');
-  }();
-  if (!on) return nullptr;
+  if (!g_pair_pacing.load(std::memory_order_relaxed)) return nullptr;
   static std::atomic<unsigned int> next{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return nullptr;
@@ -1165,14 +1166,11 @@ unsigned int* next_pace_counter() {
   return base[dev] + (next.fetch_add(1) % 64);
 }
 
-// Tile-order band of the pair kernel (see gemm_bf16_pair_kernel); TPMLP_PAIR_GROUP overrides.
+// Tile-order band of the pair kernel (see gemm_bf16_pair_kernel): PAIR_GROUP_M pair-rows unless
+// tpmlp_set_gemm_variant chose another band.
 int pair_group() {
-  static const int g = [] {
-    const char* v = std::getenv("TPMLP_PAIR_GROUP");
-    const int x = v ? std::atoi(v) : 0;
-    return x != 0 ? x : PAIR_GROUP_M;
-  }();
-  return g;
+  const int g = g_pair_group.load(std::memory_order_relaxed);
+  return g != 0 ? g : PAIR_GROUP_M;
 }
 
 template <bool A_MN, bool B_MN, int EPI>
@@ -1219,14 +1217,8 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, int M, int
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, ep, ctx.status, pair_group(), pace);
 }
 
-// Pair kernel unless TPMLP_GEMM_PAIR=0 (the single-SM kernel then runs every plain GEMM).
-bool use_pair_kernel() {
-  static const bool on = [] {
-    const char* v = std::getenv("TPMLP_GEMM_PAIR");
-    return !(v && v[0] == '0');
-  }();
-  return on;
-}
+// Pair kernel unless tpmlp_set_gemm_variant chose the single-SM kernel for every plain GEMM.
+bool use_pair_kernel() { return g_pair_kernel.load(std::memory_order_relaxed) != 0; }
 
 // 4-D bf16 tensor map over a batched operand: dimension 0 is the contiguous column index; the
 // row index and the two batch indices take dimensions 1..3 in order of increasing stride.
@@ -1264,6 +1256,12 @@ cudaError_t make_tmap_batched(CUtensorMap* map, const BatchedOperand& op, int64_
 }
 
 }  // namespace
+
+void set_gemm_variant(int pair_kernel, int pair_pacing, int pair_group) {
+  g_pair_kernel.store(pair_kernel, std::memory_order_relaxed);
+  g_pair_pacing.store(pair_pacing, std::memory_order_relaxed);
+  g_pair_group.store(pair_group, std::memory_order_relaxed);
+}
 
 cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
                          const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx) {

@@ -199,21 +199,29 @@ size_t colsum_bytes(int64_t n, int64_t d, int64_t m) {
   return round_up(colsum_partials_floats(n, m > d ? m : d) * sizeof(float), 256);
 }
 
+// The backward's checks of dtype, shape and pointers, which come before its workspace check.
+tpmlp_status backward_arg_checks(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
+                                 const void* Y_save, const void* dX, const float* dA, const float* dB, int64_t n,
+                                 int64_t d, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt) {
+  TPMLP_TRY(check_common(gelu, dt));
+  TPMLP_TRY(check_mlp_shape(n, d, m, t, dt));
+  TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
+  TPMLP_TRY(check_ptrs(dt, {{dA, "dA"}, {dB, "dB"}}));
+  if (n > 0)  // token-sized buffers may be NULL when there are no tokens
+    TPMLP_TRY(check_ptrs(dt, {{X, "X"}, {G, "G"}, {Z_save, "Z_save"}, {Y_save, "Y_save"}, {dX, "dX"}}));
+  return TPMLP_OK;
+}
+
 // Backward GEMMs; with dbias1/dbias2 non-null also the bias gradients (column sums of D and G),
 // whose partial sums use the workspace after D.
 tpmlp_status backward_impl(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
                            const void* Y_save, void* dX, float* dA, float* dB, float* dbias1, float* dbias2, int64_t n,
                            int64_t d, int64_t m, int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace,
                            size_t ws_bytes, void* stream, bool accumulate = false) {
-  TPMLP_TRY(check_common(gelu, dt));
-  TPMLP_TRY(check_mlp_shape(n, d, m, t, dt));
-  TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
-  TPMLP_TRY(check_ptrs(dt, {{dA, "dA"}, {dB, "dB"}}));
+  TPMLP_TRY(backward_arg_checks(X, A, B, G, Z_save, Y_save, dX, dA, dB, n, d, m, t, gelu, dt));
   const bool biases = dbias1 != nullptr || dbias2 != nullptr;
   if (biases && !(dbias1 && dbias2)) return fail(TPMLP_ERR_INVALID, "pass both dbias1 and dbias2");
   if (biases) TPMLP_TRY(check_ptrs(TPMLP_F32, {{dbias1, "dbias1"}, {dbias2, "dbias2"}}));
-  if (n > 0)  // token-sized buffers may be NULL when there are no tokens
-    TPMLP_TRY(check_ptrs(dt, {{X, "X"}, {G, "G"}, {Z_save, "Z_save"}, {Y_save, "Y_save"}, {dX, "dX"}}));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n > 0) {
     const size_t need = d_bytes(n, m, dt) + (biases ? colsum_bytes(n, d, m) : 0);
@@ -262,6 +270,15 @@ tpmlp_status backward_impl(const void* X, const void* A, const void* B, const vo
 }
 
 }  // namespace
+
+namespace tpmlp {
+int validate_backward_args(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
+                           const void* Y_save, const void* dX, const float* dA, const float* dB, int64_t n, int64_t d,
+                           int64_t m, int t, int gelu, int dt) {
+  return backward_arg_checks(X, A, B, G, Z_save, Y_save, dX, dA, dB, n, d, m, t, static_cast<tpmlp_gelu>(gelu),
+                             static_cast<tpmlp_dtype>(dt));
+}
+}  // namespace tpmlp
 
 extern "C" {
 
@@ -653,6 +670,15 @@ tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shard
                                      static_cast<float>(1.0 / (1.0 - p_drop)), seed, b, s, h, t,
                                      dt == TPMLP_BF16, static_cast<cudaStream_t>(stream), ctx.num_sms, ctx.status),
              "dropout+residual");
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_set_gemm_variant(int pair_kernel, int pair_pacing, int pair_group) {
+  if ((pair_kernel != 0 && pair_kernel != 1) || (pair_pacing != 0 && pair_pacing != 1))
+    return fail(TPMLP_ERR_INVALID, "pair_kernel and pair_pacing must be 0 or 1 (got %d, %d)", pair_kernel, pair_pacing);
+  if (pair_group < -4096 || pair_group > 4096)
+    return fail(TPMLP_ERR_INVALID, "pair_group must lie in [-4096, 4096], got %d", pair_group);
+  set_gemm_variant(pair_kernel, pair_pacing, pair_group);
   return TPMLP_OK;
 }
 

@@ -100,6 +100,15 @@ cudaError_t get_device_ctx(DeviceCtx* ctx);
 // Sets the calling thread's tpmlp_last_error() message; returns `status`.
 int report_error(int status, const char* msg);
 
+// tpmlp_backward's checks of dtype, shape and pointers (everything before its workspace check);
+// returns a tpmlp_status and sets the last-error message as tpmlp_backward would.
+int validate_backward_args(const void* X, const void* A, const void* B, const void* G, const void* Z_save,
+                           const void* Y_save, const void* dX, const float* dA, const float* dB, int64_t n, int64_t d,
+                           int64_t m, int t, int gelu, int dt);
+
+// Selects the kernel of later plain bf16 GEMMs (validated by tpmlp_set_gemm_variant).
+void set_gemm_variant(int pair_kernel, int pair_pacing, int pair_group);
+
 // bf16 tensor-core GEMM (tcgen05 + TMA). C = Aop(M x K) * Bop(K x N), fp32 accumulation.
 cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, const Operand& b, EpiKind epi,
                          const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx);

@@ -29,7 +29,10 @@ std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once per device
-// (the host-side name of a __device__ array is only a stand-in for it).
+// (the host-side name of a __device__ array is only a stand-in for it). The address is cached
+// by device number for the life of the process, so the array must stay where the first lookup
+// found it: a cudaDeviceReset, or a context other than the device's primary one, is not
+// supported (the library's per-device status word is cached the same way).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -53,6 +56,10 @@ extern "C" tpmlp_status tpmlp_backward_noalloc(const void* X, const void* A, con
                                                const void* Z_save, const void* Y_save, void* dX, float* dA,
                                                float* dB, int64_t n, int64_t d, int64_t m, int t,
                                                tpmlp_gelu gelu, tpmlp_dtype dt, void* stream) {
+  // The same argument checks as tpmlp_backward first, so that both entry points report the same
+  // status for the same bad arguments; only then the size of D against the scratch array.
+  const int st = tpmlp::validate_backward_args(X, A, B, G, Z_save, Y_save, dX, dA, dB, n, d, m, t, gelu, dt);
+  if (st != TPMLP_OK) return static_cast<tpmlp_status>(st);
   const size_t need = tpmlp_backward_workspace_size(n, m, dt);
   if (need > kScratchBytes) {
     char msg[200];

@@ -118,6 +118,27 @@ def test_backward_validation(lib):
     assert lib.tpmlp_backward_workspace_size(0, 1024, BF16) == 0
 
 
+def test_backward_noalloc_validation(lib):
+    # The no-allocation backward keeps D in a 64 MiB static array. Everything below is rejected on
+    # the host before any device work, so fake pointers are safe here; the accepted edge case
+    # (exactly 64 MiB) runs on the GPU in test_zz_no_alloc.py.
+    def noalloc(n, d=64, m=4096, t=8, dt=BF16, Z=FAKE):
+        args = [FAKE] * 4 + [Z] + [FAKE] * 4
+        return lib.tpmlp_backward_noalloc(*args, n, d, m, t, TANH, dt, None)
+
+    assert noalloc(8193) == WORKSPACE                 # bf16: one row past 8192 x 4096 x 2 bytes
+    assert b"static scratch" in lib.tpmlp_last_error()
+    assert noalloc(4097, dt=F32) == WORKSPACE         # fp32 D takes twice the bytes per element
+    assert noalloc(16384, d=8192, m=32768) == WORKSPACE
+    # Bad arguments get tpmlp_backward's status even when D would not fit either.
+    assert noalloc(1 << 20, m=4100, t=8) == SHAPE     # m % t
+    assert lib.tpmlp_backward(*([FAKE] * 9), 1 << 20, 64, 4100, 8, TANH, BF16, FAKE, 1 << 40, None) == SHAPE
+    assert noalloc(1 << 20, d=-1) == SHAPE
+    assert noalloc(1 << 20, Z=None) == INVALID
+    assert noalloc(1 << 20, Z=FAKE + 8) == ALIGN
+    assert noalloc(1 << 20, dt=9) == DTYPE
+
+
 def sp(lib, t=4, s=64, h=256, m=512, p=0.1, mask=FAKE, ws=FAKE, wsb=1 << 30, rs=0, eps=1e-5):
     return lib.tpmlp_sp_block(FAKE, FAKE, FAKE, eps, FAKE, FAKE, p, 0, FAKE, mask, None, None, 2, s, h, m, t, TANH,
                               BF16, rs, ws, wsb, None)
@@ -198,3 +219,20 @@ def test_rmsnorm_validation(lib):
 
 def test_last_error_never_null(lib):
     assert isinstance(lib.tpmlp_last_error(), bytes)
+
+
+def test_gemm_variant_validation(lib):
+    # Only this call selects the GEMM kernel (no environment variable does); it touches no device.
+    assert lib.tpmlp_set_gemm_variant(2, 1, 0) == INVALID
+    assert lib.tpmlp_set_gemm_variant(1, -1, 0) == INVALID
+    assert lib.tpmlp_set_gemm_variant(1, 1, 5000) == INVALID
+    assert lib.tpmlp_set_gemm_variant(0, 0, -4) == OK
+    assert lib.tpmlp_set_gemm_variant(1, 1, 0) == OK  # back to the defaults
+
+
+def test_library_reads_no_environment_switch():
+    # The shipped library's behaviour must not depend on the caller's environment.
+    srcdir = os.path.join(ROOT, "tensor_transformer_mlp_gb300", "csrc")
+    for name in os.listdir(srcdir):
+        text = open(os.path.join(srcdir, name)).read()
+        assert "getenv" not in text, name

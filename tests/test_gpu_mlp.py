@@ -2,8 +2,6 @@
 the float64 oracle, element by element on seeded inputs; sampled rows and columns at the
 full sizes the benchmark runs."""
 import os
-import subprocess
-import sys
 
 import numpy as np
 import pytest
@@ -18,6 +16,20 @@ from helpers import TOL_BF16, TOL_F32, assert_close, dev, host
 pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_example_seed0.txt")
+
+# The plain bf16 GEMMs' kernel variants (tpmlp_set_gemm_variant): the default SM-pair kernel,
+# the one-SM kernel, and the pair kernel without pacing. The parity cases that take the
+# `gemm_variant` fixture run on each.
+GEMM_VARIANTS = {"pair": (1, 1, 0), "one_sm": (0, 1, 0), "unpaced": (1, 0, 0)}
+
+
+@pytest.fixture(params=list(GEMM_VARIANTS))
+def gemm_variant(request):
+    tp.tpmlp_set_gemm_variant(*GEMM_VARIANTS[request.param])
+    try:
+        yield request.param
+    finally:
+        tp.tpmlp_set_gemm_variant(*GEMM_VARIANTS["pair"])
 
 
 def run_gpu(inp, t, gelu, dtype):
@@ -61,14 +73,14 @@ def test_worked_example_f32():
         assert_close("golden " + k, host(got[k]), gold[k], TOL_F32)
 
 
-def test_single_block_bf16():
+def test_single_block_bf16(gemm_variant):
     cfg = wl.SINGLE_BLOCK
     check_full(wl.mlp_inputs(cfg), cfg.t, cfg.gelu, "bf16", TOL_BF16)
 
 
 @pytest.mark.parametrize("gelu", ["erf", "tanh"])
 @pytest.mark.parametrize("shape", [(300, 200, 392, 7), (129, 72, 264, 3), (1, 8, 8, 1), (517, 1032, 776, 8)])
-def test_ragged_bf16(shape, gelu):
+def test_ragged_bf16(shape, gelu, gemm_variant):
     n, d, m, t = shape
     cfg = wl.MLPConfig("ragged", n, d, m, t, "bf16", gelu, 1.0, 0.05, 1.0, seed=n)
     check_full(wl.mlp_inputs(cfg), t, gelu, "bf16", TOL_BF16)
@@ -82,7 +94,7 @@ def test_ragged_f32(shape, gelu):
     check_full(wl.mlp_inputs(cfg), t, gelu, "f32", TOL_F32)
 
 
-def test_shard_count_does_not_change_results():
+def test_shard_count_does_not_change_results(gemm_variant):
     # On one GPU the shard sum is the GEMM's K-loop, in shard order for every t.
     cfg = wl.MLPConfig("t-invariance", 256, 512, 1024, 1, "bf16", "tanh", 1.0, 0.02, 1.0)
     inp = wl.mlp_inputs(cfg)
@@ -91,6 +103,56 @@ def test_shard_count_does_not_change_results():
         other = run_gpu(inp, t, "tanh", "bf16")
         for k in base:
             assert torch.equal(base[k], other[k]), (t, k)
+
+
+def _backward_keeping_d(X, A, B, G, Z, Y, t, gelu):
+    """tpmlp_backward with a caller workspace, returning D = (G B^T) * gelu'(Z) as the
+    workspace holds it ([n][m] in the operand dtype) beside dX, dA, dB."""
+    n, d = X.shape
+    m = A.shape[1]
+    ws = torch.empty(tp.tpmlp_backward_workspace_size(n, m, X.dtype), dtype=torch.uint8, device="cuda")
+    dX = torch.empty_like(X)
+    dA = torch.empty((d, m), dtype=torch.float32, device="cuda")
+    dB = torch.empty((m, d), dtype=torch.float32, device="cuda")
+    tp.tpmlp_backward(X, A, B, G, Z, Y, dX, dA, dB, t, gelu, ws)
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    D = ws[: n * m * X.element_size()].view(X.dtype).view(n, m)
+    return D, dX, dA, dB
+
+
+@pytest.mark.parametrize("dtype,tol,shape,gelu", [
+    ("bf16", TOL_BF16, (512, 1024, 4096, 2), "tanh"),
+    ("bf16", TOL_BF16, (300, 200, 392, 7), "erf"),
+    ("bf16", TOL_BF16, (129, 72, 264, 3), "tanh"),
+    ("bf16", TOL_BF16, (517, 1032, 776, 8), "erf"),
+    ("f32", TOL_F32, (37, 45, 66, 3), "tanh"),
+    ("f32", TOL_F32, (130, 70, 140, 2), "erf"),
+])
+def test_dgrad1_output_d(shape, gelu, dtype, tol):
+    """D = (G B^T) * gelu'(Z), the dgrad-1 GEMM's output ("024 | Megatron-LM", section 二, the D_i
+    equation), compared element by element with the oracle's D (not only through dA and dX)."""
+    n, d, m, t = shape
+    cfg = wl.MLPConfig("d-direct", n, d, m, t, dtype, gelu, 1.0, 0.05, 1.0, seed=n + 3)
+    inp = wl.mlp_inputs(cfg)
+    X, A, B, G = (dev(inp[k], dtype) for k in "XABG")
+    O, Z, Y = tp.forward(X, A, B, t, gelu)
+    D, _, _, _ = _backward_keeping_d(X, A, B, G, Z, Y, t, gelu)
+    ref = omlp.backward(inp["X"], inp["A"], inp["B"], inp["G"], gelu)["D"]
+    print(assert_close("D", host(D), ref, tol))
+
+
+@pytest.mark.parametrize("cfg", [wl.GPT_MLP, wl.LARGE_MLP], ids=lambda c: c.name)
+def test_dgrad1_output_d_sampled(cfg):
+    """D at the full GPT and large MLP sizes on sampled intermediate columns: column j of D needs
+    only A[:, j] and B[j, :]."""
+    inp = wl.mlp_inputs(cfg)
+    X, A, B, G = (dev(inp[k], cfg.dtype) for k in "XABG")
+    O, Z, Y = tp.forward(X, A, B, cfg.t, cfg.gelu)
+    D, _, _, _ = _backward_keeping_d(X, A, B, G, Z, Y, cfg.t, cfg.gelu)
+    J = wl.sample_indices(48, cfg.m, seed=2)
+    ref = omlp.backward(inp["X"], inp["A"][:, J], inp["B"][J, :], inp["G"], cfg.gelu)["D"]
+    print(cfg.name, assert_close("D[:,J]", host(D[:, torch.from_numpy(J).cuda()]), ref, TOL_BF16))
 
 
 def test_empty_tokens():
@@ -136,7 +198,7 @@ def sampled_parity(cfg, n_rows=48, n_cols=48):
     print(cfg.name, report)
 
 
-def test_gpt_mlp_sampled():
+def test_gpt_mlp_sampled(gemm_variant):
     sampled_parity(wl.GPT_MLP)
 
 
@@ -146,7 +208,7 @@ def test_large_mlp_sampled():
 
 @pytest.mark.parametrize("dtype,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
 @pytest.mark.parametrize("shape", [(512, 1024, 4096, 2), (300, 200, 392, 7), (37, 48, 72, 3)])
-def test_biased_block(shape, dtype, tol):
+def test_biased_block(shape, dtype, tol, gemm_variant):
     n, d, m, t = shape
     cfg = wl.MLPConfig("biased", n, d, m, t, dtype, "tanh", 1.0, 0.05, 1.0, seed=n + 7)
     inp = wl.mlp_inputs(cfg)
@@ -169,7 +231,7 @@ def test_biased_block(shape, dtype, tol):
 
 
 @pytest.mark.parametrize("dtype,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
-def test_main_grad_accumulation_over_microbatches(dtype, tol):
+def test_main_grad_accumulation_over_microbatches(dtype, tol, gemm_variant):
     """dA, dB accumulated over three micro-batches (one of them ragged) equal the oracle's
     gradients of the concatenated batch added to the buffers' starting values."""
     cfg = wl.MLPConfig("microbatches", 700, 256, 512, 4, dtype, "tanh", 1.0, 0.05, 1.0, seed=11)
@@ -209,18 +271,6 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     O, _, _ = tp.forward(X, A, B, cfg.t, "tanh")
     torch.cuda.synchronize()
     assert_close("O", host(O), omlp.forward(inp["X"], inp["A"], inp["B"], "tanh")["O"], TOL_BF16)
-
-
-@pytest.mark.parametrize("env", [{"TPMLP_GEMM_PAIR": "0"}, {"TPMLP_PAIR_PACE": "0"}])
-def test_alternative_gemm_paths(env):
-    """The same parity cases on the one-SM GEMM kernel and on the SM-pair kernel without pacing
-    (both chosen once per process, so they run in a child pytest)."""
-    repo = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    child_env = dict(os.environ, **env)
-    cmd = [sys.executable, "-m", "pytest", os.path.join(repo, "tests", "test_gpu_mlp.py"), "-m", "gpu", "-q", "-x",
-           "-k", "ragged_bf16 or single_block or biased or accumulation or shard_count or gpt_mlp_sampled"]
-    r = subprocess.run(cmd, cwd=repo, env=child_env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
 
 
 def test_step_replays_from_a_cuda_graph():

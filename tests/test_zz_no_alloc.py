@@ -3,22 +3,18 @@
 Such a caller (a host that passes only one step's tensors and owns no allocator on the
 device, or code that must not allocate once running) cannot provide the workspace that
 tpmlp_backward wants; this entry point keeps that intermediate in a static device array
-instead. The test calls it through the C ABI twice in a row, on different inputs, and
-compares each result with tpmlp_backward given a torch-allocated workspace. This file is
-named so that pytest collects it last.
+instead. The tests call it through the C ABI and compare every output with tpmlp_backward
+given a torch-allocated workspace: the kernels are the same and deterministic, so the results
+must be bit-identical. The size limit's rejections need no GPU and live in test_abi_host.py.
+This file is named so that pytest collects it last.
 """
-import numpy as np
 import pytest
 import torch
 
 import tensor_transformer_mlp_gb300 as tp
 from tensor_transformer_mlp_gb300 import workloads as wl
 
-from helpers import TOL_BF16, assert_close, host
-
 pytestmark = pytest.mark.gpu
-
-WORKSPACE_ERR = 7
 
 
 def _noalloc(lib, X, A, B, G, Z, Y, dX, dA, dB, t, gelu):
@@ -30,29 +26,49 @@ def _noalloc(lib, X, A, B, G, Z, Y, dX, dA, dB, t, gelu):
                                       torch.cuda.current_stream().cuda_stream)
 
 
+def _check_against_backward(lib, X, A, B, G, t, gelu, label):
+    d, m = A.shape
+    O, Z, Y = tp.forward(X, A, B, t, gelu)
+    ref = tp.backward(X, A, B, G, Z, Y, t, gelu)
+    dX = torch.full_like(X, float("nan"))
+    dA = torch.full((d, m), float("nan"), dtype=torch.float32, device="cuda")
+    dB = torch.full((m, d), float("nan"), dtype=torch.float32, device="cuda")
+    st = _noalloc(lib, X, A, B, G, Z, Y, dX, dA, dB, t, gelu)
+    assert st == 0, lib.tpmlp_last_error()
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    for name, got, want in (("dX", dX, ref[0]), ("dA", dA, ref[1]), ("dB", dB, ref[2])):
+        assert torch.equal(got, want), f"{label} {name}: differs from tpmlp_backward"
+
+
+def _inputs(cfg, seed, dtype):
+    inp = wl.mlp_inputs(cfg, seed=seed)
+    return [torch.from_numpy(inp[k]).cuda().to(dtype) for k in "XABG"]
+
+
 def test_backward_noalloc_matches_backward_on_two_calls():
     lib = tp.load_library()
     cfg = wl.SINGLE_BLOCK  # D is 512 x 4096 bf16 = 4 MiB, inside the static scratch
     for call, seed in enumerate((0, 1)):
-        inp = wl.mlp_inputs(cfg, seed=seed)
-        X, A, B, G = (torch.from_numpy(inp[k]).cuda().to(torch.bfloat16) for k in "XABG")
-        O, Z, Y = tp.forward(X, A, B, cfg.t, cfg.gelu)
-        ref = tp.backward(X, A, B, G, Z, Y, cfg.t, cfg.gelu)
-        dX = torch.full_like(X, float("nan"))
-        dA = torch.full((cfg.d, cfg.m), float("nan"), dtype=torch.float32, device="cuda")
-        dB = torch.full((cfg.m, cfg.d), float("nan"), dtype=torch.float32, device="cuda")
-        st = _noalloc(lib, X, A, B, G, Z, Y, dX, dA, dB, cfg.t, cfg.gelu)
-        assert st == 0, lib.tpmlp_last_error()
-        torch.cuda.synchronize()
-        tp.tpmlp_device_status()
-        for name, got, want in (("dX", dX, ref[0]), ("dA", dA, ref[1]), ("dB", dB, ref[2])):
-            assert_close(f"call {call} {name}", host(got), host(want), TOL_BF16)
+        X, A, B, G = _inputs(cfg, seed, torch.bfloat16)
+        _check_against_backward(lib, X, A, B, G, cfg.t, cfg.gelu, f"call {call}")
 
 
-def test_backward_noalloc_rejects_oversize():
+def test_backward_noalloc_f32():
     lib = tp.load_library()
-    fake = 0x10000  # never dereferenced: the size check runs before anything else
-    n, d, m = 16384, 8192, 32768  # D would be 1 GiB
-    st = lib.tpmlp_backward_noalloc(*([fake] * 9), n, d, m, 8, 1, 1, None)
-    assert st == WORKSPACE_ERR
-    assert b"static scratch" in lib.tpmlp_last_error()
+    cfg = wl.WORKED_EXAMPLE
+    X, A, B, G = _inputs(cfg, 0, torch.float32)
+    _check_against_backward(lib, X, A, B, G, cfg.t, cfg.gelu, "fp32 worked example")
+
+
+def test_backward_noalloc_at_the_size_limit():
+    # n x m x 2 bytes = 8192 x 4096 x 2 = exactly the 64 MiB the static array holds.
+    lib = tp.load_library()
+    n, d, m, t = 8192, 64, 4096, 8
+    g = torch.Generator(device="cpu").manual_seed(3)
+    X = torch.randn(n, d, generator=g).to("cuda", torch.bfloat16)
+    A = (torch.randn(d, m, generator=g) * 0.02).to("cuda", torch.bfloat16)
+    B = (torch.randn(m, d, generator=g) * 0.02).to("cuda", torch.bfloat16)
+    G = (torch.randn(n, d, generator=g) * 0.01).to("cuda", torch.bfloat16)
+    assert lib.tpmlp_backward_workspace_size(n, m, 1) == 64 << 20
+    _check_against_backward(lib, X, A, B, G, t, "tanh", "64 MiB")
