@@ -343,8 +343,21 @@ def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
            for _ in range(sets)]
     sec = timed(lambda i: tp.tpmlp_rmsnorm_backward(xs[i % sets], gamma, cfg.eps, ys[i % sets],
                                                     outs[i % sets], dgs[i % sets], wsr[i % sets], stream), reps)
-    entry("rmsnorm_backward", sec, 3 * N * elt, "read x, dy + write dx (bf16); dgamma partials are small")
-    del full, wsr
+    entry("rmsnorm_backward", sec, 3 * N * elt, "read x, dy + write dx (bf16), with the fixed-order dgamma sum")
+    wsl = [torch.empty(tp.tpmlp_sp_layernorm_backward_workspace_size(b * s, h), dtype=torch.uint8, device=dev)
+           for _ in range(sets)]
+    dbs = [torch.empty(h, dtype=torch.float32, device=dev) for _ in range(sets)]
+    # the SP backward's last step: LayerNorm backward of the shards plus the residual gradient
+    sec = timed(lambda i: tp.tpmlp_sp_layernorm_backward(xs[i % sets], gamma, cfg.eps, ys[i % sets], outs[(i + 1) % sets],
+                                                         outs[i % sets], dgs[i % sets], dbs[i % sets], wsl[i % sets],
+                                                         stream), reps)
+    entry("layernorm_backward", sec, 4 * N * elt,
+          "read x, dy, residual gradient + write dx (bf16), with the fixed-order dgamma / dbeta sums")
+    # the SP backward's first step: dropout backward fused with the gather into token order
+    sec = timed(lambda i: tp.tpmlp_sp_dropout_grad_gather(xs[i % sets], full[i % sets], cfg.p_drop, cfg.seed, stream),
+                reps)
+    entry("dropout_grad_gather", sec, 2 * N * elt, "read dout shards + write token-order gradient (bf16); mask recomputed")
+    del full, wsr, wsl
     parts = torch.randn((t, b * s, h), dtype=torch.float32, device=dev)  # 1 GiB > L2
     sec = timed(lambda i: tp.tpmlp_sp_reduce_scatter(parts, outs[i % sets], stream), max(10, reps // 4))
     entry("reduce_scatter_splitk", sec, t * N * 4 + N * elt, "read t fp32 partials + write shards (bf16)")

@@ -219,7 +219,7 @@ size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, i
  * Inputs as for tpmlp_sp_block, plus Z_save and Y_save ([b*s][m] in dt, token order) written by
  * the forward call with the same arguments. The dropout mask is recomputed from (seed, p_drop).
  * The LayerNorm output and the gathered tokens are recomputed from x (memory-bound), not saved.
- * Requires h <= 4096 and h % 8 == 0 in addition to tpmlp_sp_block's rules.
+ * Requires h <= 8192 and h % 8 == 0 in addition to tpmlp_sp_block's rules.
  */
 tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, const float* beta, float eps,
                                      const void* A, const void* B, double p_drop, uint64_t seed,
@@ -255,12 +255,41 @@ tpmlp_status tpmlp_rmsnorm(const void* x, const float* gamma, float eps, void* y
  *   dx = r * (g - x_hat * mean(g * x_hat))     ([rows][h], dt, overwritten)
  *   dgamma = sum over rows of dy * x_hat       ([h] fp32, overwritten; summed in a fixed order).
  * workspace: device memory of tpmlp_rmsnorm_backward_workspace_size(rows, h) bytes (per-CTA
- * partial sums), 16-byte aligned. Requires h % 8 == 0 and h <= 4096; rows == 0 zeroes dgamma.
+ * partial sums), 16-byte aligned. Requires h % 8 == 0 and h <= 8192; rows == 0 zeroes dgamma.
  */
 size_t tpmlp_rmsnorm_backward_workspace_size(int64_t rows, int64_t h);
 tpmlp_status tpmlp_rmsnorm_backward(const void* x, const float* gamma, float eps, const void* dy, void* dx,
                                     float* dgamma, int64_t rows, int64_t h, tpmlp_dtype dt, void* workspace,
                                     size_t ws_bytes, void* stream);
+
+/*
+ * LayerNorm backward of `rows` rows of width h, with an optional residual gradient (the SP
+ * backward's last step: "Efficient Large-Scale ... Megatron-LM" notes, section 3.5.1; formulas as
+ * in the "Megatron 训练" notes, section "LayerNorm", torch.nn.LayerNorm semantics): with
+ * x_hat = (x - mean) / sqrt(var + eps) (biased variance over the row) and g = dy * gamma,
+ *   dx = dres + (g - mean(g) - x_hat * mean(g * x_hat)) / sqrt(var + eps)   ([rows][h], dt)
+ *   dgamma = sum over rows of dy * x_hat,  dbeta = sum over rows of dy      ([h] fp32, overwritten;
+ *   summed in a fixed order, so the result is deterministic).
+ * x, dy, dres, dx: [rows][h] in dt; dres may be NULL (no residual term); gamma: [h] fp32.
+ * workspace: tpmlp_sp_layernorm_backward_workspace_size(rows, h) bytes (per-CTA partial sums),
+ * 16-byte aligned. Requires h % 8 == 0, h <= 8192, eps > 0, 16-byte aligned pointers.
+ * rows == 0 zeroes dgamma and dbeta.
+ */
+size_t tpmlp_sp_layernorm_backward_workspace_size(int64_t rows, int64_t h);
+tpmlp_status tpmlp_sp_layernorm_backward(const void* x, const float* gamma, float eps, const void* dy,
+                                         const void* dres, void* dx, float* dgamma, float* dbeta,
+                                         int64_t rows, int64_t h, tpmlp_dtype dt,
+                                         void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Dropout backward fused with the backward of g-bar (whose backward is an all-gather; "Megatron-SP
+ * 机制", f/g operator table): dtok [b][s][h] in token order from dout_shards [t][b][s/t][h],
+ *   dtok[k] = keep(k) * dout[k] / (1 - p_drop)   (k the global flat index of the logical [b][s][h]
+ * tensor, the mask recomputed from (seed, p_drop) exactly as tpmlp_sp_block draws it).
+ */
+tpmlp_status tpmlp_sp_dropout_grad_gather(const void* dout_shards, void* dtok, double p_drop, uint64_t seed,
+                                          int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype dt,
+                                          void* stream);
 
 /* g forward, all-gather ("Megatron-SP 机制", f/g operator table): [t][b][s/t][h] -> [b][s][h]. */
 tpmlp_status tpmlp_sp_gather(const void* x_shards, void* x_full,

@@ -34,8 +34,11 @@ from ._binding import (  # noqa: F401
     tpmlp_sp_block_backward,
     tpmlp_sp_block_backward_workspace_size,
     tpmlp_sp_block_workspace_size,
+    tpmlp_sp_dropout_grad_gather,
     tpmlp_sp_dropout_residual,
     tpmlp_sp_gather,
     tpmlp_sp_layernorm,
+    tpmlp_sp_layernorm_backward,
+    tpmlp_sp_layernorm_backward_workspace_size,
     tpmlp_sp_reduce_scatter,
 )

@@ -44,6 +44,9 @@ SIGNATURES = {
     "tpmlp_rmsnorm": (_I, [_P, _P, _F, _P, _I64, _I64, _I, _P]),
     "tpmlp_rmsnorm_backward_workspace_size": (_SZ, [_I64, _I64]),
     "tpmlp_rmsnorm_backward": (_I, [_P, _P, _F, _P, _P, _P, _I64, _I64, _I, _P, _SZ, _P]),
+    "tpmlp_sp_layernorm_backward_workspace_size": (_SZ, [_I64, _I64]),
+    "tpmlp_sp_layernorm_backward": (_I, [_P, _P, _F, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _SZ, _P]),
+    "tpmlp_sp_dropout_grad_gather": (_I, [_P, _P, _D, _U64, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_gather": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_reduce_scatter": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_dropout_residual": (_I, [_P, _P, _P, _P, _D, _U64, _I64, _I64, _I64, _I, _I, _P]),
@@ -258,6 +261,31 @@ def tpmlp_rmsnorm_backward(x, gamma, eps, dy, dx, dgamma, workspace, stream=None
     _cuda(x, gamma, dy, dx, dgamma, workspace)
     _check(load_library().tpmlp_rmsnorm_backward(_ptr(x), _ptr(gamma), eps, _ptr(dy), _ptr(dx), _ptr(dgamma), rows, h,
                                                  _dt(x), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def tpmlp_sp_layernorm_backward_workspace_size(rows: int, h: int) -> int:
+    return load_library().tpmlp_sp_layernorm_backward_workspace_size(rows, h)
+
+
+def tpmlp_sp_layernorm_backward(x, gamma, eps, dy, dres, dx, dgamma, dbeta, workspace, stream=None) -> None:
+    h = x.shape[-1]
+    rows = x.numel() // h
+    assert dy.shape == x.shape and dx.shape == x.shape and gamma.shape == (h,)
+    assert dres is None or (dres.shape == x.shape and dres.dtype == x.dtype)
+    assert dgamma.shape == (h,) and dbeta.shape == (h,) and dgamma.dtype == dbeta.dtype == torch.float32
+    assert workspace.dtype == torch.uint8
+    _cuda(x, gamma, dy, dres, dx, dgamma, dbeta, workspace)
+    _check(load_library().tpmlp_sp_layernorm_backward(_ptr(x), _ptr(gamma), eps, _ptr(dy), _ptr(dres), _ptr(dx),
+                                                      _ptr(dgamma), _ptr(dbeta), rows, h, _dt(x), _ptr(workspace),
+                                                      workspace.numel(), _stream(stream)))
+
+
+def tpmlp_sp_dropout_grad_gather(dout_shards, dtok, p_drop: float, seed: int, stream=None) -> None:
+    t, b, sl, h = dout_shards.shape
+    assert dtok.shape == (b, sl * t, h) and dtok.dtype == dout_shards.dtype
+    _cuda(dout_shards, dtok)
+    _check(load_library().tpmlp_sp_dropout_grad_gather(_ptr(dout_shards), _ptr(dtok), float(p_drop), seed, b, sl * t,
+                                                       h, t, _dt(dout_shards), _stream(stream)))
 
 
 def tpmlp_sp_gather(x_shards, x_full, stream=None) -> None:

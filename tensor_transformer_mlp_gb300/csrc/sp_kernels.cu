@@ -648,300 +648,368 @@ __global__ void __launch_bounds__(128, dropout_min_blocks<T>()) dropout_grad_gat
   }
 }
 
-// LayerNorm backward plus the residual, one CTA per row (persistent over rows):
-//   dx = dout + rstd * (g - mean(g) - x_hat * mean(g * x_hat)),  g = dxn * gamma,
-// with the row statistics recomputed from x in one shifted pass and all four row sums
-// (sum d, sum d^2, sum g, sum g*d with d = x - x_0) reduced together. Each thread owns CH
-// vectors of columns and accumulates dgamma (dxn * x_hat) and dbeta (dxn) for them over its
-// CTA's rows in its own slots of a shared-memory array laid out [2][CH][8][threads] (no two
-// threads share a slot, so no atomics, and a warp's accesses hit 32 consecutive words, so no
-// bank conflicts); the CTA writes them to partials[blockIdx][2][h] for a fixed-order sum.
-constexpr int kLnBwdThreads = 128;
-
-// kRms: RMSNorm's backward, dx = [dout +] rstd * (g - x_hat * mean(g * x_hat)) with
-// x_hat = x * rstd (no shift, no mean, no mean(g) term). dout may be null (no residual).
-template <typename T, int CH, bool kRms = false>
-__global__ void __launch_bounds__(kLnBwdThreads, 4)
-    layernorm_backward_kernel(const T* __restrict__ x, const T* __restrict__ dxn, const T* __restrict__ dout,
-                              const float* __restrict__ gamma, float eps, T* __restrict__ dx,
-                              float* __restrict__ partials, int64_t rows, int h) {
-  __shared__ float4 red[2][kLnBwdThreads / 32];
-  extern __shared__ float acc[];  // [2][CH][8][kLnBwdThreads]: dgamma then dbeta partial sums
-  constexpr int kHalf = CH * 8 * kLnBwdThreads;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  float gam[CH][8];
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const int col = (tid + c * kLnBwdThreads) * 8;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      gam[c][e] = col < h ? gamma[col + e] : 0.f;
-      acc[(c * 8 + e) * kLnBwdThreads + tid] = 0.f;
-      acc[kHalf + (c * 8 + e) * kLnBwdThreads + tid] = 0.f;
-    }
-  }
-  const float inv_h = 1.0f / static_cast<float>(h);
-  int p = 0;
-  for (int64_t R = blockIdx.x; R < rows; R += gridDim.x, p ^= 1) {
-    const T* xr = x + R * h;
-    const T* dr = dxn + R * h;
-    const T* gr = dout ? dout + R * h : nullptr;
-    const float shift = kRms ? 0.f : static_cast<float>(xr[0]);
-    float f[CH][8], dn[CH][8];
-    Vec8<T> gv[CH];  // dout, loaded with x and dxn so that all of the row's reads are in flight at once
-    float s_d = 0.f, s_dd = 0.f, s_g = 0.f, s_gd = 0.f;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (tid + c * kLnBwdThreads) * 8;
-      if (col < h) {
-        Vec8<T> xv, dv;
-        xv.load(xr + col);
-        dv.load(dr + col);
-        if (gr) gv[c].load(gr + col);
-        xv.to_float(f[c]);
-        dv.to_float(dn[c]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = f[c][e] - shift;
-          const float g = dn[c][e] * gam[c][e];
-          if constexpr (!kRms) {
-            s_d += d;
-            s_g += g;
-          }
-          s_dd = fmaf(d, d, s_dd);
-          s_gd = fmaf(g, d, s_gd);
-        }
-      }
-    }
-    if constexpr (!kRms) {
-      s_d = warp_sum(s_d);
-      s_g = warp_sum(s_g);
-    }
-    s_dd = warp_sum(s_dd);
-    s_gd = warp_sum(s_gd);
-    if (lane == 0) red[p][w] = make_float4(s_d, s_dd, s_g, s_gd);
-    __syncthreads();
-    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < kLnBwdThreads / 32; ++k) {
-      const float4 v = red[p][k];
-      t4.x += v.x;
-      t4.y += v.y;
-      t4.z += v.z;
-      t4.w += v.w;
-    }
-    const float md = kRms ? 0.f : t4.x * inv_h;
-    const float rstd = rsqrtf((kRms ? t4.y * inv_h : fmaxf(t4.y * inv_h - md * md, 0.f)) + eps);
-    const float mean_g = kRms ? 0.f : t4.z * inv_h;
-    const float mean_gxh = rstd * (t4.w * inv_h - md * mean_g);  // mean(g * x_hat)
-    T* outr = dx + R * h;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (tid + c * kLnBwdThreads) * 8;
-      if (col < h) {
-        float go[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, o[8];
-        if (gr) gv[c].to_float(go);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xh = (f[c][e] - shift - md) * rstd;
-          const float g = dn[c][e] * gam[c][e];
-          o[e] = go[e] + rstd * (g - mean_g - xh * mean_gxh);
-          const int slot = (c * 8 + e) * kLnBwdThreads + tid;
-          acc[slot] = fmaf(dn[c][e], xh, acc[slot]);
-          acc[kHalf + slot] += dn[c][e];
-        }
-        Vec8<T> ov;
-        ov.from_float(o);
-        ov.store(outr + col);
-      }
-    }
-  }
-  float* pg = partials + static_cast<int64_t>(blockIdx.x) * 2 * h;
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const int col = (tid + c * kLnBwdThreads) * 8;
-    if (col < h) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        pg[col + e] = acc[(c * 8 + e) * kLnBwdThreads + tid];
-        pg[h + col + e] = acc[kHalf + (c * 8 + e) * kLnBwdThreads + tid];
-      }
-    }
-  }
+// Packed fp32 pairs for the elementwise arithmetic of the norm backward: the sm_100-family
+// f32x2 instructions (add, sub, mul, fma on two fp32 lanes, round to nearest) do two elements per
+// issued instruction, with the same per-element rounding as the scalar forms.
+struct F2 {
+  unsigned long long v;
+};
+__device__ __forceinline__ F2 f2_make(float a, float b) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(F2 a) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(a.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+  F2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
 }
 
-// The same backward (LayerNorm, or RMSNorm with kRms) with the row streamed through the
-// bulk-copy ring: thread 0 keeps `stages` rows of x, dxn (and dout when given) in flight, so
-// loads never wait behind the reductions. 256 threads, CH vectors of 8 columns per thread;
-// dgamma / dbeta accumulate in registers and go to partials[blockIdx][2][h] at the end.
-// Needs 16-byte aligned row starts (bulk copies).
-constexpr int kLnBwdStagedThreads = 256;
+// 8 elements of T as four fp32 pairs, and back.
+__device__ __forceinline__ void to_f2(const uint4& u, F2 (&o)[4]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = f2_make(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+__device__ __forceinline__ void to_f2(const float4 (&u)[2], F2 (&o)[4]) {
+  o[0] = f2_make(u[0].x, u[0].y);
+  o[1] = f2_make(u[0].z, u[0].w);
+  o[2] = f2_make(u[1].x, u[1].y);
+  o[3] = f2_make(u[1].z, u[1].w);
+}
+__device__ __forceinline__ void from_f2(const F2 (&o)[4], uint4& u) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = f2_split(o[i]);
+    w[i] = pack_bf16x2(p.x, p.y);
+  }
+  u = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void from_f2(const F2 (&o)[4], float4 (&u)[2]) {
+  const float2 a = f2_split(o[0]), b = f2_split(o[1]), c = f2_split(o[2]), d = f2_split(o[3]);
+  u[0] = make_float4(a.x, a.y, b.x, b.y);
+  u[1] = make_float4(c.x, c.y, d.x, d.y);
+}
 
-template <typename T, int CH, bool kRms>
-__global__ void __launch_bounds__(kLnBwdStagedThreads)
-    norm_backward_staged_kernel(const T* __restrict__ x, const T* __restrict__ dxn, const T* __restrict__ dout,
-                                const float* __restrict__ gamma, float eps, T* __restrict__ dx,
-                                float* __restrict__ partials, int64_t rows, int h, int stages,
-                                unsigned int* status) {
+// One vector of 8 elements as it sits in registers: a uint4 of bf16 pairs, or two float4.
+template <typename T>
+struct Raw8 {
+  uint4 u;
+  __device__ __forceinline__ void load(const T* p) { u = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void store(T* p) const { *reinterpret_cast<uint4*>(p) = u; }
+  __device__ __forceinline__ void unpack(F2 (&o)[4]) const { to_f2(u, o); }
+  __device__ __forceinline__ void pack(const F2 (&o)[4]) { from_f2(o, u); }
+};
+template <>
+struct Raw8<float> {
+  float4 u[2];
+  __device__ __forceinline__ void load(const float* p) {
+    u[0] = reinterpret_cast<const float4*>(p)[0];
+    u[1] = reinterpret_cast<const float4*>(p)[1];
+  }
+  __device__ __forceinline__ void store(float* p) const {
+    reinterpret_cast<float4*>(p)[0] = u[0];
+    reinterpret_cast<float4*>(p)[1] = u[1];
+  }
+  __device__ __forceinline__ void unpack(F2 (&o)[4]) const { to_f2(u, o); }
+  __device__ __forceinline__ void pack(const F2 (&o)[4]) { from_f2(o, u); }
+};
+
+// LayerNorm backward (or RMSNorm's, kRms) with an optional residual gradient dres (kRes), for
+// rows of up to 8192 columns ("Megatron 训练" notes, section "LayerNorm"; the SP backward chain
+// of the "Efficient Large-Scale ... Megatron-LM" notes, section 3.5.1):
+//   LN : dx = dres + rstd * (g - mean(g) - x_hat * mean(g * x_hat)),   x_hat = (x - mu) * rstd
+//   RMS: dx = dres + rstd * (g - x_hat * mean(g * x_hat)),              x_hat = x * rstd
+// with g = dy * gamma; dgamma = sum over rows of dy * x_hat, dbeta = sum over rows of dy.
+// Rows stream through a shared-memory ring of bulk copies (CTA c takes rows c + i * gridDim.x).
+// R rows are processed per step: each of the NT threads owns CH vectors of 8 columns, reads
+// its columns of the R rows out of the ring into registers, adds its share of the row sums
+// (sum d, d^2, g, g*d with d = x - x_0 for LayerNorm; d^2 and g*d for RMSNorm), and the warps'
+// sums meet in shared memory behind one barrier per step; the ring stages are then refilled at
+// once, since the data is in registers. Every warp adds the per-warp sums in the same order
+// (deterministic), the row's coefficients follow, and the second pass writes dx and adds dgamma,
+// dbeta into registers, which go to partials[blockIdx][2][h] at the end for a fixed-order sum
+// (sum_partials_kernel, launched as this grid's programmatic dependent).
+// The elementwise arithmetic runs on fp32 pairs (f32x2). Every wait is bounded; on a timeout the
+// CTA stops after the step's barrier, thread 0 waits (bounded) for its copies and the CTA returns.
+template <typename T, int NT, int CH, int R, bool kRms, bool kRes, int MINB = 0>
+__global__ void __launch_bounds__(NT, MINB)
+    norm_backward_kernel(const T* __restrict__ x, const T* __restrict__ dy, const T* __restrict__ dres,
+                         const float* __restrict__ gamma, float eps, T* __restrict__ dx,
+                         float* __restrict__ partials, int64_t rows, int h, int stages, unsigned int* status) {
+  constexpr int NW = NT / 32;
+  constexpr int NTEN = kRes ? 3 : 2;  // tensors staged per row: x, dy (, dres)
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float4 red[2][kLnBwdStagedThreads / 32];
+  __shared__ float4 red[2][R][NW];
+  __shared__ int s_abort;
   const uint32_t row_bytes = static_cast<uint32_t>(h) * sizeof(T);
-  const uint32_t stage_bytes = (dout ? 3u : 2u) * row_bytes;
+  const uint32_t stage_bytes = NTEN * row_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(stages) * stage_bytes);
   const int64_t nloc = rows_for_cta(rows);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) mbar_init(&full[st], 1);
     fence_mbar_init();
+    s_abort = 0;
   }
   __syncthreads();
   auto issue = [&](int64_t i) {
-    const int64_t R = blockIdx.x + i * gridDim.x;
+    const int64_t row = blockIdx.x + i * gridDim.x;
     const int st = static_cast<int>(i % stages);
     uint8_t* dst = smem + static_cast<size_t>(st) * stage_bytes;
     mbar_arrive_expect_tx(&full[st], stage_bytes);
-    bulk_load(dst, x + R * h, row_bytes, &full[st]);
-    bulk_load(dst + row_bytes, dxn + R * h, row_bytes, &full[st]);
-    if (dout) bulk_load(dst + 2 * row_bytes, dout + R * h, row_bytes, &full[st]);
+    bulk_load(dst, x + row * h, row_bytes, &full[st]);
+    bulk_load(dst + row_bytes, dy + row * h, row_bytes, &full[st]);
+    if constexpr (kRes) bulk_load(dst + 2 * row_bytes, dres + row * h, row_bytes, &full[st]);
   };
+  int64_t issued = nloc < stages ? nloc : stages;  // meaningful in thread 0 only
   if (tid == 0)
-    for (int64_t i = 0; i < nloc && i < stages; ++i) issue(i);
-  float gam[CH][8], accg[CH][8], accb[kRms ? 1 : CH][8];
+    for (int64_t i = 0; i < issued; ++i) issue(i);
+
+  F2 gam[CH][4], accg[CH][4], accb[kRms ? 1 : CH][4];
+  const F2 zero = f2_make(0.f, 0.f);
 #pragma unroll
   for (int c = 0; c < CH; ++c) {
-    const int col = (tid + c * kLnBwdStagedThreads) * 8;
+    const int col = (tid + c * NT) * 8;
+    float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
+    if (col < h) {
+      g0 = *reinterpret_cast<const float4*>(gamma + col);
+      g1 = *reinterpret_cast<const float4*>(gamma + col + 4);
+    }
+    gam[c][0] = f2_make(g0.x, g0.y);
+    gam[c][1] = f2_make(g0.z, g0.w);
+    gam[c][2] = f2_make(g1.x, g1.y);
+    gam[c][3] = f2_make(g1.z, g1.w);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      gam[c][e] = col < h ? gamma[col + e] : 0.f;
-      accg[c][e] = 0.f;
-      if constexpr (!kRms) accb[c][e] = 0.f;
+    for (int e = 0; e < 4; ++e) {
+      accg[c][e] = zero;
+      if constexpr (!kRms) accb[c][e] = zero;
     }
   }
   const float inv_h = 1.0f / static_cast<float>(h);
-  int64_t i = 0;
-  bool aborted = false;
-  for (; i < nloc; ++i) {
-    const int st = static_cast<int>(i % stages);
-    const int p = static_cast<int>(i & 1);
-    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1), status, 23);
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    const T* xs = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes);
-    const T* ds = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes + row_bytes);
-    const T* gs = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes + 2 * row_bytes);
-    const float shift = kRms ? 0.f : static_cast<float>(xs[0]);
-    float f[CH][8], dn[CH][8], go[CH][8];
-    float s_d = 0.f, s_dd = 0.f, s_g = 0.f, s_gd = 0.f;
+
+  int64_t i0 = 0;
+  for (; i0 < nloc; i0 += R) {
+    const int par = static_cast<int>((i0 / R) & 1);
+    Raw8<T> xv[R][CH], dv[R][CH], rv[kRes ? R : 1][CH];
+    float shift[R];
+    float4 part[R];
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (tid + c * kLnBwdStagedThreads) * 8;
-      if (col < h) {
-        Vec8<T> xv, dv;
-        xv.load(xs + col);
-        dv.load(ds + col);
-        xv.to_float(f[c]);
-        dv.to_float(dn[c]);
-        if (dout) {
-          Vec8<T> gv;
-          gv.load(gs + col);
-          gv.to_float(go[c]);
-        } else {
+    for (int j = 0; j < R; ++j) {
+      part[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      shift[j] = 0.f;
+      const int64_t i = i0 + j;
+      if (i >= nloc) continue;  // the same for every thread of the CTA
+      const int st = static_cast<int>(i % stages);
+      if (!mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1), status, 23)) s_abort = 1;
+      const T* xs = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes);
+      const T* ds = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes + row_bytes);
+      if constexpr (!kRms) shift[j] = static_cast<float>(xs[0]);
+      const F2 sh = f2_make(shift[j], shift[j]);
+      F2 s_d = zero, s_dd = zero, s_g = zero, s_gd = zero;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) go[c][e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = f[c][e] - shift;
-          const float g = dn[c][e] * gam[c][e];
-          if constexpr (!kRms) {
-            s_d += d;
-            s_g += g;
+      for (int c = 0; c < CH; ++c) {
+        const int col = (tid + c * NT) * 8;
+        if (col < h) {
+          xv[j][c].load(xs + col);
+          dv[j][c].load(ds + col);
+          if constexpr (kRes) {
+            const T* rs = reinterpret_cast<const T*>(smem + static_cast<size_t>(st) * stage_bytes + 2 * row_bytes);
+            rv[j][c].load(rs + col);
           }
-          s_dd = fmaf(d, d, s_dd);
-          s_gd = fmaf(g, d, s_gd);
+          F2 xf[4], df[4];
+          xv[j][c].unpack(xf);
+          dv[j][c].unpack(df);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const F2 d = kRms ? xf[e] : f2_sub(xf[e], sh);
+            const F2 g = f2_mul(df[e], gam[c][e]);
+            if constexpr (!kRms) {
+              s_d = f2_add(s_d, d);
+              s_g = f2_add(s_g, g);
+            }
+            s_dd = f2_fma(d, d, s_dd);
+            s_gd = f2_fma(g, d, s_gd);
+          }
         }
       }
+      const float2 a = f2_split(s_d), b = f2_split(s_dd), c2 = f2_split(s_g), d2 = f2_split(s_gd);
+      part[j] = make_float4(a.x + a.y, b.x + b.y, c2.x + c2.y, d2.x + d2.y);
     }
-    if constexpr (!kRms) {
-      s_d = warp_sum(s_d);
-      s_g = warp_sum(s_g);
-    }
-    s_dd = warp_sum(s_dd);
-    s_gd = warp_sum(s_gd);
-    if (lane == 0) red[p][w] = make_float4(s_d, s_dd, s_g, s_gd);
-    __syncthreads();  // the row's sums are published, and every thread has read stage st
-    if (tid == 0 && i + stages < nloc) issue(i + stages);
-    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kLnBwdStagedThreads / 32; ++k) {
-      const float4 v = red[p][k];
-      t4.x += v.x;
-      t4.y += v.y;
-      t4.z += v.z;
-      t4.w += v.w;
-    }
-    const float md = kRms ? 0.f : t4.x * inv_h;
-    const float rstd = rsqrtf((kRms ? t4.y * inv_h : fmaxf(t4.y * inv_h - md * md, 0.f)) + eps);
-    const float mean_g = kRms ? 0.f : t4.z * inv_h;
-    const float mean_gxh = rstd * (t4.w * inv_h - md * mean_g);  // mean(g * x_hat)
-    const int64_t R = blockIdx.x + i * gridDim.x;
-    T* outr = dx + R * h;
+    for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (tid + c * kLnBwdStagedThreads) * 8;
-      if (col < h) {
-        float o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xh = (f[c][e] - shift - md) * rstd;
-          const float g = dn[c][e] * gam[c][e];
-          o[e] = go[c][e] + rstd * (g - mean_g - xh * mean_gxh);
-          accg[c][e] = fmaf(dn[c][e], xh, accg[c][e]);
-          if constexpr (!kRms) accb[c][e] += dn[c][e];
+      for (int j = 0; j < R; ++j) {
+        if constexpr (!kRms) {
+          part[j].x += __shfl_xor_sync(0xffffffffu, part[j].x, o);
+          part[j].z += __shfl_xor_sync(0xffffffffu, part[j].z, o);
         }
-        Vec8<T> ov;
-        ov.from_float(o);
-        ov.store(outr + col);
+        part[j].y += __shfl_xor_sync(0xffffffffu, part[j].y, o);
+        part[j].w += __shfl_xor_sync(0xffffffffu, part[j].w, o);
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < R; ++j) red[par][j][w] = part[j];
+    }
+    __syncthreads();  // every thread has its rows' data in registers and the warps' sums are out
+    if (s_abort) break;
+    if (tid == 0) {
+      for (int64_t i = i0; i < i0 + R && i < nloc; ++i)
+        if (i + stages < nloc) {
+          issue(i + stages);
+          issued = i + stages + 1;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int64_t i = i0 + j;
+      if (i >= nloc) continue;
+      // Every warp adds the NW per-warp sums in the same order: lanes k < NW hold sum k, a
+      // butterfly over log2(NW) lanes adds them, lane 0's total is broadcast.
+      float4 v = lane < NW ? red[par][j][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int o = 1; o < NW; o <<= 1) {
+        if constexpr (!kRms) {
+          v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+          v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+        }
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+        v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
+      }
+      float sd = 0.f, sg = 0.f;
+      if constexpr (!kRms) {
+        sd = __shfl_sync(0xffffffffu, v.x, 0);
+        sg = __shfl_sync(0xffffffffu, v.z, 0);
+      }
+      const float sdd = __shfl_sync(0xffffffffu, v.y, 0);
+      const float sgd = __shfl_sync(0xffffffffu, v.w, 0);
+      const float md = sd * inv_h;                                          // mean(x) - x_0 (0 for RMS)
+      const float rstd = rsqrtf((kRms ? sdd * inv_h : fmaxf(sdd * inv_h - md * md, 0.f)) + eps);
+      const float mean_g = sg * inv_h;                                      // 0 for RMS
+      const float mean_gxh = rstd * (sgd * inv_h - md * mean_g);            // mean(g * x_hat)
+      const float nmu_r = -(shift[j] + md) * rstd;                          // x_hat = x * rstd + nmu_r
+      const float k1 = -rstd * mean_gxh * rstd;                             // dx = rstd*g + k1*x + k0 (+ dres)
+      const float k0 = -rstd * mean_g + (-rstd * mean_gxh) * nmu_r;
+      const F2 r2 = f2_make(rstd, rstd), nm2 = f2_make(nmu_r, nmu_r), k1_2 = f2_make(k1, k1),
+               k0_2 = f2_make(k0, k0);
+      T* outr = dx + (blockIdx.x + i * gridDim.x) * h;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int col = (tid + c * NT) * 8;
+        if (col < h) {
+          F2 xf[4], df[4], o[4];
+          xv[j][c].unpack(xf);
+          dv[j][c].unpack(df);
+          F2 rf[4];
+          if constexpr (kRes) rv[j][c].unpack(rf);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const F2 xh = f2_fma(xf[e], r2, nm2);
+            accg[c][e] = f2_fma(df[e], xh, accg[c][e]);
+            if constexpr (!kRms) accb[c][e] = f2_add(accb[c][e], df[e]);
+            F2 t = f2_fma(k1_2, xf[e], k0_2);
+            if constexpr (kRes) t = f2_add(t, rf[e]);
+            o[e] = f2_fma(r2, f2_mul(df[e], gam[c][e]), t);
+          }
+          Raw8<T> ov;
+          ov.pack(o);
+          ov.store(outr + col);
+        }
       }
     }
   }
-  if (aborted && tid == 0)
-    for (int64_t k = i; k < nloc && k < i + stages; ++k) mbar_wait(&full[k % stages], (k / stages) & 1, status, 21);
+  // Lets the dependent partial-sum grid be scheduled; it still waits for this grid to complete.
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (s_abort && tid == 0) {
+    // Copies that may still be in flight: the rows of the step that gave up and every row
+    // issued after them (each is the next phase of its own stage).
+    for (int64_t k = i0; k < issued; ++k) mbar_wait(&full[k % stages], (k / stages) & 1, status, 21);
+  }
   float* pg = partials + static_cast<int64_t>(blockIdx.x) * 2 * h;
 #pragma unroll
   for (int c = 0; c < CH; ++c) {
-    const int col = (tid + c * kLnBwdStagedThreads) * 8;
+    const int col = (tid + c * NT) * 8;
     if (col < h) {
+      float2 gq[4], bq[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        pg[col + e] = accg[c][e];
-        pg[h + col + e] = kRms ? 0.f : accb[kRms ? 0 : c][e];
+      for (int e = 0; e < 4; ++e) {
+        gq[e] = f2_split(accg[c][e]);
+        bq[e] = kRms ? make_float2(0.f, 0.f) : f2_split(accb[kRms ? 0 : c][e]);
       }
+      reinterpret_cast<float4*>(pg + col)[0] = make_float4(gq[0].x, gq[0].y, gq[1].x, gq[1].y);
+      reinterpret_cast<float4*>(pg + col)[1] = make_float4(gq[2].x, gq[2].y, gq[3].x, gq[3].y);
+      reinterpret_cast<float4*>(pg + h + col)[0] = make_float4(bq[0].x, bq[0].y, bq[1].x, bq[1].y);
+      reinterpret_cast<float4*>(pg + h + col)[1] = make_float4(bq[2].x, bq[2].y, bq[3].x, bq[3].y);
     }
   }
+
 }
 
-// dgamma[c] = sum over CTAs of partials[k][0][c], dbeta likewise. A CTA takes 32 of the 2h
-// columns; thread (g, c) adds partials g, g+8, g+16, ... of its column, and the 8 group sums are
-// then added in group order, so the result does not depend on scheduling.
-__global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restrict__ partials, int nparts, int h,
-                                                           float* __restrict__ dgamma, float* __restrict__ dbeta) {
-  __shared__ float grp[8][32];
-  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
-  const int c = blockIdx.x * 32 + lane;
-  float acc = 0.f;
-  if (c < 2 * h)
-    for (int k = g; k < nparts; k += 8) acc += partials[static_cast<int64_t>(k) * 2 * h + c];
-  grp[g][lane] = acc;
-  __syncthreads();
-  if (g == 0 && c < 2 * h) {
-    float t = 0.f;
+// dgamma[c] = sum over CTAs k of partials[k][0][c], dbeta[c] likewise from partials[k][1][c]. A
+// CTA of 1024 threads takes 64 columns: thread (g, q) adds the float4 of columns 4q..4q+3 over
+// partials g, g + 64, g + 128, ... (all of them in flight for up to 512 partials); the 64 group
+// sums are then added by a fixed pairwise tree, so the result does not depend on scheduling.
+// With dbeta null only the dgamma half is read. Launched as a programmatic dependent of the norm
+// backward kernel, it waits (griddepcontrol.wait) for that grid's completion and memory first.
+constexpr int kSumPartialsThreads = 1024;
+__global__ void __launch_bounds__(kSumPartialsThreads)
+    sum_partials_kernel(const float* __restrict__ partials, int nparts, int h, float* __restrict__ dgamma,
+                        float* __restrict__ dbeta) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float4 grp[64][16];
+  const int q = threadIdx.x & 15, g = threadIdx.x >> 4;
+  const int ncols = dbeta ? 2 * h : h;
+  const int c = blockIdx.x * 64 + q * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c < ncols) {
+    const float* p = partials + c;
+#pragma unroll 8
+    for (int k = g; k < nparts; k += 64) {
+      const float4 v = *reinterpret_cast<const float4*>(p + static_cast<int64_t>(k) * 2 * h);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+  }
+  grp[g][q] = acc;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t += grp[k][lane];
-    if (c < h) dgamma[c] = t;
-    else if (dbeta) dbeta[c - h] = t;
+  for (int half = 32; half > 0; half >>= 1) {
+    __syncthreads();
+    if (g < half) {
+      const float4 o = grp[g + half][q];
+      acc.x += o.x;
+      acc.y += o.y;
+      acc.z += o.z;
+      acc.w += o.w;
+      grp[g][q] = acc;
+    }
+  }
+  if (g == 0 && c < ncols) {
+    if (c < h) *reinterpret_cast<float4*>(dgamma + c) = acc;
+    else *reinterpret_cast<float4*>(dbeta + (c - h)) = acc;
   }
 }
 
@@ -1252,89 +1320,93 @@ cudaError_t launch_column_sums(const void* M, int64_t rows, int64_t cols, bool b
   return cudaGetLastError();
 }
 
-// One resident wave: as many CTAs as fit on the SMs at once (by registers and shared memory),
-// so no CTA waits for another to finish; at most kLnBwdMaxCtas (the partials' capacity).
-template <typename KERN>
-int layernorm_backward_grid(KERN kernel, size_t smem, int64_t rows, int num_sms) {
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared memory a norm_backward_kernel CTA may fill with ring stages.
+constexpr size_t kNormBwdSmemBudget = 200 * 1024;
+
+// One launch of norm_backward_kernel with `stages` ring stages; the grid is one resident wave (as
+// many CTAs as fit on the SMs at once), at most kLnBwdMaxCtas (the partials' capacity). Then the
+// partial sums, as a programmatic dependent launch: its CTAs may be scheduled while the norm
+// kernel's last CTAs finish, and wait in griddepcontrol.wait for that grid to complete.
+template <typename T, int NT, int CH, int R, bool kRms, bool kRes, int MINB = 0>
+cudaError_t launch_norm_bwd(const void* x, const void* dy, const void* dres, const float* gamma, float eps, void* dx,
+                            float* partials, float* dgamma, float* dbeta, int64_t rows, int h, int stages,
+                            int num_sms, cudaStream_t stream, unsigned int* status) {
+  auto k = norm_backward_kernel<T, NT, CH, R, kRms, kRes, MINB>;
+  const size_t stage_bytes = (kRes ? 3 : 2) * static_cast<size_t>(h) * sizeof(T);
+  const size_t smem = staged_smem(stage_bytes, stages);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   int per_sm = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kLnBwdThreads, smem) != cudaSuccess || per_sm < 1)
-    per_sm = 1;
-  const int g = rows_grid(rows, num_sms, per_sm);
-  return g < kLnBwdMaxCtas ? g : kLnBwdMaxCtas;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, NT, smem) != cudaSuccess || per_sm < 1) per_sm = 1;
+  int grid = rows_grid(rows, num_sms, per_sm);
+  grid = grid < kLnBwdMaxCtas ? grid : kLnBwdMaxCtas;
+  k<<<grid, NT, smem, stream>>>(static_cast<const T*>(x), static_cast<const T*>(dy), static_cast<const T*>(dres),
+                                gamma, eps, static_cast<T*>(dx), partials, rows, h, stages, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int ncols = dbeta ? 2 * h : h;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((ncols + 63) / 64), 1, 1);
+  cfg.blockDim = dim3(kSumPartialsThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sum_partials_kernel, static_cast<const float*>(partials), grid, h, dgamma, dbeta);
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Threads per CTA and vectors per thread by width: at most 16 columns per thread, at least 128
+// threads; one row per step; three ring stages per CTA (or fewer for wide fp32 rows), so that
+// two or three CTAs share an SM.
+template <typename T, bool kRms, bool kRes>
+cudaError_t launch_norm_bwd_for_width(const void* x, const void* dy, const void* dres, const float* gamma, float eps,
+                                      void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int h,
+                                      int num_sms, cudaStream_t stream, unsigned int* status) {
+  const size_t stage_bytes = (kRes ? 3 : 2) * static_cast<size_t>(h) * sizeof(T);
+  int stages = static_cast<int>(kNormBwdSmemBudget / (stage_bytes + sizeof(uint64_t)));
+  stages = stages > 3 ? 3 : stages;  // >= 2: a stage holds at most 3 x 8192 x 4 bytes = 96 KiB
+  if (h <= 1024)
+    return launch_norm_bwd<T, 128, 1, 1, kRms, kRes>(x, dy, dres, gamma, eps, dx, partials, dgamma, dbeta, rows, h,
+                                                     stages, num_sms, stream, status);
+  if (h <= 2048)
+    return launch_norm_bwd<T, 128, 2, 1, kRms, kRes>(x, dy, dres, gamma, eps, dx, partials, dgamma, dbeta, rows, h,
+                                                     stages, num_sms, stream, status);
+  if (h <= 4096)
+    return launch_norm_bwd<T, 256, 2, 1, kRms, kRes>(x, dy, dres, gamma, eps, dx, partials, dgamma, dbeta, rows, h,
+                                                     stages, num_sms, stream, status);
+  return launch_norm_bwd<T, 512, 2, 1, kRms, kRes>(x, dy, dres, gamma, eps, dx, partials, dgamma, dbeta, rows, h,
+                                                   stages, num_sms, stream, status);
+}
 
 cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,
                                       bool bf16, cudaStream_t stream, int num_sms, bool rms, unsigned int* status) {
   if (rows <= 0) return cudaSuccess;
-  const size_t elt = bf16 ? 2 : 4;
-  const size_t stage_bytes = (dout ? 3 : 2) * static_cast<size_t>(h) * elt;
-  const bool staged = h % 8 == 0 && h <= kLnBwdStagedThreads * 8 * 2 && aligned16(x) && aligned16(dxn) &&
-                      (!dout || aligned16(dout)) && 2 * stage_bytes + 16 <= kStagedSmemMax;
-  if (staged) {
-    int stages = static_cast<int>(kStagedSmemMax / (stage_bytes + sizeof(uint64_t)));
-    stages = stages > 4 ? 4 : stages;
-    const size_t smem = staged_smem(stage_bytes, stages);
-    const int ch = static_cast<int>((h / 8 + kLnBwdStagedThreads - 1) / kLnBwdStagedThreads);
-    int grid = 0;
-#define TPMLP_NBS(TYPE, CHN)                                                                                       \
-  do {                                                                                                             \
-    auto k = rms ? norm_backward_staged_kernel<TYPE, CHN, true> : norm_backward_staged_kernel<TYPE, CHN, false>;   \
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);               \
-    if (e != cudaSuccess) return e;                                                                                \
-    int per_sm = 1;                                                                                                \
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kLnBwdStagedThreads, smem) != cudaSuccess ||     \
-        per_sm < 1)                                                                                                \
-      per_sm = 1;                                                                                                  \
-    grid = rows_grid(rows, num_sms, per_sm);                                                                       \
-    grid = grid < kLnBwdMaxCtas ? grid : kLnBwdMaxCtas;                                                            \
-    k<<<grid, kLnBwdStagedThreads, smem, stream>>>(static_cast<const TYPE*>(x), static_cast<const TYPE*>(dxn),     \
-                                                   static_cast<const TYPE*>(dout), gamma, eps, static_cast<TYPE*>(dx), \
-                                                   partials, rows, static_cast<int>(h), stages, status);          \
-  } while (0)
-    if (bf16) {
-      if (ch <= 1) TPMLP_NBS(__nv_bfloat16, 1);
-      else TPMLP_NBS(__nv_bfloat16, 2);
-    } else {
-      if (ch <= 1) TPMLP_NBS(float, 1);
-      else TPMLP_NBS(float, 2);
-    }
-#undef TPMLP_NBS
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int hb = static_cast<int>((2 * h + 31) / 32);
-    sum_partials_kernel<<<hb, 256, 0, stream>>>(partials, grid, static_cast<int>(h), dgamma, dbeta);
-    return cudaGetLastError();
-  }
-  if (h % 8 != 0 || h > kLnBwdThreads * 8 * 4) return cudaErrorInvalidValue;
-  const int ch = static_cast<int>((h / 8 + kLnBwdThreads - 1) / kLnBwdThreads);
-  const size_t acc_bytes = 2 * static_cast<size_t>(ch) * 8 * kLnBwdThreads * sizeof(float);  // <= 32 KiB
-  int grid = 0;
-#define TPMLP_LNB(TYPE, CHN)                                                                                     \
-  do {                                                                                                           \
-    auto k = rms ? layernorm_backward_kernel<TYPE, CHN, true> : layernorm_backward_kernel<TYPE, CHN, false>;    \
-    grid = layernorm_backward_grid(k, acc_bytes, rows, num_sms);                                                 \
-    k<<<grid, kLnBwdThreads, acc_bytes, stream>>>(static_cast<const TYPE*>(x), static_cast<const TYPE*>(dxn),    \
-                                                  static_cast<const TYPE*>(dout), gamma, eps,                   \
-                                                  static_cast<TYPE*>(dx), partials, rows, static_cast<int>(h)); \
-  } while (0)
+  if (h % 8 != 0 || h > kNormBwdMaxH || !aligned16(x) || !aligned16(dxn) || !aligned16(dx) ||
+      (dout && !aligned16(dout)) || (rms && dout) || (!rms && !dbeta) || !aligned16(dgamma) ||
+      (dbeta && !aligned16(dbeta)))
+    return cudaErrorInvalidValue;
+  const int hi = static_cast<int>(h);
   if (bf16) {
-    if (ch <= 1) TPMLP_LNB(__nv_bfloat16, 1);
-    else if (ch <= 2) TPMLP_LNB(__nv_bfloat16, 2);
-    else TPMLP_LNB(__nv_bfloat16, 4);
-  } else {
-    if (ch <= 1) TPMLP_LNB(float, 1);
-    else if (ch <= 2) TPMLP_LNB(float, 2);
-    else TPMLP_LNB(float, 4);
+    using T = __nv_bfloat16;
+    if (rms) return launch_norm_bwd_for_width<T, true, false>(x, dxn, nullptr, gamma, eps, dx, partials, dgamma,
+                                                              nullptr, rows, hi, num_sms, stream, status);
+    if (dout) return launch_norm_bwd_for_width<T, false, true>(x, dxn, dout, gamma, eps, dx, partials, dgamma, dbeta,
+                                                               rows, hi, num_sms, stream, status);
+    return launch_norm_bwd_for_width<T, false, false>(x, dxn, nullptr, gamma, eps, dx, partials, dgamma, dbeta, rows,
+                                                      hi, num_sms, stream, status);
   }
-#undef TPMLP_LNB
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int hb = static_cast<int>((2 * h + 31) / 32);
-  sum_partials_kernel<<<hb, 256, 0, stream>>>(partials, grid, static_cast<int>(h), dgamma, dbeta);
-  return cudaGetLastError();
+  using T = float;
+  if (rms) return launch_norm_bwd_for_width<T, true, false>(x, dxn, nullptr, gamma, eps, dx, partials, dgamma, nullptr,
+                                                            rows, hi, num_sms, stream, status);
+  if (dout) return launch_norm_bwd_for_width<T, false, true>(x, dxn, dout, gamma, eps, dx, partials, dgamma, dbeta,
+                                                             rows, hi, num_sms, stream, status);
+  return launch_norm_bwd_for_width<T, false, false>(x, dxn, nullptr, gamma, eps, dx, partials, dgamma, dbeta, rows, hi,
+                                                    num_sms, stream, status);
 }
 
 cudaError_t launch_softmax_combine(const void* stats, int nparts, void* rowstats, int64_t rows, cudaStream_t stream,

@@ -482,7 +482,8 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
   TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
   TPMLP_TRY(check_mlp_shape(b * s, h, m, t, dt));
   TPMLP_TRY(check_dropout(p_drop));
-  if (h > 4096) return fail(TPMLP_ERR_SHAPE, "sp_block_backward supports h <= 4096 (h=%lld)", (long long)h);
+  if (h > kNormBwdMaxH)
+    return fail(TPMLP_ERR_SHAPE, "sp_block_backward supports h <= %d (h=%lld)", kNormBwdMaxH, (long long)h);
   if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
   TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
   TPMLP_TRY(check_ptrs(TPMLP_BF16, {{gamma, "gamma"}, {beta, "beta"}, {dgamma, "dgamma"}, {dbeta, "dbeta"},
@@ -602,8 +603,9 @@ tpmlp_status tpmlp_rmsnorm_backward(const void* x, const float* gamma, float eps
                                     size_t ws_bytes, void* stream) {
   if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
   if (rows < 0 || h < 1) return fail(TPMLP_ERR_SHAPE, "need rows >= 0 and h >= 1");
-  if (h % 8 != 0 || h > 4096)
-    return fail(TPMLP_ERR_SHAPE, "rmsnorm_backward needs h %% 8 == 0 and h <= 4096 (h=%lld)", (long long)h);
+  if (h % 8 != 0 || h > kNormBwdMaxH)
+    return fail(TPMLP_ERR_SHAPE, "rmsnorm_backward needs h %% 8 == 0 and h <= %d (h=%lld)", kNormBwdMaxH,
+                (long long)h);
   if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
   if (!gamma || !dgamma) return fail(TPMLP_ERR_INVALID, "null pointer");
   if (rows > 0 && (!x || !dy || !dx)) return fail(TPMLP_ERR_INVALID, "null pointer");
@@ -623,6 +625,58 @@ tpmlp_status tpmlp_rmsnorm_backward(const void* x, const float* gamma, float eps
   TPMLP_CUDA(launch_layernorm_backward(x, dy, nullptr, gamma, eps, dx, static_cast<float*>(workspace), dgamma, nullptr,
                                        rows, h, dt == TPMLP_BF16, st, ctx.num_sms, true, ctx.status),
              "rmsnorm backward");
+  return TPMLP_OK;
+}
+
+size_t tpmlp_sp_layernorm_backward_workspace_size(int64_t rows, int64_t h) {
+  return tpmlp_rmsnorm_backward_workspace_size(rows, h);
+}
+
+tpmlp_status tpmlp_sp_layernorm_backward(const void* x, const float* gamma, float eps, const void* dy,
+                                         const void* dres, void* dx, float* dgamma, float* dbeta, int64_t rows,
+                                         int64_t h, tpmlp_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  if (rows < 0 || h < 1) return fail(TPMLP_ERR_SHAPE, "need rows >= 0 and h >= 1");
+  if (h % 8 != 0 || h > kNormBwdMaxH)
+    return fail(TPMLP_ERR_SHAPE, "layernorm_backward needs h %% 8 == 0 and h <= %d (h=%lld)", kNormBwdMaxH,
+                (long long)h);
+  if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
+  if (!gamma || !dgamma || !dbeta) return fail(TPMLP_ERR_INVALID, "null pointer");
+  if (rows > 0 && (!x || !dy || !dx)) return fail(TPMLP_ERR_INVALID, "null pointer");
+  if (rows > 0) TPMLP_TRY(check_ptrs(TPMLP_BF16, {{x, "x"}, {dy, "dy"}, {dx, "dx"}}));
+  if (rows > 0 && dres) TPMLP_TRY(check_ptrs(TPMLP_BF16, {{dres, "dres"}}));
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{gamma, "gamma"}, {dgamma, "dgamma"}, {dbeta, "dbeta"}}));
+  const size_t need = tpmlp_sp_layernorm_backward_workspace_size(rows, h);
+  if (rows > 0 && (!workspace || ws_bytes < need))
+    return fail(TPMLP_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? ws_bytes : 0);
+  if (rows > 0) TPMLP_TRY(check_ptrs(TPMLP_BF16, {{workspace, "workspace"}}));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {  // empty sums
+    TPMLP_CUDA(cudaMemsetAsync(dgamma, 0, static_cast<size_t>(h) * sizeof(float), st), "zero dgamma");
+    TPMLP_CUDA(cudaMemsetAsync(dbeta, 0, static_cast<size_t>(h) * sizeof(float), st), "zero dbeta");
+    return TPMLP_OK;
+  }
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  TPMLP_CUDA(launch_layernorm_backward(x, dy, dres, gamma, eps, dx, static_cast<float*>(workspace), dgamma, dbeta,
+                                       rows, h, dt == TPMLP_BF16, st, ctx.num_sms, false, ctx.status),
+             "layernorm backward");
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_sp_dropout_grad_gather(const void* dout_shards, void* dtok, double p_drop, uint64_t seed,
+                                          int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype dt, void* stream) {
+  if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
+  TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
+  TPMLP_TRY(check_dropout(p_drop));
+  if (b * s == 0) return TPMLP_OK;
+  TPMLP_TRY(check_ptrs(TPMLP_BF16, {{dout_shards, "dout_shards"}, {dtok, "dtok"}}));
+  DeviceCtx ctx;
+  TPMLP_CUDA(get_device_ctx(&ctx), "device context");
+  TPMLP_CUDA(launch_dropout_grad_gather(dout_shards, dtok, drop_threshold(p_drop),
+                                        static_cast<float>(1.0 / (1.0 - p_drop)), seed, b, s, h, t,
+                                        dt == TPMLP_BF16, static_cast<cudaStream_t>(stream), ctx.num_sms),
+             "dropout backward + gather");
   return TPMLP_OK;
 }
 

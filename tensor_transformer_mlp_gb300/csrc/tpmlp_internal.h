@@ -151,6 +151,7 @@ cudaError_t launch_column_sums(const void* M, int64_t rows, int64_t cols, bool b
 // backward plus the residual with per-CTA dgamma/dbeta partials ([grid][2][h] fp32, at most
 // kLnBwdMaxCtas CTAs) summed in CTA order.
 constexpr int kLnBwdMaxCtas = 1024;
+constexpr int kNormBwdMaxH = 8192;  // widest row the LayerNorm / RMSNorm backward takes
 cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint64_t threshold, float scale,
                                        uint64_t seed, int64_t b, int64_t s, int64_t h, int t, bool bf16,
                                        cudaStream_t stream, int num_sms);

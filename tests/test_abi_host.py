@@ -167,7 +167,7 @@ def test_sp_block_backward_validation(lib):
         return lib.tpmlp_sp_block_backward(FAKE, FAKE, FAKE, 1e-5, FAKE, FAKE, p, 0, Z, FAKE, FAKE, FAKE, FAKE, FAKE,
                                            FAKE, FAKE, 2, 64, h, 512, t, TANH, BF16, ws, wsb, None)
     assert bwd(t=1) == SHAPE
-    assert bwd(h=8192) == SHAPE
+    assert bwd(h=8200) == SHAPE                    # widths up to 8192
     assert bwd(p=1.0) == INVALID
     assert bwd(Z=None) == INVALID
     assert bwd(ws=None) == WORKSPACE
@@ -211,7 +211,19 @@ def test_rmsnorm_validation(lib):
     need = lib.tpmlp_rmsnorm_backward_workspace_size(4, 256)
     assert need >= 2 * 256 * 4
     P = [FAKE] * 2
-    assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 8192, BF16, FAKE, 1 << 30, None) == SHAPE
+    assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 8200, BF16, FAKE, 1 << 30, None) == SHAPE
+    # the LayerNorm backward step: same width rule, workspace, null and alignment checks
+    lnb = lib.tpmlp_sp_layernorm_backward
+    need = lib.tpmlp_sp_layernorm_backward_workspace_size(4, 256)
+    assert lnb(FAKE, FAKE, 1e-5, FAKE, None, FAKE, FAKE, FAKE, 4, 8200, BF16, FAKE, 1 << 30, None) == SHAPE
+    assert lnb(FAKE, FAKE, 1e-5, FAKE, None, FAKE, FAKE, None, 4, 256, BF16, FAKE, need, None) == INVALID
+    assert lnb(FAKE, FAKE, 1e-5, FAKE, FAKE + 8, FAKE, FAKE, FAKE, 4, 256, BF16, FAKE, need, None) == ALIGN
+    assert lnb(FAKE, FAKE, 1e-5, FAKE, None, FAKE, FAKE, FAKE, 4, 256, BF16, FAKE, need - 1, None) == WORKSPACE
+    assert lnb(FAKE, FAKE, 0.0, FAKE, None, FAKE, FAKE, FAKE, 4, 256, BF16, FAKE, need, None) == INVALID
+    dgg = lib.tpmlp_sp_dropout_grad_gather
+    assert dgg(FAKE, FAKE, 1.0, 0, 2, 64, 256, 4, BF16, None) == INVALID       # p outside [0, 1)
+    assert dgg(FAKE, FAKE, 0.1, 0, 2, 66, 256, 4, BF16, None) == SHAPE         # s % t
+    assert dgg(FAKE, None, 0.1, 0, 2, 64, 256, 4, BF16, None) == INVALID
     assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, None, 4, 256, BF16, FAKE, need, None) == INVALID
     assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 256, BF16, FAKE, need - 1, None) == WORKSPACE
     assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 256, 7, FAKE, need, None) == DTYPE

@@ -48,7 +48,19 @@ def test_rmsnorm_parity(rows, h, dtype):
 
 def test_rmsnorm_large_eps_and_width_8192():
     _check(64, 256, "bf16", 1e-1)
-    _check(257, 8192, "bf16", 1e-5, backward=False)   # forward supports h up to 8192 in bf16
+    _check(257, 8192, "bf16", 1e-5)   # forward and backward take h up to 8192 in bf16
+
+
+def test_rmsnorm_backward_width_8192_f32():
+    inp = wl.norm_inputs(33, 8192, "f32", seed=4)
+    x, dy = dev(inp["x"], "f32"), dev(inp["dy"], "f32")
+    gamma = torch.from_numpy(inp["gamma"]).cuda()
+    dx, dgamma = tp.rmsnorm_backward(x, gamma, dy, 1e-5)
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    ref_dx, ref_dg = orms.rmsnorm_backward(inp["x"], inp["gamma"], 1e-5, inp["dy"])
+    assert_close("dx", host(dx), ref_dx, TOL_F32)
+    assert_close("dgamma", host(dgamma), ref_dg, TOL_F32)
 
 
 def test_rmsnorm_empty_batch():

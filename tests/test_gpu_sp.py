@@ -307,3 +307,85 @@ def test_sp_block_crafted_seeds(which):
     ref = osp.sp_block(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop, cfg.seed, cfg.gelu)
     assert np.array_equal(mask_words(mask), osp.pack_mask_bits(ref["dropped"]))
     assert_close("out", wl.from_shards(host(out).reshape(t, b, s // t, h)), ref["out"], TOL_BF16)
+
+
+# ---------------------------------------------------------------- SP backward steps as separate calls
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("rows,h,residual", [(1, 8, True), (37, 256, False), (300, 1008, True), (129, 4096, True),
+                                             (65, 8192, True), (33, 8192, False)])
+def test_layernorm_backward_step(rows, h, residual, dtype):
+    """tpmlp_sp_layernorm_backward against the oracle's LayerNorm backward plus the residual
+    gradient, element by element, up to the large MLP's width h = 8192."""
+    inp = wl.norm_inputs(rows, h, dtype, seed=rows + h)
+    rng = np.random.default_rng(h)
+    dres = rng.standard_normal((rows, h)).astype(np.float32)
+    dres = wl.round_to_bf16(dres) if dtype == "bf16" else dres
+    x, dy = dev(inp["x"], dtype), dev(inp["dy"], dtype)
+    dres_d = dev(dres, dtype) if residual else None
+    gamma = torch.from_numpy(inp["gamma"]).cuda()
+    dx = torch.empty_like(x)
+    dg = torch.empty(h, dtype=torch.float32, device="cuda")
+    db = torch.empty(h, dtype=torch.float32, device="cuda")
+    ws = torch.empty(tp.tpmlp_sp_layernorm_backward_workspace_size(rows, h), dtype=torch.uint8, device="cuda")
+    tp.tpmlp_sp_layernorm_backward(x, gamma, 1e-5, dy, dres_d, dx, dg, db, ws)
+    torch.cuda.synchronize()
+    tp.tpmlp_device_status()
+    ref_dx, ref_dg, ref_db = osp.layernorm_backward(inp["x"], inp["gamma"], 1e-5, inp["dy"])
+    if residual:
+        ref_dx = ref_dx + dres
+    tol = TOL_BF16 if dtype == "bf16" else TOL_F32
+    rep = {}
+    assert_close("dx", host(dx), ref_dx, tol, rep)
+    assert_close("dgamma", host(dg), ref_dg, tol, rep)
+    assert_close("dbeta", host(db), ref_db, tol, rep)
+    print(rows, h, dtype, rep)
+
+
+def test_layernorm_backward_step_empty():
+    h = 64
+    x = torch.empty((0, h), dtype=torch.bfloat16, device="cuda")
+    gamma = torch.ones(h, dtype=torch.float32, device="cuda")
+    dg = torch.full((h,), 7.0, device="cuda")
+    db = torch.full((h,), 7.0, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    tp.tpmlp_sp_layernorm_backward(x, gamma, 1e-5, x, None, x, dg, db, ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dg) == 0 and torch.count_nonzero(db) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("p", [0.0, 0.1, 0.5])
+def test_dropout_grad_gather_step(p, dtype):
+    """Dropout backward fused with the gather into token order: kept elements scaled by
+    1/(1-p), dropped ones zero, the mask drawn exactly as the forward draws it."""
+    t, b, sl, h = 4, 2, 48, 264
+    rng = np.random.default_rng(31)
+    g = rng.standard_normal((t, b, sl, h)).astype(np.float32)
+    g = wl.round_to_bf16(g) if dtype == "bf16" else g
+    gd = dev(g, dtype)
+    dtok = torch.empty((b, sl * t, h), dtype=gd.dtype, device="cuda")
+    tp.tpmlp_sp_dropout_grad_gather(gd, dtok, p, 4321)
+    torch.cuda.synchronize()
+    gl = wl.from_shards(g)
+    flat = np.arange(gl.size, dtype=np.uint64).reshape(gl.shape)
+    keep = ~osp.drop_mask(flat, 4321, p)
+    ref = np.where(keep, gl.astype(np.float64) / (1.0 - p), 0.0)
+    got = host(dtok)
+    assert np.all(got[~keep] == 0)
+    assert_close("dtok", got, ref, TOL_BF16 if dtype == "bf16" else TOL_F32)
+
+
+def test_sp_block_backward_width_8192():
+    """The SP block backward at the large MLP's width h = 8192 (few tokens), against the full
+    float64 oracle."""
+    b, s, h, m, t = 1, 64, 8192, 1024, 4
+    cfg = wl.SPConfig("sp-bwd-8192", b, s, h, m, t, "tanh", 1.0, 0.02, p_drop=0.1, seed=5)
+    inp, G, out, (dx, dgamma, dbeta, dA, dB) = sp_backward_case(cfg)
+    ref = osp.sp_block_backward(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop,
+                                cfg.seed, cfg.gelu, G)
+    rep = {}
+    assert_close("dx", wl.from_shards(host(dx).reshape(t, b, s // t, h)), ref["dx"], TOL_BF16, rep)
+    for k, got in (("dgamma", dgamma), ("dbeta", dbeta), ("dA", dA), ("dB", dB)):
+        assert_close(k, host(got), ref[k], TOL_BF16, rep)
+    print(rep)
