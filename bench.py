@@ -353,10 +353,17 @@ def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
                                                          stream), reps)
     entry("layernorm_backward", sec, 4 * N * elt,
           "read x, dy, residual gradient + write dx (bf16), with the fixed-order dgamma / dbeta sums")
-    # the SP backward's first step: dropout backward fused with the gather into token order
+    # the SP backward's first step: dropout backward fused with the gather into token order, reading
+    # the forward's mask bits (the masks written by the dropout + residual timing above) ...
+    sec = timed(lambda i: tp.tpmlp_sp_dropout_grad_gather(xs[i % sets], full[i % sets], cfg.p_drop, cfg.seed, stream,
+                                                          mask_bits=masks[i % sets]), reps)
+    entry("dropout_grad_gather", sec, 2 * N * elt + N // 8,
+          "read dout shards + mask bits + write token-order gradient (bf16)")
+    # ... or recomputing the mask from the seed
     sec = timed(lambda i: tp.tpmlp_sp_dropout_grad_gather(xs[i % sets], full[i % sets], cfg.p_drop, cfg.seed, stream),
                 reps)
-    entry("dropout_grad_gather", sec, 2 * N * elt, "read dout shards + write token-order gradient (bf16); mask recomputed")
+    entry("dropout_grad_gather_recompute", sec, 2 * N * elt,
+          "read dout shards + write token-order gradient (bf16); mask recomputed from the seed")
     del full, wsr, wsl
     parts = torch.randn((t, b * s, h), dtype=torch.float32, device=dev)  # 1 GiB > L2
     sec = timed(lambda i: tp.tpmlp_sp_reduce_scatter(parts, outs[i % sets], stream), max(10, reps // 4))
@@ -376,7 +383,7 @@ def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
     Zs = torch.empty((b * s, m), dtype=bf, device=dev)
     Ys = torch.empty((b * s, m), dtype=bf, device=dev)
     ws = torch.empty(tp.tpmlp_sp_block_workspace_size(b, s, h, m, t, bf, "fused"), dtype=torch.uint8, device=dev)
-    tp.tpmlp_sp_block(x0, gamma, beta, cfg.eps, A, B, cfg.p_drop, cfg.seed, out, None, t, cfg.gelu, "fused", ws,
+    tp.tpmlp_sp_block(x0, gamma, beta, cfg.eps, A, B, cfg.p_drop, cfg.seed, out, mask, t, cfg.gelu, "fused", ws,
                       stream, Zs, Ys)
     del ws
     dout = torch.randn_like(x0)
@@ -387,9 +394,11 @@ def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
     dB = torch.empty((m, h), dtype=torch.float32, device=dev)
     wsb = torch.empty(tp.tpmlp_sp_block_backward_workspace_size(b, s, h, m, t, bf), dtype=torch.uint8, device=dev)
     sec = timed(lambda i: tp.tpmlp_sp_block_backward(x0, gamma, beta, cfg.eps, A, B, cfg.p_drop, cfg.seed, Zs, Ys,
-                                                     dout, dx, dgam, dbet, dA, dB, t, cfg.gelu, wsb, stream), 10)
+                                                     dout, dx, dgam, dbet, dA, dB, t, cfg.gelu, wsb, stream,
+                                                     mask_bits=mask), 10)
     res["sp_block_backward"] = {"ms": sec * 1e3, "mlp_tflops": 2 * cfg.flops_mlp_fwd / sec / 1e12,
-                                "note": "whole backward; TFLOP/s counts the four GEMMs' 8*n*h*m only"}
+                                "note": "whole backward, dropout mask read from the forward's mask bits; TFLOP/s "
+                                        "counts the four GEMMs' 8*n*h*m only"}
     tp.tpmlp_device_status(stream)
     return {"workload": cfg.name, "l2": f"{sets} rotating buffer sets per kernel (>= 3 x 128 MiB between reuses)",
             "kernels": res}

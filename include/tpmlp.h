@@ -217,12 +217,15 @@ size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, i
  *   dx_shards = dout + LayerNorm'(x)^T (dl/d LN output)        [t][b][s/t][h] in dt
  *   dgamma, dbeta: [h] fp32 (overwritten)      dA [h][m], dB [m][h]: fp32 (overwritten)
  * Inputs as for tpmlp_sp_block, plus Z_save and Y_save ([b*s][m] in dt, token order) written by
- * the forward call with the same arguments. The dropout mask is recomputed from (seed, p_drop).
+ * the forward call with the same arguments. The dropout mask is read from mask_bits when it is
+ * given (the forward's mask_bits output for the same seed and p_drop; needs h % 32 == 0), else
+ * recomputed from (seed, p_drop); both give the same result.
  * The LayerNorm output and the gathered tokens are recomputed from x (memory-bound), not saved.
  * Requires h <= 8192 and h % 8 == 0 in addition to tpmlp_sp_block's rules.
  */
 tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, const float* beta, float eps,
                                      const void* A, const void* B, double p_drop, uint64_t seed,
+                                     const uint32_t* mask_bits,
                                      const void* Z_save, const void* Y_save, const void* dout_shards,
                                      void* dx_shards, float* dgamma, float* dbeta, float* dA, float* dB,
                                      int64_t b, int64_t s, int64_t h, int64_t m, int t,
@@ -285,9 +288,12 @@ tpmlp_status tpmlp_sp_layernorm_backward(const void* x, const float* gamma, floa
  * Dropout backward fused with the backward of g-bar (whose backward is an all-gather; "Megatron-SP
  * 机制", f/g operator table): dtok [b][s][h] in token order from dout_shards [t][b][s/t][h],
  *   dtok[k] = keep(k) * dout[k] / (1 - p_drop)   (k the global flat index of the logical [b][s][h]
- * tensor, the mask recomputed from (seed, p_drop) exactly as tpmlp_sp_block draws it).
+ * tensor). The mask is read from mask_bits when given (the forward's output for the same seed and
+ * p_drop, layout as for tpmlp_sp_block; needs h % 32 == 0), else recomputed from (seed, p_drop)
+ * exactly as tpmlp_sp_block draws it.
  */
-tpmlp_status tpmlp_sp_dropout_grad_gather(const void* dout_shards, void* dtok, double p_drop, uint64_t seed,
+tpmlp_status tpmlp_sp_dropout_grad_gather(const void* dout_shards, void* dtok, const uint32_t* mask_bits,
+                                          double p_drop, uint64_t seed,
                                           int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype dt,
                                           void* stream);
 

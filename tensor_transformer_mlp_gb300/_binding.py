@@ -38,7 +38,7 @@ SIGNATURES = {
     "tpmlp_sp_block": (_I, [_P, _P, _P, _F, _P, _P, _D, _U64, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _I, _I, _I,
                             _P, _SZ, _P]),
     "tpmlp_sp_block_backward_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I, _I]),
-    "tpmlp_sp_block_backward": (_I, [_P, _P, _P, _F, _P, _P, _D, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+    "tpmlp_sp_block_backward": (_I, [_P, _P, _P, _F, _P, _P, _D, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                                      _I64, _I64, _I, _I, _I, _P, _SZ, _P]),
     "tpmlp_sp_layernorm": (_I, [_P, _P, _P, _F, _P, _I64, _I64, _I, _P]),
     "tpmlp_rmsnorm": (_I, [_P, _P, _F, _P, _I64, _I64, _I, _P]),
@@ -46,7 +46,7 @@ SIGNATURES = {
     "tpmlp_rmsnorm_backward": (_I, [_P, _P, _F, _P, _P, _P, _I64, _I64, _I, _P, _SZ, _P]),
     "tpmlp_sp_layernorm_backward_workspace_size": (_SZ, [_I64, _I64]),
     "tpmlp_sp_layernorm_backward": (_I, [_P, _P, _F, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _SZ, _P]),
-    "tpmlp_sp_dropout_grad_gather": (_I, [_P, _P, _D, _U64, _I64, _I64, _I64, _I, _I, _P]),
+    "tpmlp_sp_dropout_grad_gather": (_I, [_P, _P, _P, _D, _U64, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_gather": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_reduce_scatter": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tpmlp_sp_dropout_residual": (_I, [_P, _P, _P, _P, _D, _U64, _I64, _I64, _I64, _I, _I, _P]),
@@ -218,16 +218,20 @@ def tpmlp_sp_block_backward_workspace_size(b, s, h, m, t, dtype: torch.dtype) ->
 
 
 def tpmlp_sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z_save, Y_save, dout_shards, dx_shards,
-                            dgamma, dbeta, dA, dB, t: int, gelu="tanh", workspace=None, stream=None) -> None:
+                            dgamma, dbeta, dA, dB, t: int, gelu="tanh", workspace=None, stream=None,
+                            mask_bits=None) -> None:
     tt, b, sl, h = x_shards.shape
     m = A.shape[1]
     assert tt == t and dout_shards.shape == x_shards.shape and dx_shards.shape == x_shards.shape
     assert Z_save.shape == (b * sl * t, m) and Y_save.shape == (b * sl * t, m)
     assert dgamma.shape == (h,) and dbeta.shape == (h,) and dA.shape == (h, m) and dB.shape == (m, h)
-    _cuda(x_shards, gamma, beta, A, B, Z_save, Y_save, dout_shards, dx_shards, dgamma, dbeta, dA, dB, workspace)
+    assert mask_bits is None or mask_bits.numel() * 32 >= x_shards.numel()
+    _cuda(x_shards, gamma, beta, A, B, Z_save, Y_save, dout_shards, dx_shards, dgamma, dbeta, dA, dB, workspace,
+          mask_bits)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().tpmlp_sp_block_backward(
-        _ptr(x_shards), _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), p_drop, seed, _ptr(Z_save), _ptr(Y_save),
+        _ptr(x_shards), _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), p_drop, seed, _ptr(mask_bits), _ptr(Z_save),
+        _ptr(Y_save),
         _ptr(dout_shards), _ptr(dx_shards), _ptr(dgamma), _ptr(dbeta), _ptr(dA), _ptr(dB), b, sl * t, h, m, t,
         GELU[gelu], _dt(x_shards), _ptr(workspace), ws_bytes, _stream(stream)))
 
@@ -280,12 +284,13 @@ def tpmlp_sp_layernorm_backward(x, gamma, eps, dy, dres, dx, dgamma, dbeta, work
                                                       workspace.numel(), _stream(stream)))
 
 
-def tpmlp_sp_dropout_grad_gather(dout_shards, dtok, p_drop: float, seed: int, stream=None) -> None:
+def tpmlp_sp_dropout_grad_gather(dout_shards, dtok, p_drop: float, seed: int, stream=None, mask_bits=None) -> None:
     t, b, sl, h = dout_shards.shape
     assert dtok.shape == (b, sl * t, h) and dtok.dtype == dout_shards.dtype
-    _cuda(dout_shards, dtok)
-    _check(load_library().tpmlp_sp_dropout_grad_gather(_ptr(dout_shards), _ptr(dtok), float(p_drop), seed, b, sl * t,
-                                                       h, t, _dt(dout_shards), _stream(stream)))
+    assert mask_bits is None or mask_bits.numel() * 32 >= dout_shards.numel()
+    _cuda(dout_shards, dtok, mask_bits)
+    _check(load_library().tpmlp_sp_dropout_grad_gather(_ptr(dout_shards), _ptr(dtok), _ptr(mask_bits), float(p_drop),
+                                                       seed, b, sl * t, h, t, _dt(dout_shards), _stream(stream)))
 
 
 def tpmlp_sp_gather(x_shards, x_full, stream=None) -> None:
@@ -380,7 +385,7 @@ def sp_block(x_shards, gamma, beta, eps, A, B, p_drop, seed, t: int, gelu="tanh"
 
 
 def sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z, Y, dout_shards, t: int, gelu="tanh",
-                      stream=None):
+                      stream=None, mask_bits=None):
     """Allocate gradients and workspace and run tpmlp_sp_block_backward.
     Returns (dx_shards, dgamma, dbeta, dA, dB)."""
     tt, b, sl, h = x_shards.shape
@@ -394,7 +399,7 @@ def sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z, Y, dout
     ws = torch.empty(max(1, tpmlp_sp_block_backward_workspace_size(b, sl * t, h, m, t, x_shards.dtype)),
                      dtype=torch.uint8, device=dev)
     tpmlp_sp_block_backward(x_shards, gamma, beta, eps, A, B, p_drop, seed, Z, Y, dout_shards, dx, dgamma, dbeta, dA,
-                            dB, t, gelu, ws, stream)
+                            dB, t, gelu, ws, stream, mask_bits)
     return dx, dgamma, dbeta, dA, dB
 
 

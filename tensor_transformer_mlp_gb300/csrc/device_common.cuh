@@ -402,18 +402,22 @@ static __host__ __device__ __noinline__ uint32_t drop_bits8_full(uint64_t base, 
 //    Unless the low word of the first sum lies within 7 of 2^32, no key carries into the high
 //    word, so the eight high words are equal, and so are the high word after the first
 //    xor-shift and its share (high word x low word of the multiplier) of the first product.
+//    If, in addition, adding the last term changes no key's bits 30 and 31 (the low word's low
+//    30 bits are at most 2^30 - 8), the first xor-shift sends the same two bits down for every
+//    key, so the word xor-ed into each key's low word is computed once too.
 //  * The final xor-shift changes the high word only by flipping its bit 0 when its bit 31 is
 //    set. For a threshold below 2^63 (p < 1/2) that changes neither "high word < threshold's
 //    high word" nor equality with it, so high(e), the last product's high word, decides key e:
 //    dropped iff high(e) < thi, unless high(e) == thi (probability 2^-32 per key), when only the
 //    full hash decides.
-// shortcut is false in the carry case and for thresholds of 2^63 and above; a caller then uses
-// hash_below (or drop_bits8_full) for all eight keys, and it does the same on a tie.
+// shortcut is false in the carry case, when a key changes bits 30-31 of the low word (each about
+// one vector in 2^29), and for thresholds of 2^63 and above; a caller then uses hash_below (or
+// drop_bits8_full) for all eight keys, and it does the same on a tie.
 // kLow3 >= 0 promises base & 7 == kLow3 (the seed's low three bits), which makes each key's low
 // word one addition of a constant.
 template <int kLow3 = -1>
 struct DropHash8 {
-  uint32_t klo, low3, hi_in, thi;
+  uint32_t klo, low3, xs30, thi;
   uint64_t hi_product;
   bool shortcut;
 
@@ -422,9 +426,11 @@ struct DropHash8 {
     const uint32_t khi = static_cast<uint32_t>(k >> 32);
     klo = static_cast<uint32_t>(k);
     thi = static_cast<uint32_t>(threshold >> 32);
-    shortcut = klo <= 0xFFFFFFF8u && thi < 0x80000000u;
+    shortcut = klo <= 0xFFFFFFF8u && (klo & 0x3FFFFFFFu) <= 0x3FFFFFF8u && thi < 0x80000000u;
     low3 = kLow3 >= 0 ? static_cast<uint32_t>(kLow3) : static_cast<uint32_t>(base) & 7u;
-    hi_in = khi << 2;  // bits the high word sends down by >> 30
+    // what the first xor-shift brings into every key's low word: the high word's low two bits
+    // and the low word's own bits 30-31
+    xs30 = (khi << 2) ^ (klo >> 30);
     hi_product = static_cast<uint64_t>((khi ^ (khi >> 30)) * static_cast<uint32_t>(kSplitMixMul1)) << 32;
   }
 
@@ -432,7 +438,7 @@ struct DropHash8 {
     const uint32_t m1lo = static_cast<uint32_t>(kSplitMixMul1), m1hi = static_cast<uint32_t>(kSplitMixMul1 >> 32);
     const uint32_t m2lo = static_cast<uint32_t>(kSplitMixMul2), m2hi = static_cast<uint32_t>(kSplitMixMul2 >> 32);
     const uint32_t z0 = klo + (low3 ^ e);
-    const uint32_t l1 = z0 ^ (z0 >> 30) ^ hi_in;                        // low word after xor-shift 30
+    const uint32_t l1 = z0 ^ xs30;                                      // low word after xor-shift 30
     const uint64_t p1 = static_cast<uint64_t>(l1) * m1lo + hi_product;  // first product, minus l1 * m1hi
     const uint32_t a_lo = static_cast<uint32_t>(p1);
     const uint32_t a_hi = static_cast<uint32_t>(p1 >> 32) + l1 * m1hi;

@@ -736,6 +736,35 @@ struct Raw8<float> {
   __device__ __forceinline__ void pack(const F2 (&o)[4]) { from_f2(o, u); }
 };
 
+// The same dropout backward with the forward's mask bits read back instead of recomputed (bit i
+// of word w set iff element 32 w + i of the token-order tensor was dropped; rows of h % 32 == 0
+// columns start on a word): a gather with a bit test, one thread per vector of 8 elements.
+template <typename T>
+__global__ void __launch_bounds__(128) dropout_grad_gather_mask_kernel(const T* __restrict__ dout,
+                                                                       T* __restrict__ dtok,
+                                                                       const uint32_t* __restrict__ mask_bits,
+                                                                       float scale, int64_t rows, int64_t b,
+                                                                       int64_t s, int64_t sl, int h) {
+  const int nvec = h >> 3;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const T* src = dout + token_to_shard_row(r, b, s, sl) * h;
+    T* dst = dtok + r * h;
+    const uint32_t* mrow = mask_bits + ((static_cast<uint64_t>(r) * static_cast<uint64_t>(h)) >> 5);
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      Vec8<T> gv;
+      gv.load(src + v * 8);
+      const uint32_t bits = __ldg(mrow + (v >> 2)) >> ((v & 3) * 8);
+      float gf[8], o[8];
+      gv.to_float(gf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (bits >> e) & 1u ? 0.f : gf[e] * scale;
+      Vec8<T> ov;
+      ov.from_float(o);
+      ov.store(dst + v * 8);
+    }
+  }
+}
+
 // LayerNorm backward (or RMSNorm's, kRms) with an optional residual gradient dres (kRes), for
 // rows of up to 8192 columns ("Megatron 训练" notes, section "LayerNorm"; the SP backward chain
 // of the "Efficient Large-Scale ... Megatron-LM" notes, section 3.5.1):
@@ -1280,13 +1309,24 @@ cudaError_t launch_dropout_residual(const void* x_shards, const void* y_shards, 
   });
 }
 
-cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint64_t threshold, float scale,
-                                       uint64_t seed, int64_t b, int64_t s, int64_t h, int t, bool bf16,
-                                       cudaStream_t stream, int num_sms) {
+cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, const uint32_t* mask_bits,
+                                       uint64_t threshold, float scale, uint64_t seed, int64_t b, int64_t s,
+                                       int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms) {
   const int64_t rows = b * s;
   if (rows <= 0) return cudaSuccess;
-  if (h % 8 != 0) return cudaErrorInvalidValue;
+  if (h % 8 != 0 || (mask_bits && h % 32 != 0)) return cudaErrorInvalidValue;
   const int grid = rows_grid(rows, num_sms, 64);  // one row per CTA up to 64 CTAs per SM
+  if (mask_bits) {
+    if (bf16)
+      dropout_grad_gather_mask_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(dout_shards), static_cast<__nv_bfloat16*>(dtok), mask_bits, scale, rows,
+          b, s, s / t, static_cast<int>(h));
+    else
+      dropout_grad_gather_mask_kernel<float><<<grid, 128, 0, stream>>>(static_cast<const float*>(dout_shards),
+                                                                       static_cast<float*>(dtok), mask_bits, scale,
+                                                                       rows, b, s, s / t, static_cast<int>(h));
+    return cudaGetLastError();
+  }
   return with_seed_low3(seed, [&](auto low3) {
     constexpr int kLow3 = decltype(low3)::value;
     if (bf16)

@@ -473,7 +473,8 @@ size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, i
 }
 
 tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, const float* beta, float eps,
-                                     const void* A, const void* B, double p_drop, uint64_t seed, const void* Z_save,
+                                     const void* A, const void* B, double p_drop, uint64_t seed,
+                                     const uint32_t* mask_bits, const void* Z_save,
                                      const void* Y_save, const void* dout_shards, void* dx_shards, float* dgamma,
                                      float* dbeta, float* dA, float* dB, int64_t b, int64_t s, int64_t h, int64_t m,
                                      int t, tpmlp_gelu gelu, tpmlp_dtype dt, void* workspace, size_t ws_bytes,
@@ -484,6 +485,8 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
   TPMLP_TRY(check_dropout(p_drop));
   if (h > kNormBwdMaxH)
     return fail(TPMLP_ERR_SHAPE, "sp_block_backward supports h <= %d (h=%lld)", kNormBwdMaxH, (long long)h);
+  if (mask_bits && (h % 32 != 0 || !aligned(mask_bits, 4)))
+    return fail(TPMLP_ERR_SHAPE, "mask_bits needs h %% 32 == 0 and 4-byte alignment");
   if (!(eps > 0.0f)) return fail(TPMLP_ERR_INVALID, "eps must be > 0");
   TPMLP_TRY(check_ptrs(dt, {{A, "A"}, {B, "B"}}));
   TPMLP_TRY(check_ptrs(TPMLP_BF16, {{gamma, "gamma"}, {beta, "beta"}, {dgamma, "dgamma"}, {dbeta, "dbeta"},
@@ -522,7 +525,7 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
   // gradient gathered into token order (g-bar's backward).
   TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms, ctx.status), "layernorm");
   TPMLP_CUDA(launch_gather(xn, xg, b, s, h, t, bf16, st, ctx.num_sms), "gather");
-  TPMLP_CUDA(launch_dropout_grad_gather(dout_shards, dtok, drop_threshold(p_drop),
+  TPMLP_CUDA(launch_dropout_grad_gather(dout_shards, dtok, mask_bits, drop_threshold(p_drop),
                                         static_cast<float>(1.0 / (1.0 - p_drop)), seed, b, s, h,
                                         t, bf16, st, ctx.num_sms),
              "dropout backward + gather");
@@ -664,16 +667,19 @@ tpmlp_status tpmlp_sp_layernorm_backward(const void* x, const float* gamma, floa
   return TPMLP_OK;
 }
 
-tpmlp_status tpmlp_sp_dropout_grad_gather(const void* dout_shards, void* dtok, double p_drop, uint64_t seed,
-                                          int64_t b, int64_t s, int64_t h, int t, tpmlp_dtype dt, void* stream) {
+tpmlp_status tpmlp_sp_dropout_grad_gather(const void* dout_shards, void* dtok, const uint32_t* mask_bits,
+                                          double p_drop, uint64_t seed, int64_t b, int64_t s, int64_t h, int t,
+                                          tpmlp_dtype dt, void* stream) {
   if (dt != TPMLP_BF16 && dt != TPMLP_F32) return fail(TPMLP_ERR_DTYPE, "unsupported dtype %d", (int)dt);
   TPMLP_TRY(check_sp_shape(b, s, h, t, dt));
   TPMLP_TRY(check_dropout(p_drop));
+  if (mask_bits && (h % 32 != 0 || !aligned(mask_bits, 4)))
+    return fail(TPMLP_ERR_SHAPE, "mask_bits needs h %% 32 == 0 and 4-byte alignment");
   if (b * s == 0) return TPMLP_OK;
   TPMLP_TRY(check_ptrs(TPMLP_BF16, {{dout_shards, "dout_shards"}, {dtok, "dtok"}}));
   DeviceCtx ctx;
   TPMLP_CUDA(get_device_ctx(&ctx), "device context");
-  TPMLP_CUDA(launch_dropout_grad_gather(dout_shards, dtok, drop_threshold(p_drop),
+  TPMLP_CUDA(launch_dropout_grad_gather(dout_shards, dtok, mask_bits, drop_threshold(p_drop),
                                         static_cast<float>(1.0 / (1.0 - p_drop)), seed, b, s, h, t,
                                         dt == TPMLP_BF16, static_cast<cudaStream_t>(stream), ctx.num_sms),
              "dropout backward + gather");

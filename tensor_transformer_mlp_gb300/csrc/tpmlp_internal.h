@@ -152,9 +152,10 @@ cudaError_t launch_column_sums(const void* M, int64_t rows, int64_t cols, bool b
 // kLnBwdMaxCtas CTAs) summed in CTA order.
 constexpr int kLnBwdMaxCtas = 1024;
 constexpr int kNormBwdMaxH = 8192;  // widest row the LayerNorm / RMSNorm backward takes
-cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, uint64_t threshold, float scale,
-                                       uint64_t seed, int64_t b, int64_t s, int64_t h, int t, bool bf16,
-                                       cudaStream_t stream, int num_sms);
+// mask_bits: the forward's drop bits (read instead of recomputing the hash), or null.
+cudaError_t launch_dropout_grad_gather(const void* dout_shards, void* dtok, const uint32_t* mask_bits,
+                                       uint64_t threshold, float scale, uint64_t seed, int64_t b, int64_t s,
+                                       int64_t h, int t, bool bf16, cudaStream_t stream, int num_sms);
 // rms: RMSNorm's backward (dbeta may be null); dout may be null (no residual term).
 cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void* dout, const float* gamma, float eps,
                                       void* dx, float* partials, float* dgamma, float* dbeta, int64_t rows, int64_t h,

@@ -35,7 +35,7 @@ def test_header_and_binding_agree():
 
 # C parameter and return types of include/tpmlp.h -> the ctypes type the binding must declare.
 _CTYPE = {"const void*": ctypes.c_void_p, "void*": ctypes.c_void_p, "const float*": ctypes.c_void_p,
-          "float*": ctypes.c_void_p, "uint32_t*": ctypes.c_void_p, "int64_t": ctypes.c_int64, "int": ctypes.c_int,
+          "float*": ctypes.c_void_p, "uint32_t*": ctypes.c_void_p, "const uint32_t*": ctypes.c_void_p, "int64_t": ctypes.c_int64, "int": ctypes.c_int,
           "tpmlp_gelu": ctypes.c_int, "tpmlp_dtype": ctypes.c_int, "tpmlp_rs_mode": ctypes.c_int,
           "float": ctypes.c_float, "double": ctypes.c_double, "uint64_t": ctypes.c_uint64, "size_t": ctypes.c_size_t,
           "tpmlp_status": ctypes.c_int, "const char*": ctypes.c_char_p}
@@ -163,13 +163,15 @@ def test_sp_block_validation(lib):
 
 
 def test_sp_block_backward_validation(lib):
-    def bwd(h=256, t=4, ws=FAKE, wsb=1 << 30, p=0.1, Z=FAKE):
-        return lib.tpmlp_sp_block_backward(FAKE, FAKE, FAKE, 1e-5, FAKE, FAKE, p, 0, Z, FAKE, FAKE, FAKE, FAKE, FAKE,
-                                           FAKE, FAKE, 2, 64, h, 512, t, TANH, BF16, ws, wsb, None)
+    def bwd(h=256, t=4, ws=FAKE, wsb=1 << 30, p=0.1, Z=FAKE, mask=None):
+        return lib.tpmlp_sp_block_backward(FAKE, FAKE, FAKE, 1e-5, FAKE, FAKE, p, 0, mask, Z, FAKE, FAKE, FAKE, FAKE,
+                                           FAKE, FAKE, FAKE, 2, 64, h, 512, t, TANH, BF16, ws, wsb, None)
     assert bwd(t=1) == SHAPE
     assert bwd(h=8200) == SHAPE                    # widths up to 8192
     assert bwd(p=1.0) == INVALID
     assert bwd(Z=None) == INVALID
+    assert bwd(h=264, mask=FAKE) == SHAPE           # mask words need h % 32 == 0
+    assert bwd(mask=FAKE + 2) == SHAPE             # 4-byte aligned mask words
     assert bwd(ws=None) == WORKSPACE
     need = lib.tpmlp_sp_block_backward_workspace_size(2, 64, 256, 512, 4, BF16)
     assert need > 0 and bwd(wsb=need - 1) == WORKSPACE
@@ -221,9 +223,10 @@ def test_rmsnorm_validation(lib):
     assert lnb(FAKE, FAKE, 1e-5, FAKE, None, FAKE, FAKE, FAKE, 4, 256, BF16, FAKE, need - 1, None) == WORKSPACE
     assert lnb(FAKE, FAKE, 0.0, FAKE, None, FAKE, FAKE, FAKE, 4, 256, BF16, FAKE, need, None) == INVALID
     dgg = lib.tpmlp_sp_dropout_grad_gather
-    assert dgg(FAKE, FAKE, 1.0, 0, 2, 64, 256, 4, BF16, None) == INVALID       # p outside [0, 1)
-    assert dgg(FAKE, FAKE, 0.1, 0, 2, 66, 256, 4, BF16, None) == SHAPE         # s % t
-    assert dgg(FAKE, None, 0.1, 0, 2, 64, 256, 4, BF16, None) == INVALID
+    assert dgg(FAKE, FAKE, None, 1.0, 0, 2, 64, 256, 4, BF16, None) == INVALID       # p outside [0, 1)
+    assert dgg(FAKE, FAKE, None, 0.1, 0, 2, 66, 256, 4, BF16, None) == SHAPE         # s % t
+    assert dgg(FAKE, None, None, 0.1, 0, 2, 64, 256, 4, BF16, None) == INVALID
+    assert dgg(FAKE, FAKE, FAKE, 0.1, 0, 2, 64, 264, 4, BF16, None) == SHAPE         # mask needs h % 32 == 0
     assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, None, 4, 256, BF16, FAKE, need, None) == INVALID
     assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 256, BF16, FAKE, need - 1, None) == WORKSPACE
     assert lib.tpmlp_rmsnorm_backward(*P, 1e-5, FAKE, FAKE, FAKE, 4, 256, 7, FAKE, need, None) == DTYPE

@@ -2,8 +2,9 @@
 on the CPU.
 
 drop_bits8 decides eight consecutive elements at once and takes a shortcut that is exact only
-outside three rare cases (a carry out of the low word of seed ^ k + gamma, a threshold of 2^63
-or more, and a tie between the last product's high word and the threshold's). Random inputs on
+outside four rare cases (a carry out of the low word of seed ^ k + gamma, a change of that low
+word's bits 30-31 within the eight keys, a threshold of 2^63 or more, and a tie between the last
+product's high word and the threshold's). Random inputs on
 the GPU reach those cases about once in 2^32 keys, so this test compiles the helper as host
 code with nvcc and checks it, bit for bit, against the float64 oracle's splitmix64 on inputs
 built to land in each case, plus random ones. Dropout rule: "Megatron-SP 机制", section on the
@@ -115,6 +116,23 @@ def test_carry_into_high_word(harness):
                 for p in (0.1, 0.3, 0.5):
                     cases.append((base, osp.drop_threshold(p)))
     assert any((((b & ~7) + 0x9E3779B97F4A7C15) & 0xFFFFFFFF) > 0xFFFFFFF8 for b, _ in cases)
+    _check(harness, cases)
+
+
+def test_low_word_crosses_bit_30(harness):
+    # (base & ~7) + gamma has a low word whose low 30 bits lie within 7 of 2^30: some of the
+    # eight keys change bits 30-31 of the low word, which the shared first xor-shift assumes fixed.
+    rng = np.random.default_rng(23)
+    cases = []
+    for hi in (int(x) for x in rng.integers(0, 1 << 32, 8, dtype=np.uint64)):
+        for top2 in range(3):
+            for low30 in range(0x3FFFFFF8, 0x40000000):
+                lo = ((top2 << 30) | low30) - GAMMA_LO
+                for low3 in range(8):
+                    base = (hi << 32) | (lo & 0xFFFFFFF8) | low3
+                    for p in (0.1, 0.4):
+                        cases.append((base, osp.drop_threshold(p)))
+    assert any(((((b & ~7) + 0x9E3779B97F4A7C15) & 0x3FFFFFFF) > 0x3FFFFFF8) for b, _ in cases)
     _check(harness, cases)
 
 

@@ -160,7 +160,7 @@ def test_dropout_residual(p):
 
 # ---------------------------------------------------------------- SP block backward
 
-def sp_backward_case(cfg, dtype="bf16", g_std=1.0):
+def sp_backward_case(cfg, dtype="bf16", g_std=1.0, use_mask=False):
     inp = wl.sp_inputs(cfg)
     t = cfg.t
     G = np.random.default_rng(cfg.seed + 100).standard_normal(inp["x"].shape) * g_std
@@ -172,18 +172,23 @@ def sp_backward_case(cfg, dtype="bf16", g_std=1.0):
     out, mask, (Z, Y) = tp.sp_block(x_d, gam, bet, cfg.eps, A, B, cfg.p_drop, cfg.seed, t, cfg.gelu,
                                     with_mask=cfg.h % 32 == 0, save_for_backward=True)
     dout = dev(wl.to_shards(G, t), dtype)
-    grads = tp.sp_block_backward(x_d, gam, bet, cfg.eps, A, B, cfg.p_drop, cfg.seed, Z, Y, dout, t, cfg.gelu)
+    grads = tp.sp_block_backward(x_d, gam, bet, cfg.eps, A, B, cfg.p_drop, cfg.seed, Z, Y, dout, t, cfg.gelu,
+                                 mask_bits=mask if use_mask else None)
     torch.cuda.synchronize()
     tp.tpmlp_device_status()
     return inp, G, out, grads
 
 
 @pytest.mark.parametrize("dtype,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
-@pytest.mark.parametrize("shape", [(2, 256, 256, 512, 4), (3, 96, 96, 208, 2), (1, 64, 40, 72, 8)])
-def test_sp_block_backward_small(shape, dtype, tol):
+@pytest.mark.parametrize("shape,use_mask", [((2, 256, 256, 512, 4), False), ((2, 256, 256, 512, 4), True),
+                                            ((3, 96, 96, 208, 2), False), ((3, 96, 96, 208, 2), True),
+                                            ((1, 64, 40, 72, 8), False)])
+def test_sp_block_backward_small(shape, use_mask, dtype, tol):
+    """SP block backward against the oracle, with the dropout mask recomputed from the seed or
+    read from the forward's mask bits."""
     b, s, h, m, t = shape
     cfg = wl.SPConfig("sp-bwd", b, s, h, m, t, "tanh", 1.0, 0.05, p_drop=0.2, seed=s + 1, dtype=dtype)
-    inp, G, out, (dx, dgamma, dbeta, dA, dB) = sp_backward_case(cfg, dtype)
+    inp, G, out, (dx, dgamma, dbeta, dA, dB) = sp_backward_case(cfg, dtype, use_mask=use_mask)
     ref = osp.sp_block_backward(inp["x"], inp["gamma"], inp["beta"], cfg.eps, inp["A"], inp["B"], cfg.p_drop,
                                 cfg.seed, cfg.gelu, G)
     rep = {}
@@ -264,17 +269,20 @@ def crafted_seeds():
     'at': element K_AT hashes to exactly T = floor(0.1 * 2^64) = 0x1999999999999A00, so it is
     kept (a threshold taken from p in single precision, 0x199999A000000000, would drop it);
     'below': element K_BELOW hashes to T - 1 and is dropped; both tie T's high word;
-    'carry': the eight keys of the vector at K_CARRY carry out of the low word when gamma is added."""
+    'carry': the eight keys of the vector at K_CARRY carry out of the low word when gamma is added;
+    'cross30': those keys change bits 30-31 of the low word when gamma is added."""
     T = osp.drop_threshold(0.1)
     seeds = {"at": splitmix64_preimage(T) ^ K_AT, "below": splitmix64_preimage(T - 1) ^ K_BELOW,
-             "carry": (0x1234_5678 << 32) | ((0x80B583E8 | 5) ^ K_CARRY)}
+             "carry": (0x1234_5678 << 32) | ((0x80B583E8 | 5) ^ K_CARRY),
+             "cross30": (0x1234_5678 << 32) | ((0x00B583E8 | 5) ^ K_CARRY)}
     assert osp.splitmix64_scalar(seeds["at"] ^ K_AT) == T
     assert osp.splitmix64_scalar(seeds["below"] ^ K_BELOW) == T - 1
     assert (((seeds["carry"] ^ K_CARRY) & ~7) + 0x9E3779B97F4A7C15) & 0xFFFFFFFF > 0xFFFFFFF8
+    assert (((seeds["cross30"] ^ K_CARRY) & ~7) + 0x9E3779B97F4A7C15) & 0x3FFFFFFF > 0x3FFFFFF8
     return seeds
 
 
-@pytest.mark.parametrize("which", ["at", "below", "carry"])
+@pytest.mark.parametrize("which", ["at", "below", "carry", "cross30"])
 def test_dropout_residual_crafted_seeds(which):
     seed = crafted_seeds()[which]
     t, b, sl, h = 4, 2, 32, 256
@@ -298,7 +306,7 @@ def test_dropout_residual_crafted_seeds(which):
                  8e-3)
 
 
-@pytest.mark.parametrize("which", ["at", "below", "carry"])
+@pytest.mark.parametrize("which", ["at", "below", "carry", "cross30"])
 def test_sp_block_crafted_seeds(which):
     # The same seeds through the SP block, whose dropout runs in the FC2 epilogue.
     b, s, h, m, t = 2, 256, 256, 512, 4
@@ -356,19 +364,25 @@ def test_layernorm_backward_step_empty():
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("p", [0.0, 0.1, 0.5])
-def test_dropout_grad_gather_step(p, dtype):
+@pytest.mark.parametrize("mask_in", [False, True], ids=["recomputed", "mask_read"])
+def test_dropout_grad_gather_step(p, dtype, mask_in):
     """Dropout backward fused with the gather into token order: kept elements scaled by
-    1/(1-p), dropped ones zero, the mask drawn exactly as the forward draws it."""
-    t, b, sl, h = 4, 2, 48, 264
+    1/(1-p), dropped ones zero; the mask either drawn exactly as the forward draws it or read
+    from mask bits (here the oracle's, packed in the forward's layout)."""
+    t, b, sl, h = 4, 2, 48, 256 if mask_in else 264
     rng = np.random.default_rng(31)
     g = rng.standard_normal((t, b, sl, h)).astype(np.float32)
     g = wl.round_to_bf16(g) if dtype == "bf16" else g
     gd = dev(g, dtype)
     dtok = torch.empty((b, sl * t, h), dtype=gd.dtype, device="cuda")
-    tp.tpmlp_sp_dropout_grad_gather(gd, dtok, p, 4321)
-    torch.cuda.synchronize()
     gl = wl.from_shards(g)
     flat = np.arange(gl.size, dtype=np.uint64).reshape(gl.shape)
+    mask = None
+    if mask_in:
+        words = osp.pack_mask_bits(osp.drop_mask(flat, 4321, p))
+        mask = torch.from_numpy(words.view(np.int32)).cuda()
+    tp.tpmlp_sp_dropout_grad_gather(gd, dtok, p, 4321, mask_bits=mask)
+    torch.cuda.synchronize()
     keep = ~osp.drop_mask(flat, 4321, p)
     ref = np.where(keep, gl.astype(np.float64) / (1.0 - p), 0.0)
     got = host(dtok)
