@@ -359,11 +359,14 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
  * Kernel choice for the plain bf16 GEMMs of every later call in this process, for comparing
  * kernels and testing each one; a user of the library never needs it, and nothing else
  * (no environment variable) changes the choice. The defaults, 1, 1, 0, are the fast path:
- *   pair_kernel 1: 256 x 256 tiles on clusters of two SMs; 0: 128 x 256 tiles on one SM.
+ *   pair_kernel 1: clusters of two SMs, on 256 x 512 or 256 x 256 tiles per GEMM by a model of
+ *                  the launch's waves; 2: clusters of two SMs on 256 x 256 tiles only; 3: on
+ *                  256 x 512 tiles only; 0: 128 x 256 tiles on one SM.
  *   pair_pacing 1: pairs wait at intervals of 32 k-blocks for the pairs of the same round of
  *                  tiles, which keeps shared operand panels in L2; 0: no pacing.
- *   pair_group  0: the default tile band (8 pair-rows walked along N); g > 0: g pair-rows
- *                  walked along N; g < 0: -g N-blocks walked along M. |g| <= 4096.
+ *   pair_group  0: the default tile band (8 pair-rows walked along N for 256 x 256 tiles, 16
+ *                  for 256 x 512 tiles); g > 0: g pair-rows walked along N; g < 0: -g N-blocks
+ *                  walked along M. |g| <= 4096.
  * The choice is read when a GEMM is launched, so a CUDA graph keeps the one it captured.
  * Every variant computes the same contractions with fp32 accumulation. Errors: TPMLP_ERR_INVALID.
  */

@@ -9,6 +9,8 @@
 // Two persistent kernels, one CTA per SM, sharing the epilogue code:
 //   gemm_bf16_pair_kernel (plain GEMMs): 256 x 256 tiles on clusters of two SMs
 //               (tcgen05 cta_group::2), 6-stage ring of 32 KB per SM, paced pairs
+//   gemm_bf16_wide_kernel (plain GEMMs whose wave count favours it): 256 x 512 tiles on
+//               SM pairs, 4-stage ring of 48 KB per SM, 25 % fewer operand bytes per FLOP
 //   gemm_bf16_kernel (batched GEMMs, or all of them when tpmlp_set_gemm_variant asks): 128 x 256
 //               tiles on one SM with a 4-stage ring of 48 KB, or 128 x 128 tiles with a
 //               6-stage ring of 32 KB for the batched GEMMs whose N is at most 128
@@ -1093,6 +1095,256 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------- wide CTA-pair kernel
+// The pair kernel on 256 x 512 tiles: the pair's MMAs cover the tile's two 256-column halves
+// with two M256 N256 K16 instructions per K16 step that share the A tile, so each SM receives
+// 48 KB of operands per 64-deep k-block (its 128 A rows and two 128-column B chunks) for twice
+// the work of the 256 x 256 pair tile: 25 % fewer operand bytes per FLOP into every SM and out
+// of L2. The two half accumulators take all 512 tensor-memory columns, so there is one
+// accumulator set: the epilogue drains half 0, then half 1, arriving on one empty barrier per
+// half. The next tile's half 0 starts as soon as half 0 is drained and runs ahead over the first
+// WIDE_STAGES k-blocks (their stages stay resident) while half 1 is still being drained; then
+// half 1 catches up on those k-blocks and both halves proceed k-block by k-block.
+//   barriers: full[s] (even CTA), empty[s] (each CTA), tfull (each CTA; multicast commit),
+//   tempty[h] (even CTA; all epilogue threads of both CTAs arrive), drain (even CTA).
+constexpr int WIDE_STAGES = 4;
+constexpr int WIDE_GROUP_M = 16;  // tile band in pair-rows (measured: 16 beats 8 and 32 on the large MLP)
+constexpr int WIDE_BN = 2 * BN;                                 // 512 columns per pair tile
+constexpr int WIDE_CHUNK_BYTES = BN_HALF * BK * 2;              // one 128-column B chunk, 16 KiB
+constexpr int WIDE_STAGE_BYTES = A_STAGE_BYTES + 2 * WIDE_CHUNK_BYTES;  // 48 KiB
+constexpr int WIDE_SMEM_BYTES = WIDE_STAGES * WIDE_STAGE_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;
+static_assert(WIDE_SMEM_BYTES <= 227 * 1024, "shared memory budget (wide pair kernel)");
+static_assert((2 * WIDE_STAGES + 1 + 2 + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area (wide pair kernel)");
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_bf16_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                          int M, int N, int K, EpiParams ep, unsigned int* status, int group,
+                          unsigned int* pace) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* epi_stage = smem + WIDE_STAGES * WIDE_STAGE_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_stage + NUM_EPI_WARPS * EPI_STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + WIDE_STAGES;
+  uint64_t* tfull_bar = empty_bar + WIDE_STAGES;
+  uint64_t* tempty_bar = tfull_bar + 1;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+  const int num_mb = (M + 2 * BM - 1) / (2 * BM);
+  const int num_nb = (N + WIDE_BN - 1) / WIDE_BN;
+  const int num_tiles = num_mb * num_nb;
+  // group > 0: bands of `group` pair-rows walked along N; group < 0: bands of -group N-blocks
+  // walked along M (as in the 256 x 256 pair kernel).
+  auto coords = [&](int tile, int& mb, int& nb) {
+    if (group > 0) {
+      const int group_size = group * num_nb;
+      const int g = tile / group_size;
+      const int first_mb = g * group;
+      const int gsz = min(num_mb - first_mb, group);
+      const int in_group = tile - g * group_size;
+      mb = first_mb + in_group % gsz;
+      nb = in_group / gsz;
+    } else {
+      const int gn = -group;
+      const int group_size = gn * num_mb;
+      const int g = tile / group_size;
+      const int first_nb = g * gn;
+      const int gsz = min(num_nb - first_nb, gn);
+      const int in_group = tile - g * group_size;
+      nb = first_nb + in_group % gsz;
+      mb = in_group / gsz;
+    }
+  };
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (warp == 0 && lane == 0) {
+#pragma unroll
+    for (int s = 0; s < WIDE_STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(&tempty_bar[0], 2 * NUM_EPI_THREADS);
+    mbar_init(&tempty_bar[1], 2 * NUM_EPI_THREADS);
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers initialised in both CTAs before either signals the other
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer (both CTAs)
+      int kiter = 0;
+      bool ok = true;
+      const bool pacer = pace != nullptr && rank == 0;  // pacing as in the 256 x 256 pair kernel
+      unsigned int pace_target = 0;
+      for (int tile = pair, round = 0; tile < num_tiles && ok; tile += num_pairs, ++round) {
+        int mb, nb;
+        coords(tile, mb, nb);
+        const int a_row = mb * 2 * BM + static_cast<int>(rank) * BM;
+        const unsigned int active = static_cast<unsigned int>(min(num_pairs, num_tiles - round * num_pairs));
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (pacer && kb % kPaceKb == 0) {
+            pace_wait(pace, pace_target, kPaceWaitNs);
+            atomicAdd(pace, 1u);
+            pace_target += active;
+          }
+          const int s = kiter % WIDE_STAGES;
+          const uint32_t parity = ((kiter / WIDE_STAGES) & 1) ^ 1;
+          if (!mbar_wait(&empty_bar[s], parity, status, 31)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * WIDE_STAGE_BYTES);
+          const uint32_t full0 = map_to_cta(&full_bar[s], 0);
+          uint8_t* sa = smem + s * WIDE_STAGE_BYTES;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          if constexpr (!A_MN) {
+            tma_load_2d_pair(sa, &tmap_a, full0, kb * BK, a_row);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * MN_BOX_BYTES, &tmap_a, full0, a_row + j * 64, kb * BK);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {  // this CTA's 128 columns of each 256-column half
+            const int b_col = nb * WIDE_BN + h * BN + static_cast<int>(rank) * BN_HALF;
+            uint8_t* sbh = sb + h * WIDE_CHUNK_BYTES;
+            if constexpr (!B_MN) {
+              tma_load_2d_pair(sbh, &tmap_b, full0, kb * BK, b_col);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN_HALF / 64; ++j)
+                tma_load_2d_pair(sbh + j * MN_BOX_BYTES, &tmap_b, full0, b_col + j * 64, kb * BK);
+            }
+          }
+          ++kiter;
+        }
+      }
+      // The even CTA's full barriers count both CTAs' copies: once its last phases have
+      // completed (at once on the normal path), no copy of the pair is still in flight.
+      if (rank == 0)
+        for (int k = max(0, kiter - WIDE_STAGES); k < kiter; ++k)
+          mbar_wait(&full_bar[k % WIDE_STAGES], (k / WIDE_STAGES) & 1, status, 32);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA issuer (even CTA)
+      constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+      // The four K16 MMAs of k-block kb (stage s) into half h of the accumulator.
+      auto issue_half = [&](int s, int kb, int h) {
+        const uint32_t a_base = smem_u32(smem + s * WIDE_STAGE_BYTES);
+        const uint32_t bh = a_base + A_STAGE_BYTES + h * WIDE_CHUNK_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+          const uint64_t adesc = A_MN ? smem_desc_sw128(a_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                      : smem_desc_sw128(a_base + kk * 32, 16, 1024);
+          const uint64_t bdesc = B_MN ? smem_desc_sw128(bh + kk * 2048, MN_BOX_BYTES, 1024)
+                                      : smem_desc_sw128(bh + kk * 32, 16, 1024);
+          umma_bf16_pair(tmem_base + static_cast<uint32_t>(h * BN), adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+      };
+      int kiter = 0, it = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
+        const uint32_t prev = static_cast<uint32_t>(it & 1) ^ 1;  // phase of the previous tile's drain
+        // Half 0 runs ahead over the first `lead` k-blocks, while the epilogue may still be
+        // draining half 1 of the previous tile; those stages stay resident until half 1 has
+        // used them too, then each is freed.
+        const int lead = min(WIDE_STAGES, num_kb);
+        if (!mbar_wait(&tempty_bar[0], prev, status, 34)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < lead; ++kb) {
+          const int k = kiter + kb;
+          if (!mbar_wait(&full_bar[k % WIDE_STAGES], (k / WIDE_STAGES) & 1, status, 33)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_half(k % WIDE_STAGES, kb, 0);
+        }
+        if (!ok) break;
+        if (!mbar_wait(&tempty_bar[1], prev, status, 34)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < lead; ++kb) {
+          const int s = (kiter + kb) % WIDE_STAGES;
+          issue_half(s, kb, 1);
+          umma_commit_pair_mc(&empty_bar[s], 0x3);  // frees stage s in both CTAs
+        }
+        kiter += lead;
+        for (int kb = lead; kb < num_kb; ++kb) {
+          const int s = kiter % WIDE_STAGES;
+          if (!mbar_wait(&full_bar[s], (kiter / WIDE_STAGES) & 1, status, 33)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_half(s, kb, 0);
+          issue_half(s, kb, 1);
+          umma_commit_pair_mc(&empty_bar[s], 0x3);
+          ++kiter;
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(tfull_bar, 0x3);  // both halves of both CTAs' accumulators ready
+      }
+      umma_commit_pair(drain_bar);
+      mbar_wait(drain_bar, 0, status, 35);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int c_begin = ((warp - 2) / 4) * kEpiChunks;
+    int it = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
+      const bool ok = mbar_wait(tfull_bar, static_cast<uint32_t>(it & 1), status, 36);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      int mb, nb;
+      coords(tile, mb, nb);
+      const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * BN);
+        epilogue_tile<EPI, false>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N,
+                                  nb * WIDE_BN + h * BN, c_begin, t_row, 0, 1.f, row, 2 * nb + h, 2 * num_nb);
+        tc_fence_before();
+        mbar_arrive_cluster(map_to_cta(&tempty_bar[h], 0));
+      }
+    }
+  }
+
+  // Neither CTA frees tensor memory or leaves (its barriers are targets of the other's
+  // arrivals) before both are done.
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -1166,11 +1418,12 @@ unsigned int* next_pace_counter() {
   return base[dev] + (next.fetch_add(1) % 64);
 }
 
-// Tile-order band of the pair kernel (see gemm_bf16_pair_kernel): PAIR_GROUP_M pair-rows unless
-// tpmlp_set_gemm_variant chose another band.
-int pair_group() {
+// Tile-order band of the pair kernels (see gemm_bf16_pair_kernel): PAIR_GROUP_M pair-rows for
+// 256 x 256 tiles and WIDE_GROUP_M for 256 x 512 tiles, unless tpmlp_set_gemm_variant chose
+// another band.
+int pair_group(bool wide = false) {
   const int g = g_pair_group.load(std::memory_order_relaxed);
-  return g != 0 ? g : PAIR_GROUP_M;
+  return g != 0 ? g : (wide ? WIDE_GROUP_M : PAIR_GROUP_M);
 }
 
 template <bool A_MN, bool B_MN, int EPI>
@@ -1217,8 +1470,93 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, int M, int
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, ep, ctx.status, pair_group(), pace);
 }
 
-// Pair kernel unless tpmlp_set_gemm_variant chose the single-SM kernel for every plain GEMM.
-bool use_pair_kernel() { return g_pair_kernel.load(std::memory_order_relaxed) != 0; }
+// The wide pair kernel, launched like the 256 x 256 pair kernel (persistent grid of resident pairs,
+// pacing counter zeroed on the stream).
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
+                        cudaStream_t stream, const DeviceCtx& ctx) {
+  auto kernel = gemm_bf16_wide_kernel<A_MN, B_MN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WIDE_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = static_cast<int64_t>((M + 2 * BM - 1) / (2 * BM)) * ((N + WIDE_BN - 1) / WIDE_BN);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = WIDE_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int resident_pairs[16] = {};
+  static std::mutex mu;
+  int max_pairs = ctx.num_sms / 2;
+  if (ctx.device >= 0 && ctx.device < 16) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (resident_pairs[ctx.device] == 0) {
+      cfg.gridDim = dim3(2, 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) n = ctx.num_sms / 2;
+      resident_pairs[ctx.device] = n < ctx.num_sms / 2 ? n : ctx.num_sms / 2;
+    }
+    max_pairs = resident_pairs[ctx.device];
+  }
+  const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  unsigned int* pace = next_pace_counter();
+  if (pace) {
+    e = cudaMemsetAsync(pace, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, ep, ctx.status, pair_group(true), pace);
+}
+
+// The pair kernel (256 x 512 tiles if kWide, else 256 x 256) for one operand layout and epilogue.
+template <bool kWide>
+cudaError_t dispatch_pair(bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& ta, const CUtensorMap& tb, int m,
+                          int n, int k, const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx) {
+#define TPMLP_PAIR_LAUNCH(AM, BMN, E)                                               \
+  return kWide ? launch_wide<AM, BMN, E>(ta, tb, m, n, k, ep, stream, ctx)         \
+               : launch_pair<AM, BMN, E>(ta, tb, m, n, k, ep, stream, ctx)
+  if (!a_mn && b_mn) {
+    if (epi == kEpiGelu) TPMLP_PAIR_LAUNCH(false, true, kEpiGelu);
+    if (epi == kEpiStore) TPMLP_PAIR_LAUNCH(false, true, kEpiStore);
+    if (epi == kEpiStoreF32) TPMLP_PAIR_LAUNCH(false, true, kEpiStoreF32);
+    if (epi == kEpiDropoutResidual) TPMLP_PAIR_LAUNCH(false, true, kEpiDropoutResidual);
+  } else if (!a_mn && !b_mn) {
+    if (epi == kEpiDGelu) TPMLP_PAIR_LAUNCH(false, false, kEpiDGelu);
+    if (epi == kEpiStore) TPMLP_PAIR_LAUNCH(false, false, kEpiStore);
+    if (epi == kEpiStoreF32) TPMLP_PAIR_LAUNCH(false, false, kEpiStoreF32);
+  } else if (a_mn && b_mn) {
+    if (epi == kEpiStoreF32) TPMLP_PAIR_LAUNCH(true, true, kEpiStoreF32);
+    if (epi == kEpiAccumF32) TPMLP_PAIR_LAUNCH(true, true, kEpiAccumF32);
+  }
+#undef TPMLP_PAIR_LAUNCH
+  return cudaErrorNotSupported;
+}
+
+// Kernel for the plain GEMMs (tpmlp_set_gemm_variant): 0 the single-SM kernel; 1 SM pairs with
+// 256 x 512 or 256 x 256 tiles, whichever prefer_wide rates faster; 2 SM pairs with 256 x 256
+// tiles only; 3 SM pairs with 256 x 512 tiles only.
+int pair_kernel_choice() { return g_pair_kernel.load(std::memory_order_relaxed); }
+
+// Whether 256 x 512 tiles beat 256 x 256 tiles for one GEMM, by a model of the persistent launch:
+// its waves of tiles over the resident pairs (a partial last wave costs a full one); a 256 x 512
+// wave costs 2 x (0.91 + e / K) of a 256 x 256 one. 0.91 is the measured effect of 25 % fewer
+// operand bytes per FLOP on store epilogues (GB300, K = 8192-32768); the epilogues that also
+// compute GeLU / GeLU' or dropout on two outputs or an extra input are exposed once per wide tile
+// (the single accumulator set), which e = 600 k-values models (measured 0.99 at K = 8192, 1.07
+// at K = 4096).
+bool prefer_wide(int64_t M, int64_t N, int64_t K, EpiKind epi, int pairs) {
+  const int64_t mb = (M + 2 * BM - 1) / (2 * BM);
+  const int64_t t256 = mb * ((N + BN - 1) / BN), t512 = mb * ((N + WIDE_BN - 1) / WIDE_BN);
+  const int64_t w256 = (t256 + pairs - 1) / pairs, w512 = (t512 + pairs - 1) / pairs;
+  const bool heavy = epi == kEpiGelu || epi == kEpiDGelu || epi == kEpiDropoutResidual;
+  const double unit = 0.91 + (heavy ? 600.0 : 0.0) / static_cast<double>(K);
+  return 2.0 * unit * static_cast<double>(w512) < static_cast<double>(w256);
+}
 
 // 4-D bf16 tensor map over a batched operand: dimension 0 is the contiguous column index; the
 // row index and the two batch indices take dimensions 1..3 in order of increasing stride.
@@ -1270,7 +1608,9 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
   // The stored shapes must match the contraction.
   if (a.mn_major ? (a.rows != K || a.cols != M) : (a.rows != M || a.cols != K)) return cudaErrorInvalidValue;
   if (b.mn_major ? (b.rows != K || b.cols != N) : (b.rows != N || b.cols != K)) return cudaErrorInvalidValue;
-  const bool pair = use_pair_kernel() && ctx.num_sms >= 2;
+  const int choice = pair_kernel_choice();
+  const bool pair = choice >= 1 && ctx.num_sms >= 2;
+  const bool wide = pair && (choice == 3 || (choice == 1 && prefer_wide(M, N, K, epi, ctx.num_sms / 2)));
   CUtensorMap ta, tb;
   cudaError_t e = make_tmap(&ta, a, 64, a.mn_major ? BK : BM);
   if (e != cudaSuccess) return e;
@@ -1278,23 +1618,9 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
   if (e != cudaSuccess) return e;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   if (pair) {
-    if (!a.mn_major && b.mn_major) {
-      if (epi == kEpiGelu) return launch_pair<false, true, kEpiGelu>(ta, tb, m, n, k, ep, stream, ctx);
-      if (epi == kEpiStore) return launch_pair<false, true, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
-      if (epi == kEpiStoreF32) return launch_pair<false, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
-      if (epi == kEpiDropoutResidual) {
-        if (N % 32 != 0) return cudaErrorInvalidValue;
-        return launch_pair<false, true, kEpiDropoutResidual>(ta, tb, m, n, k, ep, stream, ctx);
-      }
-    } else if (!a.mn_major && !b.mn_major) {
-      if (epi == kEpiDGelu) return launch_pair<false, false, kEpiDGelu>(ta, tb, m, n, k, ep, stream, ctx);
-      if (epi == kEpiStore) return launch_pair<false, false, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
-      if (epi == kEpiStoreF32) return launch_pair<false, false, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
-    } else if (a.mn_major && b.mn_major) {
-      if (epi == kEpiStoreF32) return launch_pair<true, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
-      if (epi == kEpiAccumF32) return launch_pair<true, true, kEpiAccumF32>(ta, tb, m, n, k, ep, stream, ctx);
-    }
-    return cudaErrorNotSupported;
+    if (epi == kEpiDropoutResidual && N % 32 != 0) return cudaErrorInvalidValue;
+    return wide ? dispatch_pair<true>(a.mn_major, b.mn_major, epi, ta, tb, m, n, k, ep, stream, ctx)
+                : dispatch_pair<false>(a.mn_major, b.mn_major, epi, ta, tb, m, n, k, ep, stream, ctx);
   }
   if (!a.mn_major && b.mn_major) {
     if (epi == kEpiGelu) return launch<false, true, kEpiGelu>(ta, tb, m, n, k, ep, stream, ctx);

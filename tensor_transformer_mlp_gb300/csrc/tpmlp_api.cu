@@ -734,8 +734,9 @@ tpmlp_status tpmlp_sp_dropout_residual(const void* x_shards, const void* y_shard
 }
 
 tpmlp_status tpmlp_set_gemm_variant(int pair_kernel, int pair_pacing, int pair_group) {
-  if ((pair_kernel != 0 && pair_kernel != 1) || (pair_pacing != 0 && pair_pacing != 1))
-    return fail(TPMLP_ERR_INVALID, "pair_kernel and pair_pacing must be 0 or 1 (got %d, %d)", pair_kernel, pair_pacing);
+  if (pair_kernel < 0 || pair_kernel > 3 || (pair_pacing != 0 && pair_pacing != 1))
+    return fail(TPMLP_ERR_INVALID, "pair_kernel must lie in 0..3 and pair_pacing be 0 or 1 (got %d, %d)", pair_kernel,
+                pair_pacing);
   if (pair_group < -4096 || pair_group > 4096)
     return fail(TPMLP_ERR_INVALID, "pair_group must lie in [-4096, 4096], got %d", pair_group);
   set_gemm_variant(pair_kernel, pair_pacing, pair_group);

@@ -238,7 +238,7 @@ def test_last_error_never_null(lib):
 
 def test_gemm_variant_validation(lib):
     # Only this call selects the GEMM kernel (no environment variable does); it touches no device.
-    assert lib.tpmlp_set_gemm_variant(2, 1, 0) == INVALID
+    assert lib.tpmlp_set_gemm_variant(4, 1, 0) == INVALID
     assert lib.tpmlp_set_gemm_variant(1, -1, 0) == INVALID
     assert lib.tpmlp_set_gemm_variant(1, 1, 5000) == INVALID
     assert lib.tpmlp_set_gemm_variant(0, 0, -4) == OK

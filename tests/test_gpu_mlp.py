@@ -17,10 +17,11 @@ pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_example_seed0.txt")
 
-# The plain bf16 GEMMs' kernel variants (tpmlp_set_gemm_variant): the default SM-pair kernel,
-# the one-SM kernel, and the pair kernel without pacing. The parity cases that take the
+# The plain bf16 GEMMs' kernel variants (tpmlp_set_gemm_variant): SM pairs choosing 256 x 512 or
+# 256 x 256 tiles per shape (the default), the one-SM kernel, pairs without pacing, pairs on
+# 256 x 256 tiles only and pairs on 256 x 512 tiles only. The parity cases that take the
 # `gemm_variant` fixture run on each.
-GEMM_VARIANTS = {"pair": (1, 1, 0), "one_sm": (0, 1, 0), "unpaced": (1, 0, 0)}
+GEMM_VARIANTS = {"pair": (1, 1, 0), "one_sm": (0, 1, 0), "unpaced": (1, 0, 0), "pair256": (2, 1, 0), "wide": (3, 1, 0)}
 
 
 @pytest.fixture(params=list(GEMM_VARIANTS))
