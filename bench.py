@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 GEMM_LAUNCHES_PER_STEP = 6
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the
 # committed ncu summary named below; None until a capture of the current kernel exists.
-DOMINANT_KERNEL_TRAFFIC = 9746239531  # average over the six GEMM launches of one step
-DOMINANT_KERNEL_PROFILE = "profiles/gemm_bf16_pair_kernel_large_mlp_dram.md"
+DOMINANT_KERNEL_TRAFFIC = 7762278443  # average over the six GEMM launches of one step
+DOMINANT_KERNEL_PROFILE = "profiles/gemm_bf16_wide_kernel_large_mlp_dram.md"
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -499,6 +499,8 @@ def run_ours(args, cfg):
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
     tp.load_library()
+    variant = tuple(int(v) for v in args.gemm_variant.split(","))
+    tp.tpmlp_set_gemm_variant(*variant)
 
     inp = wl.mlp_inputs(cfg)
     bf = torch.bfloat16
@@ -625,14 +627,15 @@ def run_ours(args, cfg):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_elapsed / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(cfg),
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(config_dict(cfg), **({} if variant == (1, 1, 0) else {"gemm_variant": list(variant)})),
         "frac_of_peak": value / world / peak,
         "fwd_tflops": 4 * n * d * m * args.steps / (fwd_ms / 1e3) / 1e12,
         "bwd_tflops": 8 * n * d * m * args.steps / (bwd_ms / 1e3) / 1e12,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "traffic": DOMINANT_KERNEL_TRAFFIC if cfg is wl.LARGE_MLP else None,
-                     "kernel": "gemm_bf16_pair_kernel (tcgen05 cta_group::2, 256x256 tiles on SM pairs; "
+                     "kernel": "gemm_bf16_wide_kernel (tcgen05 cta_group::2, 256x512 tiles on SM pairs; "
                                "6 launches per step, 2*n*d*m FLOP each)",
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
                      "traffic_profile": DOMINANT_KERNEL_PROFILE if cfg is wl.LARGE_MLP else None},
@@ -674,6 +677,9 @@ def main(argv=None):
                     choices=sorted(k for k, c in wl.MLP_CONFIGS.items() if c.dtype == "bf16"))
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
     ap.add_argument("--no-sp", action="store_true", help="skip the sequence-parallel kernel measurements")
+    ap.add_argument("--gemm-variant", default="1,1,0",
+                    help="GEMM kernel choice, pacing and tile band passed to tpmlp_set_gemm_variant "
+                         "(default 1,1,0: the library's own per-GEMM choice)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
