@@ -331,6 +331,43 @@ __device__ __forceinline__ float tanh_fast(float x) {
   return y;
 }
 
+// Packed fp32 pairs: the sm_100-family f32x2 instructions (add, sub, mul, fma on two fp32 lanes,
+// round to nearest) do two elements per issued instruction, with the same per-element rounding as
+// the scalar forms.
+struct F2 {
+  unsigned long long v;
+};
+__device__ __forceinline__ F2 f2_make(float a, float b) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(F2 a) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(a.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+  F2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+
 constexpr float kSqrt2OverPi = 0.7978845608028654f;
 constexpr float kTanhC = 0.044715f;
 constexpr float kInvSqrt2 = 0.7071067811865476f;
@@ -373,6 +410,29 @@ __device__ __forceinline__ float gelu_grad_f(float x, int kind) {
     return fmaf(0.5f, th, 0.5f) + (0.5f * x * dudx) * fmaf(-th, th, 1.0f);
   }
 }
+
+// The tanh forms above on a pair of elements with f32x2 arithmetic (same operations and rounding
+// per element as gelu_f<false> / gelu_grad_f<false>; tanh.approx per element).
+__device__ __forceinline__ F2 tanh_fast2(F2 u) {
+  const float2 v = f2_split(u);
+  return f2_make(tanh_fast(v.x), tanh_fast(v.y));
+}
+__device__ __forceinline__ F2 gelu_tanh2(F2 x) {
+  const F2 th = tanh_fast2(f2_mul(x, f2_fma(f2_make(kTanhB, kTanhB), f2_mul(x, x), f2_make(kTanhA, kTanhA))));
+  const F2 hx = f2_mul(f2_make(0.5f, 0.5f), x);
+  return f2_fma(hx, th, hx);
+}
+// phi' = (1 + th) / 2 + (x / 2) (a + 3 b x^2) (1 - th^2), arranged as
+// fma((-x / 2) (a + 3 b x^2), th^2 - 1, fma(1/2, th, 1/2)).
+__device__ __forceinline__ F2 gelu_grad_tanh2(F2 x) {
+  const F2 x2 = f2_mul(x, x);
+  const F2 th = tanh_fast2(f2_mul(x, f2_fma(f2_make(kTanhB, kTanhB), x2, f2_make(kTanhA, kTanhA))));
+  const F2 dudx = f2_fma(f2_make(3.0f * kTanhB, 3.0f * kTanhB), x2, f2_make(kTanhA, kTanhA));
+  const F2 p = f2_mul(f2_mul(f2_make(-0.5f, -0.5f), x), dudx);
+  const F2 q = f2_fma(th, th, f2_make(-1.0f, -1.0f));
+  return f2_fma(p, q, f2_fma(f2_make(0.5f, 0.5f), th, f2_make(0.5f, 0.5f)));
+}
+
 
 // Drop decision for one element: splitmix64(key) < threshold, with SplitMix64 as published by
 // Steele, Lea and Flood (2014) / Vigna's splitmix64.c: add the golden-gamma increment, then the

@@ -318,13 +318,20 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
 #pragma unroll
         for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
         store_prologue8<kEpiStore, false>(ep, col0 + g * 8, col0 + g * 8 < N, a, 1.f);  // bias1
-        float y[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = gelu_f<false>(a[i], ep.gelu);
         zs[g] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
                            pack_bf16x2(a[6], a[7]));
-        ys[g] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                           pack_bf16x2(y[6], y[7]));
+        uint32_t yw[4];
+        if (ep.gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 y2 = f2_split(gelu_tanh2(f2_make(a[2 * i], a[2 * i + 1])));
+            yw[i] = pack_bf16x2(y2.x, y2.y);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) yw[i] = pack_bf16x2(gelu_f<false>(a[2 * i], ep.gelu), gelu_f<false>(a[2 * i + 1], ep.gelu));
+        }
+        ys[g] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
       }
       if (ep.out) store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
       store_staged<false>(buf, ys, lane, prow, ep.out2, ep.ldo, col0, N);
@@ -438,11 +445,22 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
 #pragma unroll
       for (int g = 0; g < 8; ++g) {  // D overwrites Z in place
         uint32_t* w = reinterpret_cast<uint32_t*>(&zs[g]);
+        if (ep.gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 zf = unpack_bf16x2(w[i]);
-          w[i] = pack_bf16x2(__uint_as_float(v[g * 8 + 2 * i]) * gelu_grad_f<false>(zf.x, ep.gelu),
-                             __uint_as_float(v[g * 8 + 2 * i + 1]) * gelu_grad_f<false>(zf.y, ep.gelu));
+          for (int i = 0; i < 4; ++i) {
+            const F2 z2 = f2_make(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+            const float2 d2 = f2_split(f2_mul(f2_make(__uint_as_float(v[g * 8 + 2 * i]),
+                                                      __uint_as_float(v[g * 8 + 2 * i + 1])),
+                                              gelu_grad_tanh2(z2)));
+            w[i] = pack_bf16x2(d2.x, d2.y);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 zf = unpack_bf16x2(w[i]);
+            w[i] = pack_bf16x2(__uint_as_float(v[g * 8 + 2 * i]) * gelu_grad_f<false>(zf.x, ep.gelu),
+                               __uint_as_float(v[g * 8 + 2 * i + 1]) * gelu_grad_f<false>(zf.y, ep.gelu));
+          }
         }
       }
       store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
@@ -996,21 +1014,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * PAIR_STAGE_BYTES);
+          // K runs backwards in odd rounds: a round starts on the k-blocks that the previous round
+          // (which shares its A panels in the band order) touched last, so more of them are in L2.
+          const int kbl = (round & 1) ? num_kb - 1 - kb : kb;
           const uint32_t full0 = map_to_cta(&full_bar[s], 0);
           uint8_t* sa = smem + s * PAIR_STAGE_BYTES;
           uint8_t* sb = sa + A_STAGE_BYTES;
           if constexpr (!A_MN) {
-            tma_load_2d_pair(sa, &tmap_a, full0, kb * BK, a_row);
+            tma_load_2d_pair(sa, &tmap_a, full0, kbl * BK, a_row);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * MN_BOX_BYTES, &tmap_a, full0, a_row + j * 64, kb * BK);
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * MN_BOX_BYTES, &tmap_a, full0, a_row + j * 64, kbl * BK);
           }
           if constexpr (!B_MN) {
-            tma_load_2d_pair(sb, &tmap_b, full0, kb * BK, b_col);
+            tma_load_2d_pair(sb, &tmap_b, full0, kbl * BK, b_col);
           } else {
 #pragma unroll
             for (int j = 0; j < BN_HALF / 64; ++j)
-              tma_load_2d_pair(sb + j * MN_BOX_BYTES, &tmap_b, full0, b_col + j * 64, kb * BK);
+              tma_load_2d_pair(sb + j * MN_BOX_BYTES, &tmap_b, full0, b_col + j * 64, kbl * BK);
           }
           ++kiter;
         }
@@ -1212,25 +1233,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * WIDE_STAGE_BYTES);
+          const int kbl = (round & 1) ? num_kb - 1 - kb : kb;  // K backwards in odd rounds (as above)
           const uint32_t full0 = map_to_cta(&full_bar[s], 0);
           uint8_t* sa = smem + s * WIDE_STAGE_BYTES;
           uint8_t* sb = sa + A_STAGE_BYTES;
           if constexpr (!A_MN) {
-            tma_load_2d_pair(sa, &tmap_a, full0, kb * BK, a_row);
+            tma_load_2d_pair(sa, &tmap_a, full0, kbl * BK, a_row);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * MN_BOX_BYTES, &tmap_a, full0, a_row + j * 64, kb * BK);
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * MN_BOX_BYTES, &tmap_a, full0, a_row + j * 64, kbl * BK);
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {  // this CTA's 128 columns of each 256-column half
             const int b_col = nb * WIDE_BN + h * BN + static_cast<int>(rank) * BN_HALF;
             uint8_t* sbh = sb + h * WIDE_CHUNK_BYTES;
             if constexpr (!B_MN) {
-              tma_load_2d_pair(sbh, &tmap_b, full0, kb * BK, b_col);
+              tma_load_2d_pair(sbh, &tmap_b, full0, kbl * BK, b_col);
             } else {
 #pragma unroll
               for (int j = 0; j < BN_HALF / 64; ++j)
-                tma_load_2d_pair(sbh + j * MN_BOX_BYTES, &tmap_b, full0, b_col + j * 64, kb * BK);
+                tma_load_2d_pair(sbh + j * MN_BOX_BYTES, &tmap_b, full0, b_col + j * 64, kbl * BK);
             }
           }
           ++kiter;

@@ -648,43 +648,6 @@ __global__ void __launch_bounds__(128, dropout_min_blocks<T>()) dropout_grad_gat
   }
 }
 
-// Packed fp32 pairs for the elementwise arithmetic of the norm backward: the sm_100-family
-// f32x2 instructions (add, sub, mul, fma on two fp32 lanes, round to nearest) do two elements per
-// issued instruction, with the same per-element rounding as the scalar forms.
-struct F2 {
-  unsigned long long v;
-};
-__device__ __forceinline__ F2 f2_make(float a, float b) {
-  F2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float2 f2_split(F2 a) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(a.v));
-  return r;
-}
-__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
-  F2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-  return r;
-}
-__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
-  F2 r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-  return r;
-}
-__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
-  F2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-  return r;
-}
-__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
-  F2 r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
-  return r;
-}
-
 // 8 elements of T as four fp32 pairs, and back.
 __device__ __forceinline__ void to_f2(const uint4& u, F2 (&o)[4]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
