@@ -960,25 +960,29 @@ __global__ void __launch_bounds__(NT, MINB)
 }
 
 // dgamma[c] = sum over CTAs k of partials[k][0][c], dbeta[c] likewise from partials[k][1][c]. A
-// CTA of 1024 threads takes 64 columns: thread (g, q) adds the float4 of columns 4q..4q+3 over
-// partials g, g + 64, g + 128, ... (all of them in flight for up to 512 partials); the 64 group
-// sums are then added by a fixed pairwise tree, so the result does not depend on scheduling.
-// With dbeta null only the dgamma half is read. Launched as a programmatic dependent of the norm
-// backward kernel, it waits (griddepcontrol.wait) for that grid's completion and memory first.
+// CTA of 1024 threads takes kSumPartialsCols = 32 columns: thread (g, q) adds the float4 of columns
+// 4q..4q+3 over partials g, g + 128, g + 256, ... (a few loads each, all in flight); the 128 group
+// sums are then added by a fixed pairwise tree, so the result does not depend on scheduling. With
+// dbeta null only the dgamma half is read. Narrow column slices give enough CTAs to cover the SMs
+// (128 for h = 4096), since the work is latency-bound. Launched as a programmatic dependent of the
+// norm backward kernel, it waits (griddepcontrol.wait) for that grid's completion and memory.
 constexpr int kSumPartialsThreads = 1024;
+constexpr int kSumPartialsCols = 32;
 __global__ void __launch_bounds__(kSumPartialsThreads)
     sum_partials_kernel(const float* __restrict__ partials, int nparts, int h, float* __restrict__ dgamma,
                         float* __restrict__ dbeta) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float4 grp[64][16];
-  const int q = threadIdx.x & 15, g = threadIdx.x >> 4;
+  constexpr int kQuads = kSumPartialsCols / 4;                  // 8
+  constexpr int kGroups = kSumPartialsThreads / kQuads;         // 128
+  __shared__ float4 grp[kGroups][kQuads];
+  const int q = threadIdx.x % kQuads, g = threadIdx.x / kQuads;
   const int ncols = dbeta ? 2 * h : h;
-  const int c = blockIdx.x * 64 + q * 4;
+  const int c = blockIdx.x * kSumPartialsCols + q * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (c < ncols) {
     const float* p = partials + c;
 #pragma unroll 8
-    for (int k = g; k < nparts; k += 64) {
+    for (int k = g; k < nparts; k += kGroups) {
       const float4 v = *reinterpret_cast<const float4*>(p + static_cast<int64_t>(k) * 2 * h);
       acc.x += v.x;
       acc.y += v.y;
@@ -988,7 +992,7 @@ __global__ void __launch_bounds__(kSumPartialsThreads)
   }
   grp[g][q] = acc;
 #pragma unroll
-  for (int half = 32; half > 0; half >>= 1) {
+  for (int half = kGroups / 2; half > 0; half >>= 1) {
     __syncthreads();
     if (g < half) {
       const float4 o = grp[g + half][q];
@@ -1351,7 +1355,7 @@ cudaError_t launch_norm_bwd(const void* x, const void* dy, const void* dres, con
   if (e != cudaSuccess) return e;
   const int ncols = dbeta ? 2 * h : h;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((ncols + 63) / 64), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>((ncols + kSumPartialsCols - 1) / kSumPartialsCols), 1, 1);
   cfg.blockDim = dim3(kSumPartialsThreads, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
