@@ -177,7 +177,7 @@ tpmlp_status tpmlp_backward_biased(const void* X, const void* A, const void* B, 
                                    tpmlp_gelu gelu, tpmlp_dtype dt,
                                    void* workspace, size_t ws_bytes, void* stream);
 
-/* Bytes of device workspace tpmlp_sp_block needs (LN output, gathered tokens, Y, row-GEMM output or partials). */
+/* Bytes of device workspace tpmlp_sp_block needs (LN output in token order, Y, row-GEMM output or partials). */
 size_t tpmlp_sp_block_workspace_size(int64_t b, int64_t s, int64_t h, int64_t m, int t,
                                      tpmlp_dtype dt, tpmlp_rs_mode rs);
 

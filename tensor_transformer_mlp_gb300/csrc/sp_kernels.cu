@@ -23,6 +23,15 @@ __device__ __forceinline__ int64_t shard_row_to_token(int64_t R, int64_t b, int6
   return bi * s + j * sl + l;
 }
 
+// Where a LayerNorm writes its output row: in place of the input row, or, for the sequence-parallel
+// block, at the row's token-order position (the all-gather g fused into the LayerNorm's store).
+struct LnOutRows {
+  int64_t b, s, sl;  // sl = 0: the input row's own position
+  __device__ __forceinline__ int64_t operator()(int64_t R) const {
+    return sl ? shard_row_to_token(R, b, s, sl) : R;
+  }
+};
+
 template <typename T>
 struct Vec8;  // 8 elements of T
 
@@ -84,7 +93,8 @@ template <typename T, int CH>
 __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const T* __restrict__ x,
                                                                const float* __restrict__ gamma,
                                                                const float* __restrict__ beta, float eps,
-                                                               T* __restrict__ y, int64_t rows, int h) {
+                                                               T* __restrict__ y, int64_t rows, int h,
+                                                               LnOutRows out_rows) {
   __shared__ float red[2][2][kLnThreads / 32];
   const int tid = threadIdx.x;
   const int lane = tid & 31, w = tid >> 5;
@@ -135,7 +145,7 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const T* __restri
 #pragma unroll
     for (int k = 0; k < kLnThreads / 32; ++k) var += red[parity][1][k];
     const float rstd = rsqrtf(var * inv_h + eps);
-    T* yr = y + r * h;
+    T* yr = y + out_rows(r) * h;
 #pragma unroll
     for (int i = 0; i < CH; ++i) {
       const int c = (tid + kLnThreads * i) * 8;
@@ -161,7 +171,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) layernorm_generic_kernel(const T* __restrict__ x,
                                                                 const float* __restrict__ gamma,
                                                                 const float* __restrict__ beta, float eps,
-                                                                T* __restrict__ y, int64_t rows, int64_t h) {
+                                                                T* __restrict__ y, int64_t rows, int64_t h,
+                                                                LnOutRows out_rows) {
   __shared__ float red[8];
   __shared__ float stat;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -194,8 +205,9 @@ __global__ void __launch_bounds__(256) layernorm_generic_kernel(const T* __restr
     }
     __syncthreads();
     const float rstd = stat;
+    T* yr = y + out_rows(r) * h;
     for (int64_t c = threadIdx.x; c < h; c += blockDim.x)
-      y[r * h + c] = static_cast<T>(fmaf((static_cast<float>(xr[c]) - mean) * rstd, gamma[c], beta[c]));
+      yr[c] = static_cast<T>(fmaf((static_cast<float>(xr[c]) - mean) * rstd, gamma[c], beta[c]));
     __syncthreads();
   }
 }
@@ -393,7 +405,8 @@ __device__ __forceinline__ void drain_rows(uint64_t* full, int64_t from, int64_t
 template <typename T, int CH, int kRowThreads, int kRowStages, bool kAffineInRegs, bool kRms = false>
 __global__ void __launch_bounds__(kRowThreads)
     layernorm_staged_kernel(const T* __restrict__ x, const float* __restrict__ gamma, const float* __restrict__ beta,
-                            float eps, T* __restrict__ y, int64_t rows, int h, unsigned int* status) {
+                            float eps, T* __restrict__ y, int64_t rows, int h, unsigned int* status,
+                            LnOutRows out_rows) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float2 red[2][kRowThreads / 32];
   const uint32_t row_bytes = static_cast<uint32_t>(h) * sizeof(T);
@@ -474,7 +487,7 @@ __global__ void __launch_bounds__(kRowThreads)
     const float rstd = rsqrtf(var + eps);
     const float a0 = kRms ? 0.f : -(md + shift) * rstd;  // (x - mean) * rstd = x * rstd + a0
     const int64_t R = blockIdx.x + i * gridDim.x;
-    T* yr = y + R * h;
+    T* yr = y + out_rows(R) * h;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int v = tid + c * kRowThreads;
@@ -1137,8 +1150,11 @@ int rows_grid(int64_t rows, int num_sms, int per_sm) {
 }  // namespace
 
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, float eps, void* y, int64_t rows,
-                             int64_t h, bool bf16, cudaStream_t stream, int num_sms, unsigned int* status, bool rms) {
+                             int64_t h, bool bf16, cudaStream_t stream, int num_sms, unsigned int* status, bool rms,
+                             const int64_t* gather_bst) {
   if (rows <= 0) return cudaSuccess;
+  LnOutRows out_rows{0, 0, 0};
+  if (gather_bst) out_rows = LnOutRows{gather_bst[0], gather_bst[1], gather_bst[1] / gather_bst[2]};
   const size_t elt = bf16 ? 2 : 4;
   const size_t ln_smem = staged_smem(static_cast<size_t>(h) * elt, kLnStages);
   const bool staged = h % 8 == 0 && h <= kLnStagedThreads * 8 * 8 && ln_smem <= kStagedSmemMax;
@@ -1156,7 +1172,7 @@ cudaError_t launch_layernorm(const void* x, const float* gamma, const float* bet
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ln_smem);         \
     if (e != cudaSuccess) return e;                                                                             \
     k<<<grid, kLnStagedThreads, ln_smem, stream>>>(static_cast<const TYPE*>(x), gamma, beta, eps,               \
-                                                   static_cast<TYPE*>(y), rows, (int)h, status);                \
+                                                   static_cast<TYPE*>(y), rows, (int)h, status, out_rows);      \
   } while (0)
     if (bf16) {
       if (ch <= 1) TPMLP_LN_STAGED(__nv_bfloat16, 1);
@@ -1176,26 +1192,26 @@ cudaError_t launch_layernorm(const void* x, const float* gamma, const float* bet
     if (bf16) {
       auto xp = static_cast<const __nv_bfloat16*>(x);
       auto yp = static_cast<__nv_bfloat16*>(y);
-      if (ch <= 1) layernorm_kernel<__nv_bfloat16, 1><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else if (ch <= 2) layernorm_kernel<__nv_bfloat16, 2><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else if (ch <= 4) layernorm_kernel<__nv_bfloat16, 4><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else layernorm_kernel<__nv_bfloat16, 8><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      if (ch <= 1) layernorm_kernel<__nv_bfloat16, 1><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h, out_rows);
+      else if (ch <= 2) layernorm_kernel<__nv_bfloat16, 2><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h, out_rows);
+      else if (ch <= 4) layernorm_kernel<__nv_bfloat16, 4><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h, out_rows);
+      else layernorm_kernel<__nv_bfloat16, 8><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h, out_rows);
     } else {
       auto xp = static_cast<const float*>(x);
       auto yp = static_cast<float*>(y);
-      if (ch <= 1) layernorm_kernel<float, 1><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else if (ch <= 2) layernorm_kernel<float, 2><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else if (ch <= 4) layernorm_kernel<float, 4><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
-      else layernorm_kernel<float, 8><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h);
+      if (ch <= 1) layernorm_kernel<float, 1><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h, out_rows);
+      else if (ch <= 2) layernorm_kernel<float, 2><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h, out_rows);
+      else if (ch <= 4) layernorm_kernel<float, 4><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h, out_rows);
+      else layernorm_kernel<float, 8><<<grid, kLnThreads, 0, stream>>>(xp, gamma, beta, eps, yp, rows, (int)h, out_rows);
     }
   } else {
     const int grid = rows_grid(rows, num_sms, 8);
     if (bf16)
       layernorm_generic_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(x), gamma, beta, eps, static_cast<__nv_bfloat16*>(y), rows, h);
+          static_cast<const __nv_bfloat16*>(x), gamma, beta, eps, static_cast<__nv_bfloat16*>(y), rows, h, out_rows);
     else
       layernorm_generic_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), gamma, beta, eps,
-                                                                 static_cast<float*>(y), rows, h);
+                                                                 static_cast<float*>(y), rows, h, out_rows);
   }
   return cudaGetLastError();
 }

@@ -329,7 +329,7 @@ tpmlp_status tpmlp_backward_biased(const void* X, const void* A, const void* B, 
 namespace {
 
 struct SPLayout {
-  size_t xn, xg, y, o, partials, total;
+  size_t xg, y, o, partials, total;
 };
 
 SPLayout sp_layout(int64_t b, int64_t s, int64_t h, int64_t m, int t, tpmlp_dtype dt, tpmlp_rs_mode rs) {
@@ -337,7 +337,6 @@ SPLayout sp_layout(int64_t b, int64_t s, int64_t h, int64_t m, int t, tpmlp_dtyp
   const size_t tok = static_cast<size_t>(b) * static_cast<size_t>(s);
   SPLayout L;
   size_t off = 0;
-  L.xn = off; off += round_up(tok * h * e, 256);
   L.xg = off; off += round_up(tok * h * e, 256);
   L.y = off;  off += round_up(tok * m * e, 256);
   L.o = off;  off += round_up(tok * h * e, 256);
@@ -405,14 +404,16 @@ tpmlp_status tpmlp_sp_block(const void* x_shards, const float* gamma, const floa
   DeviceCtx ctx;
   TPMLP_CUDA(get_device_ctx(&ctx), "device context");
   char* ws = static_cast<char*>(workspace);
-  void* xn = ws + L.xn;
   void* xg = ws + L.xg;
   void* Y = Y_save ? Y_save : static_cast<void*>(ws + L.y);
   void* o = ws + L.o;
   const bool bf16 = dt == TPMLP_BF16;
-  // LayerNorm on the shards (SP region), then g: all-gather into token order.
-  TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms, ctx.status), "layernorm");
-  TPMLP_CUDA(launch_gather(xn, xg, b, s, h, t, bf16, st, ctx.num_sms), "gather");
+  // LayerNorm on the shards (SP region) with g, the all-gather into token order, fused into its
+  // stores: each normalised row is written at its token-order position.
+  const int64_t gather_bst[3] = {b, s, t};
+  TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xg, n, h, bf16, st, ctx.num_sms, ctx.status, false,
+                              gather_bst),
+             "layernorm + gather");
   const uint64_t threshold = drop_threshold(p_drop);
   const float scale = static_cast<float>(1.0 / (1.0 - p_drop));
   RowRemap rm;
@@ -468,7 +469,7 @@ size_t tpmlp_sp_block_backward_workspace_size(int64_t b, int64_t s, int64_t h, i
   if (b <= 0 || s <= 0 || h <= 0 || m <= 0 || t <= 0) return 0;
   const size_t e = elt_size(dt);
   const size_t tok = static_cast<size_t>(b) * static_cast<size_t>(s);
-  return 4 * round_up(tok * h * e, 256) + round_up(tok * m * e, 256) +
+  return 3 * round_up(tok * h * e, 256) + round_up(tok * m * e, 256) +
          round_up(static_cast<size_t>(kLnBwdMaxCtas) * 2 * h * sizeof(float), 256);
 }
 
@@ -514,17 +515,18 @@ tpmlp_status tpmlp_sp_block_backward(const void* x_shards, const float* gamma, c
   const size_t e = elt_size(dt);
   const size_t tok = static_cast<size_t>(n);
   char* ws = static_cast<char*>(workspace);
-  void* xn = ws;
-  void* xg = ws + round_up(tok * h * e, 256);
-  void* dtok = ws + 2 * round_up(tok * h * e, 256);
-  void* D = ws + 3 * round_up(tok * h * e, 256);
+  void* xg = ws;
+  void* dtok = ws + round_up(tok * h * e, 256);
+  void* D = ws + 2 * round_up(tok * h * e, 256);
   void* dxn = static_cast<char*>(D) + round_up(tok * m * e, 256);
   float* partials = reinterpret_cast<float*>(static_cast<char*>(dxn) + round_up(tok * h * e, 256));
   const bool bf16 = dt == TPMLP_BF16;
-  // Recompute the LayerNorm output in token order (the forward's g), then the local dropout
-  // gradient gathered into token order (g-bar's backward).
-  TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xn, n, h, bf16, st, ctx.num_sms, ctx.status), "layernorm");
-  TPMLP_CUDA(launch_gather(xn, xg, b, s, h, t, bf16, st, ctx.num_sms), "gather");
+  // Recompute the LayerNorm output in token order (the forward's g, fused into the LayerNorm's
+  // stores), then the local dropout gradient gathered into token order (g-bar's backward).
+  const int64_t gather_bst[3] = {b, s, t};
+  TPMLP_CUDA(launch_layernorm(x_shards, gamma, beta, eps, xg, n, h, bf16, st, ctx.num_sms, ctx.status, false,
+                              gather_bst),
+             "layernorm + gather");
   TPMLP_CUDA(launch_dropout_grad_gather(dout_shards, dtok, mask_bits, drop_threshold(p_drop),
                                         static_cast<float>(1.0 / (1.0 - p_drop)), seed, b, s, h,
                                         t, bf16, st, ctx.num_sms),

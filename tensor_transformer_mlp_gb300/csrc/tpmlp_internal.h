@@ -125,9 +125,11 @@ cudaError_t gemm_f32_simt(int64_t M, int64_t N, int64_t K, const Operand& a, con
 
 // Sequence-parallel memory-bound kernels. `bf16` selects the element type (else fp32).
 // rms: RMSNorm instead (beta unused; staged widths only, else cudaErrorNotSupported).
+// gather_bst: null, or {b, s, t} of shard-major input rows [t][b][s/t]: the output rows are then
+// written in token order [b][s] (the all-gather g fused into the LayerNorm).
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, float eps, void* y,
                              int64_t rows, int64_t h, bool bf16, cudaStream_t stream, int num_sms,
-                             unsigned int* status, bool rms = false);
+                             unsigned int* status, bool rms = false, const int64_t* gather_bst = nullptr);
 cudaError_t launch_gather(const void* x_shards, void* x_full, int64_t b, int64_t s, int64_t h, int t, bool bf16,
                           cudaStream_t stream, int num_sms);
 cudaError_t launch_reduce_scatter(const float* partials, void* out_shards, int64_t b, int64_t s, int64_t h, int t,
