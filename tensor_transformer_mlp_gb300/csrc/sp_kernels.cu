@@ -1142,6 +1142,62 @@ __global__ void __launch_bounds__(256) row_dot_kernel(const __nv_bfloat16* __res
   }
 }
 
+// The same row dot products for dh / 8 dividing 32, heads <= kRowDotMaxHeads and s % 8 == 0: a
+// CTA takes 8 consecutive tokens of one sequence (a warp each). A warp issues the loads of eight
+// head groups before it reduces any (the groups' loads in flight together instead of one group's
+// at a time), and the CTA's results go through shared memory so that each head's 8 values are
+// stored as one 32-byte segment instead of 8 scattered words.
+constexpr int kRowDotMaxHeads = 128;
+__global__ void __launch_bounds__(256) row_dot_staged_kernel(const __nv_bfloat16* __restrict__ dO,
+                                                             const __nv_bfloat16* __restrict__ O,
+                                                             float* __restrict__ D, int64_t s, int64_t h,
+                                                             int heads) {
+  __shared__ float sd[8][kRowDotMaxHeads];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * 8;
+  const int64_t tok = tok0 + w;
+  const int64_t dh = h / heads;
+  const int vh = static_cast<int>(dh / 8);
+  const int hpw = 32 / vh, seg = lane / vh, v = lane % vh;
+  const __nv_bfloat16* a = dO + tok * h;
+  const __nv_bfloat16* c = O + tok * h;
+  constexpr int kGroups = 8;
+  for (int j0 = 0; j0 < heads; j0 += kGroups * hpw) {
+    uint4 va[kGroups], vc[kGroups];
+#pragma unroll
+    for (int u = 0; u < kGroups; ++u) {
+      const int j = j0 + u * hpw + seg;
+      if (j < heads) {
+        va[u] = *reinterpret_cast<const uint4*>(a + j * dh + v * 8);
+        vc[u] = *reinterpret_cast<const uint4*>(c + j * dh + v * 8);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGroups; ++u) {
+      const int j = j0 + u * hpw + seg;
+      float acc = 0.f;
+      if (j < heads) {
+        const uint32_t wa[4] = {va[u].x, va[u].y, va[u].z, va[u].w};
+        const uint32_t wc[4] = {vc[u].x, vc[u].y, vc[u].z, vc[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 fa = unpack_bf16x2(wa[k]), fc = unpack_bf16x2(wc[k]);
+          acc = fmaf(fa.x, fc.x, acc);
+          acc = fmaf(fa.y, fc.y, acc);
+        }
+      }
+      for (int o = vh / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (v == 0 && j < heads) sd[w][j] = acc;
+    }
+  }
+  __syncthreads();
+  const int64_t bi = tok0 / s, si0 = tok0 - bi * s;
+  for (int idx = threadIdx.x; idx < 8 * heads; idx += blockDim.x) {
+    const int j = idx >> 3, t = idx & 7;
+    D[(bi * heads + j) * s + si0 + t] = sd[t][j];
+  }
+}
+
 int rows_grid(int64_t rows, int num_sms, int per_sm) {
   const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
   return static_cast<int>(rows < cap ? (rows > 0 ? rows : 1) : cap);
@@ -1448,6 +1504,12 @@ cudaError_t launch_row_dot(const void* dO, const void* O, float* D, int64_t b, i
   const int64_t n = b * s;  // token rows, one warp each
   if (n <= 0) return cudaSuccess;
   if ((h / heads) % 8 != 0) return cudaErrorInvalidValue;
+  const int64_t vh = h / heads / 8;
+  if (vh <= 32 && 32 % vh == 0 && heads <= kRowDotMaxHeads && s % 8 == 0) {
+    row_dot_staged_kernel<<<static_cast<unsigned>(n / 8), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), D, s, h, heads);
+    return cudaGetLastError();
+  }
   row_dot_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), D, b, s, h, heads);
   return cudaGetLastError();
