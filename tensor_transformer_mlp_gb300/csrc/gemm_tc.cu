@@ -300,6 +300,43 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       }
       store_staged<kF32>(buf, seg, lane, prow, out, ep.ldo, col0, N);
     }
+  } else if constexpr (EPI == kEpiStoreRowDot) {
+    // bf16 stores as kEpiStore (64 columns per pass, staged), and each row's dot product of the
+    // stored values with aux over the warp's 128 columns (one head of 128), accumulated over the
+    // passes in column order; aux arrives through the staging buffer like Z in kEpiDGelu.
+    const int64_t prow = row < M ? row : -1;
+    float dot = 0.f;
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kChunks; c += 2) {
+      const int col0 = col_tile0 + c * 32;
+      if (col0 >= N) break;  // uniform across the warp
+      uint32_t v[64];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      uint4 os[8];
+      load_staged_bf16(buf, os, lane, prow, ep.aux, ep.ldo, col0, N);
+      tmem_ld_wait();
+      uint4 seg[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t ow[4] = {os[g].x, os[g].y, os[g].z, os[g].w};
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w[i] = pack_bf16x2(__uint_as_float(v[g * 8 + 2 * i]), __uint_as_float(v[g * 8 + 2 * i + 1]));
+          const float2 d2 = unpack_bf16x2(w[i]), o2 = unpack_bf16x2(ow[i]);
+          dot = fmaf(d2.x, o2.x, dot);
+          dot = fmaf(d2.y, o2.y, dot);
+        }
+        seg[g] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      store_staged<false>(buf, seg, lane, prow, ep.out, ep.ldo, col0, N);
+    }
+    if (row < M) {
+      const int64_t bi = row / ep.rowdot_s, si = row - bi * ep.rowdot_s;
+      const int j = (col_tile0 + c_begin * 32) / 128;
+      ep.rowdot[(bi * ep.rowdot_heads + j) * ep.rowdot_s + si] = dot;
+    }
   } else if constexpr (EPI == kEpiGelu) {
     // Z (optional) and Y = gelu(Z), 64 columns per pass, both through the staging buffer.
     const int64_t prow = row < M ? row : -1;
@@ -1550,6 +1587,7 @@ cudaError_t dispatch_pair(bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& 
   } else if (!a_mn && !b_mn) {
     if (epi == kEpiDGelu) TPMLP_PAIR_LAUNCH(false, false, kEpiDGelu);
     if (epi == kEpiStore) TPMLP_PAIR_LAUNCH(false, false, kEpiStore);
+    if (epi == kEpiStoreRowDot) TPMLP_PAIR_LAUNCH(false, false, kEpiStoreRowDot);
     if (epi == kEpiStoreF32) TPMLP_PAIR_LAUNCH(false, false, kEpiStoreF32);
   } else if (a_mn && b_mn) {
     if (epi == kEpiStoreF32) TPMLP_PAIR_LAUNCH(true, true, kEpiStoreF32);
@@ -1569,14 +1607,14 @@ int pair_kernel_choice() { return g_pair_kernel.load(std::memory_order_relaxed);
 // wave costs 2 x (0.91 + e / K) of a 256 x 256 one. 0.91 is the measured gain of 25 % fewer
 // operand bytes per FLOP (GB300, K = 8192-32768); e / K is the epilogue, exposed once per wide
 // tile (the single accumulator set) and shorter against a longer main loop: e = 600 k-values for
-// GeLU / GeLU' / dropout epilogues (measured 0.99 at K = 8192, 1.07 at K = 4096), 400 for fp32
+// GeLU / GeLU' / dropout / row-dot epilogues (measured 0.99 at K = 8192, 1.07 at K = 4096), 400 for fp32
 // stores and 250 for bf16 stores (1-2 % at K = 16384-32768, from a copy of the kernel whose MMAs
 // do not wait for the epilogue).
 bool prefer_wide(int64_t M, int64_t N, int64_t K, EpiKind epi, int pairs) {
   const int64_t mb = (M + 2 * BM - 1) / (2 * BM);
   const int64_t t256 = mb * ((N + BN - 1) / BN), t512 = mb * ((N + WIDE_BN - 1) / WIDE_BN);
   const int64_t w256 = (t256 + pairs - 1) / pairs, w512 = (t512 + pairs - 1) / pairs;
-  const bool heavy = epi == kEpiGelu || epi == kEpiDGelu || epi == kEpiDropoutResidual;
+  const bool heavy = epi == kEpiGelu || epi == kEpiDGelu || epi == kEpiDropoutResidual || epi == kEpiStoreRowDot;
   const bool f32 = epi == kEpiStoreF32 || epi == kEpiAccumF32;
   const double e = heavy ? 600.0 : (f32 ? 400.0 : 250.0);
   const double unit = 0.91 + e / static_cast<double>(K);
@@ -1658,6 +1696,7 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
   } else if (!a.mn_major && !b.mn_major) {
     if (epi == kEpiDGelu) return launch<false, false, kEpiDGelu>(ta, tb, m, n, k, ep, stream, ctx);
     if (epi == kEpiStore) return launch<false, false, kEpiStore>(ta, tb, m, n, k, ep, stream, ctx);
+    if (epi == kEpiStoreRowDot) return launch<false, false, kEpiStoreRowDot>(ta, tb, m, n, k, ep, stream, ctx);
     if (epi == kEpiStoreF32) return launch<false, false, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);
   } else if (a.mn_major && b.mn_major) {
     if (epi == kEpiStoreF32) return launch<true, true, kEpiStoreF32>(ta, tb, m, n, k, ep, stream, ctx);

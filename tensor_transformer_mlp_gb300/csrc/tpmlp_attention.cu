@@ -194,9 +194,19 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
   float* D = reinterpret_cast<float*>(ws + round_up(static_cast<size_t>(n) * h * 2, 256));
   void* dS = reinterpret_cast<char*>(D) + round_up(static_cast<size_t>(n) * heads * sizeof(float), 256);
   void* dQKV = static_cast<char*>(dS) + round_up(sc * 2, 256);
-  // output projection: dO = G W_o^T, dW_o = O^T G
-  ATT_CUDA(gemm_bf16_tc(n, h, h, Operand{G, n, h, h, false}, Operand{Wo, h, h, h, false}, kEpiStore,
-                        plain_epi(dO, h), stm, ctx),
+  // output projection: dO = G W_o^T, dW_o = O^T G. With 128-column heads, the dO GEMM's epilogue
+  // also forms D = rowsum(dO * O) per (head, query row) (an epilogue warp holds one head's 128
+  // columns of its rows); otherwise a separate kernel does, after the dV GEMM.
+  const bool fused_rowdot = dh == 128;
+  EpiParams ep_do = plain_epi(dO, h);
+  if (fused_rowdot) {
+    ep_do.aux = O_save;
+    ep_do.rowdot = D;
+    ep_do.rowdot_s = s;
+    ep_do.rowdot_heads = heads;
+  }
+  ATT_CUDA(gemm_bf16_tc(n, h, h, Operand{G, n, h, h, false}, Operand{Wo, h, h, h, false},
+                        fused_rowdot ? kEpiStoreRowDot : kEpiStore, ep_do, stm, ctx),
            "dO GEMM");
   ATT_CUDA(gemm_bf16_tc(h, h, n, Operand{O_save, n, h, h, true}, Operand{G, n, h, h, true}, kEpiStoreF32,
                         plain_epi(dWo, h), stm, ctx),
@@ -209,7 +219,7 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
            "dV GEMM");
   // dS = P * (dP - D) / sqrt(dh) with dP = dO V^T computed and consumed in the same GEMM's
   // epilogue; D = rowsum(P * dP) = rowsum(dO * O) per (head, query row), from dO and O alone.
-  ATT_CUDA(launch_row_dot(dO, O_save, D, b, s, h, heads, stm, ctx.num_sms), "rowsum(dO * O)");
+  if (!fused_rowdot) ATT_CUDA(launch_row_dot(dO, O_save, D, b, s, h, heads, stm, ctx.num_sms), "rowsum(dO * O)");
   const BatchSpec bs_p{heads, b, s * s, heads * s * s, 1.0f};
   EpiParams ep_ds = plain_epi(dS, s);
   ep_ds.aux = P_save;

@@ -27,6 +27,10 @@ enum EpiKind : int {
   kEpiRowStats = 6,     // stats[srow][2*nb + half] = (max y, sum 2^(y - max y)) over the warp's columns
   kEpiSoftmax = 7,      // out[r][c] = 2^(y - rowvec[srow].M) * rowvec[srow].invL  (P, operand dtype)
   kEpiSoftmaxGrad = 8,  // out[r][c] = escale * aux[r][c] * (x - rowvec[srow])  (dS from dP, P and D)
+  // out[r][c] = acc (bf16) and, per 128-column head j of the row, rowdot[(bi * heads + j) * s + si]
+  // = sum over the head's columns of out[r][c] * aux[r][c], with r = bi * s + si (plain GEMMs;
+  // the attention backward's dO GEMM, aux = O: D = rowsum(dO * O) per head and query row)
+  kEpiStoreRowDot = 9,
 };
 
 // Dropout of the sequence-parallel block applied in a GEMM epilogue: element (r, c) of the
@@ -61,6 +65,10 @@ struct EpiParams {
   void* stats;
   const void* rowvec;
   float escale;
+  // kEpiStoreRowDot: output of the row dots, the sequence length s and the number of heads
+  float* rowdot;
+  int64_t rowdot_s;
+  int rowdot_heads;
 };
 
 // A stored operand matrix [rows][cols] with row stride `ld` elements.
