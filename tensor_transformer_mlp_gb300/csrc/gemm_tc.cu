@@ -1159,11 +1159,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // 48 KB of operands per 64-deep k-block (its 128 A rows and two 128-column B chunks) for twice
 // the work of the 256 x 256 pair tile: 25 % fewer operand bytes per FLOP into every SM and out
 // of L2. The two half accumulators take all 512 tensor-memory columns, so there is one
-// accumulator set: the epilogue drains half 0, then half 1, arriving on one empty barrier per
-// half. The next tile's half 0 starts as soon as half 0 is drained and runs ahead over the first
-// WIDE_STAGES k-blocks (their stages stay resident) while half 1 is still being drained; then
-// half 1 catches up on those k-blocks and both halves proceed k-block by k-block.
-//   barriers: full[s] (even CTA), empty[s] (each CTA), tfull (each CTA; multicast commit),
+// accumulator set: the epilogue drains half 0, then half 1, waiting on one full barrier and
+// arriving on one empty barrier per half. Both ends of a tile's K-loop are skewed so that a
+// drain overlaps MMAs of the other half: over the last WIDE_STAGES k-blocks (their stages stay
+// resident) half 0 goes first and is committed on its own, so its drain runs while half 1
+// finishes those k-blocks; the next tile's half 0 starts as soon as half 0 is drained and runs
+// ahead over the first WIDE_STAGES k-blocks while half 1 is still being drained, then half 1
+// catches up on those k-blocks; in between both halves proceed k-block by k-block.
+//   barriers: full[s] (even CTA), empty[s] (each CTA), tfull[h] (each CTA; multicast commit),
 //   tempty[h] (even CTA; all epilogue threads of both CTAs arrive), drain (even CTA).
 constexpr int WIDE_STAGES = 4;
 constexpr int WIDE_GROUP_M = 16;  // tile band in pair-rows (measured: 16 beats 8 and 32 on the large MLP)
@@ -1172,7 +1175,7 @@ constexpr int WIDE_CHUNK_BYTES = BN_HALF * BK * 2;              // one 128-colum
 constexpr int WIDE_STAGE_BYTES = A_STAGE_BYTES + 2 * WIDE_CHUNK_BYTES;  // 48 KiB
 constexpr int WIDE_SMEM_BYTES = WIDE_STAGES * WIDE_STAGE_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;
 static_assert(WIDE_SMEM_BYTES <= 227 * 1024, "shared memory budget (wide pair kernel)");
-static_assert((2 * WIDE_STAGES + 1 + 2 + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area (wide pair kernel)");
+static_assert((2 * WIDE_STAGES + 2 + 2 + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area (wide pair kernel)");
 
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -1186,7 +1189,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_stage + NUM_EPI_WARPS * EPI_STAGE_BYTES);
   uint64_t* empty_bar = full_bar + WIDE_STAGES;
   uint64_t* tfull_bar = empty_bar + WIDE_STAGES;
-  uint64_t* tempty_bar = tfull_bar + 1;
+  uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
 
@@ -1228,7 +1231,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(tfull_bar, 1);
+    mbar_init(&tfull_bar[0], 1);
+    mbar_init(&tfull_bar[1], 1);
     mbar_init(&tempty_bar[0], 2 * NUM_EPI_THREADS);
     mbar_init(&tempty_bar[1], 2 * NUM_EPI_THREADS);
     mbar_init(drain_bar, 1);
@@ -1324,8 +1328,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t prev = static_cast<uint32_t>(it & 1) ^ 1;  // phase of the previous tile's drain
         // Half 0 runs ahead over the first `lead` k-blocks, while the epilogue may still be
         // draining half 1 of the previous tile; those stages stay resident until half 1 has
-        // used them too, then each is freed.
+        // used them too, then each is freed. Over the last `tail` k-blocks half 0 goes first
+        // again and is committed on its own, so that its drain overlaps half 1's last MMAs.
         const int lead = min(WIDE_STAGES, num_kb);
+        const int tail = min(WIDE_STAGES, num_kb - lead);
         if (!mbar_wait(&tempty_bar[0], prev, status, 34)) {
           ok = false;
           break;
@@ -1341,6 +1347,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           issue_half(k % WIDE_STAGES, kb, 0);
         }
         if (!ok) break;
+        if (tail == 0) umma_commit_pair_mc(&tfull_bar[0], 0x3);  // half 0 complete (num_kb <= lead)
         if (!mbar_wait(&tempty_bar[1], prev, status, 34)) {
           ok = false;
           break;
@@ -1352,7 +1359,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           umma_commit_pair_mc(&empty_bar[s], 0x3);  // frees stage s in both CTAs
         }
         kiter += lead;
-        for (int kb = lead; kb < num_kb; ++kb) {
+        for (int kb = lead; kb < num_kb - tail; ++kb) {
           const int s = kiter % WIDE_STAGES;
           if (!mbar_wait(&full_bar[s], (kiter / WIDE_STAGES) & 1, status, 33)) {
             ok = false;
@@ -1365,7 +1372,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++kiter;
         }
         if (!ok) break;
-        umma_commit_pair_mc(tfull_bar, 0x3);  // both halves of both CTAs' accumulators ready
+        if (tail > 0) {
+          for (int j = 0; j < tail; ++j) {
+            const int k = kiter + j;
+            if (!mbar_wait(&full_bar[k % WIDE_STAGES], (k / WIDE_STAGES) & 1, status, 33)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_half(k % WIDE_STAGES, num_kb - tail + j, 0);
+          }
+          if (!ok) break;
+          umma_commit_pair_mc(&tfull_bar[0], 0x3);  // half 0 of both CTAs' accumulators ready
+          for (int j = 0; j < tail; ++j) {
+            const int s = (kiter + j) % WIDE_STAGES;
+            issue_half(s, num_kb - tail + j, 1);
+            umma_commit_pair_mc(&empty_bar[s], 0x3);
+          }
+          kiter += tail;
+        }
+        umma_commit_pair_mc(&tfull_bar[1], 0x3);  // half 1 ready
       }
       umma_commit_pair(drain_bar);
       mbar_wait(drain_bar, 0, status, 35);
@@ -1375,15 +1401,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int c_begin = ((warp - 2) / 4) * kEpiChunks;
     int it = 0;
-    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
-      const bool ok = mbar_wait(tfull_bar, static_cast<uint32_t>(it & 1), status, 36);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
+    bool ok = true;
+    for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
       int mb, nb;
       coords(tile, mb, nb);
       const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[h], static_cast<uint32_t>(it & 1), status, 36));
+        if (!ok) break;
+        tc_fence_after();
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * BN);
         epilogue_tile<EPI, false>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N,
                                   nb * WIDE_BN + h * BN, c_begin, t_row, 0, 1.f, row, 2 * nb + h, 2 * num_nb);
