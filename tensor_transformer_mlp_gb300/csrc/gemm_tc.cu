@@ -122,6 +122,34 @@ struct BatchDev {
   float alpha;
 };
 
+// GeLU and GeLU' epilogue steps for the GeLU kinds other than the tanh form (eight accumulator
+// values as raw bits; for GeLU', z holds the eight bf16 inputs and the result is acc * gelu'(z)),
+// packed to bf16. Kept out of line: inlined and unrolled, the erf form's registers would add to
+// the tanh path's in the same kernel.
+__device__ __noinline__ uint4 gelu_other8(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4, uint32_t a5,
+                                          uint32_t a6, uint32_t a7, int kind) {
+  const uint32_t a[8] = {a0, a1, a2, a3, a4, a5, a6, a7};
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = pack_bf16x2(gelu_f<false>(__uint_as_float(a[2 * i]), kind), gelu_f<false>(__uint_as_float(a[2 * i + 1]), kind));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __noinline__ uint4 dgelu_other8(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4, uint32_t a5,
+                                           uint32_t a6, uint32_t a7, uint4 z, int kind) {
+  const uint32_t a[8] = {a0, a1, a2, a3, a4, a5, a6, a7};
+  const uint32_t zw[4] = {z.x, z.y, z.z, z.w};
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 zf = unpack_bf16x2(zw[i]);
+    w[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * gelu_grad_f<false>(zf.x, kind),
+                       __uint_as_float(a[2 * i + 1]) * gelu_grad_f<false>(zf.y, kind));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Applies the epilogues that read as well as write (kEpiAccumF32, kEpiDropoutResidual) to
 // 32 consecutive accumulator columns of one row.
 template <int EPI>
@@ -197,6 +225,29 @@ __device__ __forceinline__ void store_staged(uint8_t* buf, const uint4 (&seg)[8]
   __syncwarp();
 }
 
+// The bulk-copy form of store_staged, for outputs with a tensor map (rows not remapped): the
+// warp's 32 rows x 128 bytes go into its staging buffer in the 128-byte-swizzled layout of the
+// map's 32-row box, and lane 0 stores the block with one tensor copy (parts past M or N are not
+// written), so the warp moves on without waiting for the global writes. The buffer is rewritten
+// only once the previous copy out of it has read it (buf_acquire).
+__device__ __forceinline__ void buf_acquire(int lane) {
+  if (lane == 0) bulk_wait_group_read<0>();
+  __syncwarp();
+}
+
+__device__ __forceinline__ void store_tma(uint8_t* buf, const uint4 (&seg)[8], int lane, const CUtensorMap* map,
+                                          int col0, int row0) {
+  buf_acquire(lane);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = seg[j];
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, col0, row0);
+    bulk_commit_group();
+  }
+}
+
 // The inverse of store_staged for bf16 (load_staged_bf16), in two steps. issue_block_loads: the
 // warp reads 32 rows x 64 columns of src with line-wide loads (8 rows x 128 bytes per
 // instruction; lane gets rows i*4 + lane/8, segment lane%8; zeros past M or N).
@@ -262,10 +313,19 @@ __device__ __forceinline__ void store_prologue8(const EpiParams& ep, int col, bo
 // the row across the batch (row statistics), nb / num_nb give the tile's N-block.
 constexpr int kEpiChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp, 256-wide tiles
 
-template <int EPI, bool BATCHED, int kChunks = kEpiChunks>
+// tm_out / tm_out2 (non-null: the plain store kinds in the pair kernels, rows not remapped) send
+// ep.out / ep.out2 through bulk tensor stores instead of store_staged. kTmaOnly (GeLU and GeLU' in
+// the pair kernels, whose outputs always have tensor maps) compiles the bulk-store path alone.
+template <int EPI>
+constexpr bool kTmaEpi = EPI == kEpiGelu || EPI == kEpiDGelu;
+
+template <int EPI, bool BATCHED, int kChunks = kEpiChunks, bool kTmaOnly = false>
 __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf, int lane, int64_t row, int M, int N,
                                               int col_tile0, int c_begin, uint32_t t_row, int64_t out_off,
-                                              float alpha, int64_t srow, int nb, int num_nb) {
+                                              float alpha, int64_t srow, int nb, int num_nb,
+                                              const CUtensorMap* tm_out = nullptr,
+                                              const CUtensorMap* tm_out2 = nullptr) {
+  const int row0 = static_cast<int>(row - lane);  // the warp's first row (bulk stores)
   if constexpr (EPI == kEpiStore || EPI == kEpiStoreF32) {
     constexpr bool kF32 = EPI == kEpiStoreF32;
     constexpr int kCols = kF32 ? 32 : 64;  // 128 bytes of output per row per pass
@@ -298,7 +358,10 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
                               pack_bf16x2(a[6], a[7]));
         }
       }
-      store_staged<kF32>(buf, seg, lane, prow, out, ep.ldo, col0, N);
+      if (tm_out)
+        store_tma(buf, seg, lane, tm_out, col0, row0);
+      else
+        store_staged<kF32>(buf, seg, lane, prow, out, ep.ldo, col0, N);
     }
   } else if constexpr (EPI == kEpiStoreRowDot) {
     // bf16 stores as kEpiStore (64 columns per pass, staged), and each row's dot product of the
@@ -348,30 +411,46 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
       tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       tmem_ld_wait();
-      uint4 zs[8], ys[8];
+      // Z first (bias added in place in v), so its store is under way while Y is computed.
+      uint4 zs[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
         float a[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(v[g * 8 + i]);
         store_prologue8<kEpiStore, false>(ep, col0 + g * 8, col0 + g * 8 < N, a, 1.f);  // bias1
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[g * 8 + i] = __float_as_uint(a[i]);
         zs[g] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
                            pack_bf16x2(a[6], a[7]));
+      }
+      if (ep.out) {
+        if constexpr (kTmaOnly)
+          store_tma(buf, zs, lane, tm_out, col0, row0);
+        else
+          store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
+      }
+      uint4 ys[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
         uint32_t yw[4];
         if (ep.gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float2 y2 = f2_split(gelu_tanh2(f2_make(a[2 * i], a[2 * i + 1])));
+            const float2 y2 = f2_split(gelu_tanh2(f2_make(__uint_as_float(v[g * 8 + 2 * i]),
+                                                          __uint_as_float(v[g * 8 + 2 * i + 1]))));
             yw[i] = pack_bf16x2(y2.x, y2.y);
           }
+          ys[g] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
         } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) yw[i] = pack_bf16x2(gelu_f<false>(a[2 * i], ep.gelu), gelu_f<false>(a[2 * i + 1], ep.gelu));
+          ys[g] = gelu_other8(v[g * 8], v[g * 8 + 1], v[g * 8 + 2], v[g * 8 + 3], v[g * 8 + 4], v[g * 8 + 5],
+                              v[g * 8 + 6], v[g * 8 + 7], ep.gelu);
         }
-        ys[g] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
       }
-      if (ep.out) store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
-      store_staged<false>(buf, ys, lane, prow, ep.out2, ep.ldo, col0, N);
+      if constexpr (kTmaOnly)
+        store_tma(buf, ys, lane, tm_out2, col0, row0);
+      else
+        store_staged<false>(buf, ys, lane, prow, ep.out2, ep.ldo, col0, N);
     }
   } else if constexpr (EPI == kEpiRowStats) {
     // Online max / sum of exp over the warp's 128 columns of the row, in base 2: with
@@ -477,7 +556,24 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
       tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       uint4 zs[8];
-      load_staged_bf16(buf, zs, lane, prow, ep.aux, ep.ldo, col0, N);
+      {
+        uint4 r8[8];
+        if constexpr (kTmaOnly) {
+          // rows are not remapped: lane reads rows row0 + i * 4 + lane / 8, segment lane % 8
+          const int64_t r_first = static_cast<int64_t>(row0) + (lane >> 3);
+          const int col = col0 + (lane & 7) * 8;
+          const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(ep.aux) + r_first * ep.ldo + col;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            r8[i] = make_uint4(0, 0, 0, 0);
+            if (r_first + i * 4 < M && col < N) r8[i] = *reinterpret_cast<const uint4*>(src + i * 4 * ep.ldo);
+          }
+          buf_acquire(lane);  // the previous pass's bulk store has read the buffer
+        } else {
+          issue_block_loads(r8, lane, prow, ep.aux, ep.ldo, col0, N);
+        }
+        transpose_block(buf, r8, zs, lane);
+      }
       tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 8; ++g) {  // D overwrites Z in place
@@ -492,15 +588,14 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
             w[i] = pack_bf16x2(d2.x, d2.y);
           }
         } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 zf = unpack_bf16x2(w[i]);
-            w[i] = pack_bf16x2(__uint_as_float(v[g * 8 + 2 * i]) * gelu_grad_f<false>(zf.x, ep.gelu),
-                               __uint_as_float(v[g * 8 + 2 * i + 1]) * gelu_grad_f<false>(zf.y, ep.gelu));
-          }
+          zs[g] = dgelu_other8(v[g * 8], v[g * 8 + 1], v[g * 8 + 2], v[g * 8 + 3], v[g * 8 + 4], v[g * 8 + 5],
+                               v[g * 8 + 6], v[g * 8 + 7], zs[g], ep.gelu);
         }
       }
-      store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
+      if constexpr (kTmaOnly)
+        store_tma(buf, zs, lane, tm_out, col0, row0);
+      else
+        store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
     }
   } else {
 #pragma unroll 1
@@ -929,6 +1024,9 @@ static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory budget (pair kernel)
 static_assert((2 * PAIR_STAGES + 2 * NUM_ACC + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area");
 
 constexpr int kPaceKb = 32;                 // k-blocks between pacing points
+// GeLU' epilogue: the producer prefetches the tile's Z rows into L2 this many k-blocks before the
+// end of the tile's K-loop (map in the second output slot, tma_out bit 2).
+constexpr int kAuxPrefetchKb = 16;
 constexpr uint64_t kPaceWaitNs = 50000;     // longest pause at one pacing point
 
 // Spins (bounded by limit_ns) until *ctr >= target; a pacing hint, so expiry is not an error.
@@ -949,7 +1047,8 @@ __device__ __forceinline__ void pace_wait(const unsigned int* ctr, unsigned int 
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                          int M, int N, int K, EpiParams ep, unsigned int* status, int group,
+                          const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_c2,
+                          int tma_out, int M, int N, int K, EpiParams ep, unsigned int* status, int group,
                           unsigned int* pace) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -1039,6 +1138,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int b_col = nb * BN + static_cast<int>(rank) * BN_HALF;
         const unsigned int active = static_cast<unsigned int>(min(num_pairs, num_tiles - round * num_pairs));
         for (int kb = 0; kb < num_kb; ++kb) {
+          if constexpr (EPI == kEpiDGelu) {
+            // Z of this CTA's 128 output rows into L2 some k-blocks before the epilogue reads it
+            if ((tma_out & 4) && kb == max(0, num_kb - kAuxPrefetchKb))
+              for (int j = 0; j < BN / 64; ++j) tma_prefetch_l2_2d(&tmap_c2, nb * BN + j * 64, a_row);
+          }
           if (pacer && kb % kPaceKb == 0) {
             pace_wait(pace, pace_target, kPaceWaitNs);
             atomicAdd(pace, 1u);
@@ -1124,6 +1228,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     const int c_begin = ((warp - 2) / 4) * kEpiChunks;
+    const CUtensorMap* tm_out = (tma_out & 1) ? &tmap_c : nullptr;  // bulk stores of ep.out / ep.out2
+    const CUtensorMap* tm_out2 = (tma_out & 2) ? &tmap_c2 : nullptr;
     int it = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs, ++it) {
       const int acc = it & 1;
@@ -1135,11 +1241,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       coords(tile, mb, nb);
       const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<EPI, false>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N, nb * BN, c_begin,
-                                t_row, 0, 1.f, row, nb, num_nb);
+      epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M,
+                                                          N, nb * BN, c_begin, t_row, 0, 1.f, row, nb, num_nb,
+                                                          tm_out, tm_out2);
       tc_fence_before();
       mbar_arrive_cluster(map_to_cta(&tempty_bar[acc], 0));
     }
+    if (lane == 0) bulk_wait_group_all();  // the last bulk stores have completed
+    __syncwarp();
   }
 
   // Neither CTA frees tensor memory or leaves (its barriers are targets of the other's
@@ -1180,7 +1289,8 @@ static_assert((2 * WIDE_STAGES + 2 + 2 + 1) * 8 + 4 <= BARRIER_BYTES, "barrier a
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                          int M, int N, int K, EpiParams ep, unsigned int* status, int group,
+                          const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_c2,
+                          int tma_out, int M, int N, int K, EpiParams ep, unsigned int* status, int group,
                           unsigned int* pace) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -1262,6 +1372,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int a_row = mb * 2 * BM + static_cast<int>(rank) * BM;
         const unsigned int active = static_cast<unsigned int>(min(num_pairs, num_tiles - round * num_pairs));
         for (int kb = 0; kb < num_kb; ++kb) {
+          if constexpr (EPI == kEpiDGelu) {
+            if ((tma_out & 4) && kb == max(0, num_kb - kAuxPrefetchKb))  // as in the 256 x 256 pair kernel
+              for (int j = 0; j < WIDE_BN / 64; ++j) tma_prefetch_l2_2d(&tmap_c2, nb * WIDE_BN + j * 64, a_row);
+          }
           if (pacer && kb % kPaceKb == 0) {
             pace_wait(pace, pace_target, kPaceWaitNs);
             atomicAdd(pace, 1u);
@@ -1400,6 +1514,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     const int c_begin = ((warp - 2) / 4) * kEpiChunks;
+    const CUtensorMap* tm_out = (tma_out & 1) ? &tmap_c : nullptr;  // bulk stores of ep.out / ep.out2
+    const CUtensorMap* tm_out2 = (tma_out & 2) ? &tmap_c2 : nullptr;
     int it = 0;
     bool ok = true;
     for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
@@ -1412,12 +1528,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * BN);
-        epilogue_tile<EPI, false>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M, N,
-                                  nb * WIDE_BN + h * BN, c_begin, t_row, 0, 1.f, row, 2 * nb + h, 2 * num_nb);
+        epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row,
+                                                            M, N, nb * WIDE_BN + h * BN, c_begin, t_row, 0, 1.f, row,
+                                                            2 * nb + h, 2 * num_nb, tm_out, tm_out2);
         tc_fence_before();
         mbar_arrive_cluster(map_to_cta(&tempty_bar[h], 0));
       }
     }
+    if (lane == 0) bulk_wait_group_all();  // the last bulk stores have completed
+    __syncwarp();
   }
 
   // Neither CTA frees tensor memory or leaves (its barriers are targets of the other's
@@ -1462,6 +1581,64 @@ cudaError_t make_tmap(CUtensorMap* map, const Operand& op, uint32_t box_inner, u
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Tensor maps of the pair kernels' outputs for bulk tensor stores: 32-row boxes of 128 bytes
+// (64 bf16 or 32 fp32 columns), 128-byte swizzle, matching the epilogue's staging layout. flags
+// bit 0: ep.out has a map in c; bit 1: ep.out2 has one in c2. Outputs whose rows are remapped,
+// and the kinds that read or reduce in place, keep the per-thread stores.
+struct OutMaps {
+  CUtensorMap c, c2;
+  int flags = 0;
+};
+
+cudaError_t make_out_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool f32,
+                         uint32_t box_rows = 32) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+  cudaError_t e = get_encode(&encode);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t elt = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elt};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                      const_cast<void*>(ptr), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_out_maps(OutMaps* om, EpiKind epi, const EpiParams& ep, int64_t M, int64_t N) {
+  om->flags = 0;
+  const bool kind_ok = epi == kEpiStore || epi == kEpiStoreF32 || epi == kEpiGelu || epi == kEpiDGelu;
+  if (!kind_ok || ep.remap.enabled) return cudaSuccess;
+  const bool f32 = epi == kEpiStoreF32;
+  const int64_t elt = f32 ? 4 : 2;
+  // A tensor map wants a 16-byte aligned base and a row stride that is a multiple of 16 bytes.
+  auto fits = [&](const void* p) {
+    return p != nullptr && reinterpret_cast<uintptr_t>(p) % 16 == 0 && (ep.ldo * elt) % 16 == 0 && ep.ldo >= N;
+  };
+  if (fits(ep.out)) {
+    cudaError_t e = make_out_map(&om->c, ep.out, M, N, ep.ldo, f32);
+    if (e != cudaSuccess) return e;
+    om->flags |= 1;
+  }
+  if (epi == kEpiGelu && fits(ep.out2)) {
+    cudaError_t e = make_out_map(&om->c2, ep.out2, M, N, ep.ldo, false);
+    if (e != cudaSuccess) return e;
+    om->flags |= 2;
+  }
+  if (epi == kEpiDGelu && fits(ep.aux)) {  // Z, for the producer's L2 prefetch (128-row boxes)
+    cudaError_t e = make_out_map(&om->c2, ep.aux, M, N, ep.ldo, false, BM);
+    if (e != cudaSuccess) return e;
+    om->flags |= 4;
+  }
+  // GeLU and GeLU' compile the bulk-store path alone in the pair kernels: every output they
+  // write needs its map (the API's shape and alignment checks guarantee it).
+  if (epi == kEpiGelu && ((ep.out && !(om->flags & 1)) || !(om->flags & 2))) return cudaErrorInvalidValue;
+  if (epi == kEpiDGelu && !(om->flags & 1)) return cudaErrorInvalidValue;
+  return cudaSuccess;
 }
 
 template <bool A_MN, bool B_MN, int EPI, bool BATCHED = false, int BN_T = 256>
@@ -1513,8 +1690,8 @@ int pair_group(bool wide = false) {
 }
 
 template <bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
-                        cudaStream_t stream, const DeviceCtx& ctx) {
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const OutMaps& om, int M, int N, int K,
+                        const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx) {
   auto kernel = gemm_bf16_pair_kernel<A_MN, B_MN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -1553,14 +1730,14 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, int M, int
     e = cudaMemsetAsync(pace, 0, sizeof(unsigned int), stream);
     if (e != cudaSuccess) return e;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, ep, ctx.status, pair_group(), pace);
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, om.c, om.c2, om.flags, M, N, K, ep, ctx.status, pair_group(), pace);
 }
 
 // The wide pair kernel, launched like the 256 x 256 pair kernel (persistent grid of resident pairs,
 // pacing counter zeroed on the stream).
 template <bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const EpiParams& ep,
-                        cudaStream_t stream, const DeviceCtx& ctx) {
+cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const OutMaps& om, int M, int N, int K,
+                        const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx) {
   auto kernel = gemm_bf16_wide_kernel<A_MN, B_MN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WIDE_SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -1596,16 +1773,18 @@ cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, int M, int
     e = cudaMemsetAsync(pace, 0, sizeof(unsigned int), stream);
     if (e != cudaSuccess) return e;
   }
-  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, ep, ctx.status, pair_group(true), pace);
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, om.c, om.c2, om.flags, M, N, K, ep, ctx.status, pair_group(true),
+                            pace);
 }
 
 // The pair kernel (256 x 512 tiles if kWide, else 256 x 256) for one operand layout and epilogue.
 template <bool kWide>
-cudaError_t dispatch_pair(bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& ta, const CUtensorMap& tb, int m,
-                          int n, int k, const EpiParams& ep, cudaStream_t stream, const DeviceCtx& ctx) {
+cudaError_t dispatch_pair(bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& ta, const CUtensorMap& tb,
+                          const OutMaps& om, int m, int n, int k, const EpiParams& ep, cudaStream_t stream,
+                          const DeviceCtx& ctx) {
 #define TPMLP_PAIR_LAUNCH(AM, BMN, E)                                               \
-  return kWide ? launch_wide<AM, BMN, E>(ta, tb, m, n, k, ep, stream, ctx)         \
-               : launch_pair<AM, BMN, E>(ta, tb, m, n, k, ep, stream, ctx)
+  return kWide ? launch_wide<AM, BMN, E>(ta, tb, om, m, n, k, ep, stream, ctx)     \
+               : launch_pair<AM, BMN, E>(ta, tb, om, m, n, k, ep, stream, ctx)
   if (!a_mn && b_mn) {
     if (epi == kEpiGelu) TPMLP_PAIR_LAUNCH(false, true, kEpiGelu);
     if (epi == kEpiStore) TPMLP_PAIR_LAUNCH(false, true, kEpiStore);
@@ -1709,8 +1888,11 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   if (pair) {
     if (epi == kEpiDropoutResidual && N % 32 != 0) return cudaErrorInvalidValue;
-    return wide ? dispatch_pair<true>(a.mn_major, b.mn_major, epi, ta, tb, m, n, k, ep, stream, ctx)
-                : dispatch_pair<false>(a.mn_major, b.mn_major, epi, ta, tb, m, n, k, ep, stream, ctx);
+    OutMaps om;
+    e = make_out_maps(&om, epi, ep, M, N);
+    if (e != cudaSuccess) return e;
+    return wide ? dispatch_pair<true>(a.mn_major, b.mn_major, epi, ta, tb, om, m, n, k, ep, stream, ctx)
+                : dispatch_pair<false>(a.mn_major, b.mn_major, epi, ta, tb, om, m, n, k, ep, stream, ctx);
   }
   if (!a.mn_major && b.mn_major) {
     if (epi == kEpiGelu) return launch<false, true, kEpiGelu>(ta, tb, m, n, k, ep, stream, ctx);
