@@ -314,10 +314,12 @@ __device__ __forceinline__ void store_prologue8(const EpiParams& ep, int col, bo
 constexpr int kEpiChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks per warp, 256-wide tiles
 
 // tm_out / tm_out2 (non-null: the plain store kinds in the pair kernels, rows not remapped) send
-// ep.out / ep.out2 through bulk tensor stores instead of store_staged. kTmaOnly (GeLU and GeLU' in
-// the pair kernels, whose outputs always have tensor maps) compiles the bulk-store path alone.
-template <int EPI>
-constexpr bool kTmaEpi = EPI == kEpiGelu || EPI == kEpiDGelu;
+// ep.out / ep.out2 through bulk tensor stores instead of store_staged. kTmaOnly (GeLU in the pair
+// kernels, GeLU' in the wide one: their outputs always have tensor maps) compiles the bulk-store
+// path alone. (The 256 x 256 kernel's GeLU' epilogue, which overlaps the next tile's main loop,
+// measured 15 % slower with bulk stores or with the L2 prefetch of Z, so it keeps both out.)
+template <int EPI, bool kWide>
+constexpr bool kTmaEpi = EPI == kEpiGelu || (kWide && EPI == kEpiDGelu);
 
 template <int EPI, bool BATCHED, int kChunks = kEpiChunks, bool kTmaOnly = false>
 __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf, int lane, int64_t row, int M, int N,
@@ -431,10 +433,10 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
           store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
       }
       uint4 ys[8];
+      if (ep.gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        uint32_t yw[4];
-        if (ep.gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path
+        for (int g = 0; g < 8; ++g) {
+          uint32_t yw[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 y2 = f2_split(gelu_tanh2(f2_make(__uint_as_float(v[g * 8 + 2 * i]),
@@ -442,10 +444,12 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
             yw[i] = pack_bf16x2(y2.x, y2.y);
           }
           ys[g] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-        } else {
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
           ys[g] = gelu_other8(v[g * 8], v[g * 8 + 1], v[g * 8 + 2], v[g * 8 + 3], v[g * 8 + 4], v[g * 8 + 5],
                               v[g * 8 + 6], v[g * 8 + 7], ep.gelu);
-        }
       }
       if constexpr (kTmaOnly)
         store_tma(buf, ys, lane, tm_out2, col0, row0);
@@ -575,10 +579,10 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
         transpose_block(buf, r8, zs, lane);
       }
       tmem_ld_wait();
+      if (ep.gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path; D overwrites Z in place
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {  // D overwrites Z in place
-        uint32_t* w = reinterpret_cast<uint32_t*>(&zs[g]);
-        if (ep.gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path
+        for (int g = 0; g < 8; ++g) {
+          uint32_t* w = reinterpret_cast<uint32_t*>(&zs[g]);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const F2 z2 = f2_make(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
@@ -587,10 +591,12 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
                                               gelu_grad_tanh2(z2)));
             w[i] = pack_bf16x2(d2.x, d2.y);
           }
-        } else {
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
           zs[g] = dgelu_other8(v[g * 8], v[g * 8 + 1], v[g * 8 + 2], v[g * 8 + 3], v[g * 8 + 4], v[g * 8 + 5],
                                v[g * 8 + 6], v[g * 8 + 7], zs[g], ep.gelu);
-        }
       }
       if constexpr (kTmaOnly)
         store_tma(buf, zs, lane, tm_out, col0, row0);
@@ -1024,8 +1030,8 @@ static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory budget (pair kernel)
 static_assert((2 * PAIR_STAGES + 2 * NUM_ACC + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area");
 
 constexpr int kPaceKb = 32;                 // k-blocks between pacing points
-// GeLU' epilogue: the producer prefetches the tile's Z rows into L2 this many k-blocks before the
-// end of the tile's K-loop (map in the second output slot, tma_out bit 2).
+// GeLU' epilogue of the wide kernel: the producer prefetches the tile's Z rows into L2 this many
+// k-blocks before the end of the tile's K-loop (map in the second output slot, tma_out bit 2).
 constexpr int kAuxPrefetchKb = 16;
 constexpr uint64_t kPaceWaitNs = 50000;     // longest pause at one pacing point
 
@@ -1138,11 +1144,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int b_col = nb * BN + static_cast<int>(rank) * BN_HALF;
         const unsigned int active = static_cast<unsigned int>(min(num_pairs, num_tiles - round * num_pairs));
         for (int kb = 0; kb < num_kb; ++kb) {
-          if constexpr (EPI == kEpiDGelu) {
-            // Z of this CTA's 128 output rows into L2 some k-blocks before the epilogue reads it
-            if ((tma_out & 4) && kb == max(0, num_kb - kAuxPrefetchKb))
-              for (int j = 0; j < BN / 64; ++j) tma_prefetch_l2_2d(&tmap_c2, nb * BN + j * 64, a_row);
-          }
           if (pacer && kb % kPaceKb == 0) {
             pace_wait(pace, pace_target, kPaceWaitNs);
             atomicAdd(pace, 1u);
@@ -1241,7 +1242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       coords(tile, mb, nb);
       const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M,
+      epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI, false>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M,
                                                           N, nb * BN, c_begin, t_row, 0, 1.f, row, nb, num_nb,
                                                           tm_out, tm_out2);
       tc_fence_before();
@@ -1373,7 +1374,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const unsigned int active = static_cast<unsigned int>(min(num_pairs, num_tiles - round * num_pairs));
         for (int kb = 0; kb < num_kb; ++kb) {
           if constexpr (EPI == kEpiDGelu) {
-            if ((tma_out & 4) && kb == max(0, num_kb - kAuxPrefetchKb))  // as in the 256 x 256 pair kernel
+            // Z of this CTA's 128 output rows into L2 some k-blocks before the epilogue reads it
+            if ((tma_out & 4) && kb == max(0, num_kb - kAuxPrefetchKb))
               for (int j = 0; j < WIDE_BN / 64; ++j) tma_prefetch_l2_2d(&tmap_c2, nb * WIDE_BN + j * 64, a_row);
           }
           if (pacer && kb % kPaceKb == 0) {
@@ -1528,7 +1530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * BN);
-        epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row,
+        epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI, true>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row,
                                                             M, N, nb * WIDE_BN + h * BN, c_begin, t_row, 0, 1.f, row,
                                                             2 * nb + h, 2 * num_nb, tm_out, tm_out2);
         tc_fence_before();
@@ -1609,9 +1611,9 @@ cudaError_t make_out_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_out_maps(OutMaps* om, EpiKind epi, const EpiParams& ep, int64_t M, int64_t N) {
+cudaError_t make_out_maps(OutMaps* om, EpiKind epi, const EpiParams& ep, int64_t M, int64_t N, bool wide) {
   om->flags = 0;
-  const bool kind_ok = epi == kEpiStore || epi == kEpiStoreF32 || epi == kEpiGelu || epi == kEpiDGelu;
+  const bool kind_ok = epi == kEpiStore || epi == kEpiStoreF32 || epi == kEpiGelu || (wide && epi == kEpiDGelu);
   if (!kind_ok || ep.remap.enabled) return cudaSuccess;
   const bool f32 = epi == kEpiStoreF32;
   const int64_t elt = f32 ? 4 : 2;
@@ -1634,10 +1636,10 @@ cudaError_t make_out_maps(OutMaps* om, EpiKind epi, const EpiParams& ep, int64_t
     if (e != cudaSuccess) return e;
     om->flags |= 4;
   }
-  // GeLU and GeLU' compile the bulk-store path alone in the pair kernels: every output they
-  // write needs its map (the API's shape and alignment checks guarantee it).
+  // GeLU (both pair kernels) and GeLU' (the wide one) compile the bulk-store path alone: every
+  // output they write needs its map (the API's shape and alignment checks guarantee it).
   if (epi == kEpiGelu && ((ep.out && !(om->flags & 1)) || !(om->flags & 2))) return cudaErrorInvalidValue;
-  if (epi == kEpiDGelu && !(om->flags & 1)) return cudaErrorInvalidValue;
+  if (wide && epi == kEpiDGelu && !(om->flags & 1)) return cudaErrorInvalidValue;
   return cudaSuccess;
 }
 
@@ -1889,7 +1891,7 @@ cudaError_t gemm_bf16_tc(int64_t M, int64_t N, int64_t K, const Operand& a, cons
   if (pair) {
     if (epi == kEpiDropoutResidual && N % 32 != 0) return cudaErrorInvalidValue;
     OutMaps om;
-    e = make_out_maps(&om, epi, ep, M, N);
+    e = make_out_maps(&om, epi, ep, M, N, wide);
     if (e != cudaSuccess) return e;
     return wide ? dispatch_pair<true>(a.mn_major, b.mn_major, epi, ta, tb, om, m, n, k, ep, stream, ctx)
                 : dispatch_pair<false>(a.mn_major, b.mn_major, epi, ta, tb, om, m, n, k, ep, stream, ctx);
