@@ -1812,20 +1812,29 @@ int pair_kernel_choice() { return g_pair_kernel.load(std::memory_order_relaxed);
 
 // Whether 256 x 512 tiles beat 256 x 256 tiles for one GEMM, by a model of the persistent launch:
 // its waves of tiles over the resident pairs (a partial last wave costs a full one); a 256 x 512
-// wave costs 2 x (0.91 + e / K) of a 256 x 256 one. 0.91 is the measured gain of 25 % fewer
-// operand bytes per FLOP (GB300, K = 8192-32768); e / K is the epilogue, exposed once per wide
-// tile (the single accumulator set) and shorter against a longer main loop: e = 600 k-values for
-// GeLU / GeLU' / dropout / row-dot epilogues (measured 0.99 at K = 8192, 1.07 at K = 4096), 400 for fp32
-// stores and 250 for bf16 stores (1-2 % at K = 16384-32768, from a copy of the kernel whose MMAs
-// do not wait for the epilogue).
+// wave costs 2 x (u + e / K) of a 256 x 256 one. u is the gain of 25 % fewer operand bytes per
+// FLOP, e / K the epilogue that the single accumulator set leaves exposed once per wide tile, in
+// k-values of main loop. Fitted per epilogue kind on GB300 (serialised launch times of both tile
+// shapes at K = 4096-32768: the three MLP shapes and the attention projections): fp32 stores
+// (weight gradients, both operands MN-major) u 0.875, e 40; bf16 stores u 0.905, e 180; GeLU
+// u 0.92, e 200; GeLU' (reads Z) u 0.90, e 540; the row-dot epilogue u 0.91, e 450. The dropout
+// and fp32 read-add-write epilogues are not fitted and keep the earlier, cautious u 0.91 with
+// e 600 and 400.
 bool prefer_wide(int64_t M, int64_t N, int64_t K, EpiKind epi, int pairs) {
   const int64_t mb = (M + 2 * BM - 1) / (2 * BM);
   const int64_t t256 = mb * ((N + BN - 1) / BN), t512 = mb * ((N + WIDE_BN - 1) / WIDE_BN);
   const int64_t w256 = (t256 + pairs - 1) / pairs, w512 = (t512 + pairs - 1) / pairs;
-  const bool heavy = epi == kEpiGelu || epi == kEpiDGelu || epi == kEpiDropoutResidual || epi == kEpiStoreRowDot;
-  const bool f32 = epi == kEpiStoreF32 || epi == kEpiAccumF32;
-  const double e = heavy ? 600.0 : (f32 ? 400.0 : 250.0);
-  const double unit = 0.91 + e / static_cast<double>(K);
+  double u = 0.905, e = 180.0;  // bf16 stores
+  switch (epi) {
+    case kEpiStoreF32: u = 0.875; e = 40.0; break;
+    case kEpiGelu: u = 0.92; e = 200.0; break;
+    case kEpiDGelu: u = 0.90; e = 540.0; break;
+    case kEpiStoreRowDot: u = 0.91; e = 450.0; break;
+    case kEpiDropoutResidual: u = 0.91; e = 600.0; break;
+    case kEpiAccumF32: u = 0.91; e = 400.0; break;
+    default: break;
+  }
+  const double unit = u + e / static_cast<double>(K);
   return 2.0 * unit * static_cast<double>(w512) < static_cast<double>(w256);
 }
 
