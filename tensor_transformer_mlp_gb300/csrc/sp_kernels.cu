@@ -14,8 +14,17 @@
 namespace tpmlp {
 namespace {
 
-// Token row r = bi*s + j*sl + l  <->  shard-major row R = (j*b + bi)*sl + l.
+// Token row r = bi*s + j*sl + l  <->  shard-major row R = (j*b + bi)*sl + l. Row indices and
+// sizes below 2^31 take 32-bit divisions (a 64-bit division costs a few times more instructions,
+// paid by every thread of a row-per-CTA kernel).
 __device__ __forceinline__ int64_t shard_row_to_token(int64_t R, int64_t b, int64_t s, int64_t sl) {
+  if (((R | b | s) >> 31) == 0) {
+    const uint32_t jb = static_cast<uint32_t>(R) / static_cast<uint32_t>(sl);
+    const uint32_t l = static_cast<uint32_t>(R) - jb * static_cast<uint32_t>(sl);
+    const uint32_t j = jb / static_cast<uint32_t>(b);
+    const uint32_t bi = jb - j * static_cast<uint32_t>(b);
+    return static_cast<int64_t>(bi) * s + static_cast<int64_t>(j) * sl + l;
+  }
   const int64_t jb = R / sl;
   const int64_t l = R - jb * sl;
   const int64_t j = jb / b;
@@ -326,8 +335,8 @@ constexpr int dropout_min_blocks() { return sizeof(T) == 2 ? 16 : 8; }
 // tensor is dropped iff splitmix64(seed ^ k) < threshold. One thread per vector of 8
 // consecutive elements, one row per CTA (grid = rows, so the block scheduler balances the
 // tail); each element is decided by the high word of the last product (DropHash8) and the
-// rare cases redo the vector in full. 4 neighbouring lanes OR their bits into one 32-bit
-// mask word. kLow3 = seed & 7.
+// rare cases redo the vector in full. Each thread stores its vector's 8 mask bits as one byte
+// of the mask words. kLow3 = seed & 7.
 template <typename T, int kLow3>
 __global__ void __launch_bounds__(128, dropout_min_blocks<T>()) dropout_residual_kernel(
     const T* __restrict__ x, const T* __restrict__ y, T* __restrict__ out, uint32_t* __restrict__ mask_bits,
@@ -367,12 +376,10 @@ __global__ void __launch_bounds__(128, dropout_min_blocks<T>()) dropout_residual
         }
         if (redo) bits = dropout_vector_full(xr + v * 8, yr + v * 8, orow + v * 8, base, threshold, scale);
       }
-      if (mask_bits != nullptr) {
-        bits <<= 8 * (threadIdx.x & 3);
-        bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
-        bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
-        if (v < nvec && (threadIdx.x & 3) == 0) mask_bits[(flat_row + static_cast<uint64_t>(v) * 8) >> 5] = bits;
-      }
+      // The vector's 8 mask bits are byte k0 / 8 of the little-endian mask words (bit k of word
+      // k / 32): one byte store per thread, the warp's 32 bytes contiguous.
+      if (mask_bits != nullptr && v < nvec)
+        reinterpret_cast<uint8_t*>(mask_bits)[(flat_row + static_cast<uint64_t>(v) * 8) >> 3] = static_cast<uint8_t>(bits);
     }
   }
 }
@@ -619,6 +626,12 @@ constexpr size_t kStagedSmemMax = 100 * 1024;  // at least two CTAs per SM
 // ------------------------------------------------------------------ SP backward kernels
 // Inverse of shard_row_to_token: token row r = bi*s + j*sl + l -> shard-major row (j*b + bi)*sl + l.
 __device__ __forceinline__ int64_t token_to_shard_row(int64_t r, int64_t b, int64_t s, int64_t sl) {
+  if (((r | b | s) >> 31) == 0) {  // 32-bit divisions, as in shard_row_to_token
+    const uint32_t bi = static_cast<uint32_t>(r) / static_cast<uint32_t>(s);
+    const uint32_t si = static_cast<uint32_t>(r) - bi * static_cast<uint32_t>(s);
+    const uint32_t j = si / static_cast<uint32_t>(sl);
+    return (static_cast<int64_t>(j) * b + bi) * sl + (si - j * static_cast<uint32_t>(sl));
+  }
   const int64_t bi = r / s;
   const int64_t si = r - bi * s;
   const int64_t j = si / sl;
@@ -647,10 +660,12 @@ __global__ void __launch_bounds__(128, dropout_min_blocks<T>()) dropout_grad_gat
         float gf[8], o[8];
         gv.to_float(gf);
 #pragma unroll
-        for (uint32_t e = 0; e < 8; ++e) {
-          const uint32_t c = hs.high(e);
-          redo |= c == hs.thi;
-          o[e] = c < hs.thi ? 0.f : gf[e] * scale;
+        for (uint32_t e = 0; e < 8; e += 2) {  // pairs: g * scale on the f32x2 path
+          const uint32_t c0 = hs.high(e), c1 = hs.high(e + 1);
+          redo |= (c0 == hs.thi) | (c1 == hs.thi);
+          const float2 f = f2_split(f2_mul(f2_make(gf[e], gf[e + 1]), f2_make(scale, scale)));
+          o[e] = c0 < hs.thi ? 0.f : f.x;
+          o[e + 1] = c1 < hs.thi ? 0.f : f.y;
         }
         Vec8<T> ov;
         ov.from_float(o);
