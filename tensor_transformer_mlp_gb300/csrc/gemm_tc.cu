@@ -315,11 +315,11 @@ constexpr int kEpiChunks = BN / 32 / (NUM_EPI_WARPS / 4);  // 32-column chunks p
 
 // tm_out / tm_out2 (non-null: the plain store kinds in the pair kernels, rows not remapped) send
 // ep.out / ep.out2 through bulk tensor stores instead of store_staged. kTmaOnly (GeLU in the pair
-// kernels, GeLU' in the wide one: their outputs always have tensor maps) compiles the bulk-store
-// path alone. (The 256 x 256 kernel's GeLU' epilogue, which overlaps the next tile's main loop,
-// measured 15 % slower with bulk stores or with the L2 prefetch of Z, so it keeps both out.)
-template <int EPI, bool kWide>
-constexpr bool kTmaEpi = EPI == kEpiGelu || (kWide && EPI == kEpiDGelu);
+// kernels: both outputs always have tensor maps) compiles the bulk-store path alone. The wide
+// kernel has its own GeLU' epilogue; the 256 x 256 kernel's, which overlaps the next tile's main
+// loop, measured 15 % slower with bulk stores or with an L2 prefetch of Z, so it keeps both out.
+template <int EPI>
+constexpr bool kTmaEpi = EPI == kEpiGelu;
 
 template <int EPI, bool BATCHED, int kChunks = kEpiChunks, bool kTmaOnly = false>
 __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf, int lane, int64_t row, int M, int N,
@@ -560,24 +560,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
       tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       uint4 zs[8];
-      {
-        uint4 r8[8];
-        if constexpr (kTmaOnly) {
-          // rows are not remapped: lane reads rows row0 + i * 4 + lane / 8, segment lane % 8
-          const int64_t r_first = static_cast<int64_t>(row0) + (lane >> 3);
-          const int col = col0 + (lane & 7) * 8;
-          const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(ep.aux) + r_first * ep.ldo + col;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            r8[i] = make_uint4(0, 0, 0, 0);
-            if (r_first + i * 4 < M && col < N) r8[i] = *reinterpret_cast<const uint4*>(src + i * 4 * ep.ldo);
-          }
-          buf_acquire(lane);  // the previous pass's bulk store has read the buffer
-        } else {
-          issue_block_loads(r8, lane, prow, ep.aux, ep.ldo, col0, N);
-        }
-        transpose_block(buf, r8, zs, lane);
-      }
+      load_staged_bf16(buf, zs, lane, prow, ep.aux, ep.ldo, col0, N);
       tmem_ld_wait();
       if (ep.gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path; D overwrites Z in place
 #pragma unroll
@@ -598,10 +581,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
           zs[g] = dgelu_other8(v[g * 8], v[g * 8 + 1], v[g * 8 + 2], v[g * 8 + 3], v[g * 8 + 4], v[g * 8 + 5],
                                v[g * 8 + 6], v[g * 8 + 7], zs[g], ep.gelu);
       }
-      if constexpr (kTmaOnly)
-        store_tma(buf, zs, lane, tm_out, col0, row0);
-      else
-        store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
+      store_staged<false>(buf, zs, lane, prow, ep.out, ep.ldo, col0, N);
     }
   } else {
 #pragma unroll 1
@@ -1242,7 +1222,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       coords(tile, mb, nb);
       const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI, false>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M,
+      epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row, M,
                                                           N, nb * BN, c_begin, t_row, 0, 1.f, row, nb, num_nb,
                                                           tm_out, tm_out2);
       tc_fence_before();
@@ -1260,6 +1240,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+// GeLU' epilogue pieces of the wide kernel. load_z_block: the warp's 32 rows x 64 columns of Z
+// from row0 / col0 into registers, line-wide (lane: rows row0 + i * 4 + lane / 8, segment
+// lane % 8; zeros past M or N), as issue_block_loads for rows that are not remapped.
+__device__ __forceinline__ void load_z_block(uint4 (&r8)[8], const EpiParams& ep, int lane, int64_t row0, int col0,
+                                             int M, int N) {
+  const int64_t r_first = row0 + (lane >> 3);
+  const int col = col0 + (lane & 7) * 8;
+  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(ep.aux) + r_first * ep.ldo + col;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    r8[i] = make_uint4(0, 0, 0, 0);
+    if (r_first + i * 4 < M && col < N) r8[i] = *reinterpret_cast<const uint4*>(src + i * 4 * ep.ldo);
+  }
+}
+
+// D = acc * gelu'(Z) for 32 columns of the lane's row: z[0..3] hold the 32 bf16 Z values and
+// receive D; v the 32 accumulator values.
+__device__ __forceinline__ void dgelu_32(uint4* z, const uint32_t (&v)[32], int gelu) {
+  if (gelu == kGeluTanh) {  // uniform: pairs of elements on the f32x2 path
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(&z[g]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const F2 z2 = f2_make(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+        const float2 d2 = f2_split(f2_mul(f2_make(__uint_as_float(v[g * 8 + 2 * i]), __uint_as_float(v[g * 8 + 2 * i + 1])),
+                                          gelu_grad_tanh2(z2)));
+        w[i] = pack_bf16x2(d2.x, d2.y);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      z[g] = dgelu_other8(v[g * 8], v[g * 8 + 1], v[g * 8 + 2], v[g * 8 + 3], v[g * 8 + 4], v[g * 8 + 5], v[g * 8 + 6],
+                          v[g * 8 + 7], z[g], gelu);
   }
 }
 
@@ -1520,21 +1538,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const CUtensorMap* tm_out2 = (tma_out & 2) ? &tmap_c2 : nullptr;
     int it = 0;
     bool ok = true;
-    for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
-      int mb, nb;
-      coords(tile, mb, nb);
-      const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
+    if constexpr (EPI == kEpiDGelu) {
+      // The warp's four 64-column passes of a tile (two per half) are pipelined on Z: the next
+      // pass's Z is loaded into registers while this one is computed, and the tile's first pass
+      // is loaded before its accumulator is ready, so no pass waits for its Z. Stores by bulk
+      // tensor copies (tm_out is always set for this kind).
+      uint8_t* buf = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
+        int mb, nb;
+        coords(tile, mb, nb);
+        const int64_t row0 = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32;
+        auto pass_col = [&](int p) { return nb * WIDE_BN + (p >> 1) * BN + (c_begin + 2 * (p & 1)) * 32; };
+        uint4 r8[8];
+        load_z_block(r8, ep, lane, row0, pass_col(0), M, N);
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[h], static_cast<uint32_t>(it & 1), status, 36));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * BN);
-        epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI, true>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row,
-                                                            M, N, nb * WIDE_BN + h * BN, c_begin, t_row, 0, 1.f, row,
-                                                            2 * nb + h, 2 * num_nb, tm_out, tm_out2);
-        tc_fence_before();
-        mbar_arrive_cluster(map_to_cta(&tempty_bar[h], 0));
+        for (int h = 0; h < 2; ++h) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[h], static_cast<uint32_t>(it & 1), status, 36));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * BN);
+#pragma unroll 1
+          for (int k = 0; k < 2; ++k) {
+            const int p = 2 * h + k;
+            const int col0 = pass_col(p);
+            uint4 zs[8];
+            buf_acquire(lane);  // the previous pass's bulk store has read the buffer
+            transpose_block(buf, r8, zs, lane);
+            if (p < 3) load_z_block(r8, ep, lane, row0, pass_col(p + 1), M, N);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>((c_begin + 2 * k + j) * 32), v);
+              tmem_ld_wait();
+              dgelu_32(&zs[4 * j], v, ep.gelu);
+            }
+            if (col0 < N) store_tma(buf, zs, lane, tm_out, col0, static_cast<int>(row0));
+          }
+          tc_fence_before();
+          mbar_arrive_cluster(map_to_cta(&tempty_bar[h], 0));
+        }
+      }
+    } else {
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
+        int mb, nb;
+        coords(tile, mb, nb);
+        const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[h], static_cast<uint32_t>(it & 1), status, 36));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * BN);
+          epilogue_tile<EPI, false, kEpiChunks, kTmaEpi<EPI>>(ep, epi_stage + (warp - 2) * EPI_STAGE_BYTES, lane, row,
+                                                              M, N, nb * WIDE_BN + h * BN, c_begin, t_row, 0, 1.f, row,
+                                                              2 * nb + h, 2 * num_nb, tm_out, tm_out2);
+          tc_fence_before();
+          mbar_arrive_cluster(map_to_cta(&tempty_bar[h], 0));
+        }
       }
     }
     if (lane == 0) bulk_wait_group_all();  // the last bulk stores have completed
