@@ -68,12 +68,15 @@ constexpr int EPI_STAGE_BYTES = 32 * 128;
 constexpr int AUX_BUF_BYTES = 32 * 128;  // one 32-row x 64-column bf16 block
 // kAuxBufs > 0 (the batched softmax and dS epilogues): each epilogue warp owns that many 4 KB
 // buffers for TMA loads of P and TMA stores of its output instead of the generic staging buffer,
-// and the ring shrinks to 2 stages (the score-shaped GEMMs have K = head_dim = two k-blocks).
+// and the ring shrinks to 3 stages with 2 buffers a warp, 2 stages with 4 (the score-shaped GEMMs
+// have K = head_dim = two k-blocks, so with 2 stages the next tile's operands cannot be loaded
+// before the current tile's MMAs have freed a stage: the softmax pass measured 128.7 us with
+// 2 stages and 4 buffers, 115.3 us with 3 stages and 2, the same with 4 stages and 1).
 template <int BN_T, int kAuxBufs = 0>
 struct OneSm {
   static constexpr bool kAux = kAuxBufs > 0;
   static constexpr int kBN = BN_T;
-  static constexpr int kStages = kAux ? 2 : (BN_T == 256 ? 4 : 6);
+  static constexpr int kStages = kAux ? (kAuxBufs >= 4 ? 2 : 3) : (BN_T == 256 ? 4 : 6);
   static constexpr int kStageBytes = A_STAGE_BYTES + BN_T * BK * 2;
   static constexpr int kEpiStageBytes = kAux ? 0 : NUM_EPI_WARPS * EPI_STAGE_BYTES;
   static constexpr int kAuxBytes = NUM_EPI_WARPS * kAuxBufs * AUX_BUF_BYTES;
@@ -596,10 +599,10 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
   }
 }
 
-// Per-warp TMA buffers of the batched epilogues: kEpiSoftmax stores P through four (up to three
-// stores in flight while the next pass is computed); kEpiSoftmaxGrad loads P through two and
-// stores dS through two more.
-constexpr int kSoftmaxStoreBufs = 4;
+// Per-warp TMA buffers of the batched epilogues: kEpiSoftmax stores P through two (one store in
+// flight while the next pass is computed); kEpiSoftmaxGrad loads P through two and stores dS
+// through two more.
+constexpr int kSoftmaxStoreBufs = 2;
 template <int EPI, bool BATCHED>
 __host__ __device__ constexpr int aux_bufs() {
   return !BATCHED ? 0 : (EPI == kEpiSoftmax ? kSoftmaxStoreBufs : (EPI == kEpiSoftmaxGrad ? 4 : 0));
@@ -1877,7 +1880,7 @@ int pair_kernel_choice() { return g_pair_kernel.load(std::memory_order_relaxed);
 // k-values of main loop. Fitted per epilogue kind on GB300 (serialised launch times of both tile
 // shapes at K = 4096-32768: the three MLP shapes and the attention projections): fp32 stores
 // (weight gradients, both operands MN-major) u 0.875, e 40; bf16 stores u 0.905, e 180; GeLU
-// u 0.92, e 200; GeLU' (reads Z) u 0.90, e 540; the row-dot epilogue u 0.91, e 450. The dropout
+// u 0.92, e 200; GeLU' (reads Z, pipelined) u 0.90, e 370; the row-dot epilogue u 0.91, e 450. The dropout
 // and fp32 read-add-write epilogues are not fitted and keep the earlier, cautious u 0.91 with
 // e 600 and 400.
 bool prefer_wide(int64_t M, int64_t N, int64_t K, EpiKind epi, int pairs) {
@@ -1888,7 +1891,7 @@ bool prefer_wide(int64_t M, int64_t N, int64_t K, EpiKind epi, int pairs) {
   switch (epi) {
     case kEpiStoreF32: u = 0.875; e = 40.0; break;
     case kEpiGelu: u = 0.92; e = 200.0; break;
-    case kEpiDGelu: u = 0.90; e = 540.0; break;
+    case kEpiDGelu: u = 0.90; e = 370.0; break;
     case kEpiStoreRowDot: u = 0.91; e = 450.0; break;
     case kEpiDropoutResidual: u = 0.91; e = 600.0; break;
     case kEpiAccumF32: u = 0.91; e = 400.0; break;
