@@ -803,11 +803,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // P = 2^(acc * c - M) / L written by TMA stores: each 64-column pass of the warp's 32 rows
       // goes into one of its kSoftmaxStoreBufs 4 KB buffers in the 128-byte-swizzled layout the
       // store expects, and lane 0 issues the store; a buffer is reused once the store
-      // kSoftmaxStoreBufs passes back has read it.
+      // kSoftmaxStoreBufs passes back has read it. The row statistics of the next tile are
+      // loaded while this one is processed, and the warp's four 32-column tensor-memory loads
+      // are double-buffered (chunk j + 1 in flight while chunk j is converted).
       uint8_t* sb = aux_buf + (warp - 2) * kAuxBufs * AUX_BUF_BYTES;
+      const float c2 = bd.alpha * kLog2e;
+      auto load_stats = [&](int tile) {
+        int z1, z2, mb, nb;
+        tile_coords(tile, z1, z2, mb, nb);
+        const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+        const int64_t srow = (static_cast<int64_t>(z2) * bd.nz1 + z1) * M + row;
+        return row < M ? static_cast<const float2*>(ep.rowvec)[srow] : make_float2(0.f, 0.f);
+      };
       int nstore = 0;
       int it = 0;
+      float2 st_next = blockIdx.x < total_tiles ? load_stats(blockIdx.x) : make_float2(0.f, 0.f);
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+        const float2 st = st_next;
+        if (tile + static_cast<int>(gridDim.x) < total_tiles) st_next = load_stats(tile + gridDim.x);
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
         const bool ok = mbar_wait(&tfull_bar[acc], use & 1, status, 6);
@@ -815,43 +828,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         int z1, z2, mb, nb;
         tile_coords(tile, z1, z2, mb, nb);
-        const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-        const int64_t srow = (static_cast<int64_t>(z2) * bd.nz1 + z1) * M + row;
-        const float c2 = bd.alpha * kLog2e;
-        const float2 st = row < M ? static_cast<const float2*>(ep.rowvec)[srow] : make_float2(0.f, 0.f);
-#pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
-          const int c = c_begin + 2 * k;
-          const int col0 = nb * BN + c * 32;
-          if (col0 >= N) break;  // uniform across the warp
-          uint32_t v[64];
-          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v));
-          tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32 + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-          tmem_ld_wait();
-          uint4 seg[8];
+        uint32_t va[32], vb[32];
+        uint4 seg[8];
+        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c_begin * 32), va);
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
+        for (int j = 0; j < 4; ++j) {
+          tmem_ld_wait();
+          uint32_t(&cur)[32] = (j & 1) ? vb : va;
+          uint32_t(&nxt)[32] = (j & 1) ? va : vb;
+          if (j < 3) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>((c_begin + j + 1) * 32), nxt);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
             float pv[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(v[g * 8 + i]), c2, -st.x)) * st.y;
-            seg[g] = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
-                                pack_bf16x2(pv[6], pv[7]));
+            for (int i = 0; i < 8; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(cur[g * 8 + i]), c2, -st.x)) * st.y;
+            seg[(j & 1) * 4 + g] = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
+                                              pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
           }
-          uint8_t* buf = sb + (nstore % kSoftmaxStoreBufs) * AUX_BUF_BYTES;
-          if (lane == 0 && nstore >= kSoftmaxStoreBufs) bulk_wait_group_read<kSoftmaxStoreBufs - 1>();
-          __syncwarp();
+          if (j & 1) {  // a 64-column block is complete
+            const int col0 = nb * BN + (c_begin + j - 1) * 32;
+            uint8_t* buf = sb + (nstore % kSoftmaxStoreBufs) * AUX_BUF_BYTES;
+            if (lane == 0 && nstore >= kSoftmaxStoreBufs) bulk_wait_group_read<kSoftmaxStoreBufs - 1>();
+            __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = seg[j];
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            int cc[4];
-            aux_coords(col0, mb * BM + q * 32, z1, z2, cc);
-            tma_store_4d(&tmap_out, buf, cc[0], cc[1], cc[2], cc[3]);
-            bulk_commit_group();
+            for (int jj = 0; jj < 8; ++jj)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((jj ^ (lane & 7)) << 4)) = seg[jj];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && col0 < N) {  // a block wholly past N is not stored
+              int cc[4];
+              aux_coords(col0, mb * BM + q * 32, z1, z2, cc);
+              tma_store_4d(&tmap_out, buf, cc[0], cc[1], cc[2], cc[3]);
+            }
+            if (lane == 0) bulk_commit_group();  // (an empty group for a skipped block keeps the count)
+            ++nstore;
           }
-          ++nstore;
         }
         tc_fence_before();
         mbar_arrive(&tempty_bar[acc]);
