@@ -497,8 +497,8 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       static_cast<float2*>(ep.stats)[srow * (2 * num_nb) + 2 * nb + half] = make_float2(m, l);
     }
   } else if constexpr (EPI == kEpiSoftmax) {
-    // P = 2^(acc * c - M) / L with the row's combined base-2 statistics (M, 1/L), 64 columns
-    // per pass, staged.
+    // P = 2^(acc * c - M) / L = 2^(acc * c - (M + log2 L)) with the row's combined base-2
+    // statistics (rowvec .x = M + log2 L), 64 columns per pass, staged.
     const float c2 = alpha * kLog2e;
     const float2 st = row < M ? static_cast<const float2*>(ep.rowvec)[srow] : make_float2(0.f, 0.f);
     const int64_t prow = row < M ? row : -1;
@@ -516,7 +516,7 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
       for (int g = 0; g < 8; ++g) {
         float p[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) p[i] = ex2_approx(fmaf(__uint_as_float(v[g * 8 + i]), c2, -st.x)) * st.y;
+        for (int i = 0; i < 8; ++i) p[i] = ex2_approx(fmaf(__uint_as_float(v[g * 8 + i]), c2, -st.x));
         seg[g] = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
                             pack_bf16x2(p[6], p[7]));
       }
@@ -800,7 +800,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     cc[3] = bd.x_row == 3 ? row : (bd.x_z1 == 3 ? z1 : z2);
   };
   if constexpr (kAux && EPI == kEpiSoftmax) {
-      // P = 2^(acc * c - M) / L written by TMA stores: each 64-column pass of the warp's 32 rows
+      // P = 2^(acc * c - M) / L = 2^(acc * c - (M + log2 L)), one FFMA and one ex2 per score
+      // (the row statistics carry M + log2 L), written by TMA stores: each 64-column pass of the warp's 32 rows
       // goes into one of its kSoftmaxStoreBufs 4 KB buffers in the 128-byte-swizzled layout the
       // store expects, and lane 0 issues the store; a buffer is reused once the store
       // kSoftmaxStoreBufs passes back has read it. The row statistics of the next tile are
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int g = 0; g < 4; ++g) {
             float pv[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(cur[g * 8 + i]), c2, -st.x)) * st.y;
+            for (int i = 0; i < 8; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(cur[g * 8 + i]), c2, -st.x));
             seg[(j & 1) * 4 + g] = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
                                               pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
           }

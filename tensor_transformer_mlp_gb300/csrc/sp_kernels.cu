@@ -1079,7 +1079,7 @@ __global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restri
 // ------------------------------------------------------------------ attention softmax (fused form)
 // Row r's partial statistics (m_j, l_j) from the scores GEMM's kEpiRowStats epilogue (base 2:
 // m_j = max of the scaled scores times log2(e), l_j = sum of 2^(y - m_j)) become M = max_j m_j
-// and 1/L with L = sum_j l_j * 2^(m_j - M); one warp per row, lanes over j.
+// and L = sum_j l_j * 2^(m_j - M), stored as (M + log2 L, 1/L); one warp per row, lanes over j.
 __global__ void __launch_bounds__(256) softmax_combine_kernel(const float2* __restrict__ stats, int nparts,
                                                               float2* __restrict__ rowstats, int64_t rows) {
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -1100,7 +1100,8 @@ __global__ void __launch_bounds__(256) softmax_combine_kernel(const float2* __re
 #pragma unroll
   for (int k = 0; k < 2; ++k) L += v[k].y > 0.f ? v[k].y * ex2_approx(v[k].x - M) : 0.f;
   L = warp_sum(L);
-  if (lane == 0) rowstats[r] = make_float2(M, 1.0f / L);
+  // the softmax pass needs only M + log2(L): P = 2^(y - M) / L = 2^(y - (M + log2 L))
+  if (lane == 0) rowstats[r] = make_float2(M + log2f(L), 1.0f / L);
 }
 
 // D[(bi*heads + j)*s + si] = sum over head j's dh columns of dO * O in token row bi*s + si

@@ -25,7 +25,7 @@ enum EpiKind : int {
   // Attention softmax in two GEMM passes over the same scores x = alpha * acc (batched only):
   // (statistics in base 2: y = x * log2(e), so exp(x - max x) = 2^(y - max y))
   kEpiRowStats = 6,     // stats[srow][2*nb + half] = (max y, sum 2^(y - max y)) over the warp's columns
-  kEpiSoftmax = 7,      // out[r][c] = 2^(y - rowvec[srow].M) * rowvec[srow].invL  (P, operand dtype)
+  kEpiSoftmax = 7,      // out[r][c] = 2^(y - rowvec[srow].x), .x = M + log2 L  (P, operand dtype)
   kEpiSoftmaxGrad = 8,  // out[r][c] = escale * aux[r][c] * (x - rowvec[srow])  (dS from dP, P and D)
   // out[r][c] = acc (bf16) and, per 128-column head j of the row, rowdot[(bi * heads + j) * s + si]
   // = sum over the head's columns of out[r][c] * aux[r][c], with r = bi * s + si (plain GEMMs;
@@ -59,7 +59,7 @@ struct EpiParams {
   int gelu;
   RowRemap remap;
   DropoutParams drop;
-  // kEpiRowStats: float2 partial row statistics [rows][2 * N-blocks]; kEpiSoftmax: float2 (M, 1/L)
+  // kEpiRowStats: float2 partial row statistics [rows][2 * N-blocks]; kEpiSoftmax: float2 (M + log2 L, 1/L)
   // per row; kEpiSoftmaxGrad: float D per row. Rows of a batched launch are numbered
   // srow = (z2 * nz1 + z1) * M + r.
   void* stats;
@@ -172,7 +172,7 @@ cudaError_t launch_layernorm_backward(const void* x, const void* dxn, const void
                                       bool bf16, cudaStream_t stream, int num_sms, bool rms = false,
                                       unsigned int* status = nullptr);
 
-// Attention helpers: combine the kEpiRowStats partials of each row into (M, 1/L); and
+// Attention helpers: combine the kEpiRowStats partials of each row into (M + log2 L, 1/L); and
 // D[(bi*heads + j)*s + si] = dot(dO, O) over head j's columns of token row bi*s + si.
 cudaError_t launch_softmax_combine(const void* stats, int nparts, void* rowstats, int64_t rows, cudaStream_t stream,
                                    int num_sms);
