@@ -14,17 +14,8 @@
 namespace tpmlp {
 namespace {
 
-// Token row r = bi*s + j*sl + l  <->  shard-major row R = (j*b + bi)*sl + l. Row indices and
-// sizes below 2^31 take 32-bit divisions (a 64-bit division costs a few times more instructions,
-// paid by every thread of a row-per-CTA kernel).
+// Token row r = bi*s + j*sl + l  <->  shard-major row R = (j*b + bi)*sl + l.
 __device__ __forceinline__ int64_t shard_row_to_token(int64_t R, int64_t b, int64_t s, int64_t sl) {
-  if (((R | b | s) >> 31) == 0) {
-    const uint32_t jb = static_cast<uint32_t>(R) / static_cast<uint32_t>(sl);
-    const uint32_t l = static_cast<uint32_t>(R) - jb * static_cast<uint32_t>(sl);
-    const uint32_t j = jb / static_cast<uint32_t>(b);
-    const uint32_t bi = jb - j * static_cast<uint32_t>(b);
-    return static_cast<int64_t>(bi) * s + static_cast<int64_t>(j) * sl + l;
-  }
   const int64_t jb = R / sl;
   const int64_t l = R - jb * sl;
   const int64_t j = jb / b;
@@ -626,12 +617,6 @@ constexpr size_t kStagedSmemMax = 100 * 1024;  // at least two CTAs per SM
 // ------------------------------------------------------------------ SP backward kernels
 // Inverse of shard_row_to_token: token row r = bi*s + j*sl + l -> shard-major row (j*b + bi)*sl + l.
 __device__ __forceinline__ int64_t token_to_shard_row(int64_t r, int64_t b, int64_t s, int64_t sl) {
-  if (((r | b | s) >> 31) == 0) {  // 32-bit divisions, as in shard_row_to_token
-    const uint32_t bi = static_cast<uint32_t>(r) / static_cast<uint32_t>(s);
-    const uint32_t si = static_cast<uint32_t>(r) - bi * static_cast<uint32_t>(s);
-    const uint32_t j = si / static_cast<uint32_t>(sl);
-    return (static_cast<int64_t>(j) * b + bi) * sl + (si - j * static_cast<uint32_t>(sl));
-  }
   const int64_t bi = r / s;
   const int64_t si = r - bi * s;
   const int64_t j = si / sl;
