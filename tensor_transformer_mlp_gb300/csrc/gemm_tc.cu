@@ -1326,7 +1326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                           const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_c2,
                           int tma_out, int M, int N, int K, EpiParams ep, unsigned int* status, int group,
-                          unsigned int* pace) {
+                          unsigned int* pace, int tail_split) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -1369,6 +1369,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   };
   const int num_kb = (K + BK - 1) / BK;
+  // Work of round r: wide tile pair + r * num_pairs (half = -1: both halves). With tail_split the
+  // last, partial round is split in 256-column half-tiles, one per pair (pairs 2i and 2i + 1 take
+  // the two halves of the round's i-th tile), so that it takes about half a round.
+  const int rounds_full = (num_tiles + num_pairs - 1) / num_pairs - (tail_split ? 1 : 0);
+  const int tail_tiles = num_tiles - rounds_full * num_pairs;
+  auto work = [&](int round, int& tile, int& half) -> bool {
+    if (round < rounds_full) {
+      tile = pair + round * num_pairs;
+      half = -1;
+      return tile < num_tiles;
+    }
+    if (!tail_split || round > rounds_full || pair >= 2 * tail_tiles) return false;
+    tile = rounds_full * num_pairs + (pair >> 1);
+    half = pair & 1;
+    return true;
+  };
 
   if (warp == 0 && lane == 0) {
 #pragma unroll
@@ -1401,16 +1417,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       const bool pacer = pace != nullptr && rank == 0;  // pacing as in the 256 x 256 pair kernel
       unsigned int pace_target = 0;
-      for (int tile = pair, round = 0; tile < num_tiles && ok; tile += num_pairs, ++round) {
+      int tile, half;
+      for (int round = 0; ok && work(round, tile, half); ++round) {
         int mb, nb;
         coords(tile, mb, nb);
         const int a_row = mb * 2 * BM + static_cast<int>(rank) * BM;
-        const unsigned int active = static_cast<unsigned int>(min(num_pairs, num_tiles - round * num_pairs));
+        const unsigned int active = static_cast<unsigned int>(
+            round < rounds_full ? min(num_pairs, num_tiles - round * num_pairs) : 2 * tail_tiles);
+        const uint32_t stage_tx = half < 0 ? 2 * WIDE_STAGE_BYTES : 2 * (A_STAGE_BYTES + WIDE_CHUNK_BYTES);
         for (int kb = 0; kb < num_kb; ++kb) {
           if constexpr (EPI == kEpiDGelu) {
             // Z of this CTA's 128 output rows into L2 some k-blocks before the epilogue reads it
             if ((tma_out & 4) && kb == max(0, num_kb - kAuxPrefetchKb))
-              for (int j = 0; j < WIDE_BN / 64; ++j) tma_prefetch_l2_2d(&tmap_c2, nb * WIDE_BN + j * 64, a_row);
+              for (int j = (half == 1 ? 4 : 0); j < (half == 0 ? 4 : 8); ++j)
+                tma_prefetch_l2_2d(&tmap_c2, nb * WIDE_BN + j * 64, a_row);
           }
           if (pacer && kb % kPaceKb == 0) {
             pace_wait(pace, pace_target, kPaceWaitNs);
@@ -1423,7 +1443,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * WIDE_STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], stage_tx);
           const int kbl = (round & 1) ? num_kb - 1 - kb : kb;  // K backwards in odd rounds (as above)
           const uint32_t full0 = map_to_cta(&full_bar[s], 0);
           uint8_t* sa = smem + s * WIDE_STAGE_BYTES;
@@ -1436,6 +1456,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {  // this CTA's 128 columns of each 256-column half
+            if (half >= 0 && h != half) continue;
             const int b_col = nb * WIDE_BN + h * BN + static_cast<int>(rank) * BN_HALF;
             uint8_t* sbh = sb + h * WIDE_CHUNK_BYTES;
             if constexpr (!B_MN) {
@@ -1474,8 +1495,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
       int kiter = 0, it = 0;
       bool ok = true;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
+      int tile, half;
+      for (; ok && work(it, tile, half); ++it) {
         const uint32_t prev = static_cast<uint32_t>(it & 1) ^ 1;  // phase of the previous tile's drain
+        if (half >= 0) {
+          // A half-tile of the split last round: only accumulator half `half`, committed on its
+          // full barrier (the other half's barriers see no more phases).
+          if (!mbar_wait(&tempty_bar[half], prev, status, 34)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kb = 0; kb < num_kb; ++kb) {
+            const int s = kiter % WIDE_STAGES;
+            if (!mbar_wait(&full_bar[s], (kiter / WIDE_STAGES) & 1, status, 33)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_half(s, kb, half);
+            umma_commit_pair_mc(&empty_bar[s], 0x3);
+            ++kiter;
+          }
+          if (!ok) break;
+          umma_commit_pair_mc(&tfull_bar[half], 0x3);
+          continue;
+        }
         // Half 0 runs ahead over the first `lead` k-blocks, while the epilogue may still be
         // draining half 1 of the previous tile; those stages stay resident until half 1 has
         // used them too, then each is freed. Over the last `tail` k-blocks half 0 goes first
@@ -1560,15 +1605,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // is loaded before its accumulator is ready, so no pass waits for its Z. Stores by bulk
       // tensor copies (tm_out is always set for this kind).
       uint8_t* buf = epi_stage + (warp - 2) * EPI_STAGE_BYTES;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
+      int tile, half;
+      for (; ok && work(it, tile, half); ++it) {
         int mb, nb;
         coords(tile, mb, nb);
         const int64_t row0 = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32;
         auto pass_col = [&](int p) { return nb * WIDE_BN + (p >> 1) * BN + (c_begin + 2 * (p & 1)) * 32; };
+        const int h_first = half < 0 ? 0 : half, h_last = half < 0 ? 1 : half;  // a half-tile: one half
         uint4 r8[8];
-        load_z_block(r8, ep, lane, row0, pass_col(0), M, N);
+        load_z_block(r8, ep, lane, row0, pass_col(2 * h_first), M, N);
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
+        for (int h = h_first; h <= h_last; ++h) {
           ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[h], static_cast<uint32_t>(it & 1), status, 36));
           if (!ok) break;
           tc_fence_after();
@@ -1580,7 +1627,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint4 zs[8];
             buf_acquire(lane);  // the previous pass's bulk store has read the buffer
             transpose_block(buf, r8, zs, lane);
-            if (p < 3) load_z_block(r8, ep, lane, row0, pass_col(p + 1), M, N);
+            if (p < 2 * h_last + 1) load_z_block(r8, ep, lane, row0, pass_col(p + 1), M, N);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               uint32_t v[32];
@@ -1595,12 +1642,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     } else {
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++it) {
+      int tile, half;
+      for (; ok && work(it, tile, half); ++it) {
         int mb, nb;
         coords(tile, mb, nb);
         const int64_t row = static_cast<int64_t>(mb) * 2 * BM + rank * BM + q * 32 + lane;
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
+        for (int h = (half < 0 ? 0 : half); h <= (half < 0 ? 1 : half); ++h) {
           ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[h], static_cast<uint32_t>(it & 1), status, 36));
           if (!ok) break;
           tc_fence_after();
@@ -1844,7 +1892,14 @@ cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
     }
     max_pairs = resident_pairs[ctx.device];
   }
-  const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+  // A last round with at most half the pairs busy is split into half-tiles (one per pair).
+  int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+  int tail_split = 0;
+  const int64_t waves = (tiles + max_pairs - 1) / max_pairs, tail = tiles - (waves - 1) * max_pairs;
+  if (2 * tail <= max_pairs) {
+    tail_split = 1;
+    pairs = static_cast<int>(waves > 1 ? max_pairs : 2 * tail);
+  }
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   unsigned int* pace = next_pace_counter();
   if (pace) {
@@ -1852,7 +1907,7 @@ cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const OutM
     if (e != cudaSuccess) return e;
   }
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, om.c, om.c2, om.flags, M, N, K, ep, ctx.status, pair_group(true),
-                            pace);
+                            pace, tail_split);
 }
 
 // The pair kernel (256 x 512 tiles if kWide, else 256 x 256) for one operand layout and epilogue.
@@ -1893,7 +1948,7 @@ int pair_kernel_choice() { return g_pair_kernel.load(std::memory_order_relaxed);
 // k-values of main loop. Fitted per epilogue kind on GB300 (serialised launch times of both tile
 // shapes at K = 4096-32768: the three MLP shapes and the attention projections): fp32 stores
 // (weight gradients, both operands MN-major) u 0.875, e 40; bf16 stores u 0.905, e 180; GeLU
-// u 0.92, e 200; GeLU' (reads Z, pipelined) u 0.90, e 370; the row-dot epilogue u 0.91, e 450. The dropout
+// u 0.92, e 200; GeLU' (reads Z, pipelined) u 0.87, e 570; the row-dot epilogue u 0.91, e 450. The dropout
 // and fp32 read-add-write epilogues are not fitted and keep the earlier, cautious u 0.91 with
 // e 600 and 400.
 bool prefer_wide(int64_t M, int64_t N, int64_t K, EpiKind epi, int pairs) {
@@ -1904,14 +1959,19 @@ bool prefer_wide(int64_t M, int64_t N, int64_t K, EpiKind epi, int pairs) {
   switch (epi) {
     case kEpiStoreF32: u = 0.875; e = 40.0; break;
     case kEpiGelu: u = 0.92; e = 200.0; break;
-    case kEpiDGelu: u = 0.90; e = 370.0; break;
+    case kEpiDGelu: u = 0.87; e = 570.0; break;
     case kEpiStoreRowDot: u = 0.91; e = 450.0; break;
     case kEpiDropoutResidual: u = 0.91; e = 600.0; break;
     case kEpiAccumF32: u = 0.91; e = 400.0; break;
     default: break;
   }
   const double unit = u + e / static_cast<double>(K);
-  return 2.0 * unit * static_cast<double>(w512) < static_cast<double>(w256);
+  // The wide kernel splits a last round that would keep at most half the pairs busy into
+  // half-tiles: that round then costs about one 256 x 256 wave.
+  const int64_t tail = t512 - (w512 - 1) * pairs;
+  const double wide = 2 * tail <= pairs ? 2.0 * unit * static_cast<double>(w512 - 1) + 1.0
+                                        : 2.0 * unit * static_cast<double>(w512);
+  return wide < static_cast<double>(w256);
 }
 
 // 4-D bf16 tensor map over a batched operand: dimension 0 is the contiguous column index; the
