@@ -282,7 +282,7 @@ def config_dict(cfg):
 
 # ----------------------------------------------------------------------------- SP kernels
 
-def measure_sp(dev, peaks, reps: int = 60, sets: int = 4):
+def measure_sp(dev, peaks, reps: int = 100, sets: int = 4):
     """Times the sequence-parallel block and each of its memory-bound kernels on the SP
     workload. Each kernel is launched `reps` times back to back, rotating over `sets` buffer
     sets so that the bytes touched between two uses of a set exceed the L2 cache."""
