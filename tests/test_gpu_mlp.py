@@ -19,9 +19,11 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "wor
 
 # The plain bf16 GEMMs' kernel variants (tpmlp_set_gemm_variant): SM pairs choosing 256 x 512 or
 # 256 x 256 tiles per shape (the default), the one-SM kernel, pairs without pacing, pairs on
-# 256 x 256 tiles only and pairs on 256 x 512 tiles only. The parity cases that take the
-# `gemm_variant` fixture run on each.
-GEMM_VARIANTS = {"pair": (1, 1, 0), "one_sm": (0, 1, 0), "unpaced": (1, 0, 0), "pair256": (2, 1, 0), "wide": (3, 1, 0)}
+# 256 x 256 tiles only, pairs on 256 x 512 tiles only, and two non-default tile bands. The
+# parity cases that take the `gemm_variant` fixture run on each.
+GEMM_VARIANTS = {"pair": (1, 1, 0), "one_sm": (0, 1, 0), "unpaced": (1, 0, 0), "pair256": (2, 1, 0), "wide": (3, 1, 0),
+                 # non-default tile bands: 3 N-blocks walked along M; 5 pair-rows (ragged last band)
+                 "nband3": (1, 1, -3), "wide_band5": (3, 1, 5)}
 
 
 @pytest.fixture(params=list(GEMM_VARIANTS))
