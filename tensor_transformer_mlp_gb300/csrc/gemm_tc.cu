@@ -486,10 +486,16 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
 #pragma unroll
       for (int i = 4; i < 32; ++i) c4[i & 3] = fmaxf(c4[i & 3], x[i]);
       const float mn = fmaxf(m, fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3])) * c2);
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      // y - mn = fma(acc, c, -mn) and the sums on fp32 pairs (f32x2): two accumulator pairs
+      const F2 c22 = f2_make(c2, c2), nmn = f2_make(-mn, -mn);
+      F2 s2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s4[i & 3] += ex2_approx(fmaf(x[i], c2, -mn));
-      l = l * ex2_approx(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+      for (int i = 0; i < 16; ++i) {
+        const float2 t = f2_split(f2_fma(f2_make(x[2 * i], x[2 * i + 1]), c22, nmn));
+        s2[i & 1] = f2_add(s2[i & 1], f2_make(ex2_approx(t.x), ex2_approx(t.y)));
+      }
+      const float2 a = f2_split(s2[0]), b = f2_split(s2[1]);
+      l = l * ex2_approx(m - mn) + ((a.x + b.x) + (a.y + b.y));
       m = mn;
     }
     if (row < M) {
