@@ -845,13 +845,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t(&cur)[32] = (j & 1) ? vb : va;
           uint32_t(&nxt)[32] = (j & 1) ? va : vb;
           if (j < 3) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>((c_begin + j + 1) * 32), nxt);
+          const F2 c22 = f2_make(c2, c2), nst = f2_make(-st.x, -st.x);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            float pv[8];
+            uint32_t w[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(cur[g * 8 + i]), c2, -st.x));
-            seg[(j & 1) * 4 + g] = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
-                                              pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
+            for (int i = 0; i < 4; ++i) {  // the exponent arguments on fp32 pairs
+              const float2 t = f2_split(f2_fma(f2_make(__uint_as_float(cur[g * 8 + 2 * i]),
+                                                       __uint_as_float(cur[g * 8 + 2 * i + 1])),
+                                               c22, nst));
+              w[i] = pack_bf16x2(ex2_approx(t.x), ex2_approx(t.y));
+            }
+            seg[(j & 1) * 4 + g] = make_uint4(w[0], w[1], w[2], w[3]);
           }
           if (j & 1) {  // a 64-column block is complete
             const int col0 = nb * BN + (c_begin + j - 1) * 32;
