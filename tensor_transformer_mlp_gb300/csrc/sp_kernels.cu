@@ -1064,29 +1064,49 @@ __global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restri
 // ------------------------------------------------------------------ attention softmax (fused form)
 // Row r's partial statistics (m_j, l_j) from the scores GEMM's kEpiRowStats epilogue (base 2:
 // m_j = max of the scaled scores times log2(e), l_j = sum of 2^(y - m_j)) become M = max_j m_j
-// and L = sum_j l_j * 2^(m_j - M), stored as (M + log2 L, 1/L); one warp per row, lanes over j.
+// and L = sum_j l_j * 2^(m_j - M), stored as (M + log2 L, 1/L). A warp takes 32 rows: chunks of
+// 16 partials (128 bytes of each row) are read line-wide (4 rows x 128 bytes per instruction)
+// into the warp's shared-memory block (16-byte segments XOR-swizzled by row), each lane then
+// takes its own row out of it and folds the chunk into a running (M, L) in index order.
 __global__ void __launch_bounds__(256) softmax_combine_kernel(const float2* __restrict__ stats, int nparts,
                                                               float2* __restrict__ rowstats, int64_t rows) {
-  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;  // uniform across the warp
-  const float2* st = stats + r * nparts;
-  float2 v[2];
-  float M = -INFINITY;
+  __shared__ __align__(16) uint8_t sbuf[8][32 * 128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r0 = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * 32;
+  if (r0 >= rows) return;  // uniform across the warp
+  uint8_t* buf = sbuf[warp];
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(stats);
+  const int64_t row_bytes = static_cast<int64_t>(nparts) * 8;
+  float M = -INFINITY, L = 0.f;
+  for (int c = 0; c * 16 < nparts; ++c) {
+    const int segs = min(8, (nparts - c * 16) / 2);  // 16-byte segments of this chunk in a row
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int j = lane + 32 * k;
-    v[k] = j < nparts ? st[j] : make_float2(-INFINITY, 0.f);
-    M = fmaxf(M, v[k].x);
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + (lane >> 3), j = lane & 7;
+      float4 v = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      if (r0 + rr < rows && j < segs)
+        v = *reinterpret_cast<const float4*>(base + (r0 + rr) * row_bytes + c * 128 + j * 16);
+      *reinterpret_cast<float4*>(buf + rr * 128 + ((j ^ (rr & 7)) << 4)) = v;
+    }
+    __syncwarp();
+    float4 mine[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mine[j] = *reinterpret_cast<const float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4));
+    __syncwarp();
+    float mc = M;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mc = fmaxf(mc, fmaxf(mine[j].x, mine[j].z));
+    float lc = L > 0.f ? L * ex2_approx(M - mc) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      lc += mine[j].y > 0.f ? mine[j].y * ex2_approx(mine[j].x - mc) : 0.f;
+      lc += mine[j].w > 0.f ? mine[j].w * ex2_approx(mine[j].z - mc) : 0.f;
+    }
+    M = mc;
+    L = lc;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float L = 0.f;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) L += v[k].y > 0.f ? v[k].y * ex2_approx(v[k].x - M) : 0.f;
-  L = warp_sum(L);
   // the softmax pass needs only M + log2(L): P = 2^(y - M) / L = 2^(y - (M + log2 L))
-  if (lane == 0) rowstats[r] = make_float2(M + log2f(L), 1.0f / L);
+  if (r0 + lane < rows) rowstats[r0 + lane] = make_float2(M + log2f(L), 1.0f / L);
 }
 
 // D[(bi*heads + j)*s + si] = sum over head j's dh columns of dO * O in token row bi*s + si
@@ -1493,8 +1513,8 @@ cudaError_t launch_softmax_combine(const void* stats, int nparts, void* rowstats
                                    int num_sms) {
   (void)num_sms;
   if (rows <= 0) return cudaSuccess;
-  if (nparts > 64) return cudaErrorInvalidValue;  // s <= 8192: at most 2 * 32 parts
-  softmax_combine_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+  if (nparts > 64 || nparts % 2 != 0) return cudaErrorInvalidValue;  // s <= 8192: at most 2 * 32 parts
+  softmax_combine_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(  // 8 warps x 32 rows
       static_cast<const float2*>(stats), nparts, static_cast<float2*>(rowstats), rows);
   return cudaGetLastError();
 }
