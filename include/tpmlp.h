@@ -363,7 +363,7 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
  *                  the launch's waves; 2: clusters of two SMs on 256 x 256 tiles only; 3: on
  *                  256 x 512 tiles only (a last round that would keep at most half the SM pairs
  *                  busy runs as 256 x 256 half-tiles, one per pair); 0: 128 x 256 tiles on one SM.
- *   pair_pacing 1: pairs wait at intervals of 32 k-blocks for the pairs of the same round of
+ *   pair_pacing 1: pairs wait at intervals of 16 k-blocks for the pairs of the same round of
  *                  tiles, which keeps shared operand panels in L2; 0: no pacing.
  *   pair_group  0: the default tile band (8 pair-rows walked along N for 256 x 256 tiles, 16
  *                  for 256 x 512 tiles); g > 0: g pair-rows walked along N; g < 0: -g N-blocks

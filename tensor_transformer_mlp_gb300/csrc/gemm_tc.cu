@@ -1036,7 +1036,7 @@ constexpr int PAIR_GROUP_M = GROUP_M / 2;                     // in 256-row pair
 static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory budget (pair kernel)");
 static_assert((2 * PAIR_STAGES + 2 * NUM_ACC + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area");
 
-constexpr int kPaceKb = 32;                 // k-blocks between pacing points
+constexpr int kPaceKb = 16;                 // k-blocks between pacing points (16 and 32 measured alike; 64: +0.4 %)
 // GeLU' epilogue of the wide kernel: the producer prefetches the tile's Z rows into L2 this many
 // k-blocks before the end of the tile's K-loop (map in the second output slot, tma_out bit 2).
 constexpr int kAuxPrefetchKb = 16;
