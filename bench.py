@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 GEMM_LAUNCHES_PER_STEP = 6
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the
 # committed ncu summary named below; None until a capture of the current kernel exists.
-DOMINANT_KERNEL_TRAFFIC = 7261305856  # average over the six GEMM launches of one step
+DOMINANT_KERNEL_TRAFFIC = 7013003349  # average over the six GEMM launches of one step
 DOMINANT_KERNEL_PROFILE = "profiles/gemm_bf16_wide_kernel_large_mlp_dram.md"
 
 

@@ -1427,6 +1427,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int kiter = 0;
       bool ok = true;
       const bool pacer = pace != nullptr && rank == 0;  // pacing as in the 256 x 256 pair kernel
+      // A panels are reused by every tile of a band: their lines are kept in L2 before others
+      // (DRAM reads per large-MLP step 37.8 -> 36.3 GB; marking B evict-first as well re-read
+      // B: 49 GB)
+      const uint64_t pol_a = l2_policy_evict_last();
       unsigned int pace_target = 0;
       int tile, half;
       for (int round = 0; ok && work(round, tile, half); ++round) {
@@ -1460,10 +1464,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* sa = smem + s * WIDE_STAGE_BYTES;
           uint8_t* sb = sa + A_STAGE_BYTES;
           if constexpr (!A_MN) {
-            tma_load_2d_pair(sa, &tmap_a, full0, kbl * BK, a_row);
+            tma_load_2d_pair_hint(sa, &tmap_a, full0, kbl * BK, a_row, pol_a);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(sa + j * MN_BOX_BYTES, &tmap_a, full0, a_row + j * 64, kbl * BK);
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair_hint(sa + j * MN_BOX_BYTES, &tmap_a, full0, a_row + j * 64, kbl * BK, pol_a);
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {  // this CTA's 128 columns of each 256-column half
