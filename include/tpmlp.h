@@ -365,8 +365,8 @@ tpmlp_status tpmlp_attention_backward(const void* X, const void* Wqkv, const voi
  *                  busy runs as 256 x 256 half-tiles, one per pair); 0: 128 x 256 tiles on one SM.
  *   pair_pacing 1: pairs wait at intervals of 16 k-blocks for the pairs of the same round of
  *                  tiles, which keeps shared operand panels in L2; 0: no pacing.
- *   pair_group  0: the default tile band (8 pair-rows walked along N for 256 x 256 tiles, 16
- *                  for 256 x 512 tiles); g > 0: g pair-rows walked along N; g < 0: -g N-blocks
+ *   pair_group  0: the default tile band (16 pair-rows walked along N, for 256 x 256 and
+ *                  256 x 512 tiles); g > 0: g pair-rows walked along N; g < 0: -g N-blocks
  *                  walked along M. |g| <= 4096.
  * The choice is read when a GEMM is launched, so a CUDA graph keeps the one it captured.
  * Every variant computes the same contractions with fp32 accumulation. Errors: TPMLP_ERR_INVALID.

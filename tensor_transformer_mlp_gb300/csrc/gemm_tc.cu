@@ -1032,7 +1032,9 @@ constexpr int PAIR_STAGES = 6;
 constexpr int BN_HALF = BN / 2;                               // B columns loaded per CTA
 constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + BN_HALF * BK * 2;  // 32 KiB
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + BARRIER_BYTES + 1024;
-constexpr int PAIR_GROUP_M = GROUP_M / 2;                     // in 256-row pair blocks
+// Tile band in 256-row pair blocks. Measured on the GPT MLP shape (where the wave model still
+// sends GEMMs here): 16 pair-rows 3654 us for the six GEMMs serialised, 12: 3668, 8: 3683, 4: 3724.
+constexpr int PAIR_GROUP_M = 16;
 static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory budget (pair kernel)");
 static_assert((2 * PAIR_STAGES + 2 * NUM_ACC + 1) * 8 + 4 <= BARRIER_BYTES, "barrier area");
 
