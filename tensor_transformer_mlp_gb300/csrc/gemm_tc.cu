@@ -68,15 +68,16 @@ constexpr int EPI_STAGE_BYTES = 32 * 128;
 constexpr int AUX_BUF_BYTES = 32 * 128;  // one 32-row x 64-column bf16 block
 // kAuxBufs > 0 (the batched softmax and dS epilogues): each epilogue warp owns that many 4 KB
 // buffers for TMA loads of P and TMA stores of its output instead of the generic staging buffer,
-// and the ring shrinks to 3 stages with 2 buffers a warp, 2 stages with 4 (the score-shaped GEMMs
-// have K = head_dim = two k-blocks, so with 2 stages the next tile's operands cannot be loaded
-// before the current tile's MMAs have freed a stage: the softmax pass measured 128.7 us with
-// 2 stages and 4 buffers, 115.3 us with 3 stages and 2, the same with 4 stages and 1).
+// and the ring shrinks to 4 stages with 1 buffer a warp, 3 with 2, 2 with 4 (the score-shaped
+// GEMMs have K = head_dim = two k-blocks, so with 2 stages the next tile's operands cannot be
+// loaded before the current tile's MMAs have freed a stage: the softmax pass measured 128.7 us
+// with 2 stages and 4 buffers, 115.3 us with 3 stages and 2; with its later epilogue changes
+// 103.6 us with 3 stages and 2 buffers, 101.3 us with 4 stages and 1).
 template <int BN_T, int kAuxBufs = 0>
 struct OneSm {
   static constexpr bool kAux = kAuxBufs > 0;
   static constexpr int kBN = BN_T;
-  static constexpr int kStages = kAux ? (kAuxBufs >= 4 ? 2 : 3) : (BN_T == 256 ? 4 : 6);
+  static constexpr int kStages = kAux ? (kAuxBufs >= 4 ? 2 : (kAuxBufs >= 2 ? 3 : 4)) : (BN_T == 256 ? 4 : 6);
   static constexpr int kStageBytes = A_STAGE_BYTES + BN_T * BK * 2;
   static constexpr int kEpiStageBytes = kAux ? 0 : NUM_EPI_WARPS * EPI_STAGE_BYTES;
   static constexpr int kAuxBytes = NUM_EPI_WARPS * kAuxBufs * AUX_BUF_BYTES;
@@ -605,10 +606,9 @@ __device__ __forceinline__ void epilogue_tile(const EpiParams& ep, uint8_t* buf,
   }
 }
 
-// Per-warp TMA buffers of the batched epilogues: kEpiSoftmax stores P through two (one store in
-// flight while the next pass is computed); kEpiSoftmaxGrad loads P through two and stores dS
-// through two more.
-constexpr int kSoftmaxStoreBufs = 2;
+// Per-warp TMA buffers of the batched epilogues: kEpiSoftmax stores P through one (its ring gets
+// the room for a fourth stage); kEpiSoftmaxGrad loads P through two and stores dS through two more.
+constexpr int kSoftmaxStoreBufs = 1;
 template <int EPI, bool BATCHED>
 __host__ __device__ constexpr int aux_bufs() {
   return !BATCHED ? 0 : (EPI == kEpiSoftmax ? kSoftmaxStoreBufs : (EPI == kEpiSoftmaxGrad ? 4 : 0));
